@@ -1,0 +1,275 @@
+/*
+ * rlscan.h -- C ABI of librlscan, batched first-order linear recurrences for
+ * reinforcement-learning credit assignment on NVIDIA GB300 (sm_103a).
+ *
+ * Every estimator solves, for each row (environment) of a [N, T] rollout
+ * buffer, the affine recurrence
+ *
+ *     backward:  A_t = alpha_t + beta_t * A_{t+1}      (t = T-1 .. 0)
+ *     forward:   A_t = alpha_t + beta_t * A_{t-1}      (t = 0 .. T-1)
+ *
+ * ("rl-triton: High-Performance Triton GPU Kernels for Reinforcement Learning
+ * Credit Assignment", Eq. 1 and its forward mirror in Sec. 1), with the
+ * per-step coefficients alpha_t, beta_t built inside the kernel from the raw
+ * rollout tensors (same paper, Table 1 and Sec. 3.3).  The recurrence is
+ * evaluated as an associative scan under (a1,b1) o (a2,b2) = (a1 + b1 a2,
+ * b1 b2) (Eq. 2, Prop. 1).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers are DEVICE pointers owned by the caller.  The library never
+ *    allocates, frees or retains them.
+ *  - [N,T] arrays are float32, row-major, element stride 1, row stride
+ *    `row_stride` elements (row_stride >= T), the same stride for every
+ *    [N,T] argument of a call, inputs and outputs alike.  [N] arrays are
+ *    dense float32.
+ *  - Flags (terminateds, truncateds, dones) are float32 0.0 / 1.0.  The
+ *    combined boundary flag is done_t = min(1, terminated_t + truncated_t).
+ *    terminated and truncated are mutually exclusive; other flag values are
+ *    outside the contract.
+ *  - Outputs must not overlap any input or each other.  Passing the same
+ *    pointer for an output and an input returns RLSCAN_ERR_ARG_CONFLICT;
+ *    partial overlaps are not detected.
+ *  - Nullable arguments are marked; NULL selects the documented default.
+ *  - Every call only enqueues work on `stream` and returns; nothing is
+ *    synchronised except in rlscan_workspace_status().
+ *  - N == 0 or T == 0 is a no-op returning RLSCAN_OK.
+ *  - Alignment: when T and row_stride are multiples of 4 and every [N,T]
+ *    pointer is 16-byte aligned, rows are staged into shared memory with
+ *    bulk asynchronous copies (TMA); otherwise an element-wise path is used.
+ *    Both give the same results.
+ *  - Workspace: rows longer than one kernel tile are scanned by several
+ *    thread blocks that pass carries through a caller-provided workspace
+ *    (decoupled look-back).  rlscan_workspace_bytes(N, T) gives the size
+ *    that suffices for every entry point at that shape (0 when none needs
+ *    one, in which case `ws` may be NULL).  A workspace must be zeroed once
+ *    with rlscan_workspace_init() before its first use; afterwards it needs
+ *    no clearing between calls.  One workspace serves one call at a time:
+ *    calls that use the same workspace must be ordered (same stream, or
+ *    synchronised).  Calls on different workspaces may run concurrently.
+ *  - Arithmetic is float32 (exp via expf, IEEE division).
+ */
+#ifndef RLSCAN_H
+#define RLSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA runtime headers. */
+typedef struct CUstream_st *rlscan_stream_t;
+
+typedef enum rlscan_status {
+    RLSCAN_OK = 0,
+    RLSCAN_ERR_NULL = 1,          /* a required pointer is NULL */
+    RLSCAN_ERR_SHAPE = 2,         /* N < 0, T < 0 or row_stride < T */
+    RLSCAN_ERR_ARG_CONFLICT = 3,  /* mutually exclusive arguments, or an output equals an input */
+    RLSCAN_ERR_ARG_VALUE = 4,     /* enum or scalar argument out of range */
+    RLSCAN_ERR_WORKSPACE = 5,     /* workspace needed but NULL, too small or misaligned */
+    RLSCAN_ERR_CUDA = 6,          /* the CUDA runtime refused the launch */
+    RLSCAN_ERR_INVALID_INPUT = 7, /* content check failed (only with RLSCAN_CHECKS=1) */
+    RLSCAN_ERR_TIMEOUT = 8        /* a cross-block wait gave up (reported by rlscan_workspace_status) */
+} rlscan_status;
+
+typedef enum rlscan_boundary {
+    RLSCAN_ENDS_AT = 0,   /* done[t] = 1: the segment ends at t, reset lands at t+1 */
+    RLSCAN_STARTS_AT = 1  /* done[t] = 1: the segment starts at t, reset lands at t  */
+} rlscan_boundary;
+
+typedef enum rlscan_direction {
+    RLSCAN_BACKWARD = 0,  /* A_t = alpha_t + beta_t A_{t+1}, A_T    = carry */
+    RLSCAN_FORWARD = 1    /* A_t = alpha_t + beta_t A_{t-1}, A_{-1} = carry */
+} rlscan_direction;
+
+/* Library version, (major << 16) | (minor << 8) | patch. */
+int rlscan_version(void);
+
+/* Static description of a status code.  Never NULL. */
+const char *rlscan_status_string(rlscan_status status);
+
+/* Bytes of workspace that suffice for every entry point on an [N, T] buffer.
+ * 0 when no entry point needs one at this shape.  Returns 0 for N <= 0 or
+ * T <= 0. */
+size_t rlscan_workspace_bytes(int64_t N, int64_t T);
+
+/* Zero a workspace of `ws_bytes` bytes (asynchronously on `stream`).  Call
+ * once after allocating it.  ws must be 16-byte aligned.
+ * Errors: RLSCAN_ERR_NULL, RLSCAN_ERR_WORKSPACE (misaligned), RLSCAN_ERR_CUDA. */
+rlscan_status rlscan_workspace_init(void *ws, size_t ws_bytes, rlscan_stream_t stream);
+
+/* Synchronise `stream`, then return and clear the error recorded in the
+ * workspace by earlier calls (RLSCAN_OK if none; RLSCAN_ERR_TIMEOUT if a
+ * cross-block wait gave up, in which case the affected outputs hold NaN).
+ * A CUDA error raised by the synchronisation is returned as RLSCAN_ERR_CUDA. */
+rlscan_status rlscan_workspace_status(void *ws, size_t ws_bytes, rlscan_stream_t stream);
+
+/*
+ * Generalized Advantage Estimation.
+ * rl-triton API reference, compute_gae; rl-triton paper Table 1 row "GAE",
+ * Sec. 3.2 and Sec. 3.3.1; "Technical Deep Dive into the GAE Triton Kernel"
+ * Sec. 5.
+ *   delta_t = r_t + gamma (1 - term_t) Vn_t - V_t
+ *   A_t     = delta_t + gamma lambda (1 - done_t) A_{t+1},   A_T = 0
+ * Vn_t, the successor value: with truncateds,
+ *   Vn_t = (t < T-1 ? (1 - trunc_t) V_{t+1} : 0) + bs_t;
+ * without truncateds, Vn_t = V_{t+1} for t < T-1 and Vn_{T-1} = bs_{T-1}
+ * (interior bootstrap entries are not read).  bs = bootstrap_values (zero
+ * when NULL); last_value supplies bs_{T-1} alone.
+ * Inputs : rewards, values, terminateds [N,T]; truncateds [N,T] nullable;
+ *          bootstrap_values [N,T] nullable; last_value [N] nullable.
+ * Output : advantages [N,T].
+ * Errors : RLSCAN_ERR_ARG_CONFLICT when both bootstrap_values and
+ *          last_value are given, or last_value together with truncateds.
+ */
+rlscan_status rlscan_gae(const float *rewards, const float *values, const float *terminateds,
+                         const float *truncateds, const float *bootstrap_values,
+                         const float *last_value, int64_t N, int64_t T, int64_t row_stride,
+                         float gamma, float lambda, float *advantages,
+                         void *ws, size_t ws_bytes, rlscan_stream_t stream);
+
+/*
+ * V-trace targets and advantages.
+ * rl-triton API reference, compute_vtrace; rl-triton paper Table 1 row
+ * "V-Trace" and Sec. 3.3.2.
+ *   ratio_t = exp(log_pi_target_t - log_pi_behavior_t)
+ *   rho_t = min(rho_bar, ratio_t),  c_t = min(c_bar, ratio_t)
+ *   D_t   = rho_t (r_t + gamma (1 - term_t) Vn_t - V_t) + gamma c_t (1 - done_t) D_{t+1},  D_T = 0
+ *   vs_t  = D_t + V_t
+ *   adv_t = rho_t (r_t + gamma (1 - term_t) vsn_t - V_t)
+ * Vn and vsn follow the successor rule of rlscan_gae (vsn with vs in place
+ * of V).  last_value may be combined with truncateds (it then supplies
+ * bs_{T-1}, interior bootstrap zero).
+ * Inputs : log_pi_target, log_pi_behavior, values, rewards, terminateds [N,T];
+ *          truncateds, bootstrap_values [N,T] nullable; last_value [N] nullable.
+ * Outputs: vtrace_targets, vtrace_advantages [N,T].
+ * Errors : RLSCAN_ERR_ARG_CONFLICT when both bootstrap_values and last_value.
+ */
+rlscan_status rlscan_vtrace(const float *log_pi_target, const float *log_pi_behavior,
+                            const float *values, const float *rewards, const float *terminateds,
+                            const float *truncateds, const float *bootstrap_values,
+                            const float *last_value, int64_t N, int64_t T, int64_t row_stride,
+                            float gamma, float rho_bar, float c_bar,
+                            float *vtrace_targets, float *vtrace_advantages,
+                            void *ws, size_t ws_bytes, rlscan_stream_t stream);
+
+/*
+ * Retrace(lambda) targets and advantages from per-step inputs.
+ * rl-triton API reference, compute_retrace (recurrence, targets and
+ * advantages); rl-triton paper Table 1 row "Retrace" and Sec. 3.3.3;
+ * "Retrace(lambda) with Triton Associative Scans" Sec. 3, 4 and 6.
+ *   ratio_t = pi_t / mu_t,  c_t = lambda min(c_bar, ratio_t),  rho_t = min(rho_bar, ratio_t)
+ *   D_t    = r_t + gamma (1 - term_t) EQ_t - Q_t + gamma c_{t+1} (1 - done_t) D_{t+1}
+ *            with c_T = 0 and D_T = 0
+ *   Qret_t = Q_t + D_t
+ *   adv_t  = rho_t (r_t + gamma (1 - term_t) Qret_{t+1} - Q_t),   Qret_T = 0
+ * pi_taken = pi(a_t|s_t), mu_taken = mu(a_t|s_t), expected_next_q =
+ * E_pi[Q(s_{t+1}, .)] (the caller supplies Q(s_T, .) at t = T-1).
+ * Inputs : pi_taken, mu_taken, q_values, expected_next_q, rewards,
+ *          terminateds [N,T]; truncateds [N,T] nullable (zero).
+ * Outputs: retrace_targets, advantages [N,T].
+ */
+rlscan_status rlscan_retrace(const float *pi_taken, const float *mu_taken, const float *q_values,
+                             const float *expected_next_q, const float *rewards,
+                             const float *terminateds, const float *truncateds,
+                             int64_t N, int64_t T, int64_t row_stride,
+                             float gamma, float lambda, float c_bar, float rho_bar,
+                             float *retrace_targets, float *advantages,
+                             void *ws, size_t ws_bytes, rlscan_stream_t stream);
+
+/*
+ * TD(lambda) returns.
+ * rl-triton API reference, compute_lambda_returns; rl-triton paper Table 1
+ * row "TD(lambda)" and Sec. 3.3.4; "Returns and Eligibility Traces with
+ * Triton Associative Scans" Sec. 2.
+ *   G_t = r_t + gamma (1-lambda)(1 - done_t) nv_t + gamma trunc_t bs_t
+ *         + gamma lambda (1 - done_t) G_{t+1},        G_T = bs_{T-1}
+ * nv = next_values (V(s_{t+1}), zeroed by the caller at truncated steps).
+ * bs = bootstrap_values (zero when NULL); last_value supplies bs_{T-1}
+ * alone (an addition to the pages' signature: their 1-D window bootstrap).
+ * Without truncateds only bs_{T-1} is read.
+ * Inputs : rewards, next_values, terminateds [N,T]; truncateds,
+ *          bootstrap_values [N,T] nullable; last_value [N] nullable.
+ * Output : returns [N,T].
+ * Errors : RLSCAN_ERR_ARG_CONFLICT when both bootstrap_values and last_value.
+ */
+rlscan_status rlscan_lambda_returns(const float *rewards, const float *next_values,
+                                    const float *terminateds, const float *truncateds,
+                                    const float *bootstrap_values, const float *last_value,
+                                    int64_t N, int64_t T, int64_t row_stride,
+                                    float gamma, float lambda, float *returns,
+                                    void *ws, size_t ws_bytes, rlscan_stream_t stream);
+
+/*
+ * Discounted returns (reward-to-go).
+ * rl-triton API reference, compute_discounted_returns; rl-triton paper
+ * Table 1 row "Disc. Returns" and Sec. 3.3.4; "Returns and Eligibility
+ * Traces with Triton Associative Scans" Sec. 1.
+ *   G_t = r_t + gamma trunc_t bs_t + gamma (1 - done_t) G_{t+1},   G_T = bs_{T-1}
+ * bs and last_value as for rlscan_lambda_returns.
+ * Inputs : rewards, terminateds [N,T]; truncateds, bootstrap_values [N,T]
+ *          nullable; last_value [N] nullable.
+ * Output : returns [N,T].
+ * Errors : RLSCAN_ERR_ARG_CONFLICT when both bootstrap_values and last_value.
+ */
+rlscan_status rlscan_discounted_returns(const float *rewards, const float *terminateds,
+                                        const float *truncateds, const float *bootstrap_values,
+                                        const float *last_value, int64_t N, int64_t T,
+                                        int64_t row_stride, float gamma, float *returns,
+                                        void *ws, size_t ws_bytes, rlscan_stream_t stream);
+
+/*
+ * Accumulating eligibility traces, forward in time.
+ * rl-triton API reference, compute_eligibility_traces; rl-triton paper
+ * Table 1 row "Elig. Traces" and Sec. 3.3.5.
+ *   z_t = g_t + gamma lambda (1 - d_{t-1}) z_{t-1},   d_{-1} = 0,  z_{-1} = seed
+ * dones[t] = 1 means the episode ends at t (pass terminated OR truncated,
+ * unshifted).  seed_values [N] nullable (zero).
+ * Inputs : gradients, dones [N,T]; seed_values [N] nullable.
+ * Output : traces [N,T].
+ */
+rlscan_status rlscan_eligibility_traces(const float *gradients, const float *dones,
+                                        const float *seed_values, int64_t N, int64_t T,
+                                        int64_t row_stride, float gamma, float lambda,
+                                        float *traces, void *ws, size_t ws_bytes,
+                                        rlscan_stream_t stream);
+
+/*
+ * Episodic prefix sum, forward in time.
+ * rl-triton API reference, compute_episodic_prefix_sum; rl-triton paper
+ * Table 1 row "Prefix Sum" and Sec. 3.3.6.
+ *   RLSCAN_ENDS_AT:   C_t = x_t + (1 - d_{t-1}) C_{t-1},   d_{-1} = 0
+ *   RLSCAN_STARTS_AT: C_t = x_t + (1 - d_t) C_{t-1}
+ *   C_{-1} = seed (zero when seed_values is NULL)
+ * Inputs : inputs, dones [N,T]; seed_values [N] nullable.
+ * Output : prefix_sums [N,T].
+ * Errors : RLSCAN_ERR_ARG_VALUE for an unknown boundary.
+ */
+rlscan_status rlscan_episodic_prefix_sum(const float *inputs, const float *dones,
+                                         const float *seed_values, rlscan_boundary boundary,
+                                         int64_t N, int64_t T, int64_t row_stride,
+                                         float *prefix_sums, void *ws, size_t ws_bytes,
+                                         rlscan_stream_t stream);
+
+/*
+ * Generic affine recurrence on caller-supplied coefficients.
+ * rl-triton paper Eq. 1 (backward) and its forward mirror (Sec. 1); the
+ * carry is applied as in Sec. 4.1 step 4.
+ *   RLSCAN_BACKWARD: A_t = alpha_t + beta_t A_{t+1},  A_T    = carry
+ *   RLSCAN_FORWARD:  A_t = alpha_t + beta_t A_{t-1},  A_{-1} = carry
+ * Inputs : alpha, beta [N,T]; carry [N] nullable (zero).
+ * Output : out [N,T].
+ * Errors : RLSCAN_ERR_ARG_VALUE for an unknown direction.
+ */
+rlscan_status rlscan_linear_scan(const float *alpha, const float *beta, const float *carry,
+                                 rlscan_direction direction, int64_t N, int64_t T,
+                                 int64_t row_stride, float *out, void *ws, size_t ws_bytes,
+                                 rlscan_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLSCAN_H */
