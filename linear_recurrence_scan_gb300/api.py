@@ -1,0 +1,298 @@
+"""PyTorch-facing functions with the rl-triton API reference's names and
+defaults.  Each one checks its arguments (CUDA residency, float32, shapes --
+the pages' always-on structural checks), allocates the outputs with torch,
+and makes exactly one librlscan call on the current CUDA stream.  There is no
+CPU path: a missing library or a non-CUDA tensor raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import _native
+
+__all__ = [
+    "compute_gae", "compute_vtrace", "compute_retrace_from_probs", "compute_lambda_returns",
+    "compute_discounted_returns", "compute_eligibility_traces", "compute_episodic_prefix_sum",
+    "linear_scan", "workspace_status",
+]
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+
+def _vp(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(name, t, shape, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on CUDA")
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name}: expected float32, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} shape {tuple(t.shape)} != {tuple(shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+class _Call:
+    """Collects the [N,T] and [N] tensors of one call, finds a common row
+    stride (making copies contiguous only when the strides differ), and
+    allocates outputs with that stride."""
+
+    def __init__(self, ref_name, ref):
+        _check(ref_name, ref, ref.shape)
+        if ref.dim() != 2:
+            raise ValueError(f"{ref_name} must be [num_envs, seq_len]")
+        self.N, self.T = ref.shape
+        self.device = ref.device
+        self.mats = {}
+        self.vecs = {}
+
+    def mat(self, name, t, required=True):
+        if t is None:
+            if required:
+                raise ValueError(f"{name} is required")
+            return
+        _check(name, t, (self.N, self.T), self.device)
+        self.mats[name] = t
+
+    def vec(self, name, t):
+        if t is None:
+            return
+        _check(name, t, (self.N,), self.device)
+        self.vecs[name] = t.contiguous()
+
+    def finish(self, n_out):
+        def unit_inner(t):
+            return self.T <= 1 or t.stride(1) == 1
+        strides = {t.stride(0) if self.N > 1 else max(self.T, 1) for t in self.mats.values()}
+        ok = all(unit_inner(t) for t in self.mats.values()) and len(strides) == 1
+        rs = strides.pop() if ok else self.T
+        if not ok or rs < self.T:
+            self.mats = {k: t.contiguous() for k, t in self.mats.items()}
+            rs = self.T
+        self.rs = max(rs, self.T)
+        if self.rs == self.T:
+            outs = [torch.empty((self.N, self.T), dtype=torch.float32, device=self.device)
+                    for _ in range(n_out)]
+        else:
+            outs = [torch.empty_strided((self.N, self.T), (self.rs, 1), dtype=torch.float32,
+                                        device=self.device) for _ in range(n_out)]
+        self.outs = outs
+        return outs
+
+    def m(self, name):
+        return _vp(self.mats.get(name))
+
+    def v(self, name):
+        return _vp(self.vecs.get(name))
+
+    def stream(self):
+        return ctypes.c_void_p(torch.cuda.current_stream(self.device).cuda_stream)
+
+
+_ws_lock = threading.Lock()
+_ws_cache = {}
+
+
+def _workspace(device, stream_handle, nbytes):
+    """A zero-initialised workspace for (device, stream), grown on demand.
+    Calls on one stream are ordered, so they may share a workspace."""
+    if nbytes == 0:
+        return None, 0
+    key = (device.index, stream_handle.value)
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < nbytes:
+            size = max(nbytes, 0 if ws is None else 2 * ws.numel())
+            size = (size + 255) // 256 * 256
+            ws = torch.empty(size, dtype=torch.uint8, device=device)
+            _native.check(_native.lib().rlscan_workspace_init(_vp(ws), size, stream_handle),
+                          "rlscan_workspace_init")
+            _ws_cache[key] = ws
+        return _vp(ws), ws.numel()
+
+
+def _ws_for(c):
+    s = c.stream()
+    need = _native.lib().rlscan_workspace_bytes(c.N, c.T)
+    p, n = _workspace(c.device, s, need)
+    return p, n, s
+
+
+def workspace_status(device=None):
+    """Synchronise the current stream and raise if a kernel recorded an
+    error (a cross-block wait that timed out) in its workspace."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    s = ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    ws = _ws_cache.get((device.index, s.value))
+    if ws is None:
+        torch.cuda.current_stream(device).synchronize()
+        return
+    _native.check(_native.lib().rlscan_workspace_status(_vp(ws), ws.numel(), s),
+                  "rlscan_workspace_status")
+
+
+# ---------------------------------------------------------------------------
+# estimators (rl-triton API reference signatures)
+
+def compute_gae(rewards, values, terminateds, truncateds=None, gamma=0.99, lambda_=0.95,
+                bootstrap_values=None, last_value=None):
+    """GAE advantages [num_envs, seq_len] (rl-triton API reference, compute_gae)."""
+    c = _Call("rewards", rewards)
+    c.mat("values", values)
+    c.mat("terminateds", terminateds)
+    c.mat("truncateds", truncateds, False)
+    c.mat("bootstrap_values", bootstrap_values, False)
+    c.vec("last_value", last_value)
+    if last_value is not None and bootstrap_values is not None:
+        raise ValueError("pass either last_value or bootstrap_values, not both")
+    if last_value is not None and truncateds is not None:
+        raise ValueError("last_value cannot be combined with truncateds; use bootstrap_values")
+    (out,) = c.finish(1)
+    ws, wsn, s = _ws_for(c)
+    _native.check(_native.lib().rlscan_gae(
+        c.m("rewards"), c.m("values"), c.m("terminateds"), c.m("truncateds"),
+        c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma), float(lambda_),
+        _vp(out), ws, wsn, s), "rlscan_gae")
+    return out
+
+
+def compute_vtrace(log_pi_target, log_pi_behavior, values, rewards, terminateds, truncateds=None,
+                   gamma=0.99, rho_bar=1.0, c_bar=1.0, bootstrap_values=None, last_value=None):
+    """V-trace (targets, advantages) (rl-triton API reference, compute_vtrace)."""
+    c = _Call("rewards", rewards)
+    c.mat("log_pi_target", log_pi_target)
+    c.mat("log_pi_behavior", log_pi_behavior)
+    c.mat("values", values)
+    c.mat("rewards", rewards)
+    c.mat("terminateds", terminateds)
+    c.mat("truncateds", truncateds, False)
+    c.mat("bootstrap_values", bootstrap_values, False)
+    c.vec("last_value", last_value)
+    if last_value is not None and bootstrap_values is not None:
+        raise ValueError("pass either last_value or bootstrap_values, not both")
+    vs, adv = c.finish(2)
+    ws, wsn, s = _ws_for(c)
+    _native.check(_native.lib().rlscan_vtrace(
+        c.m("log_pi_target"), c.m("log_pi_behavior"), c.m("values"), c.m("rewards"),
+        c.m("terminateds"), c.m("truncateds"), c.m("bootstrap_values"), c.v("last_value"),
+        c.N, c.T, c.rs, float(gamma), float(rho_bar), float(c_bar), _vp(vs), _vp(adv),
+        ws, wsn, s), "rlscan_vtrace")
+    return vs, adv
+
+
+def compute_retrace_from_probs(pi_taken, mu_taken, q_values, expected_next_q, rewards,
+                               terminateds, truncateds=None, gamma=0.99, lambda_=1.0, c_bar=1.0,
+                               rho_bar=1.0):
+    """Retrace(lambda) (targets, advantages) from per-step inputs:
+    pi(a_t|s_t), mu(a_t|s_t), Q(s_t,a_t), E_pi[Q(s_{t+1},.)] (rl-triton API
+    reference, compute_retrace, after its action-dimension reduction)."""
+    c = _Call("rewards", rewards)
+    for name, t in (("pi_taken", pi_taken), ("mu_taken", mu_taken), ("q_values", q_values),
+                    ("expected_next_q", expected_next_q), ("rewards", rewards),
+                    ("terminateds", terminateds)):
+        c.mat(name, t)
+    c.mat("truncateds", truncateds, False)
+    qret, adv = c.finish(2)
+    ws, wsn, s = _ws_for(c)
+    _native.check(_native.lib().rlscan_retrace(
+        c.m("pi_taken"), c.m("mu_taken"), c.m("q_values"), c.m("expected_next_q"),
+        c.m("rewards"), c.m("terminateds"), c.m("truncateds"), c.N, c.T, c.rs,
+        float(gamma), float(lambda_), float(c_bar), float(rho_bar), _vp(qret), _vp(adv),
+        ws, wsn, s), "rlscan_retrace")
+    return qret, adv
+
+
+def compute_lambda_returns(rewards, next_values, terminateds, truncateds=None, gamma=0.99,
+                           lambda_=0.95, bootstrap_values=None, last_value=None):
+    """TD(lambda) returns (rl-triton API reference, compute_lambda_returns;
+    ``last_value`` is an addition: the window bootstrap as an [N] vector)."""
+    c = _Call("rewards", rewards)
+    c.mat("next_values", next_values)
+    c.mat("terminateds", terminateds)
+    c.mat("truncateds", truncateds, False)
+    c.mat("bootstrap_values", bootstrap_values, False)
+    c.vec("last_value", last_value)
+    if last_value is not None and bootstrap_values is not None:
+        raise ValueError("pass either last_value or bootstrap_values, not both")
+    (out,) = c.finish(1)
+    ws, wsn, s = _ws_for(c)
+    _native.check(_native.lib().rlscan_lambda_returns(
+        c.m("rewards"), c.m("next_values"), c.m("terminateds"), c.m("truncateds"),
+        c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma), float(lambda_),
+        _vp(out), ws, wsn, s), "rlscan_lambda_returns")
+    return out
+
+
+def compute_discounted_returns(rewards, terminateds, truncateds=None, gamma=0.99,
+                               bootstrap_values=None, last_value=None):
+    """Discounted returns (rl-triton API reference, compute_discounted_returns)."""
+    c = _Call("rewards", rewards)
+    c.mat("terminateds", terminateds)
+    c.mat("truncateds", truncateds, False)
+    c.mat("bootstrap_values", bootstrap_values, False)
+    c.vec("last_value", last_value)
+    if last_value is not None and bootstrap_values is not None:
+        raise ValueError("pass either last_value or bootstrap_values, not both")
+    (out,) = c.finish(1)
+    ws, wsn, s = _ws_for(c)
+    _native.check(_native.lib().rlscan_discounted_returns(
+        c.m("rewards"), c.m("terminateds"), c.m("truncateds"), c.m("bootstrap_values"),
+        c.v("last_value"), c.N, c.T, c.rs, float(gamma), _vp(out), ws, wsn, s),
+        "rlscan_discounted_returns")
+    return out
+
+
+def compute_eligibility_traces(gradients, dones, gamma, lambda_, seed_values=None):
+    """Forward eligibility traces (rl-triton API reference, compute_eligibility_traces)."""
+    c = _Call("gradients", gradients)
+    c.mat("gradients", gradients)
+    c.mat("dones", dones)
+    c.vec("seed_values", seed_values)
+    (out,) = c.finish(1)
+    ws, wsn, s = _ws_for(c)
+    _native.check(_native.lib().rlscan_eligibility_traces(
+        c.m("gradients"), c.m("dones"), c.v("seed_values"), c.N, c.T, c.rs, float(gamma),
+        float(lambda_), _vp(out), ws, wsn, s), "rlscan_eligibility_traces")
+    return out
+
+
+def compute_episodic_prefix_sum(inputs, dones, seed_values=None, boundary="ends_at"):
+    """Episodic prefix sum (rl-triton API reference, compute_episodic_prefix_sum)."""
+    if boundary not in ("ends_at", "starts_at"):
+        raise ValueError(f"boundary must be 'ends_at' or 'starts_at', got {boundary!r}")
+    c = _Call("inputs", inputs)
+    c.mat("inputs", inputs)
+    c.mat("dones", dones)
+    c.vec("seed_values", seed_values)
+    (out,) = c.finish(1)
+    ws, wsn, s = _ws_for(c)
+    _native.check(_native.lib().rlscan_episodic_prefix_sum(
+        c.m("inputs"), c.m("dones"), c.v("seed_values"),
+        _native.ENDS_AT if boundary == "ends_at" else _native.STARTS_AT,
+        c.N, c.T, c.rs, _vp(out), ws, wsn, s), "rlscan_episodic_prefix_sum")
+    return out
+
+
+def linear_scan(alpha, beta, carry=None, direction="backward"):
+    """Generic affine recurrence (rl-triton paper Eq. 1 and its forward mirror)."""
+    if direction not in ("backward", "forward"):
+        raise ValueError(f"direction must be 'backward' or 'forward', got {direction!r}")
+    c = _Call("alpha", alpha)
+    c.mat("alpha", alpha)
+    c.mat("beta", beta)
+    c.vec("carry", carry)
+    (out,) = c.finish(1)
+    ws, wsn, s = _ws_for(c)
+    _native.check(_native.lib().rlscan_linear_scan(
+        c.m("alpha"), c.m("beta"), c.v("carry"),
+        _native.BACKWARD if direction == "backward" else _native.FORWARD,
+        c.N, c.T, c.rs, _vp(out), ws, wsn, s), "rlscan_linear_scan")
+    return out

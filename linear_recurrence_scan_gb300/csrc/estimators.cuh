@@ -1,0 +1,420 @@
+// estimators.cuh -- per-estimator coefficient and output functors.
+//
+// Each estimator turns the raw rollout inputs of one thread's ITEMS
+// consecutive time steps into the affine-scan coefficients (alpha_t, beta_t)
+// in registers, names the boundary value folded into the scan at the row
+// end (backward) or row start (forward), and turns the scan result A_t into
+// the outputs.  Sources: rl-triton paper Table 1 and Sec. 3.2-3.3; rl-triton
+// API reference (compute_* docstrings); "Retrace(lambda) with Triton
+// Associative Scans" Sec. 3-6.
+//
+// Interface (all static, I = items per thread):
+//   NIN, NOUT       number of [N,T] inputs and outputs
+//   FWD             true for forward-in-time recurrences
+//   HALO            bit j set: input j is also read one step outside the
+//                   thread's range (t+1 backward, t-1 forward)
+//   ROWSCALAR       the per-row scalar argument is used
+//   Keep<I>         values saved from coeffs() for post()
+//   coeffs(x, xn, t0, p, rsc, a, b, keep)
+//       x[j][k] = input j at time t0+k; xn[j] = input j at the neighbouring
+//       time outside the range (only meaningful for HALO inputs);
+//       rsc = this row's scalar (only meaningful where the row boundary lies
+//       in the thread's range).
+//   boundary(x, k, rsc, p)
+//       value folded in at the row boundary element k: A_T (backward) or
+//       A_{-1} (forward); the kernel sets a_k += b_k * value, b_k = 0.
+//   post(x, xn, t0, p, rsc, A, A_after, keep, o)
+//       A[k] = scan result at t0+k; A_after = result at the step after the
+//       range (backward only; used for successor targets).
+#pragma once
+
+#include "params.cuh"
+
+namespace rlscan {
+namespace est {
+
+// done_t = min(1, terminated_t + truncated_t)
+__device__ __forceinline__ float done_of(float term, float trunc) { return fminf(1.f, term + trunc); }
+
+// ---------------------------------------------------------------------------
+// GAE: alpha = r + gamma (1-term) Vn - V, beta = gamma lambda (1-done), A_T = 0.
+// Inputs: 0 rewards, 1 values, 2 terminateds, [3 truncateds], [3+TRUNC bootstrap].
+// Vn at T-1 is the bootstrap (bootstrap column or last_value / scalar column).
+template <bool TRUNC, bool BS2D>
+struct GAE {
+    static_assert(TRUNC || !BS2D, "2-D bootstrap is read only with truncation flags");
+    static constexpr int NIN = 3 + TRUNC + BS2D, NOUT = 1;
+    static constexpr bool FWD = false, ROWSCALAR = !BS2D;
+    static constexpr unsigned HALO = 1u << 1;
+    static constexpr int TR = 3, BS = 3 + TRUNC;
+    template <int I> struct Keep {};
+
+    template <int I>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+                                  const Params &p, float rsc, float (&a)[I], float (&b)[I], Keep<I> &)
+    {
+        const float g = p.c0, gl = p.c0 * p.c1;
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            const bool last = (t0 + k == p.T - 1);
+            const float vnext = (k + 1 < I) ? x[1][k + 1] : xn[1];
+            const float term = x[2][k];
+            float vn, done;
+            if constexpr (TRUNC) {
+                const float tr = x[TR][k];
+                float bs;
+                if constexpr (BS2D) bs = x[BS][k];
+                else bs = last ? rsc : 0.f;
+                vn = last ? bs : fmaf(1.f - tr, vnext, bs);
+                done = done_of(term, tr);
+            } else {
+                vn = last ? rsc : vnext;
+                done = term;
+            }
+            a[k] = fmaf(g * (1.f - term), vn, x[0][k]) - x[1][k];
+            b[k] = gl * (1.f - done);
+        }
+    }
+    template <int I>
+    __device__ static float boundary(const float (&)[NIN][I], int, float, const Params &) { return 0.f; }
+    template <int I>
+    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int64_t, const Params &,
+                                float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
+    {
+#pragma unroll
+        for (int k = 0; k < I; ++k) o[0][k] = A[k];
+    }
+};
+
+// ---------------------------------------------------------------------------
+// V-trace: ratio = exp(lpt - lpb), rho = min(rho_bar, ratio), c = min(c_bar, ratio);
+// alpha = rho (r + gamma (1-term) Vn - V), beta = gamma c (1-done), D_T = 0;
+// vs = D + V, adv = rho (r + gamma (1-term) vsn - V).
+// Inputs: 0 lpt, 1 lpb, 2 values, 3 rewards, 4 terminateds, [5 truncateds], [5+TRUNC bootstrap].
+// Constants: c0 gamma, c1 rho_bar, c2 c_bar.
+template <bool TRUNC, bool BS2D>
+struct VTrace {
+    static_assert(TRUNC || !BS2D, "2-D bootstrap is read only with truncation flags");
+    static constexpr int NIN = 5 + TRUNC + BS2D, NOUT = 2;
+    static constexpr bool FWD = false, ROWSCALAR = !BS2D;
+    static constexpr unsigned HALO = 1u << 2;
+    static constexpr int TR = 5, BS = 5 + TRUNC;
+    template <int I> struct Keep { float rho[I]; };
+
+    // successor of x at element k: bootstrap rule shared by Vn and vsn
+    template <int I>
+    __device__ static float successor(const float (&x)[NIN][I], int k, bool last, float nxt, float rsc)
+    {
+        if constexpr (TRUNC) {
+            float bs;
+            if constexpr (BS2D) bs = x[BS][k];
+            else bs = last ? rsc : 0.f;
+            return last ? bs : fmaf(1.f - x[TR][k], nxt, bs);
+        } else {
+            return last ? rsc : nxt;
+        }
+    }
+
+    template <int I>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+                                  const Params &p, float rsc, float (&a)[I], float (&b)[I], Keep<I> &keep)
+    {
+        const float g = p.c0;
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            const bool last = (t0 + k == p.T - 1);
+            const float ratio = expf(x[0][k] - x[1][k]);
+            const float rho = fminf(p.c1, ratio), c = fminf(p.c2, ratio);
+            const float term = x[4][k];
+            const float vn = successor<I>(x, k, last, (k + 1 < I) ? x[2][k + 1] : xn[2], rsc);
+            float done;
+            if constexpr (TRUNC) done = done_of(term, x[TR][k]);
+            else done = term;
+            a[k] = rho * (fmaf(g * (1.f - term), vn, x[3][k]) - x[2][k]);
+            b[k] = g * c * (1.f - done);
+            keep.rho[k] = rho;
+        }
+    }
+    template <int I>
+    __device__ static float boundary(const float (&)[NIN][I], int, float, const Params &) { return 0.f; }
+    template <int I>
+    __device__ static void post(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+                                const Params &p, float rsc, const float (&A)[I], float A_after,
+                                const Keep<I> &keep, float (&o)[NOUT][I])
+    {
+        const float g = p.c0;
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            const bool last = (t0 + k == p.T - 1);
+            const float vs_next = (k + 1 < I) ? A[k + 1] + x[2][k + 1] : A_after + xn[2];
+            const float nvs = successor<I>(x, k, last, vs_next, rsc);
+            const float term = x[4][k];
+            o[0][k] = A[k] + x[2][k];
+            o[1][k] = keep.rho[k] * (fmaf(g * (1.f - term), nvs, x[3][k]) - x[2][k]);
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Retrace on per-step inputs: ratio = pi/mu, c = lambda min(c_bar, ratio),
+// rho = min(rho_bar, ratio); alpha = r + gamma (1-term) EQ - Q,
+// beta = gamma c_{t+1} (1-done) with c_T = 0; Qret = D + Q;
+// adv = rho (r + gamma (1-term) Qret_{t+1} - Q), Qret_T = 0.
+// Inputs: 0 pi, 1 mu, 2 q, 3 eq, 4 rewards, 5 terminateds, [6 truncateds].
+// Constants: c0 gamma, c1 lambda, c2 c_bar, c3 rho_bar.
+template <bool TRUNC>
+struct Retrace {
+    static constexpr int NIN = 6 + TRUNC, NOUT = 2;
+    static constexpr bool FWD = false, ROWSCALAR = false;
+    static constexpr unsigned HALO = (1u << 0) | (1u << 1) | (1u << 2);
+    template <int I> struct Keep { float rho[I]; };
+
+    template <int I>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+                                  const Params &p, float, float (&a)[I], float (&b)[I], Keep<I> &keep)
+    {
+        const float g = p.c0, lam = p.c1;
+        float c[I + 1];
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            const float ratio = x[0][k] / x[1][k];
+            c[k] = lam * fminf(p.c2, ratio);
+            keep.rho[k] = fminf(p.c3, ratio);
+        }
+        c[I] = lam * fminf(p.c2, xn[0] / xn[1]);
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            const bool last = (t0 + k == p.T - 1);
+            const float term = x[5][k];
+            float done;
+            if constexpr (TRUNC) done = done_of(term, x[6][k]);
+            else done = term;
+            const float cn = last ? 0.f : c[k + 1];
+            a[k] = fmaf(g * (1.f - term), x[3][k], x[4][k]) - x[2][k];
+            b[k] = g * cn * (1.f - done);
+        }
+    }
+    template <int I>
+    __device__ static float boundary(const float (&)[NIN][I], int, float, const Params &) { return 0.f; }
+    template <int I>
+    __device__ static void post(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+                                const Params &p, float, const float (&A)[I], float A_after,
+                                const Keep<I> &keep, float (&o)[NOUT][I])
+    {
+        const float g = p.c0;
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            const bool last = (t0 + k == p.T - 1);
+            const float qn = last ? 0.f : ((k + 1 < I) ? A[k + 1] + x[2][k + 1] : A_after + xn[2]);
+            const float term = x[5][k];
+            o[0][k] = A[k] + x[2][k];
+            o[1][k] = keep.rho[k] * (fmaf(g * (1.f - term), qn, x[4][k]) - x[2][k]);
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// TD(lambda): alpha = r + gamma (1-lambda)(1-done) nv + gamma trunc bs,
+// beta = gamma lambda (1-done), A_T = bs_{T-1}.
+// Inputs: 0 rewards, 1 next_values, 2 terminateds, [3 truncateds], [3+TRUNC bootstrap].
+// Row scalar: bs_{T-1} (last_value, or the bootstrap column) when no 2-D bootstrap.
+template <bool TRUNC, bool BS2D>
+struct LambdaReturns {
+    static_assert(TRUNC || !BS2D, "2-D bootstrap is read only with truncation flags");
+    static constexpr int NIN = 3 + TRUNC + BS2D, NOUT = 1;
+    static constexpr bool FWD = false, ROWSCALAR = !BS2D;
+    static constexpr unsigned HALO = 0;
+    static constexpr int TR = 3, BS = 3 + TRUNC;
+    template <int I> struct Keep {};
+
+    template <int I>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&)[NIN], int64_t t0,
+                                  const Params &p, float rsc, float (&a)[I], float (&b)[I], Keep<I> &)
+    {
+        const float g = p.c0, gl = p.c0 * p.c1, g1l = p.c0 * (1.f - p.c1);
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            const float term = x[2][k];
+            if constexpr (TRUNC) {
+                const bool last = (t0 + k == p.T - 1);
+                const float tr = x[TR][k];
+                float bs;
+                if constexpr (BS2D) bs = x[BS][k];
+                else bs = last ? rsc : 0.f;
+                const float nd = 1.f - done_of(term, tr);
+                a[k] = fmaf(g * tr, bs, fmaf(g1l * nd, x[1][k], x[0][k]));
+                b[k] = gl * nd;
+            } else {
+                const float nd = 1.f - term;
+                a[k] = fmaf(g1l * nd, x[1][k], x[0][k]);
+                b[k] = gl * nd;
+            }
+        }
+    }
+    template <int I>
+    __device__ static float boundary(const float (&x)[NIN][I], int k, float rsc, const Params &)
+    {
+        if constexpr (BS2D) return x[BS][k];
+        else return rsc;
+    }
+    template <int I>
+    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int64_t, const Params &,
+                                float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
+    {
+#pragma unroll
+        for (int k = 0; k < I; ++k) o[0][k] = A[k];
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Discounted returns: alpha = r + gamma trunc bs, beta = gamma (1-done), A_T = bs_{T-1}.
+// Inputs: 0 rewards, 1 terminateds, [2 truncateds], [2+TRUNC bootstrap].
+template <bool TRUNC, bool BS2D>
+struct Discounted {
+    static_assert(TRUNC || !BS2D, "2-D bootstrap is read only with truncation flags");
+    static constexpr int NIN = 2 + TRUNC + BS2D, NOUT = 1;
+    static constexpr bool FWD = false, ROWSCALAR = !BS2D;
+    static constexpr unsigned HALO = 0;
+    static constexpr int TR = 2, BS = 2 + TRUNC;
+    template <int I> struct Keep {};
+
+    template <int I>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&)[NIN], int64_t t0,
+                                  const Params &p, float rsc, float (&a)[I], float (&b)[I], Keep<I> &)
+    {
+        const float g = p.c0;
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            const float term = x[1][k];
+            if constexpr (TRUNC) {
+                const bool last = (t0 + k == p.T - 1);
+                const float tr = x[TR][k];
+                float bs;
+                if constexpr (BS2D) bs = x[BS][k];
+                else bs = last ? rsc : 0.f;
+                a[k] = fmaf(g * tr, bs, x[0][k]);
+                b[k] = g * (1.f - done_of(term, tr));
+            } else {
+                a[k] = x[0][k];
+                b[k] = g * (1.f - term);
+            }
+        }
+    }
+    template <int I>
+    __device__ static float boundary(const float (&x)[NIN][I], int k, float rsc, const Params &)
+    {
+        if constexpr (BS2D) return x[BS][k];
+        else return rsc;
+    }
+    template <int I>
+    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int64_t, const Params &,
+                                float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
+    {
+#pragma unroll
+        for (int k = 0; k < I; ++k) o[0][k] = A[k];
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Eligibility traces (forward): alpha = g_t, beta = gamma lambda (1 - d_{t-1}),
+// d_{-1} = 0, A_{-1} = seed.  Inputs: 0 gradients, 1 dones.
+struct Eligibility {
+    static constexpr int NIN = 2, NOUT = 1;
+    static constexpr bool FWD = true, ROWSCALAR = true;
+    static constexpr unsigned HALO = 1u << 1;
+    template <int I> struct Keep {};
+
+    template <int I>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+                                  const Params &p, float, float (&a)[I], float (&b)[I], Keep<I> &)
+    {
+        const float gl = p.c0 * p.c1;
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            float dprev = (k > 0) ? x[1][k - 1] : xn[1];
+            if (t0 + k == 0) dprev = 0.f;
+            a[k] = x[0][k];
+            b[k] = gl * (1.f - dprev);
+        }
+    }
+    template <int I>
+    __device__ static float boundary(const float (&)[NIN][I], int, float rsc, const Params &) { return rsc; }
+    template <int I>
+    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int64_t, const Params &,
+                                float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
+    {
+#pragma unroll
+        for (int k = 0; k < I; ++k) o[0][k] = A[k];
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Episodic prefix sum (forward): alpha = x_t; beta = 1 - d_{t-1} (ends_at,
+// d_{-1} = 0) or 1 - d_t (starts_at); A_{-1} = seed.  Inputs: 0 inputs, 1 dones.
+template <bool STARTS_AT>
+struct Prefix {
+    static constexpr int NIN = 2, NOUT = 1;
+    static constexpr bool FWD = true, ROWSCALAR = true;
+    static constexpr unsigned HALO = STARTS_AT ? 0u : (1u << 1);
+    template <int I> struct Keep {};
+
+    template <int I>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+                                  const Params &, float, float (&a)[I], float (&b)[I], Keep<I> &)
+    {
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            float d;
+            if constexpr (STARTS_AT) {
+                d = x[1][k];
+            } else {
+                d = (k > 0) ? x[1][k - 1] : xn[1];
+                if (t0 + k == 0) d = 0.f;
+            }
+            a[k] = x[0][k];
+            b[k] = 1.f - d;
+        }
+    }
+    template <int I>
+    __device__ static float boundary(const float (&)[NIN][I], int, float rsc, const Params &) { return rsc; }
+    template <int I>
+    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int64_t, const Params &,
+                                float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
+    {
+#pragma unroll
+        for (int k = 0; k < I; ++k) o[0][k] = A[k];
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Generic affine scan on given alpha, beta; boundary = carry.  Inputs: 0 alpha, 1 beta.
+template <bool FORWARD>
+struct Linear {
+    static constexpr int NIN = 2, NOUT = 1;
+    static constexpr bool FWD = FORWARD, ROWSCALAR = true;
+    static constexpr unsigned HALO = 0;
+    template <int I> struct Keep {};
+
+    template <int I>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&)[NIN], int64_t,
+                                  const Params &, float, float (&a)[I], float (&b)[I], Keep<I> &)
+    {
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            a[k] = x[0][k];
+            b[k] = x[1][k];
+        }
+    }
+    template <int I>
+    __device__ static float boundary(const float (&)[NIN][I], int, float rsc, const Params &) { return rsc; }
+    template <int I>
+    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int64_t, const Params &,
+                                float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
+    {
+#pragma unroll
+        for (int k = 0; k < I; ++k) o[0][k] = A[k];
+    }
+};
+
+}  // namespace est
+}  // namespace rlscan

@@ -1,0 +1,65 @@
+// params.cuh -- the argument block every scan kernel receives, and the
+// internal launcher entry points the C ABI dispatches to.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "rlscan.h"
+
+namespace rlscan {
+
+constexpr int kMaxIn = 8;
+
+// Workspace layout: a 64-byte header followed by one 16-byte state per tile.
+//   bytes  0.. 7  u64 tile ticket (dynamic tile ids, reset by the last CTA)
+//   bytes  8..11  u32 count of CTAs that finished (reset by the last CTA)
+//   bytes 12..15  u32 first error code recorded on the device (0 = none)
+//   bytes 16..19  u32 detail of that error (tile index / stage)
+constexpr size_t kHeaderBytes = 64;
+constexpr size_t kStateBytes = 16;
+enum HeaderWord : int { kHdrExit = 2, kHdrError = 3, kHdrDetail = 4 };
+
+// Smallest tile (elements per row segment) any kernel uses; the workspace
+// size query is computed with it, so it covers every entry point.
+constexpr int kMinTile = 1024;
+
+struct Params {
+    const float *in[kMaxIn];   // [N, rs] inputs, order defined by the estimator
+    float *out[2];             // [N, rs] outputs
+    const float *rowscalar;    // per-row scalar (bootstrap / carry / seed), nullable
+    int64_t rowscalar_stride;  // elements between consecutive rows' scalars
+    int64_t N, T, rs;
+    float c0, c1, c2, c3;      // estimator constants (gamma, lambda, clips)
+
+    // tiling, filled by the launcher
+    int64_t num_tiles;         // tiles in the whole problem
+    int64_t tiles_per_row;     // 1 when whole rows are packed into a tile
+    int32_t C;                 // smem row pitch of a tile (elements)
+    int32_t R;                 // rows per tile (packed) or 1
+    int32_t packed;            // 1: tiles hold whole rows; 0: rows split into tiles
+    int32_t tma;               // 1: bulk asynchronous copies; 0: element-wise loads
+    int32_t dynamic;           // 1: tile ids from the workspace ticket (look-back)
+    uint32_t epoch;            // tag of this call's tile states (30 bits)
+    unsigned long long *states;
+    uint32_t *hdr;
+    uint64_t spin_limit_ns;    // bound on every cross-block wait
+};
+
+// Launchers (one translation unit per estimator family).
+rlscan_status launch_gae(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
+rlscan_status launch_vtrace(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
+rlscan_status launch_retrace(bool trunc, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
+rlscan_status launch_lambda_returns(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
+rlscan_status launch_discounted(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
+rlscan_status launch_eligibility(Params p, void *ws, size_t ws_bytes, cudaStream_t s);
+rlscan_status launch_prefix(bool starts_at, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
+rlscan_status launch_linear(bool forward, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
+
+// Host helpers shared by the launchers (rlscan_abi.cu).
+uint32_t next_epoch();
+uint64_t spin_limit_ns();
+
+}  // namespace rlscan

@@ -1,0 +1,382 @@
+// rlscan_abi.cu -- the extern "C" entry points of librlscan: argument
+// validation (the pages' always-on structural checks, rl-triton API
+// reference, compute_* functions), choice of the kernel specialisation from
+// which optional arguments are present (the pages' HAS_TRUNCATIONS /
+// HAS_BOOTSTRAP / HAS_SEED / BOUNDARY_ENDS_AT specialisations, paper
+// Sec. 4.2), and the workspace helpers.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <initializer_list>
+
+#include <cuda_runtime.h>
+
+#include "params.cuh"
+
+namespace rlscan {
+
+uint32_t next_epoch()
+{
+    static std::atomic<uint32_t> counter{0};
+    uint32_t e;
+    do {
+        e = (counter.fetch_add(1, std::memory_order_relaxed) + 1) & 0x3FFFFFFFu;
+    } while (e == 0);
+    return e;
+}
+
+uint64_t spin_limit_ns()
+{
+    static const uint64_t limit = [] {
+        const char *s = std::getenv("RLSCAN_SPIN_LIMIT_NS");
+        if (s != nullptr) {
+            const unsigned long long v = std::strtoull(s, nullptr, 10);
+            if (v > 0) return static_cast<uint64_t>(v);
+        }
+        return static_cast<uint64_t>(1000000000ull);  // one second
+    }();
+    return limit;
+}
+
+namespace {
+
+__global__ void zero_words(uint32_t *p, size_t n)
+{
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        p[i] = 0u;
+}
+
+inline cudaStream_t cs(rlscan_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline rlscan_status check_shape(int64_t N, int64_t T, int64_t rs)
+{
+    if (N < 0 || T < 0 || rs < T) return RLSCAN_ERR_SHAPE;
+    return RLSCAN_OK;
+}
+
+// An output equal to any input (or to the other output) is a conflict.
+inline bool same_as_any(const void *out, std::initializer_list<const void *> others)
+{
+    for (const void *o : others)
+        if (o != nullptr && o == out) return true;
+    return false;
+}
+
+inline Params base_params(int64_t N, int64_t T, int64_t rs)
+{
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.N = N;
+    p.T = T;
+    p.rs = rs;
+    p.rowscalar_stride = 1;
+    return p;
+}
+
+}  // namespace
+}  // namespace rlscan
+
+using namespace rlscan;
+
+#define RLSCAN_TRY(expr)                           \
+    do {                                           \
+        const rlscan_status st_ = (expr);          \
+        if (st_ != RLSCAN_OK) return st_;          \
+    } while (0)
+
+#define RLSCAN_API __attribute__((visibility("default")))
+
+extern "C" {
+
+RLSCAN_API int rlscan_version(void) { return (0 << 16) | (1 << 8) | 0; }
+
+RLSCAN_API const char *rlscan_status_string(rlscan_status status)
+{
+    switch (status) {
+    case RLSCAN_OK: return "ok";
+    case RLSCAN_ERR_NULL: return "a required pointer is NULL";
+    case RLSCAN_ERR_SHAPE: return "invalid shape (N < 0, T < 0 or row_stride < T)";
+    case RLSCAN_ERR_ARG_CONFLICT: return "conflicting arguments (exclusive options, or an output equal to an input)";
+    case RLSCAN_ERR_ARG_VALUE: return "argument value out of range";
+    case RLSCAN_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case RLSCAN_ERR_CUDA: return "CUDA runtime error";
+    case RLSCAN_ERR_INVALID_INPUT: return "input content check failed";
+    case RLSCAN_ERR_TIMEOUT: return "a cross-block wait timed out";
+    }
+    return "unknown status";
+}
+
+RLSCAN_API size_t rlscan_workspace_bytes(int64_t N, int64_t T)
+{
+    if (N <= 0 || T <= 0 || T <= kMinTile) return 0;
+    const int64_t tiles = N * ((T + kMinTile - 1) / kMinTile);
+    return kHeaderBytes + kStateBytes * static_cast<size_t>(tiles);
+}
+
+RLSCAN_API rlscan_status rlscan_workspace_init(void *ws, size_t ws_bytes, rlscan_stream_t stream)
+{
+    if (ws == nullptr) return RLSCAN_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(ws) & 15u) != 0 || ws_bytes % 4 != 0) return RLSCAN_ERR_WORKSPACE;
+    const size_t words = ws_bytes / 4;
+    if (words == 0) return RLSCAN_OK;
+    size_t blocks = (words + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    zero_words<<<static_cast<unsigned>(blocks), 256, 0, cs(stream)>>>(static_cast<uint32_t *>(ws), words);
+    return cudaGetLastError() == cudaSuccess ? RLSCAN_OK : RLSCAN_ERR_CUDA;
+}
+
+RLSCAN_API rlscan_status rlscan_workspace_status(void *ws, size_t ws_bytes, rlscan_stream_t stream)
+{
+    if (cudaStreamSynchronize(cs(stream)) != cudaSuccess) return RLSCAN_ERR_CUDA;
+    if (ws == nullptr || ws_bytes < kHeaderBytes) return RLSCAN_OK;
+    uint32_t *hdr = static_cast<uint32_t *>(ws);
+    uint32_t code = 0;
+    if (cudaMemcpy(&code, hdr + kHdrError, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return RLSCAN_ERR_CUDA;
+    if (code != 0) {
+        const uint32_t zero[2] = {0u, 0u};
+        if (cudaMemcpy(hdr + kHdrError, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return RLSCAN_ERR_CUDA;
+    }
+    return static_cast<rlscan_status>(code);
+}
+
+RLSCAN_API rlscan_status rlscan_gae(const float *rewards, const float *values, const float *terminateds,
+                         const float *truncateds, const float *bootstrap_values,
+                         const float *last_value, int64_t N, int64_t T, int64_t row_stride,
+                         float gamma, float lambda, float *advantages,
+                         void *ws, size_t ws_bytes, rlscan_stream_t stream)
+{
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!rewards || !values || !terminateds || !advantages) return RLSCAN_ERR_NULL;
+    if (bootstrap_values && last_value) return RLSCAN_ERR_ARG_CONFLICT;
+    if (last_value && truncateds) return RLSCAN_ERR_ARG_CONFLICT;
+    if (same_as_any(advantages, {rewards, values, terminateds, truncateds, bootstrap_values, last_value}))
+        return RLSCAN_ERR_ARG_CONFLICT;
+    Params p = base_params(N, T, row_stride);
+    p.c0 = gamma;
+    p.c1 = lambda;
+    p.out[0] = advantages;
+    p.in[0] = rewards;
+    p.in[1] = values;
+    p.in[2] = terminateds;
+    if (truncateds) {
+        p.in[3] = truncateds;
+        p.in[4] = bootstrap_values;
+        return launch_gae(true, bootstrap_values != nullptr, p, ws, ws_bytes, cs(stream));
+    }
+    if (last_value) {
+        p.rowscalar = last_value;
+    } else if (bootstrap_values) {  // window bootstrap column only
+        p.rowscalar = bootstrap_values + (T - 1);
+        p.rowscalar_stride = row_stride;
+    }
+    return launch_gae(false, false, p, ws, ws_bytes, cs(stream));
+}
+
+RLSCAN_API rlscan_status rlscan_vtrace(const float *log_pi_target, const float *log_pi_behavior,
+                            const float *values, const float *rewards, const float *terminateds,
+                            const float *truncateds, const float *bootstrap_values,
+                            const float *last_value, int64_t N, int64_t T, int64_t row_stride,
+                            float gamma, float rho_bar, float c_bar,
+                            float *vtrace_targets, float *vtrace_advantages,
+                            void *ws, size_t ws_bytes, rlscan_stream_t stream)
+{
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!log_pi_target || !log_pi_behavior || !values || !rewards || !terminateds || !vtrace_targets ||
+        !vtrace_advantages)
+        return RLSCAN_ERR_NULL;
+    if (bootstrap_values && last_value) return RLSCAN_ERR_ARG_CONFLICT;
+    for (const float *o : {static_cast<const float *>(vtrace_targets), static_cast<const float *>(vtrace_advantages)})
+        if (same_as_any(o, {log_pi_target, log_pi_behavior, values, rewards, terminateds, truncateds,
+                            bootstrap_values, last_value}))
+            return RLSCAN_ERR_ARG_CONFLICT;
+    if (vtrace_targets == vtrace_advantages) return RLSCAN_ERR_ARG_CONFLICT;
+    Params p = base_params(N, T, row_stride);
+    p.c0 = gamma;
+    p.c1 = rho_bar;
+    p.c2 = c_bar;
+    p.out[0] = vtrace_targets;
+    p.out[1] = vtrace_advantages;
+    p.in[0] = log_pi_target;
+    p.in[1] = log_pi_behavior;
+    p.in[2] = values;
+    p.in[3] = rewards;
+    p.in[4] = terminateds;
+    if (truncateds) {
+        p.in[5] = truncateds;
+        p.in[6] = bootstrap_values;
+        p.rowscalar = last_value;  // last_value with truncations: bs_{T-1} only
+        return launch_vtrace(true, bootstrap_values != nullptr, p, ws, ws_bytes, cs(stream));
+    }
+    if (last_value) {
+        p.rowscalar = last_value;
+    } else if (bootstrap_values) {
+        p.rowscalar = bootstrap_values + (T - 1);
+        p.rowscalar_stride = row_stride;
+    }
+    return launch_vtrace(false, false, p, ws, ws_bytes, cs(stream));
+}
+
+RLSCAN_API rlscan_status rlscan_retrace(const float *pi_taken, const float *mu_taken, const float *q_values,
+                             const float *expected_next_q, const float *rewards,
+                             const float *terminateds, const float *truncateds,
+                             int64_t N, int64_t T, int64_t row_stride,
+                             float gamma, float lambda, float c_bar, float rho_bar,
+                             float *retrace_targets, float *advantages,
+                             void *ws, size_t ws_bytes, rlscan_stream_t stream)
+{
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!pi_taken || !mu_taken || !q_values || !expected_next_q || !rewards || !terminateds ||
+        !retrace_targets || !advantages)
+        return RLSCAN_ERR_NULL;
+    for (const float *o : {static_cast<const float *>(retrace_targets), static_cast<const float *>(advantages)})
+        if (same_as_any(o, {pi_taken, mu_taken, q_values, expected_next_q, rewards, terminateds, truncateds}))
+            return RLSCAN_ERR_ARG_CONFLICT;
+    if (retrace_targets == advantages) return RLSCAN_ERR_ARG_CONFLICT;
+    Params p = base_params(N, T, row_stride);
+    p.c0 = gamma;
+    p.c1 = lambda;
+    p.c2 = c_bar;
+    p.c3 = rho_bar;
+    p.out[0] = retrace_targets;
+    p.out[1] = advantages;
+    p.in[0] = pi_taken;
+    p.in[1] = mu_taken;
+    p.in[2] = q_values;
+    p.in[3] = expected_next_q;
+    p.in[4] = rewards;
+    p.in[5] = terminateds;
+    p.in[6] = truncateds;
+    return launch_retrace(truncateds != nullptr, p, ws, ws_bytes, cs(stream));
+}
+
+RLSCAN_API rlscan_status rlscan_lambda_returns(const float *rewards, const float *next_values,
+                                    const float *terminateds, const float *truncateds,
+                                    const float *bootstrap_values, const float *last_value,
+                                    int64_t N, int64_t T, int64_t row_stride,
+                                    float gamma, float lambda, float *returns,
+                                    void *ws, size_t ws_bytes, rlscan_stream_t stream)
+{
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!rewards || !next_values || !terminateds || !returns) return RLSCAN_ERR_NULL;
+    if (bootstrap_values && last_value) return RLSCAN_ERR_ARG_CONFLICT;
+    if (same_as_any(returns, {rewards, next_values, terminateds, truncateds, bootstrap_values, last_value}))
+        return RLSCAN_ERR_ARG_CONFLICT;
+    Params p = base_params(N, T, row_stride);
+    p.c0 = gamma;
+    p.c1 = lambda;
+    p.out[0] = returns;
+    p.in[0] = rewards;
+    p.in[1] = next_values;
+    p.in[2] = terminateds;
+    if (truncateds) {
+        p.in[3] = truncateds;
+        p.in[4] = bootstrap_values;
+        p.rowscalar = last_value;
+        return launch_lambda_returns(true, bootstrap_values != nullptr, p, ws, ws_bytes, cs(stream));
+    }
+    if (last_value) {
+        p.rowscalar = last_value;
+    } else if (bootstrap_values) {
+        p.rowscalar = bootstrap_values + (T - 1);
+        p.rowscalar_stride = row_stride;
+    }
+    return launch_lambda_returns(false, false, p, ws, ws_bytes, cs(stream));
+}
+
+RLSCAN_API rlscan_status rlscan_discounted_returns(const float *rewards, const float *terminateds,
+                                        const float *truncateds, const float *bootstrap_values,
+                                        const float *last_value, int64_t N, int64_t T,
+                                        int64_t row_stride, float gamma, float *returns,
+                                        void *ws, size_t ws_bytes, rlscan_stream_t stream)
+{
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!rewards || !terminateds || !returns) return RLSCAN_ERR_NULL;
+    if (bootstrap_values && last_value) return RLSCAN_ERR_ARG_CONFLICT;
+    if (same_as_any(returns, {rewards, terminateds, truncateds, bootstrap_values, last_value}))
+        return RLSCAN_ERR_ARG_CONFLICT;
+    Params p = base_params(N, T, row_stride);
+    p.c0 = gamma;
+    p.out[0] = returns;
+    p.in[0] = rewards;
+    p.in[1] = terminateds;
+    if (truncateds) {
+        p.in[2] = truncateds;
+        p.in[3] = bootstrap_values;
+        p.rowscalar = last_value;
+        return launch_discounted(true, bootstrap_values != nullptr, p, ws, ws_bytes, cs(stream));
+    }
+    if (last_value) {
+        p.rowscalar = last_value;
+    } else if (bootstrap_values) {
+        p.rowscalar = bootstrap_values + (T - 1);
+        p.rowscalar_stride = row_stride;
+    }
+    return launch_discounted(false, false, p, ws, ws_bytes, cs(stream));
+}
+
+RLSCAN_API rlscan_status rlscan_eligibility_traces(const float *gradients, const float *dones,
+                                        const float *seed_values, int64_t N, int64_t T,
+                                        int64_t row_stride, float gamma, float lambda,
+                                        float *traces, void *ws, size_t ws_bytes,
+                                        rlscan_stream_t stream)
+{
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!gradients || !dones || !traces) return RLSCAN_ERR_NULL;
+    if (same_as_any(traces, {gradients, dones, seed_values})) return RLSCAN_ERR_ARG_CONFLICT;
+    Params p = base_params(N, T, row_stride);
+    p.c0 = gamma;
+    p.c1 = lambda;
+    p.out[0] = traces;
+    p.in[0] = gradients;
+    p.in[1] = dones;
+    p.rowscalar = seed_values;
+    return launch_eligibility(p, ws, ws_bytes, cs(stream));
+}
+
+RLSCAN_API rlscan_status rlscan_episodic_prefix_sum(const float *inputs, const float *dones,
+                                         const float *seed_values, rlscan_boundary boundary,
+                                         int64_t N, int64_t T, int64_t row_stride,
+                                         float *prefix_sums, void *ws, size_t ws_bytes,
+                                         rlscan_stream_t stream)
+{
+    if (boundary != RLSCAN_ENDS_AT && boundary != RLSCAN_STARTS_AT) return RLSCAN_ERR_ARG_VALUE;
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!inputs || !dones || !prefix_sums) return RLSCAN_ERR_NULL;
+    if (same_as_any(prefix_sums, {inputs, dones, seed_values})) return RLSCAN_ERR_ARG_CONFLICT;
+    Params p = base_params(N, T, row_stride);
+    p.out[0] = prefix_sums;
+    p.in[0] = inputs;
+    p.in[1] = dones;
+    p.rowscalar = seed_values;
+    return launch_prefix(boundary == RLSCAN_STARTS_AT, p, ws, ws_bytes, cs(stream));
+}
+
+RLSCAN_API rlscan_status rlscan_linear_scan(const float *alpha, const float *beta, const float *carry,
+                                 rlscan_direction direction, int64_t N, int64_t T,
+                                 int64_t row_stride, float *out, void *ws, size_t ws_bytes,
+                                 rlscan_stream_t stream)
+{
+    if (direction != RLSCAN_BACKWARD && direction != RLSCAN_FORWARD) return RLSCAN_ERR_ARG_VALUE;
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!alpha || !beta || !out) return RLSCAN_ERR_NULL;
+    if (same_as_any(out, {alpha, beta, carry})) return RLSCAN_ERR_ARG_CONFLICT;
+    Params p = base_params(N, T, row_stride);
+    p.out[0] = out;
+    p.in[0] = alpha;
+    p.in[1] = beta;
+    p.rowscalar = carry;
+    return launch_linear(direction == RLSCAN_FORWARD, p, ws, ws_bytes, cs(stream));
+}
+
+}  // extern "C"

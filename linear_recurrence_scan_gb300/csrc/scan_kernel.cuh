@@ -1,0 +1,499 @@
+// scan_kernel.cuh -- the one kernel template behind every entry point.
+//
+// Problem: for each row of an [N, T] buffer, A_t = alpha_t + beta_t A_{t-+1}
+// with (alpha_t, beta_t) built in registers by an estimator functor
+// (estimators.cuh).  The recurrence is an associative scan of affine maps
+// f_t(x) = alpha_t + beta_t x under composition (rl-triton paper Eq. 2 and
+// Prop. 1); the backward recurrences scan in decreasing time (Sec. 2.2).
+//
+// GB300 design:
+//  * Persistent CTAs (grid = SMs x resident CTAs) walk a sequence of tiles.
+//    A tile is THREADS*ITEMS elements: either several whole rows ("packed",
+//    T <= tile) or one segment of a long row.
+//  * Staging: one thread issues bulk asynchronous copies (cp.async.bulk, the
+//    TMA engine's non-tensor form) of every input array of a tile into a
+//    shared-memory stage, completing on an mbarrier.  STAGES stages form a
+//    ring, so the copies of the next STAGES-1 tiles are in flight while one
+//    tile is computed.  Unaligned shapes fall back to element-wise loads.
+//  * Scan inside a tile: each thread owns ITEMS consecutive steps and folds
+//    them serially; a warp shuffle scan combines the 32 threads; warp 0
+//    combines the warps.  Then each thread re-runs its serial recurrence
+//    from its exact incoming value, so every output is one fused multiply-add
+//    chain from a known value (no separate "apply carry" pass).
+//  * Row boundaries are folded into the coefficients: at the row's first
+//    element in scan order (t = T-1 backward, t = 0 forward) the kernel sets
+//    alpha += beta * boundary and beta = 0.  A packed tile is then one flat
+//    scan (beta = 0 severs rows), and the first tile of a long row never
+//    depends on anything before it.
+//  * Long rows: decoupled look-back.  Each tile publishes its aggregate
+//    (a, b) and later its inclusive value in a 16-byte state in the caller's
+//    workspace; a tile waits only for its predecessors' aggregates.  Each
+//    64-bit state word carries a 32-bit tag (call epoch << 2 | kind) next to
+//    its payload, so a reader validates it without fences and stale words of
+//    earlier calls are never mistaken for fresh ones (no memset per call).
+//    Tiles are numbered in scan order and handed out by an atomic ticket, so
+//    every tile's predecessors are held by CTAs that are already running.
+//  * Every wait (mbarrier phase, predecessor state) is bounded in time; on
+//    expiry the kernel records RLSCAN_ERR_TIMEOUT in the workspace, uses NaN
+//    for the missing value and carries on, so it always terminates.
+#pragma once
+
+#include <cstdint>
+
+#include "estimators.cuh"
+#include "params.cuh"
+#include "ptx.cuh"
+
+namespace rlscan {
+
+struct Pair {
+    float a, b;
+};
+
+// outer o inner: x -> outer.a + outer.b * (inner.a + inner.b * x)
+__device__ __forceinline__ Pair compose(Pair outer, Pair inner)
+{
+    return Pair{fmaf(outer.b, inner.a, outer.a), outer.b * inner.b};
+}
+
+constexpr uint32_t kTagAgg = 1u, kTagPrefix = 2u;
+
+__device__ __forceinline__ unsigned long long pack_word(uint32_t tag, float v)
+{
+    return (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(v);
+}
+
+__device__ __forceinline__ void record_error(const Params &p, uint32_t code, uint32_t detail)
+{
+    if (p.hdr == nullptr) return;
+    if (atomicCAS(&p.hdr[kHdrError], 0u, code) == 0u) atomicExch(&p.hdr[kHdrDetail], detail);
+}
+
+struct TileGeo {
+    int64_t row0;  // first row of the tile
+    int64_t t0;    // first time step held by the tile
+    int64_t j;     // position of the tile within its row, in scan order
+    int32_t nrows; // rows present (packed) or 1
+    int32_t len;   // time steps present per row
+};
+
+template <bool FWD, int TILE>
+__device__ __forceinline__ TileGeo decode_tile(const Params &p, int64_t g)
+{
+    TileGeo tg;
+    if (p.packed) {
+        tg.row0 = g * p.R;
+        const int64_t rem = p.N - tg.row0;
+        tg.nrows = rem < p.R ? static_cast<int32_t>(rem) : p.R;
+        tg.t0 = 0;
+        tg.len = static_cast<int32_t>(p.T);
+        tg.j = 0;
+    } else {
+        tg.row0 = g / p.tiles_per_row;
+        tg.j = g - tg.row0 * p.tiles_per_row;
+        const int64_t chrono = FWD ? tg.j : (p.tiles_per_row - 1 - tg.j);
+        tg.t0 = chrono * TILE;
+        const int64_t rem = p.T - tg.t0;
+        tg.len = rem < TILE ? static_cast<int32_t>(rem) : TILE;
+        tg.nrows = 1;
+    }
+    return tg;
+}
+
+// Issue the bulk copies of tile g into `stage` (called by one thread).
+// Array j of the stage occupies AST floats; its data start at offset 4, the
+// step before the tile at offset 3 and the step after it at offset 4+TILE.
+template <class E, int TILE, int AST>
+__device__ void issue_tile_copies(const Params &p, int64_t g, float *stage, uint64_t *bar)
+{
+    const TileGeo tg = decode_tile<E::FWD, TILE>(p, g);
+    if (p.packed) {
+        if (p.rs == p.T && p.C == p.T) {  // rows contiguous in global and in shared memory
+            const uint32_t nb = static_cast<uint32_t>(tg.nrows * p.T * 4);
+            ptx::mbar_arrive_expect_tx(bar, nb * E::NIN);
+#pragma unroll
+            for (int j = 0; j < E::NIN; ++j)
+                ptx::bulk_g2s(stage + j * AST + 4, p.in[j] + tg.row0 * p.rs, nb, bar);
+        } else {
+            const uint32_t nb = static_cast<uint32_t>(p.T * 4);
+            ptx::mbar_arrive_expect_tx(bar, nb * E::NIN * tg.nrows);
+            for (int i = 0; i < tg.nrows; ++i) {
+#pragma unroll
+                for (int j = 0; j < E::NIN; ++j)
+                    ptx::bulk_g2s(stage + j * AST + 4 + i * p.C, p.in[j] + (tg.row0 + i) * p.rs, nb, bar);
+            }
+        }
+        return;
+    }
+    const int64_t base = tg.row0 * p.rs;
+    int64_t lo[E::NIN], hi[E::NIN];
+    uint32_t bytes = 0;
+#pragma unroll
+    for (int j = 0; j < E::NIN; ++j) {
+        lo[j] = tg.t0;
+        hi[j] = tg.t0 + tg.len;
+        if ((E::HALO >> j) & 1u) {
+            if (!E::FWD && hi[j] < p.T) hi[j] += 4;   // next step (T % 4 == 0 keeps it in the row)
+            if (E::FWD && lo[j] > 0) lo[j] -= 4;      // previous step
+        }
+        bytes += static_cast<uint32_t>((hi[j] - lo[j]) * 4);
+    }
+    ptx::mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+    for (int j = 0; j < E::NIN; ++j)
+        ptx::bulk_g2s(stage + j * AST + 4 + (lo[j] - tg.t0), p.in[j] + base + lo[j],
+                      static_cast<uint32_t>((hi[j] - lo[j]) * 4), bar);
+}
+
+// Element-wise cooperative load of tile g (any alignment), same layout.
+template <class E, int THREADS, int TILE, int AST>
+__device__ void load_tile_elementwise(const Params &p, int64_t g, float *stage)
+{
+    const TileGeo tg = decode_tile<E::FWD, TILE>(p, g);
+    const int total = tg.nrows * p.C;
+    for (int e = threadIdx.x; e < total; e += THREADS) {
+        const int i = e / p.C;
+        const int c = e - i * p.C;
+        if (c < tg.len) {
+            const int64_t src = (tg.row0 + i) * p.rs + tg.t0 + c;
+#pragma unroll
+            for (int j = 0; j < E::NIN; ++j) stage[j * AST + 4 + e] = __ldg(p.in[j] + src);
+        }
+    }
+    if (!p.packed && threadIdx.x < E::NIN) {
+        const int j = threadIdx.x;
+        if ((E::HALO >> j) & 1u) {
+            const int64_t base = tg.row0 * p.rs;
+            if (!E::FWD && tg.t0 + tg.len < p.T) stage[j * AST + 4 + TILE] = __ldg(p.in[j] + base + tg.t0 + tg.len);
+            if (E::FWD && tg.t0 > 0) stage[j * AST + 3] = __ldg(p.in[j] + base + tg.t0 - 1);
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t start = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - start > limit_ns) return false;
+    }
+    return true;
+}
+
+// Decoupled look-back for tile g (one thread).  `total` is the tile's
+// aggregate map.  Returns the value entering the tile from its scan-order
+// predecessor (A at the step just outside the tile), or 0 for a row's first
+// tile.  Publishes the tile's own states on the way.
+template <bool FWD>
+__device__ float lookback(const Params &p, const TileGeo &tg, int64_t g, Pair total)
+{
+    if (p.packed) return 0.f;
+    unsigned long long *st = p.states;
+    const uint32_t tagA = (p.epoch << 2) | kTagAgg;
+    const uint32_t tagP = (p.epoch << 2) | kTagPrefix;
+    if (tg.j == 0 || total.b == 0.f) {
+        // the inclusive value does not depend on anything before the tile
+        ptx::st_relaxed(&st[2 * g], pack_word(tagP, total.a));
+        if (tg.j == 0) return 0.f;
+    } else {
+        ptx::st_relaxed(&st[2 * g + 1], pack_word(tagA, total.b));
+        ptx::st_relaxed(&st[2 * g], pack_word(tagA, total.a));
+    }
+    Pair acc{0.f, 1.f};
+    int64_t k = g - 1;
+    const int64_t kmin = g - tg.j;
+    float carry = 0.f;
+    uint64_t waited_since = 0;
+    uint32_t nap = 32;
+    for (;;) {
+        const unsigned long long w0 = ptx::ld_relaxed(&st[2 * k]);
+        const uint32_t tag = static_cast<uint32_t>(w0 >> 32);
+        if (tag == tagP) {
+            carry = fmaf(acc.b, __uint_as_float(static_cast<uint32_t>(w0)), acc.a);
+            break;
+        }
+        if (tag == tagA) {
+            const unsigned long long w1 = ptx::ld_relaxed(&st[2 * k + 1]);
+            if (static_cast<uint32_t>(w1 >> 32) == tagA) {
+                acc = compose(acc, Pair{__uint_as_float(static_cast<uint32_t>(w0)),
+                                        __uint_as_float(static_cast<uint32_t>(w1))});
+                if (acc.b == 0.f || k == kmin) {
+                    carry = acc.a;
+                    break;
+                }
+                --k;
+                waited_since = 0;
+                nap = 32;
+                continue;
+            }
+        }
+        const uint64_t now = ptx::globaltimer_ns();
+        if (waited_since == 0) {
+            waited_since = now;
+        } else if (now - waited_since > p.spin_limit_ns) {
+            record_error(p, RLSCAN_ERR_TIMEOUT, static_cast<uint32_t>(g));
+            carry = __int_as_float(0x7fc00000);
+            break;
+        }
+        __nanosleep(nap);
+        if (nap < 1024) nap <<= 1;
+    }
+    if (total.b != 0.f) ptx::st_relaxed(&st[2 * g], pack_word(tagP, fmaf(total.b, carry, total.a)));
+    return carry;
+}
+
+template <bool FWD>
+__device__ __forceinline__ Pair shfl_pred(Pair v, int off)
+{
+    Pair o;
+    if (FWD) {
+        o.a = __shfl_up_sync(0xffffffffu, v.a, off);
+        o.b = __shfl_up_sync(0xffffffffu, v.b, off);
+    } else {
+        o.a = __shfl_down_sync(0xffffffffu, v.a, off);
+        o.b = __shfl_down_sync(0xffffffffu, v.b, off);
+    }
+    return o;
+}
+
+// Inclusive warp scan in scan order: lane l ends with f_l o f_{pred} o ...
+template <bool FWD>
+__device__ __forceinline__ Pair warp_inclusive(Pair v, int lane)
+{
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const Pair o = shfl_pred<FWD>(v, off);
+        const bool has = FWD ? (lane >= off) : (lane + off < 32);
+        if (has) v = compose(v, o);
+    }
+    return v;
+}
+
+template <bool FWD>
+__device__ __forceinline__ Pair warp_exclusive_from(Pair inc, int lane)
+{
+    Pair ex = shfl_pred<FWD>(inc, 1);
+    if (FWD ? (lane == 0) : (lane == 31)) ex = Pair{0.f, 1.f};
+    return ex;
+}
+
+template <class E, int THREADS, int ITEMS, int STAGES>
+__global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ Params p)
+{
+    constexpr int NIN = E::NIN, NOUT = E::NOUT;
+    constexpr int TILE = THREADS * ITEMS, AST = TILE + 8, WARPS = THREADS / 32;
+    constexpr bool FWD = E::FWD;
+    static_assert(STAGES >= 2, "the ring needs two stages");
+    static_assert(ITEMS % 4 == 0, "items per thread are moved as float4");
+    static_assert(TILE >= kMinTile, "workspace sizing assumes tiles of at least kMinTile");
+
+    extern __shared__ __align__(128) float smem[];
+    __shared__ __align__(8) uint64_t mbar[STAGES];
+    __shared__ int64_t tile_ids[STAGES];
+    __shared__ Pair wexcl[WARPS];
+    __shared__ Pair wagg[WARPS];
+    __shared__ float s_carry;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const bool tma = p.tma != 0;
+
+    // Tile sequence: an atomic ticket when tiles depend on each other, a
+    // static stride otherwise.  Only thread 0 draws.
+    int64_t static_next = blockIdx.x;
+    auto next_tile = [&]() -> int64_t {
+        if (p.dynamic)
+            return static_cast<int64_t>(atomicAdd(reinterpret_cast<unsigned long long *>(p.hdr), 1ull));
+        const int64_t t = static_next;
+        static_next += gridDim.x;
+        return t;
+    };
+
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) ptx::mbar_init(&mbar[s], 1);
+        ptx::fence_mbar_init();
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) {
+            const int64_t g = next_tile();
+            tile_ids[s] = g;
+            if (g < p.num_tiles && tma) issue_tile_copies<E, TILE, AST>(p, g, smem + s * NIN * AST, &mbar[s]);
+        }
+    }
+    __syncthreads();
+
+    const int li = tid * ITEMS;
+    const int rit = p.packed ? li / p.C : 0;
+    const int col = p.packed ? li - rit * p.C : li;
+
+    // Row scalar of the row this thread covers, when the row's boundary step
+    // falls in its range; fetched one tile ahead so its latency is hidden.
+    auto load_row_scalar = [&](int64_t g) -> float {
+        if (!E::ROWSCALAR || p.rowscalar == nullptr || g >= p.num_tiles) return 0.f;
+        const TileGeo tg = decode_tile<FWD, TILE>(p, g);
+        if (rit >= tg.nrows) return 0.f;
+        const int64_t tf = tg.t0 + col;
+        const bool need = FWD ? (tf == 0) : (tf <= p.T - 1 && p.T - 1 < tf + ITEMS);
+        if (!need) return 0.f;
+        return __ldg(p.rowscalar + (tg.row0 + rit) * p.rowscalar_stride);
+    };
+    float rsc_next = load_row_scalar(tile_ids[0]);
+    uint32_t lost_stages = 0, lost_parity = 0;  // waits that timed out (thread 0)
+
+    for (int it = 0;; ++it) {
+        const int s = it % STAGES;
+        const int64_t g = tile_ids[s];
+        if (g >= p.num_tiles) break;
+        const float rsc = rsc_next;
+        float *stage = smem + s * NIN * AST;
+
+        if (tma) {
+            const uint32_t parity = static_cast<uint32_t>((it / STAGES) & 1);
+            if (!wait_phase(&mbar[s], parity, p.spin_limit_ns) && tid == 0) {
+                lost_stages |= 1u << s;
+                lost_parity = (lost_parity & ~(1u << s)) | (parity << s);
+                record_error(p, RLSCAN_ERR_TIMEOUT, 0x80000000u | static_cast<uint32_t>(s));
+            }
+        } else {
+            load_tile_elementwise<E, THREADS, TILE, AST>(p, g, stage);
+            __syncthreads();
+        }
+
+        const TileGeo tg = decode_tile<FWD, TILE>(p, g);
+        const bool row_ok = rit < tg.nrows;
+        const int64_t row = tg.row0 + rit;
+        const int64_t t_first = tg.t0 + col;
+
+        // inputs of this thread's ITEMS steps, plus the neighbour step
+        float x[NIN][ITEMS], xn[NIN];
+        const float *sp = stage + 4 + li;
+#pragma unroll
+        for (int j = 0; j < NIN; ++j) {
+#pragma unroll
+            for (int k = 0; k < ITEMS; k += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(sp + j * AST + k);
+                x[j][k] = v.x;
+                x[j][k + 1] = v.y;
+                x[j][k + 2] = v.z;
+                x[j][k + 3] = v.w;
+            }
+            xn[j] = ((E::HALO >> j) & 1u) ? (FWD ? sp[j * AST - 1] : sp[j * AST + ITEMS]) : 0.f;
+        }
+
+        float a[ITEMS], b[ITEMS];
+        typename E::template Keep<ITEMS> keep;
+        E::template coeffs<ITEMS>(x, xn, t_first, p, rsc, a, b, keep);
+#pragma unroll
+        for (int k = 0; k < ITEMS; ++k) {
+            const int64_t t = t_first + k;
+            if (t == (FWD ? 0 : p.T - 1)) {
+                a[k] = fmaf(b[k], E::template boundary<ITEMS>(x, k, rsc, p), a[k]);
+                b[k] = 0.f;
+            }
+            if (!(row_ok && t < p.T)) {  // outside the data: identity map
+                a[k] = 0.f;
+                b[k] = 1.f;
+            }
+        }
+
+        // thread aggregate, in scan order
+        Pair agg;
+        if (FWD) {
+            agg = Pair{a[0], b[0]};
+#pragma unroll
+            for (int k = 1; k < ITEMS; ++k) agg = compose(Pair{a[k], b[k]}, agg);
+        } else {
+            agg = Pair{a[ITEMS - 1], b[ITEMS - 1]};
+#pragma unroll
+            for (int k = ITEMS - 2; k >= 0; --k) agg = compose(Pair{a[k], b[k]}, agg);
+        }
+        const Pair inc = warp_inclusive<FWD>(agg, lane);
+        const Pair ex = warp_exclusive_from<FWD>(inc, lane);
+        if (lane == (FWD ? 31 : 0)) wagg[warp] = inc;
+        __syncthreads();
+
+        rsc_next = load_row_scalar(tile_ids[(it + 1) % STAGES]);
+
+        if (warp == 0) {
+            const Pair w = lane < WARPS ? wagg[lane] : Pair{0.f, 1.f};
+            const Pair winc = warp_inclusive<FWD>(w, lane);
+            const Pair wex = warp_exclusive_from<FWD>(winc, lane);
+            if (lane < WARPS) wexcl[lane] = wex;
+            Pair total;
+            total.a = __shfl_sync(0xffffffffu, winc.a, FWD ? 31 : 0);
+            total.b = __shfl_sync(0xffffffffu, winc.b, FWD ? 31 : 0);
+            if (lane == 0) s_carry = lookback<FWD>(p, tg, g, total);
+        }
+        __syncthreads();
+
+        // exact value entering this thread's range, then its serial recurrence
+        const Pair we = wexcl[warp];
+        const float x_in = fmaf(ex.b, fmaf(we.b, s_carry, we.a), ex.a);
+        float A[ITEMS];
+        {
+            float v = x_in;
+            if (FWD) {
+#pragma unroll
+                for (int k = 0; k < ITEMS; ++k) {
+                    v = fmaf(b[k], v, a[k]);
+                    A[k] = v;
+                }
+            } else {
+#pragma unroll
+                for (int k = ITEMS - 1; k >= 0; --k) {
+                    v = fmaf(b[k], v, a[k]);
+                    A[k] = v;
+                }
+            }
+        }
+        float o[NOUT][ITEMS];
+        E::template post<ITEMS>(x, xn, t_first, p, rsc, A, x_in, keep, o);
+
+        if (row_ok) {
+            const int64_t off = row * p.rs + t_first;
+            if (tma) {
+#pragma unroll
+                for (int q = 0; q < NOUT; ++q) {
+#pragma unroll
+                    for (int k = 0; k < ITEMS; k += 4) {
+                        if (t_first + k < p.T)
+                            *reinterpret_cast<float4 *>(p.out[q] + off + k) =
+                                make_float4(o[q][k], o[q][k + 1], o[q][k + 2], o[q][k + 3]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < NOUT; ++q) {
+#pragma unroll
+                    for (int k = 0; k < ITEMS; ++k)
+                        if (t_first + k < p.T) p.out[q][off + k] = o[q][k];
+                }
+            }
+        }
+        __syncthreads();  // stage s and tile_ids[s] are free again
+
+        if (tid == 0) {
+            const int64_t gn = next_tile();
+            tile_ids[s] = gn;
+            if (gn < p.num_tiles && tma) issue_tile_copies<E, TILE, AST>(p, gn, stage, &mbar[s]);
+        }
+    }
+
+    // A copy whose wait timed out may still be landing: give it one more
+    // bounded wait before the shared memory is released.
+    if (lost_stages != 0 && tid == 0) {
+        for (int s = 0; s < STAGES; ++s)
+            if ((lost_stages >> s) & 1u) wait_phase(&mbar[s], (lost_parity >> s) & 1u, p.spin_limit_ns);
+    }
+    if (p.dynamic && tid == 0) {
+        __threadfence();
+        const uint32_t done = atomicAdd(&p.hdr[kHdrExit], 1u);
+        if (done == gridDim.x - 1) {  // last CTA out: re-arm the ticket for the next call
+            atomicExch(reinterpret_cast<unsigned long long *>(p.hdr), 0ull);
+            atomicExch(&p.hdr[kHdrExit], 0u);
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace rlscan
