@@ -1,0 +1,599 @@
+"""Throughput benchmark: env-steps/s and achieved HBM GB/s per estimator.
+
+Default workload (N=1): GAE + discounted returns + TD(lambda) returns on a
+4096 x 1024 float32 rollout buffer with a last_value bootstrap (one "step"
+= the three estimators over one batch).  Other workloads: --workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload gae_returns_4096x1024|...]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
+(rows are independent: weak scaling, no collective on the data path); the
+time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures
+import ctypes
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from linear_recurrence_scan_gb300 import synthetic  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# workloads: estimators, their inputs and algorithmic bytes per env-step
+# (fp32 inputs read once + outputs written once; [N] vectors and the
+# one-step halo are not counted)
+
+def _cfg_workloads():
+    c1, c2, c3, c4 = (synthetic.CONFIGS[i] for i in (1, 2, 3, 4))
+    return {
+        "gae_returns_4096x1024": dict(
+            desc="GAE + discounted returns + TD(lambda) returns, last_value bootstrap, no truncations",
+            N=4096, T=1024, gen=lambda N, T: synthetic.config_batch(1, N=N, T=T),
+            estimators=[("gae", 16, c1), ("discounted_returns", 12, c1), ("lambda_returns", 16, c1)]),
+        "gae_8x128": dict(
+            desc="GAE with truncations and 2-D bootstrap", N=8, T=128,
+            gen=lambda N, T: synthetic.config_batch(0, N=N, T=T),
+            estimators=[("gae_trunc_bs", 24, synthetic.CONFIGS[0])]),
+        "vtrace_2048x4096": dict(
+            desc="V-trace with truncations and 2-D bootstrap", N=2048, T=4096,
+            gen=lambda N, T: synthetic.config_batch(2, N=N, T=T),
+            estimators=[("vtrace", 36, c2)]),
+        "retrace_1024x16384": dict(
+            desc="Retrace(lambda) on per-step inputs, no truncations", N=1024, T=16384,
+            gen=lambda N, T: synthetic.config_batch(3, N=N, T=T),
+            estimators=[("retrace", 32, c3)]),
+        "long_rows_64x1048576": dict(
+            desc="eligibility traces + episodic prefix sum (starts_at, integer inputs)",
+            N=64, T=1 << 20, gen=lambda N, T: synthetic.config_batch(4, N=N, T=T),
+            estimators=[("eligibility_traces", 12, c4), ("episodic_prefix_sum", 12, c4)]),
+        "gae_64x1048576": dict(
+            desc="GAE on 1M-step rows (last_value, no truncations)", N=64, T=1 << 20,
+            gen=lambda N, T: synthetic.gae_batch(N, T, 0, 41, c1["p_term"], 0.0, "last"),
+            estimators=[("gae", 16, c1)]),
+        "vtrace_64x1048576": dict(
+            desc="V-trace on 1M-step rows (truncations, 2-D bootstrap)", N=64, T=1 << 20,
+            gen=lambda N, T: synthetic.vtrace_batch(N, T, 0, 42, c2["p_term"], c2["p_trunc"], "2d"),
+            estimators=[("vtrace", 36, c2)]),
+        "retrace_64x1048576": dict(
+            desc="Retrace on 1M-step rows", N=64, T=1 << 20,
+            gen=lambda N, T: synthetic.retrace_batch(N, T, 0, 43, c3["p_term"], 0.0),
+            estimators=[("retrace", 32, c3)]),
+    }
+
+
+WORKLOADS = _cfg_workloads()
+
+# inputs and outputs of each estimator (names in the synthetic batch)
+IO = {
+    "gae": (["rewards", "values", "terminateds"], ["last_value"], 1),
+    "gae_trunc_bs": (["rewards", "values", "terminateds", "truncateds", "bootstrap_values"], [], 1),
+    "discounted_returns": (["rewards", "terminateds"], ["last_value"], 1),
+    "lambda_returns": (["rewards", "next_values", "terminateds"], ["last_value"], 1),
+    "vtrace": (["log_pi_target", "log_pi_behavior", "values", "rewards", "terminateds",
+                "truncateds", "bootstrap_values"], [], 2),
+    "retrace": (["pi_taken", "mu_taken", "q_values", "expected_next_q", "rewards", "terminateds"],
+                [], 2),
+    "eligibility_traces": (["gradients", "trace_dones"], [], 1),
+    "episodic_prefix_sum": (["inputs", "prefix_dones"], [], 1),
+}
+
+
+def _csrc_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "linear_recurrence_scan_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def _measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _ncu_traffic(kernel, workload):
+    """DRAM bytes per launch recorded under profiles/ for this kernel and
+    workload, if taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    e = rec.get(f"{kernel}@{workload}")
+    if not e or e.get("csrc_sha") != _csrc_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the run
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,utilization.gpu,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) >= 10:
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        loaded = [r for r in rows if (num(r[3]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in loaded if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in loaded:
+            for name, val in zip(names, r[6:10]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": num(loaded[0][2]), "samples": len(rows),
+                "samples_under_load": len(loaded), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+def _launcher(name, c, bufs, outs, N, T, ws, wsn, stream):
+    """ABI call of one estimator on preallocated device buffers."""
+    from linear_recurrence_scan_gb300 import _native
+    lib = _native.lib()
+    vp = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    b = {k: vp(v) for k, v in bufs.items()}
+    o = [vp(t) for t in outs]
+    g = float(c.get("gamma", 0.99))
+    if name == "gae":
+        return lambda: lib.rlscan_gae(b["rewards"], b["values"], b["terminateds"], None, None,
+                                      b["last_value"], N, T, T, g, float(c["lambda_"]), o[0], ws,
+                                      wsn, stream)
+    if name == "gae_trunc_bs":
+        return lambda: lib.rlscan_gae(b["rewards"], b["values"], b["terminateds"], b["truncateds"],
+                                      b["bootstrap_values"], None, N, T, T, g, float(c["lambda_"]),
+                                      o[0], ws, wsn, stream)
+    if name == "discounted_returns":
+        return lambda: lib.rlscan_discounted_returns(b["rewards"], b["terminateds"], None, None,
+                                                     b["last_value"], N, T, T, g, o[0], ws, wsn,
+                                                     stream)
+    if name == "lambda_returns":
+        return lambda: lib.rlscan_lambda_returns(b["rewards"], b["next_values"], b["terminateds"],
+                                                 None, None, b["last_value"], N, T, T, g,
+                                                 float(c["lambda_"]), o[0], ws, wsn, stream)
+    if name == "vtrace":
+        return lambda: lib.rlscan_vtrace(b["log_pi_target"], b["log_pi_behavior"], b["values"],
+                                         b["rewards"], b["terminateds"], b["truncateds"],
+                                         b["bootstrap_values"], None, N, T, T, g,
+                                         float(c["rho_bar"]), float(c["c_bar"]), o[0], o[1], ws,
+                                         wsn, stream)
+    if name == "retrace":
+        return lambda: lib.rlscan_retrace(b["pi_taken"], b["mu_taken"], b["q_values"],
+                                          b["expected_next_q"], b["rewards"], b["terminateds"],
+                                          None, N, T, T, g, float(c["lambda_"]), float(c["c_bar"]),
+                                          float(c["rho_bar"]), o[0], o[1], ws, wsn, stream)
+    if name == "eligibility_traces":
+        return lambda: lib.rlscan_eligibility_traces(b["gradients"], b["trace_dones"], None, N, T,
+                                                     T, g, float(c["lambda_"]), o[0], ws, wsn,
+                                                     stream)
+    if name == "episodic_prefix_sum":
+        return lambda: lib.rlscan_episodic_prefix_sum(b["inputs"], b["prefix_dones"], None, 1, N,
+                                                      T, T, o[0], ws, wsn, stream)
+    raise KeyError(name)
+
+
+def _public_call(name, c, t):
+    """The same estimator through the public PyTorch API (for e2e)."""
+    import linear_recurrence_scan_gb300 as Lb
+    g = float(c.get("gamma", 0.99))
+    if name == "gae":
+        return [Lb.compute_gae(t["rewards"], t["values"], t["terminateds"], None, g, c["lambda_"],
+                               None, t["last_value"])]
+    if name == "gae_trunc_bs":
+        return [Lb.compute_gae(t["rewards"], t["values"], t["terminateds"], t["truncateds"], g,
+                               c["lambda_"], t["bootstrap_values"])]
+    if name == "discounted_returns":
+        return [Lb.compute_discounted_returns(t["rewards"], t["terminateds"], None, g, None,
+                                              t["last_value"])]
+    if name == "lambda_returns":
+        return [Lb.compute_lambda_returns(t["rewards"], t["next_values"], t["terminateds"], None, g,
+                                          c["lambda_"], None, t["last_value"])]
+    if name == "vtrace":
+        return list(Lb.compute_vtrace(t["log_pi_target"], t["log_pi_behavior"], t["values"],
+                                      t["rewards"], t["terminateds"], t["truncateds"], g,
+                                      c["rho_bar"], c["c_bar"], t["bootstrap_values"]))
+    if name == "retrace":
+        return list(Lb.compute_retrace_from_probs(t["pi_taken"], t["mu_taken"], t["q_values"],
+                                                  t["expected_next_q"], t["rewards"],
+                                                  t["terminateds"], None, g, c["lambda_"],
+                                                  c["c_bar"], c["rho_bar"]))
+    if name == "eligibility_traces":
+        return [Lb.compute_eligibility_traces(t["gradients"], t["trace_dones"], g, c["lambda_"])]
+    if name == "episodic_prefix_sum":
+        return [Lb.compute_episodic_prefix_sum(t["inputs"], t["prefix_dones"], None, "starts_at")]
+    raise KeyError(name)
+
+
+def run_ours(args, wl_name, rank, world, local_rank):
+    import torch
+    from linear_recurrence_scan_gb300 import _native, build
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = WORKLOADS[wl_name]
+    N, T = wl["N"], wl["T"]
+    batch = wl["gen"](N, T)
+    names = [e[0] for e in wl["estimators"]]
+    need_in = sorted({k for n in names for k in IO[n][0] + IO[n][1]})
+    host = {k: batch[k] for k in need_in}
+    set_bytes = sum(v.nbytes for v in host.values()) + sum(
+        IO[n][2] * N * T * 4 for n in names)
+    n_sets = 1 if set_bytes > 4 * L2_BYTES else min(16, max(2, math.ceil(4 * L2_BYTES / set_bytes)))
+    stream = torch.cuda.current_stream(dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    lib = _native.lib()
+    wsn = lib.rlscan_workspace_bytes(N, T)
+    ws = None
+    if wsn:
+        ws_t = torch.empty(wsn, dtype=torch.uint8, device=dev)
+        _native.check(lib.rlscan_workspace_init(ctypes.c_void_p(ws_t.data_ptr()), wsn, sh), "init")
+        ws = ctypes.c_void_p(ws_t.data_ptr())
+    sets = []
+    for _ in range(n_sets):
+        bufs = {k: torch.from_numpy(v).to(dev) for k, v in host.items()}
+        calls = []
+        for (name, bps, c) in wl["estimators"]:
+            outs = [torch.empty((N, T), dtype=torch.float32, device=dev) for _ in range(IO[name][2])]
+            calls.append((name, _launcher(name, c, bufs, outs, N, T, ws, wsn, sh), outs))
+        sets.append((bufs, calls))
+    torch.cuda.synchronize()
+
+    def step(i, evs=None):
+        _, calls = sets[i % n_sets]
+        for j, (name, fn, _) in enumerate(calls):
+            if evs is not None:
+                evs[j][0].record(stream)
+            st = fn()
+            if st != 0:
+                raise _native.RlscanError(st, name)
+            if evs is not None:
+                evs[j][1].record(stream)
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    K = args.steps
+    kev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in names] for _ in range(K)]
+    t0e = torch.cuda.Event(enable_timing=True)
+    t1e = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    t0e.record(stream)
+    for i in range(K):
+        step(args.warmup + i, kev[i])
+    t1e.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    total_ms = t0e.elapsed_time(t1e)
+    per_kernel = {n: [kev[i][j][0].elapsed_time(kev[i][j][1]) for i in range(K)]
+                  for j, n in enumerate(names)}
+    ms_step = total_ms / K
+    if dist is not None:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    # e2e through the public API: pinned host inputs -> device, three calls,
+    # results back to pinned host memory, every step
+    pinned = {k: torch.from_numpy(v).pin_memory() for k, v in host.items()}
+    dbufs = {k: torch.empty(v.shape, dtype=torch.float32, device=dev) for k, v in host.items()}
+    out_host = [torch.empty((N, T), dtype=torch.float32).pin_memory()
+                for n in names for _ in range(IO[n][2])]
+    h2d = sum(v.nbytes for v in host.values())
+    d2h = sum(o.numel() * 4 for o in out_host)
+
+    def e2e_step():
+        for k in pinned:
+            dbufs[k].copy_(pinned[k], non_blocking=True)
+        outs = []
+        for (name, _, c) in wl["estimators"]:
+            outs += _public_call(name, c, dbufs)
+        for o, hbuf in zip(outs, out_host):
+            hbuf.copy_(o, non_blocking=True)
+    for _ in range(max(1, min(args.warmup, 3))):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = time.perf_counter()
+    for _ in range(K):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - e0) / K
+    if dist is not None:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    clocks = sampler.stop()
+
+    steps_per_call = N * T
+    peak, peak_kind = _measured_peak()
+    per_est = {}
+    dominant, dom_total = None, -1.0
+    for (name, bps, _) in wl["estimators"]:
+        ts = np.array(per_kernel[name])
+        avg_us = float(ts.mean() * 1e3)
+        gbs = bps * steps_per_call / (avg_us * 1e-6) / 1e9
+        per_est[name] = {"us_mean": round(avg_us, 2), "us_median": round(float(np.median(ts)) * 1e3, 2),
+                         "env_steps_per_s": steps_per_call / (avg_us * 1e-6),
+                         "bytes_per_env_step": bps, "gb_per_s": round(gbs, 1),
+                         "frac_of_measured_hbm": round(gbs / peak, 4),
+                         "frac_of_nominal_8tbs": round(gbs / 8000.0, 4)}
+        if ts.sum() > dom_total:
+            dominant, dom_total = name, float(ts.sum())
+    d = per_est[dominant]
+    result = {
+        "metric": "env-steps/sec and achieved HBM GB/s (% of GB300 peak) per estimator, 1 GPU",
+        "value": world * steps_per_call / (ms_step * 1e-3),
+        "unit": "env-steps/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl_name, "description": wl["desc"], "num_envs": N, "seq_len": T,
+                   "estimators": names, "parallelism": f"rows, {world} independent batch(es)",
+                   "l2": f"{n_sets} rotating input sets of {set_bytes / 1e6:.0f} MB "
+                         f"({n_sets * set_bytes / 1e6:.0f} MB > 129 MB L2)"},
+        "per_estimator": per_est,
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": d["gb_per_s"], "peak": peak,
+                     "peak_source": peak_kind, "unit": "GB/s", "frac": d["frac_of_measured_hbm"],
+                     "traffic": _ncu_traffic(dominant, wl_name),
+                     "algorithmic_bytes_per_launch": d["bytes_per_env_step"] * steps_per_call},
+        "e2e": {"value": world * steps_per_call / e2e_s, "unit": "env-steps/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "pinned host -> device copies, public compute_* API, results -> pinned host"},
+        "gpu_launches": K * len(names),
+        "wall_s_timed": round(wall, 4),
+        "clocks": clocks,
+    }
+    return result
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+
+def _oracle_call(name, c, b):
+    import oracle
+    g = float(c.get("gamma", 0.99))
+    if name == "gae":
+        return oracle.gae(b["rewards"], b["values"], b["terminateds"], None, g, c["lambda_"], None,
+                          b["last_value"])
+    if name == "gae_trunc_bs":
+        return oracle.gae(b["rewards"], b["values"], b["terminateds"], b["truncateds"], g,
+                          c["lambda_"], b["bootstrap_values"])
+    if name == "discounted_returns":
+        return oracle.discounted_returns(b["rewards"], b["terminateds"], None, g, None, b["last_value"])
+    if name == "lambda_returns":
+        return oracle.lambda_returns(b["rewards"], b["next_values"], b["terminateds"], None, g,
+                                     c["lambda_"], None, b["last_value"])
+    if name == "vtrace":
+        return oracle.vtrace(b["log_pi_target"], b["log_pi_behavior"], b["values"], b["rewards"],
+                             b["terminateds"], b["truncateds"], g, c["rho_bar"], c["c_bar"],
+                             b["bootstrap_values"])
+    if name == "retrace":
+        return oracle.retrace(b["pi_taken"], b["mu_taken"], b["q_values"], b["expected_next_q"],
+                              b["rewards"], b["terminateds"], None, g, c["lambda_"], c["c_bar"],
+                              c["rho_bar"])
+    if name == "eligibility_traces":
+        return oracle.eligibility_traces(b["gradients"], b["trace_dones"], g, c["lambda_"])
+    if name == "episodic_prefix_sum":
+        return oracle.episodic_prefix_sum(b["inputs"], b["prefix_dones"], None, "starts_at")
+    raise KeyError(name)
+
+
+def _slice(batch, r0, r1):
+    out = {}
+    for k, v in batch.items():
+        if v is None:
+            out[k] = None
+        elif v.ndim == 2:
+            out[k] = v[r0:r1]
+        else:
+            out[k] = v[r0:r1]
+    return out
+
+
+def oracle_time(wl_name, rows, threads, min_seconds=2.0, max_reps=50):
+    """Time the oracle (as it is) on `rows` rows of the workload, rows split
+    across `threads` host threads.  Returns env-steps/s and the description."""
+    import oracle
+    oracle.build()
+    wl = WORKLOADS[wl_name]
+    T = wl["T"]
+    rows = min(rows, wl["N"])
+    batch = wl["gen"](rows, T)
+    chunks = [(i * rows // threads, (i + 1) * rows // threads) for i in range(threads)]
+    chunks = [c for c in chunks if c[1] > c[0]]
+
+    def one_pass():
+        with concurrent.futures.ThreadPoolExecutor(max_workers=len(chunks)) as ex:
+            futs = [ex.submit(lambda c: [_oracle_call(n, cfg, _slice(batch, *c))
+                                         for (n, _, cfg) in wl["estimators"]], c) for c in chunks]
+            for f in futs:
+                f.result()
+    one_pass()  # warm (page in, build)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        one_pass()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    per_pass = el / reps
+    return rows * T / per_pass, {"rows": rows, "seq_len": T, "passes": reps,
+                                 "seconds": round(el, 3)}
+
+
+def _cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            txt = f.read()
+        m = re.search(r"model name\s*:\s*(.+)", txt) or re.search(r"CPU part\s*:\s*(.+)", txt)
+        return m.group(1).strip() if m else "unknown"
+    except Exception:
+        return "unknown"
+
+
+def cpu_baseline(wl_name):
+    wl = WORKLOADS[wl_name]
+    threads = os.cpu_count() or 1
+    rows = min(wl["N"], max(threads, int(4_194_304 * 2 // wl["T"])))
+    v, info = oracle_time(wl_name, rows, threads)
+    return {"value": v, "unit": "env-steps/s", "cores": threads, "kind": "oracle",
+            "cpu": _cpu_model(),
+            "sample": f"{info['rows']} of {wl['N']} rows x {info['seq_len']} steps, "
+                      f"all estimators of the step, {info['passes']} passes in {info['seconds']} s, "
+                      f"rows split over {threads} threads"}
+
+
+def run_reference(args, wl_name):
+    wl = WORKLOADS[wl_name]
+    threads = os.cpu_count() or 1
+    rows = min(wl["N"], max(threads, int(262_144 * 4 // wl["T"])))
+    import oracle
+    oracle.build()
+    batch = wl["gen"](rows, wl["T"])
+    chunks = [(i * rows // threads, (i + 1) * rows // threads) for i in range(threads)]
+    chunks = [c for c in chunks if c[1] > c[0]]
+
+    def step():
+        with concurrent.futures.ThreadPoolExecutor(max_workers=len(chunks)) as ex:
+            list(ex.map(lambda c: [_oracle_call(n, cfg, _slice(batch, *c))
+                                   for (n, _, cfg) in wl["estimators"]], chunks))
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = (time.perf_counter() - t0) / args.steps
+    v = rows * wl["T"] / el
+    sample = (f"{rows} of {wl['N']} rows x {wl['T']} steps per step, all estimators, "
+              f"rows split over {threads} threads")
+    return {"impl": "reference",
+            "metric": "env-steps/sec and achieved HBM GB/s (% of GB300 peak) per estimator, 1 GPU",
+            "value": v, "unit": "env-steps/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl_name, "description": wl["desc"], "num_envs": wl["N"],
+                       "seq_len": wl["T"], "estimators": [e[0] for e in wl["estimators"]]},
+            "cpu_baseline": {"value": v, "unit": "env-steps/s", "cores": threads, "kind": "oracle",
+                             "cpu": _cpu_model(), "sample": sample},
+            "e2e": {"value": v, "unit": "env-steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gae_returns_4096x1024", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, args.workload)))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    res = run_ours(args, args.workload, rank, world, local_rank)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(args.workload)
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

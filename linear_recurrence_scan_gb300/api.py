@@ -51,7 +51,7 @@ class _Call:
             raise ValueError(f"{ref_name} must be [num_envs, seq_len]")
         self.N, self.T = ref.shape
         self.device = ref.device
-        self.mats = {}
+        self.mats = {ref_name: ref}
         self.vecs = {}
 
     def mat(self, name, t, required=True):
