@@ -32,6 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from linear_recurrence_scan_gb300 import synthetic  # noqa: E402
+from linear_recurrence_scan_gb300.sharding import max_over_ranks  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
@@ -345,11 +346,7 @@ def run_ours(args, wl_name, rank, world, local_rank):
     total_ms = t0e.elapsed_time(t1e)
     per_kernel = {n: [kev[i][j][0].elapsed_time(kev[i][j][1]) for i in range(K)]
                   for j, n in enumerate(names)}
-    ms_step = total_ms / K
-    if dist is not None:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(total_ms / K)
 
     # e2e through the public API: pinned host inputs -> device, three calls,
     # results back to pinned host memory, every step
@@ -375,11 +372,7 @@ def run_ours(args, wl_name, rank, world, local_rank):
     for _ in range(K):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - e0) / K
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks((time.perf_counter() - e0) / K)
     clocks = sampler.stop()
 
     steps_per_call = N * T
@@ -469,7 +462,7 @@ def _slice(batch, r0, r1):
     return out
 
 
-def oracle_time(wl_name, rows, threads, min_seconds=2.0, max_reps=50):
+def oracle_time(wl_name, rows, threads, min_seconds=10.0, max_reps=10000):
     """Time the oracle (as it is) on `rows` rows of the workload, rows split
     across `threads` host threads.  Returns env-steps/s and the description."""
     import oracle
