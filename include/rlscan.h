@@ -71,7 +71,8 @@ typedef enum rlscan_status {
     RLSCAN_ERR_WORKSPACE = 5,     /* workspace needed but NULL, too small or misaligned */
     RLSCAN_ERR_CUDA = 6,          /* the CUDA runtime refused the launch */
     RLSCAN_ERR_INVALID_INPUT = 7, /* content check failed (only with RLSCAN_CHECKS=1) */
-    RLSCAN_ERR_TIMEOUT = 8        /* a cross-block wait gave up (reported by rlscan_workspace_status) */
+    RLSCAN_ERR_TIMEOUT = 8,       /* a cross-block wait gave up (reported by rlscan_workspace_status) */
+    RLSCAN_ERR_SCRATCH_LIMIT = 9  /* shape needs more scratch than rlscan_gae_noalloc's built-in buffer */
 } rlscan_status;
 
 typedef enum rlscan_boundary {
@@ -129,6 +130,33 @@ rlscan_status rlscan_gae(const float *rewards, const float *values, const float 
                          const float *last_value, int64_t N, int64_t T, int64_t row_stride,
                          float gamma, float lambda, float *advantages,
                          void *ws, size_t ws_bytes, rlscan_stream_t stream);
+
+/*
+ * GAE without any device allocation, for callers that cannot allocate.
+ * The rl-triton pages have no counterpart: this is a deployment variant of
+ * rlscan_gae.  Some callers may not allocate device memory when they call
+ * in: a plugin inside a framework that owns all device memory through its
+ * own pool, a latency-critical loop that bans cudaMalloc/cudaFree after
+ * start-up (both can synchronise the device), or an embedded runtime with a
+ * fixed memory budget.  Rows longer than one tile need scratch for the
+ * cross-block carries; this entry point takes it from a 4 MiB buffer built
+ * into the library (each GPU that loads the library keeps it until the
+ * process exits) instead of a caller workspace.  That covers shapes with
+ * rlscan_workspace_bytes(N, T) <= 4 MiB, i.e. N * ceil(T / 1024) <= 262140
+ * (e.g. 64 rows of 4M steps); larger shapes return RLSCAN_ERR_SCRATCH_LIMIT
+ * before any device work.  Same arguments and results as rlscan_gae, minus
+ * the workspace.  The first call on a device looks up the buffer's address
+ * and zeroes it on `stream`; make that first call before any stream
+ * capture.  Every call clears the buffer's header on `stream` before its
+ * kernel; calls that share the buffer and overlap on the GPU (unordered
+ * streams) race and must not be issued.  A timed-out cross-block wait shows
+ * up as NaN outputs (this variant has no status query).
+ */
+rlscan_status rlscan_gae_noalloc(const float *rewards, const float *values,
+                                 const float *terminateds, const float *truncateds,
+                                 const float *bootstrap_values, const float *last_value,
+                                 int64_t N, int64_t T, int64_t row_stride, float gamma,
+                                 float lambda, float *advantages, rlscan_stream_t stream);
 
 /*
  * V-trace targets and advantages.

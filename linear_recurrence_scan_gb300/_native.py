@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(HERE, "_build", "librlscan.so")
 STATUS = {
     0: "RLSCAN_OK", 1: "RLSCAN_ERR_NULL", 2: "RLSCAN_ERR_SHAPE", 3: "RLSCAN_ERR_ARG_CONFLICT",
     4: "RLSCAN_ERR_ARG_VALUE", 5: "RLSCAN_ERR_WORKSPACE", 6: "RLSCAN_ERR_CUDA",
-    7: "RLSCAN_ERR_INVALID_INPUT", 8: "RLSCAN_ERR_TIMEOUT",
+    7: "RLSCAN_ERR_INVALID_INPUT", 8: "RLSCAN_ERR_TIMEOUT", 9: "RLSCAN_ERR_SCRATCH_LIMIT",
 }
 ENDS_AT, STARTS_AT = 0, 1
 BACKWARD, FORWARD = 0, 1
@@ -46,6 +46,7 @@ SIGNATURES = {
     "rlscan_workspace_init": ([_P, _SZ, _P], _I),
     "rlscan_workspace_status": ([_P, _SZ, _P], _I),
     "rlscan_gae": ([_P] * 6 + [_I64] * 3 + [_F, _F, _P, _P, _SZ, _P], _I),
+    "rlscan_gae_noalloc": ([_P] * 6 + [_I64] * 3 + [_F, _F, _P, _P], _I),
     "rlscan_vtrace": ([_P] * 8 + [_I64] * 3 + [_F, _F, _F, _P, _P, _P, _SZ, _P], _I),
     "rlscan_retrace": ([_P] * 7 + [_I64] * 3 + [_F] * 4 + [_P, _P, _P, _SZ, _P], _I),
     "rlscan_lambda_returns": ([_P] * 6 + [_I64] * 3 + [_F, _F, _P, _P, _SZ, _P], _I),

@@ -103,6 +103,7 @@ RLSCAN_API const char *rlscan_status_string(rlscan_status status)
     case RLSCAN_ERR_CUDA: return "CUDA runtime error";
     case RLSCAN_ERR_INVALID_INPUT: return "input content check failed";
     case RLSCAN_ERR_TIMEOUT: return "a cross-block wait timed out";
+    case RLSCAN_ERR_SCRATCH_LIMIT: return "shape needs more scratch than the built-in no-allocation buffer holds";
     }
     return "unknown status";
 }
