@@ -15,17 +15,19 @@
 //                   thread's range (t+1 backward, t-1 forward)
 //   ROWSCALAR       the per-row scalar argument is used
 //   Keep<I>         values saved from coeffs() for post()
-//   coeffs(x, xn, t0, p, rsc, a, b, keep)
-//       x[j][k] = input j at time t0+k; xn[j] = input j at the neighbouring
-//       time outside the range (only meaningful for HALO inputs);
-//       rsc = this row's scalar (only meaningful where the row boundary lies
-//       in the thread's range).
+//   coeffs<I, EDGE>(x, xn, kb, p, rsc, a, b, keep)
+//       x[j][k] = input j at the thread's k-th step; xn[j] = input j at the
+//       neighbouring step outside the range (only meaningful for HALO
+//       inputs); EDGE: the row's boundary step (t = T-1 backward, t = 0
+//       forward) is element kb of the range (otherwise kb is ignored and the
+//       boundary tests compile away); rsc = this row's scalar (only
+//       meaningful when EDGE).
 //   boundary(x, k, rsc, p)
 //       value folded in at the row boundary element k: A_T (backward) or
 //       A_{-1} (forward); the kernel sets a_k += b_k * value, b_k = 0.
-//   post(x, xn, t0, p, rsc, A, A_after, keep, o)
-//       A[k] = scan result at t0+k; A_after = result at the step after the
-//       range (backward only; used for successor targets).
+//   post<I, EDGE>(x, xn, kb, p, rsc, A, A_after, keep, o)
+//       A[k] = scan result at the k-th step; A_after = result at the step
+//       after the range (backward only; used for successor targets).
 #pragma once
 
 #include "params.cuh"
@@ -49,14 +51,14 @@ struct GAE {
     static constexpr int TR = 3, BS = 3 + TRUNC;
     template <int I> struct Keep {};
 
-    template <int I>
-    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+    template <int I, bool EDGE>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
                                   const Params &p, float rsc, float (&a)[I], float (&b)[I], Keep<I> &)
     {
         const float g = p.c0, gl = p.c0 * p.c1;
 #pragma unroll
         for (int k = 0; k < I; ++k) {
-            const bool last = (t0 + k == p.T - 1);
+            const bool last = (EDGE && k == kb);
             const float vnext = (k + 1 < I) ? x[1][k + 1] : xn[1];
             const float term = x[2][k];
             float vn, done;
@@ -77,8 +79,8 @@ struct GAE {
     }
     template <int I>
     __device__ static float boundary(const float (&)[NIN][I], int, float, const Params &) { return 0.f; }
-    template <int I>
-    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int64_t, const Params &,
+    template <int I, bool EDGE>
+    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int, const Params &,
                                 float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
     {
 #pragma unroll
@@ -115,14 +117,14 @@ struct VTrace {
         }
     }
 
-    template <int I>
-    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+    template <int I, bool EDGE>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
                                   const Params &p, float rsc, float (&a)[I], float (&b)[I], Keep<I> &keep)
     {
         const float g = p.c0;
 #pragma unroll
         for (int k = 0; k < I; ++k) {
-            const bool last = (t0 + k == p.T - 1);
+            const bool last = (EDGE && k == kb);
             const float ratio = expf(x[0][k] - x[1][k]);
             const float rho = fminf(p.c1, ratio), c = fminf(p.c2, ratio);
             const float term = x[4][k];
@@ -137,15 +139,15 @@ struct VTrace {
     }
     template <int I>
     __device__ static float boundary(const float (&)[NIN][I], int, float, const Params &) { return 0.f; }
-    template <int I>
-    __device__ static void post(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+    template <int I, bool EDGE>
+    __device__ static void post(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
                                 const Params &p, float rsc, const float (&A)[I], float A_after,
                                 const Keep<I> &keep, float (&o)[NOUT][I])
     {
         const float g = p.c0;
 #pragma unroll
         for (int k = 0; k < I; ++k) {
-            const bool last = (t0 + k == p.T - 1);
+            const bool last = (EDGE && k == kb);
             const float vs_next = (k + 1 < I) ? A[k + 1] + x[2][k + 1] : A_after + xn[2];
             const float nvs = successor<I>(x, k, last, vs_next, rsc);
             const float term = x[4][k];
@@ -169,8 +171,8 @@ struct Retrace {
     static constexpr unsigned HALO = (1u << 0) | (1u << 1) | (1u << 2);
     template <int I> struct Keep { float rho[I]; };
 
-    template <int I>
-    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+    template <int I, bool EDGE>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
                                   const Params &p, float, float (&a)[I], float (&b)[I], Keep<I> &keep)
     {
         const float g = p.c0, lam = p.c1;
@@ -184,7 +186,7 @@ struct Retrace {
         c[I] = lam * fminf(p.c2, xn[0] / xn[1]);
 #pragma unroll
         for (int k = 0; k < I; ++k) {
-            const bool last = (t0 + k == p.T - 1);
+            const bool last = (EDGE && k == kb);
             const float term = x[5][k];
             float done;
             if constexpr (TRUNC) done = done_of(term, x[6][k]);
@@ -196,15 +198,15 @@ struct Retrace {
     }
     template <int I>
     __device__ static float boundary(const float (&)[NIN][I], int, float, const Params &) { return 0.f; }
-    template <int I>
-    __device__ static void post(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+    template <int I, bool EDGE>
+    __device__ static void post(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
                                 const Params &p, float, const float (&A)[I], float A_after,
                                 const Keep<I> &keep, float (&o)[NOUT][I])
     {
         const float g = p.c0;
 #pragma unroll
         for (int k = 0; k < I; ++k) {
-            const bool last = (t0 + k == p.T - 1);
+            const bool last = (EDGE && k == kb);
             const float qn = last ? 0.f : ((k + 1 < I) ? A[k + 1] + x[2][k + 1] : A_after + xn[2]);
             const float term = x[5][k];
             o[0][k] = A[k] + x[2][k];
@@ -227,8 +229,8 @@ struct LambdaReturns {
     static constexpr int TR = 3, BS = 3 + TRUNC;
     template <int I> struct Keep {};
 
-    template <int I>
-    __device__ static void coeffs(const float (&x)[NIN][I], const float (&)[NIN], int64_t t0,
+    template <int I, bool EDGE>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&)[NIN], int kb,
                                   const Params &p, float rsc, float (&a)[I], float (&b)[I], Keep<I> &)
     {
         const float g = p.c0, gl = p.c0 * p.c1, g1l = p.c0 * (1.f - p.c1);
@@ -236,7 +238,7 @@ struct LambdaReturns {
         for (int k = 0; k < I; ++k) {
             const float term = x[2][k];
             if constexpr (TRUNC) {
-                const bool last = (t0 + k == p.T - 1);
+                const bool last = (EDGE && k == kb);
                 const float tr = x[TR][k];
                 float bs;
                 if constexpr (BS2D) bs = x[BS][k];
@@ -257,8 +259,8 @@ struct LambdaReturns {
         if constexpr (BS2D) return x[BS][k];
         else return rsc;
     }
-    template <int I>
-    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int64_t, const Params &,
+    template <int I, bool EDGE>
+    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int, const Params &,
                                 float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
     {
 #pragma unroll
@@ -278,8 +280,8 @@ struct Discounted {
     static constexpr int TR = 2, BS = 2 + TRUNC;
     template <int I> struct Keep {};
 
-    template <int I>
-    __device__ static void coeffs(const float (&x)[NIN][I], const float (&)[NIN], int64_t t0,
+    template <int I, bool EDGE>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&)[NIN], int kb,
                                   const Params &p, float rsc, float (&a)[I], float (&b)[I], Keep<I> &)
     {
         const float g = p.c0;
@@ -287,7 +289,7 @@ struct Discounted {
         for (int k = 0; k < I; ++k) {
             const float term = x[1][k];
             if constexpr (TRUNC) {
-                const bool last = (t0 + k == p.T - 1);
+                const bool last = (EDGE && k == kb);
                 const float tr = x[TR][k];
                 float bs;
                 if constexpr (BS2D) bs = x[BS][k];
@@ -306,8 +308,8 @@ struct Discounted {
         if constexpr (BS2D) return x[BS][k];
         else return rsc;
     }
-    template <int I>
-    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int64_t, const Params &,
+    template <int I, bool EDGE>
+    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int, const Params &,
                                 float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
     {
 #pragma unroll
@@ -324,23 +326,23 @@ struct Eligibility {
     static constexpr unsigned HALO = 1u << 1;
     template <int I> struct Keep {};
 
-    template <int I>
-    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+    template <int I, bool EDGE>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
                                   const Params &p, float, float (&a)[I], float (&b)[I], Keep<I> &)
     {
         const float gl = p.c0 * p.c1;
 #pragma unroll
         for (int k = 0; k < I; ++k) {
             float dprev = (k > 0) ? x[1][k - 1] : xn[1];
-            if (t0 + k == 0) dprev = 0.f;
+            if (EDGE && k == kb) dprev = 0.f;
             a[k] = x[0][k];
             b[k] = gl * (1.f - dprev);
         }
     }
     template <int I>
     __device__ static float boundary(const float (&)[NIN][I], int, float rsc, const Params &) { return rsc; }
-    template <int I>
-    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int64_t, const Params &,
+    template <int I, bool EDGE>
+    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int, const Params &,
                                 float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
     {
 #pragma unroll
@@ -358,8 +360,8 @@ struct Prefix {
     static constexpr unsigned HALO = STARTS_AT ? 0u : (1u << 1);
     template <int I> struct Keep {};
 
-    template <int I>
-    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int64_t t0,
+    template <int I, bool EDGE>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
                                   const Params &, float, float (&a)[I], float (&b)[I], Keep<I> &)
     {
 #pragma unroll
@@ -369,7 +371,7 @@ struct Prefix {
                 d = x[1][k];
             } else {
                 d = (k > 0) ? x[1][k - 1] : xn[1];
-                if (t0 + k == 0) d = 0.f;
+                if (EDGE && k == kb) d = 0.f;
             }
             a[k] = x[0][k];
             b[k] = 1.f - d;
@@ -377,8 +379,8 @@ struct Prefix {
     }
     template <int I>
     __device__ static float boundary(const float (&)[NIN][I], int, float rsc, const Params &) { return rsc; }
-    template <int I>
-    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int64_t, const Params &,
+    template <int I, bool EDGE>
+    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int, const Params &,
                                 float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
     {
 #pragma unroll
@@ -395,8 +397,8 @@ struct Linear {
     static constexpr unsigned HALO = 0;
     template <int I> struct Keep {};
 
-    template <int I>
-    __device__ static void coeffs(const float (&x)[NIN][I], const float (&)[NIN], int64_t,
+    template <int I, bool EDGE>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&)[NIN], int,
                                   const Params &, float, float (&a)[I], float (&b)[I], Keep<I> &)
     {
 #pragma unroll
@@ -407,8 +409,8 @@ struct Linear {
     }
     template <int I>
     __device__ static float boundary(const float (&)[NIN][I], int, float rsc, const Params &) { return rsc; }
-    template <int I>
-    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int64_t, const Params &,
+    template <int I, bool EDGE>
+    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int, const Params &,
                                 float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
     {
 #pragma unroll

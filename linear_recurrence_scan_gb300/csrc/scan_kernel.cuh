@@ -31,8 +31,15 @@
 //    64-bit state word carries a 32-bit tag (call epoch << 2 | kind) next to
 //    its payload, so a reader validates it without fences and stale words of
 //    earlier calls are never mistaken for fresh ones (no memset per call).
-//    Tiles are numbered in scan order and handed out by an atomic ticket, so
-//    every tile's predecessors are held by CTAs that are already running.
+//    Tiles are handed out by an atomic ticket in the order (position in row,
+//    row): a tile's predecessor in its row was handed out N tickets earlier,
+//    so it is usually finished before it is needed, and every predecessor is
+//    held by a CTA that is already running (no deadlock).  The predecessor's
+//    state is fetched when the tile starts, off the critical path.
+//  * Roles: the last warp's lane 0 draws tickets and issues the copies; warp
+//    0 scans the warp aggregates and its lane 0 does the look-back.  Two
+//    CTA barriers per tile; a stage is refilled as soon as every thread has
+//    read it into registers.
 //  * Every wait (mbarrier phase, predecessor state) is bounded in time; on
 //    expiry the kernel records RLSCAN_ERR_TIMEOUT in the workspace, uses NaN
 //    for the missing value and carries on, so it always terminates.
@@ -77,6 +84,9 @@ struct TileGeo {
     int32_t len;   // time steps present per row
 };
 
+// Tile g -> rows and time range.  Packed: rows [g R, g R + R).  Long rows:
+// ticket g = j * N + row (all rows' j-th tiles before any (j+1)-th tile);
+// j counts tiles in scan order (from t = T-1 backward, from t = 0 forward).
 template <bool FWD, int TILE>
 __device__ __forceinline__ TileGeo decode_tile(const Params &p, int64_t g)
 {
@@ -89,8 +99,8 @@ __device__ __forceinline__ TileGeo decode_tile(const Params &p, int64_t g)
         tg.len = static_cast<int32_t>(p.T);
         tg.j = 0;
     } else {
-        tg.row0 = g / p.tiles_per_row;
-        tg.j = g - tg.row0 * p.tiles_per_row;
+        tg.j = g / p.N;
+        tg.row0 = g - tg.j * p.N;
         const int64_t chrono = FWD ? tg.j : (p.tiles_per_row - 1 - tg.j);
         tg.t0 = chrono * TILE;
         const int64_t rem = p.T - tg.t0;
@@ -100,13 +110,12 @@ __device__ __forceinline__ TileGeo decode_tile(const Params &p, int64_t g)
     return tg;
 }
 
-// Issue the bulk copies of tile g into `stage` (called by one thread).
+// Issue the bulk copies of one tile into `stage` (called by one thread).
 // Array j of the stage occupies AST floats; its data start at offset 4, the
 // step before the tile at offset 3 and the step after it at offset 4+TILE.
 template <class E, int TILE, int AST>
-__device__ void issue_tile_copies(const Params &p, int64_t g, float *stage, uint64_t *bar)
+__device__ void issue_tile_copies(const Params &p, const TileGeo &tg, float *stage, uint64_t *bar)
 {
-    const TileGeo tg = decode_tile<E::FWD, TILE>(p, g);
     if (p.packed) {
         if (p.rs == p.T && p.C == p.T) {  // rows contiguous in global and in shared memory
             const uint32_t nb = static_cast<uint32_t>(tg.nrows * p.T * 4);
@@ -145,11 +154,10 @@ __device__ void issue_tile_copies(const Params &p, int64_t g, float *stage, uint
                       static_cast<uint32_t>((hi[j] - lo[j]) * 4), bar);
 }
 
-// Element-wise cooperative load of tile g (any alignment), same layout.
+// Element-wise cooperative load of one tile (any alignment), same layout.
 template <class E, int THREADS, int TILE, int AST>
-__device__ void load_tile_elementwise(const Params &p, int64_t g, float *stage)
+__device__ void load_tile_elementwise(const Params &p, const TileGeo &tg, float *stage)
 {
-    const TileGeo tg = decode_tile<E::FWD, TILE>(p, g);
     const int total = tg.nrows * p.C;
     for (int e = threadIdx.x; e < total; e += THREADS) {
         const int i = e / p.C;
@@ -180,52 +188,54 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, uint6
     return true;
 }
 
-// Decoupled look-back for tile g (one thread).  `total` is the tile's
-// aggregate map.  Returns the value entering the tile from its scan-order
-// predecessor (A at the step just outside the tile), or 0 for a row's first
-// tile.  Publishes the tile's own states on the way.
-template <bool FWD>
-__device__ float lookback(const Params &p, const TileGeo &tg, int64_t g, Pair total)
+// Decoupled look-back for tile g at position j of its row (one thread).
+// `total` is the tile's aggregate map; (w0, w1) the predecessor's state as
+// fetched when the tile started.  Publishes this tile's state and returns
+// the value entering the tile from its scan-order predecessor (A at the step
+// just outside the tile), 0 for a row's first tile.
+__device__ inline float lookback(const Params &p, int64_t g, int64_t j, Pair total, unsigned long long w0,
+                          unsigned long long w1)
 {
-    if (p.packed) return 0.f;
     unsigned long long *st = p.states;
     const uint32_t tagA = (p.epoch << 2) | kTagAgg;
     const uint32_t tagP = (p.epoch << 2) | kTagPrefix;
-    if (tg.j == 0 || total.b == 0.f) {
+    if (j == 0 || total.b == 0.f) {
         // the inclusive value does not depend on anything before the tile
         ptx::st_relaxed(&st[2 * g], pack_word(tagP, total.a));
-        if (tg.j == 0) return 0.f;
+        if (j == 0) return 0.f;
     } else {
         ptx::st_relaxed(&st[2 * g + 1], pack_word(tagA, total.b));
         ptx::st_relaxed(&st[2 * g], pack_word(tagA, total.a));
     }
     Pair acc{0.f, 1.f};
-    int64_t k = g - 1;
-    const int64_t kmin = g - tg.j;
+    int64_t k = g - p.N;
+    int64_t left = j;  // predecessors not yet folded in
     float carry = 0.f;
     uint64_t waited_since = 0;
     uint32_t nap = 32;
+    bool fresh = true;  // (w0, w1) hold a probe of tile k
     for (;;) {
-        const unsigned long long w0 = ptx::ld_relaxed(&st[2 * k]);
+        if (!fresh) {
+            w0 = ptx::ld_relaxed(&st[2 * k]);
+            w1 = ptx::ld_relaxed(&st[2 * k + 1]);
+        }
+        fresh = false;
         const uint32_t tag = static_cast<uint32_t>(w0 >> 32);
         if (tag == tagP) {
             carry = fmaf(acc.b, __uint_as_float(static_cast<uint32_t>(w0)), acc.a);
             break;
         }
-        if (tag == tagA) {
-            const unsigned long long w1 = ptx::ld_relaxed(&st[2 * k + 1]);
-            if (static_cast<uint32_t>(w1 >> 32) == tagA) {
-                acc = compose(acc, Pair{__uint_as_float(static_cast<uint32_t>(w0)),
-                                        __uint_as_float(static_cast<uint32_t>(w1))});
-                if (acc.b == 0.f || k == kmin) {
-                    carry = acc.a;
-                    break;
-                }
-                --k;
-                waited_since = 0;
-                nap = 32;
-                continue;
+        if (tag == tagA && static_cast<uint32_t>(w1 >> 32) == tagA) {
+            acc = compose(acc, Pair{__uint_as_float(static_cast<uint32_t>(w0)),
+                                    __uint_as_float(static_cast<uint32_t>(w1))});
+            if (acc.b == 0.f || --left == 0) {
+                carry = acc.a;
+                break;
             }
+            k -= p.N;
+            waited_since = 0;
+            nap = 32;
+            continue;
         }
         const uint64_t now = ptx::globaltimer_ns();
         if (waited_since == 0) {
@@ -236,7 +246,7 @@ __device__ float lookback(const Params &p, const TileGeo &tg, int64_t g, Pair to
             break;
         }
         __nanosleep(nap);
-        if (nap < 1024) nap <<= 1;
+        if (nap < 512) nap <<= 1;
     }
     if (total.b != 0.f) ptx::st_relaxed(&st[2 * g], pack_word(tagP, fmaf(total.b, carry, total.a)));
     return carry;
@@ -277,11 +287,34 @@ __device__ __forceinline__ Pair warp_exclusive_from(Pair inc, int lane)
     return ex;
 }
 
+// Where this thread's ITEMS steps sit in a tile: row, first step, number of
+// valid steps (kv) and the index of the row's boundary step in the range
+// (kb; -1 if none).
+struct ThreadSpan {
+    int64_t row, t_first;
+    int kv, kb;
+};
+
+template <bool FWD, int ITEMS>
+__device__ __forceinline__ ThreadSpan thread_span(const Params &p, const TileGeo &tg, int rit, int col)
+{
+    ThreadSpan sp;
+    sp.row = tg.row0 + rit;
+    sp.t_first = tg.t0 + col;
+    const bool row_ok = rit < tg.nrows;
+    const int64_t rem = p.T - sp.t_first;
+    sp.kv = row_ok ? static_cast<int>(rem < 0 ? 0 : (rem > ITEMS ? ITEMS : rem)) : 0;
+    const int64_t d = FWD ? -sp.t_first : (p.T - 1 - sp.t_first);
+    sp.kb = (row_ok && d >= 0 && d < ITEMS) ? static_cast<int>(d) : -1;
+    return sp;
+}
+
 template <class E, int THREADS, int ITEMS, int STAGES>
 __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ Params p)
 {
     constexpr int NIN = E::NIN, NOUT = E::NOUT;
     constexpr int TILE = THREADS * ITEMS, AST = TILE + 8, WARPS = THREADS / 32;
+    constexpr int PRODUCER = THREADS - 32;  // lane 0 of the last warp
     constexpr bool FWD = E::FWD;
     static_assert(STAGES >= 2, "the ring needs two stages");
     static_assert(ITEMS % 4 == 0, "items per thread are moved as float4");
@@ -290,6 +323,7 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
     extern __shared__ __align__(128) float smem[];
     __shared__ __align__(8) uint64_t mbar[STAGES];
     __shared__ int64_t tile_ids[STAGES];
+    __shared__ TileGeo s_geo[STAGES];
     __shared__ Pair wexcl[WARPS];
     __shared__ Pair wagg[WARPS];
     __shared__ float s_carry;
@@ -299,7 +333,7 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
     const bool tma = p.tma != 0;
 
     // Tile sequence: an atomic ticket when tiles depend on each other, a
-    // static stride otherwise.  Only thread 0 draws.
+    // static stride otherwise.  Only the producer thread draws.
     int64_t static_next = blockIdx.x;
     auto next_tile = [&]() -> int64_t {
         if (p.dynamic)
@@ -308,17 +342,22 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
         static_next += gridDim.x;
         return t;
     };
+    // producer: record tile g in ring slot s and start its copies
+    auto fill_slot = [&](int s, int64_t g) {
+        tile_ids[s] = g;
+        if (g < p.num_tiles) {
+            const TileGeo tg = decode_tile<FWD, TILE>(p, g);
+            s_geo[s] = tg;
+            if (tma) issue_tile_copies<E, TILE, AST>(p, tg, smem + s * NIN * AST, &mbar[s]);
+        }
+    };
 
-    if (tid == 0) {
+    if (tid == PRODUCER) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) ptx::mbar_init(&mbar[s], 1);
         ptx::fence_mbar_init();
 #pragma unroll
-        for (int s = 0; s < STAGES; ++s) {
-            const int64_t g = next_tile();
-            tile_ids[s] = g;
-            if (g < p.num_tiles && tma) issue_tile_copies<E, TILE, AST>(p, g, smem + s * NIN * AST, &mbar[s]);
-        }
+        for (int s = 0; s < STAGES; ++s) fill_slot(s, next_tile());
     }
     __syncthreads();
 
@@ -326,26 +365,35 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
     const int rit = p.packed ? li / p.C : 0;
     const int col = p.packed ? li - rit * p.C : li;
 
-    // Row scalar of the row this thread covers, when the row's boundary step
-    // falls in its range; fetched one tile ahead so its latency is hidden.
-    auto load_row_scalar = [&](int64_t g) -> float {
-        if (!E::ROWSCALAR || p.rowscalar == nullptr || g >= p.num_tiles) return 0.f;
-        const TileGeo tg = decode_tile<FWD, TILE>(p, g);
-        if (rit >= tg.nrows) return 0.f;
-        const int64_t tf = tg.t0 + col;
-        const bool need = FWD ? (tf == 0) : (tf <= p.T - 1 && p.T - 1 < tf + ITEMS);
-        if (!need) return 0.f;
-        return __ldg(p.rowscalar + (tg.row0 + rit) * p.rowscalar_stride);
+    // Row scalar of this thread's row when the row's boundary step falls in
+    // its range; fetched one tile ahead so its latency is hidden.
+    auto load_row_scalar = [&](int s) -> float {
+        if (!E::ROWSCALAR || p.rowscalar == nullptr || tile_ids[s] >= p.num_tiles) return 0.f;
+        const ThreadSpan sp = thread_span<FWD, ITEMS>(p, s_geo[s], rit, col);
+        if (sp.kb < 0) return 0.f;
+        return __ldg(p.rowscalar + sp.row * p.rowscalar_stride);
     };
-    float rsc_next = load_row_scalar(tile_ids[0]);
+    float rsc_next = load_row_scalar(0);
     uint32_t lost_stages = 0, lost_parity = 0;  // waits that timed out (thread 0)
 
     for (int it = 0;; ++it) {
         const int s = it % STAGES;
         const int64_t g = tile_ids[s];
         if (g >= p.num_tiles) break;
+        const TileGeo tg = s_geo[s];
         const float rsc = rsc_next;
         float *stage = smem + s * NIN * AST;
+
+        // the ticket for the refill of this slot, drawn early (its latency
+        // overlaps this tile's work)
+        int64_t refill = 0;
+        if (tid == PRODUCER) refill = next_tile();
+        // predecessor state for the look-back, also fetched early
+        unsigned long long pw0 = 0, pw1 = 0;
+        if (tid == 0 && !p.packed && tg.j > 0) {
+            pw0 = ptx::ld_relaxed(&p.states[2 * (g - p.N)]);
+            pw1 = ptx::ld_relaxed(&p.states[2 * (g - p.N) + 1]);
+        }
 
         if (tma) {
             const uint32_t parity = static_cast<uint32_t>((it / STAGES) & 1);
@@ -355,44 +403,45 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
                 record_error(p, RLSCAN_ERR_TIMEOUT, 0x80000000u | static_cast<uint32_t>(s));
             }
         } else {
-            load_tile_elementwise<E, THREADS, TILE, AST>(p, g, stage);
+            load_tile_elementwise<E, THREADS, TILE, AST>(p, tg, stage);
             __syncthreads();
         }
 
-        const TileGeo tg = decode_tile<FWD, TILE>(p, g);
-        const bool row_ok = rit < tg.nrows;
-        const int64_t row = tg.row0 + rit;
-        const int64_t t_first = tg.t0 + col;
+        const ThreadSpan sp = thread_span<FWD, ITEMS>(p, tg, rit, col);
+        const bool edge = sp.kb >= 0 || sp.kv < ITEMS;
 
         // inputs of this thread's ITEMS steps, plus the neighbour step
         float x[NIN][ITEMS], xn[NIN];
-        const float *sp = stage + 4 + li;
+        const float *src = stage + 4 + li;
 #pragma unroll
         for (int j = 0; j < NIN; ++j) {
 #pragma unroll
             for (int k = 0; k < ITEMS; k += 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(sp + j * AST + k);
+                const float4 v = *reinterpret_cast<const float4 *>(src + j * AST + k);
                 x[j][k] = v.x;
                 x[j][k + 1] = v.y;
                 x[j][k + 2] = v.z;
                 x[j][k + 3] = v.w;
             }
-            xn[j] = ((E::HALO >> j) & 1u) ? (FWD ? sp[j * AST - 1] : sp[j * AST + ITEMS]) : 0.f;
+            xn[j] = ((E::HALO >> j) & 1u) ? (FWD ? src[j * AST - 1] : src[j * AST + ITEMS]) : 0.f;
         }
 
         float a[ITEMS], b[ITEMS];
         typename E::template Keep<ITEMS> keep;
-        E::template coeffs<ITEMS>(x, xn, t_first, p, rsc, a, b, keep);
+        if (!edge) {
+            E::template coeffs<ITEMS, false>(x, xn, -1, p, rsc, a, b, keep);
+        } else {
+            E::template coeffs<ITEMS, true>(x, xn, sp.kb, p, rsc, a, b, keep);
 #pragma unroll
-        for (int k = 0; k < ITEMS; ++k) {
-            const int64_t t = t_first + k;
-            if (t == (FWD ? 0 : p.T - 1)) {
-                a[k] = fmaf(b[k], E::template boundary<ITEMS>(x, k, rsc, p), a[k]);
-                b[k] = 0.f;
-            }
-            if (!(row_ok && t < p.T)) {  // outside the data: identity map
-                a[k] = 0.f;
-                b[k] = 1.f;
+            for (int k = 0; k < ITEMS; ++k) {
+                if (k == sp.kb) {  // fold the row's boundary value; sever
+                    a[k] = fmaf(b[k], E::template boundary<ITEMS>(x, k, rsc, p), a[k]);
+                    b[k] = 0.f;
+                }
+                if (k >= sp.kv) {  // outside the data: identity map
+                    a[k] = 0.f;
+                    b[k] = 1.f;
+                }
             }
         }
 
@@ -410,9 +459,10 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
         const Pair inc = warp_inclusive<FWD>(agg, lane);
         const Pair ex = warp_exclusive_from<FWD>(inc, lane);
         if (lane == (FWD ? 31 : 0)) wagg[warp] = inc;
-        __syncthreads();
+        __syncthreads();  // every thread has its inputs in registers: the stage is free
 
-        rsc_next = load_row_scalar(tile_ids[(it + 1) % STAGES]);
+        if (tid == PRODUCER) fill_slot(s, refill);
+        rsc_next = load_row_scalar((it + 1) % STAGES);
 
         if (warp == 0) {
             const Pair w = lane < WARPS ? wagg[lane] : Pair{0.f, 1.f};
@@ -422,7 +472,7 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
             Pair total;
             total.a = __shfl_sync(0xffffffffu, winc.a, FWD ? 31 : 0);
             total.b = __shfl_sync(0xffffffffu, winc.b, FWD ? 31 : 0);
-            if (lane == 0) s_carry = lookback<FWD>(p, tg, g, total);
+            if (lane == 0) s_carry = p.packed ? 0.f : lookback(p, g, tg.j, total, pw0, pw1);
         }
         __syncthreads();
 
@@ -447,16 +497,17 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
             }
         }
         float o[NOUT][ITEMS];
-        E::template post<ITEMS>(x, xn, t_first, p, rsc, A, x_in, keep, o);
+        if (!edge) E::template post<ITEMS, false>(x, xn, -1, p, rsc, A, x_in, keep, o);
+        else E::template post<ITEMS, true>(x, xn, sp.kb, p, rsc, A, x_in, keep, o);
 
-        if (row_ok) {
-            const int64_t off = row * p.rs + t_first;
+        if (sp.kv > 0) {
+            const int64_t off = sp.row * p.rs + sp.t_first;
             if (tma) {
 #pragma unroll
                 for (int q = 0; q < NOUT; ++q) {
 #pragma unroll
                     for (int k = 0; k < ITEMS; k += 4) {
-                        if (t_first + k < p.T)
+                        if (k < sp.kv)
                             *reinterpret_cast<float4 *>(p.out[q] + off + k) =
                                 make_float4(o[q][k], o[q][k + 1], o[q][k + 2], o[q][k + 3]);
                     }
@@ -466,16 +517,9 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
                 for (int q = 0; q < NOUT; ++q) {
 #pragma unroll
                     for (int k = 0; k < ITEMS; ++k)
-                        if (t_first + k < p.T) p.out[q][off + k] = o[q][k];
+                        if (k < sp.kv) p.out[q][off + k] = o[q][k];
                 }
             }
-        }
-        __syncthreads();  // stage s and tile_ids[s] are free again
-
-        if (tid == 0) {
-            const int64_t gn = next_tile();
-            tile_ids[s] = gn;
-            if (gn < p.num_tiles && tma) issue_tile_copies<E, TILE, AST>(p, gn, stage, &mbar[s]);
         }
     }
 
@@ -485,13 +529,16 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
         for (int s = 0; s < STAGES; ++s)
             if ((lost_stages >> s) & 1u) wait_phase(&mbar[s], (lost_parity >> s) & 1u, p.spin_limit_ns);
     }
-    if (p.dynamic && tid == 0) {
-        __threadfence();
-        const uint32_t done = atomicAdd(&p.hdr[kHdrExit], 1u);
-        if (done == gridDim.x - 1) {  // last CTA out: re-arm the ticket for the next call
-            atomicExch(reinterpret_cast<unsigned long long *>(p.hdr), 0ull);
-            atomicExch(&p.hdr[kHdrExit], 0u);
+    if (p.dynamic) {
+        __syncthreads();  // every ticket this CTA will draw has been drawn
+        if (tid == PRODUCER) {
             __threadfence();
+            const uint32_t done = atomicAdd(&p.hdr[kHdrExit], 1u);
+            if (done == gridDim.x - 1) {  // last CTA out: re-arm the ticket for the next call
+                atomicExch(reinterpret_cast<unsigned long long *>(p.hdr), 0ull);
+                atomicExch(&p.hdr[kHdrExit], 0u);
+                __threadfence();
+            }
         }
     }
 }
