@@ -12,18 +12,35 @@
 
 namespace rlscan {
 
-// Launch shape per estimator: 256 threads; 8 steps per thread (2048-step
-// tiles) for the light estimators, 4 (1024-step tiles) for those with five
-// or more input streams, so that STAGES stages of every input fit twice per
-// SM.  The ring holds up to ~96 KB per CTA.
+// Launch shape per estimator, from the bytes one time step moves
+// (4 * (inputs + outputs)): tiles of 1024, 2048 or 4096 steps, whichever is
+// closest to TILE_BYTES_TARGET bytes of traffic, so the per-tile fixed cost
+// (barrier, warp scans, look-back) is amortised over enough data; 256
+// threads for 2048+ step tiles, 128 for 1024; as many ring stages
+// (2..MAX_STAGES) as fit in SMEM_BUDGET_KB per CTA.  Sweeps on GB300 chose
+// the defaults: short kernels prefer a shallow ring (more CTAs per SM, and
+// every CTA's first tile arrives sooner).  The macros exist for such sweeps.
+#ifndef RLSCAN_TILE_BYTES_TARGET
+#define RLSCAN_TILE_BYTES_TARGET 40960
+#endif
+#ifndef RLSCAN_SMEM_BUDGET_KB
+#define RLSCAN_SMEM_BUDGET_KB 64
+#endif
+#ifndef RLSCAN_MAX_STAGES
+#define RLSCAN_MAX_STAGES 4
+#endif
+
 template <class E>
 struct Shape {
-    static constexpr int THREADS = 256;
-    static constexpr int ITEMS = (E::NIN >= 5) ? 4 : 8;
-    static constexpr int TILE = THREADS * ITEMS;
+    static constexpr int BYTES_PER_STEP = 4 * (E::NIN + E::NOUT);
+    static constexpr int TILE_RAW = RLSCAN_TILE_BYTES_TARGET / BYTES_PER_STEP;
+    static constexpr int TILE = TILE_RAW >= 3072 ? 4096 : (TILE_RAW >= 1536 ? 2048 : 1024);
+    static constexpr int THREADS = TILE >= 2048 ? 256 : 128;
+    static constexpr int ITEMS = TILE / THREADS;
     static constexpr int STAGE_BYTES = E::NIN * (TILE + 8) * 4;
-    static constexpr int RAW = (96 * 1024) / STAGE_BYTES;
-    static constexpr int STAGES = RAW < 2 ? 2 : (RAW > 4 ? 4 : RAW);
+    static constexpr int RAW = (RLSCAN_SMEM_BUDGET_KB * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = RAW < 2 ? 2 : (RAW > RLSCAN_MAX_STAGES ? RLSCAN_MAX_STAGES : RAW);
+    static_assert(TILE == THREADS * ITEMS, "tile shape");
 };
 
 constexpr int kMaxDevices = 64;
@@ -67,6 +84,8 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
     for (int q = 0; q < E::NOUT; ++q) tma = tma && aligned16(p.out[q]);
     p.tma = tma ? 1 : 0;
     p.spin_limit_ns = spin_limit_ns();
+    p.copy_limit_ns = 2000000000ull;  // bulk copies land in microseconds; never cut short
+    p.withhold_tile = withhold_tile();
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RLSCAN_ERR_CUDA;
@@ -89,7 +108,20 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
     }
     const int64_t slots = static_cast<int64_t>(sm_count[dev]) * blocks_per_sm[dev];
     const int64_t grid = p.num_tiles < slots ? p.num_tiles : slots;
-    kernel<<<static_cast<unsigned>(grid), S::THREADS, smem, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(S::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) {
+        cudaGetLastError();
+        return RLSCAN_ERR_CUDA;
+    }
     return cudaGetLastError() == cudaSuccess ? RLSCAN_OK : RLSCAN_ERR_CUDA;
 }
 

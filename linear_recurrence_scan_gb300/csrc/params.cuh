@@ -45,7 +45,9 @@ struct Params {
     uint32_t epoch;            // tag of this call's tile states (30 bits)
     unsigned long long *states;
     uint32_t *hdr;
-    uint64_t spin_limit_ns;    // bound on every cross-block wait
+    uint64_t spin_limit_ns;    // bound on every look-back wait
+    uint64_t copy_limit_ns;    // bound on every wait for a bulk copy
+    int64_t withhold_tile;     // test hook: this tile never publishes (-1: none)
 };
 
 // Launchers (one translation unit per estimator family).
@@ -61,5 +63,7 @@ rlscan_status launch_linear(bool forward, Params p, void *ws, size_t ws_bytes, c
 // Host helpers shared by the launchers (rlscan_abi.cu).
 uint32_t next_epoch();
 uint64_t spin_limit_ns();
+int64_t withhold_tile();  // RLSCAN_TEST_WITHHOLD_TILE, -1 when unset
+bool pdl_enabled();  // programmatic dependent launch (RLSCAN_PDL=0 disables)
 
 }  // namespace rlscan

@@ -73,6 +73,20 @@ __device__ __forceinline__ void st_relaxed(unsigned long long *p, unsigned long 
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel in the stream (if it
+// was launched with programmatic serialization) be scheduled now, and wait
+// until the previous kernel has completed and its writes are visible.
+// Both are no-ops for kernels launched without the attribute.
+__device__ __forceinline__ void pdl_trigger_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_prerequisites()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;

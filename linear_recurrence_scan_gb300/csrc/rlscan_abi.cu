@@ -38,6 +38,24 @@ uint64_t spin_limit_ns()
     return limit;
 }
 
+int64_t withhold_tile()
+{
+    static const int64_t tile = [] {
+        const char *s = std::getenv("RLSCAN_TEST_WITHHOLD_TILE");
+        return s != nullptr ? static_cast<int64_t>(std::strtoll(s, nullptr, 10)) : int64_t(-1);
+    }();
+    return tile;
+}
+
+bool pdl_enabled()
+{
+    static const bool on = [] {
+        const char *s = std::getenv("RLSCAN_PDL");
+        return !(s != nullptr && s[0] == '0');
+    }();
+    return on;
+}
+
 namespace {
 
 __global__ void zero_words(uint32_t *p, size_t n)
@@ -48,6 +66,60 @@ __global__ void zero_words(uint32_t *p, size_t n)
 }
 
 inline cudaStream_t cs(rlscan_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// ---- opt-in content checks (RLSCAN_CHECKS=1) --------------------------------
+// The rl-triton API reference's correctness-warning checks: terminated and
+// truncated are mutually exclusive, and bootstrap_values is zero at interior
+// non-truncated steps (compute_gae / compute_vtrace).  Debug only: the call
+// synchronises the stream to return the verdict.
+
+__device__ uint32_t g_check_flags;
+
+__global__ void check_inputs(const float *term, const float *trunc, const float *bs, int64_t N,
+                             int64_t T, int64_t rs)
+{
+    uint32_t bad = 0;
+    const int64_t total = N * T;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row = i / T, t = i - row * T;
+        const int64_t e = row * rs + t;
+        const float tr = trunc[e];
+        if (term != nullptr && term[e] != 0.f && tr != 0.f) bad |= 1u;
+        if (bs != nullptr && t < T - 1 && tr == 0.f && bs[e] != 0.f) bad |= 2u;
+    }
+    if (bad) atomicOr(&g_check_flags, bad);
+}
+
+bool checks_enabled()
+{
+    static const bool on = [] {
+        const char *s = std::getenv("RLSCAN_CHECKS");
+        return s != nullptr && s[0] == '1';
+    }();
+    return on;
+}
+
+// RLSCAN_OK when the inputs pass (or checks are off), RLSCAN_ERR_INVALID_INPUT otherwise.
+rlscan_status run_checks(const float *term, const float *trunc, const float *bs, int64_t N,
+                         int64_t T, int64_t rs, cudaStream_t stream)
+{
+    if (!checks_enabled() || trunc == nullptr) return RLSCAN_OK;
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_check_flags, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice,
+                                stream) != cudaSuccess)
+        return RLSCAN_ERR_CUDA;
+    int64_t blocks = (N * T + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    check_inputs<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(term, trunc, bs, N, T, rs);
+    uint32_t flags = 0;
+    if (cudaGetLastError() != cudaSuccess ||
+        cudaMemcpyFromSymbolAsync(&flags, g_check_flags, sizeof(flags), 0, cudaMemcpyDeviceToHost,
+                                  stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return RLSCAN_ERR_CUDA;
+    return flags ? RLSCAN_ERR_INVALID_INPUT : RLSCAN_OK;
+}
 
 inline rlscan_status check_shape(int64_t N, int64_t T, int64_t rs)
 {
@@ -156,6 +228,7 @@ RLSCAN_API rlscan_status rlscan_gae(const float *rewards, const float *values, c
     if (last_value && truncateds) return RLSCAN_ERR_ARG_CONFLICT;
     if (same_as_any(advantages, {rewards, values, terminateds, truncateds, bootstrap_values, last_value}))
         return RLSCAN_ERR_ARG_CONFLICT;
+    RLSCAN_TRY(run_checks(terminateds, truncateds, bootstrap_values, N, T, row_stride, cs(stream)));
     Params p = base_params(N, T, row_stride);
     p.c0 = gamma;
     p.c1 = lambda;
@@ -196,6 +269,7 @@ RLSCAN_API rlscan_status rlscan_vtrace(const float *log_pi_target, const float *
                             bootstrap_values, last_value}))
             return RLSCAN_ERR_ARG_CONFLICT;
     if (vtrace_targets == vtrace_advantages) return RLSCAN_ERR_ARG_CONFLICT;
+    RLSCAN_TRY(run_checks(terminateds, truncateds, bootstrap_values, N, T, row_stride, cs(stream)));
     Params p = base_params(N, T, row_stride);
     p.c0 = gamma;
     p.c1 = rho_bar;
@@ -239,6 +313,7 @@ RLSCAN_API rlscan_status rlscan_retrace(const float *pi_taken, const float *mu_t
         if (same_as_any(o, {pi_taken, mu_taken, q_values, expected_next_q, rewards, terminateds, truncateds}))
             return RLSCAN_ERR_ARG_CONFLICT;
     if (retrace_targets == advantages) return RLSCAN_ERR_ARG_CONFLICT;
+    RLSCAN_TRY(run_checks(terminateds, truncateds, nullptr, N, T, row_stride, cs(stream)));
     Params p = base_params(N, T, row_stride);
     p.c0 = gamma;
     p.c1 = lambda;
@@ -269,6 +344,7 @@ RLSCAN_API rlscan_status rlscan_lambda_returns(const float *rewards, const float
     if (bootstrap_values && last_value) return RLSCAN_ERR_ARG_CONFLICT;
     if (same_as_any(returns, {rewards, next_values, terminateds, truncateds, bootstrap_values, last_value}))
         return RLSCAN_ERR_ARG_CONFLICT;
+    RLSCAN_TRY(run_checks(terminateds, truncateds, nullptr, N, T, row_stride, cs(stream)));
     Params p = base_params(N, T, row_stride);
     p.c0 = gamma;
     p.c1 = lambda;
@@ -303,6 +379,7 @@ RLSCAN_API rlscan_status rlscan_discounted_returns(const float *rewards, const f
     if (bootstrap_values && last_value) return RLSCAN_ERR_ARG_CONFLICT;
     if (same_as_any(returns, {rewards, terminateds, truncateds, bootstrap_values, last_value}))
         return RLSCAN_ERR_ARG_CONFLICT;
+    RLSCAN_TRY(run_checks(terminateds, truncateds, nullptr, N, T, row_stride, cs(stream)));
     Params p = base_params(N, T, row_stride);
     p.c0 = gamma;
     p.out[0] = returns;

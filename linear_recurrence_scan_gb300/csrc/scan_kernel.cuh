@@ -36,10 +36,15 @@
 //    so it is usually finished before it is needed, and every predecessor is
 //    held by a CTA that is already running (no deadlock).  The predecessor's
 //    state is fetched when the tile starts, off the critical path.
-//  * Roles: the last warp's lane 0 draws tickets and issues the copies; warp
-//    0 scans the warp aggregates and its lane 0 does the look-back.  Two
-//    CTA barriers per tile; a stage is refilled as soon as every thread has
-//    read it into registers.
+//  * Launched with programmatic stream serialization: the next kernel may be
+//    scheduled while this one drains, and this one touches global memory
+//    only after griddepcontrol.wait (previous kernel complete and visible).
+//  * Roles: the last warp's lane 0 draws tickets and issues the copies.
+//    One CTA barrier per tile: after it each warp composes the aggregates of
+//    the warps before it (double-buffered in shared memory) and, for a
+//    chained tile, its lane 0 reads the predecessor states itself; the warp
+//    holding the tile's last element in scan order publishes.  A stage is
+//    refilled as soon as every thread has read it into registers.
 //  * Every wait (mbarrier phase, predecessor state) is bounded in time; on
 //    expiry the kernel records RLSCAN_ERR_TIMEOUT in the workspace, uses NaN
 //    for the missing value and carries on, so it always terminates.
@@ -182,35 +187,48 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, uint6
 {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t start = ptx::globaltimer_ns();
-    while (!ptx::mbar_try_wait(bar, parity)) {
-        if (ptx::globaltimer_ns() - start > limit_ns) return false;
+    for (uint32_t n = 1;; ++n) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((n & 31u) == 0 && ptx::globaltimer_ns() - start > limit_ns) return false;
     }
-    return true;
 }
 
-// Decoupled look-back for tile g at position j of its row (one thread).
-// `total` is the tile's aggregate map; (w0, w1) the predecessor's state as
-// fetched when the tile started.  Publishes this tile's state and returns
-// the value entering the tile from its scan-order predecessor (A at the step
-// just outside the tile), 0 for a row's first tile.
-__device__ inline float lookback(const Params &p, int64_t g, int64_t j, Pair total, unsigned long long w0,
-                          unsigned long long w1)
+// Decoupled look-back, publishing side (one thread per tile): the tile's
+// aggregate map `total`, or directly its inclusive value when that does not
+// depend on anything before the tile (first tile of the row, or b == 0).
+__device__ __forceinline__ void publish_first(const Params &p, int64_t g, int64_t j, Pair total)
 {
+    if (g == p.withhold_tile) return;  // test hook: successors must time out
     unsigned long long *st = p.states;
+    if (j == 0 || total.b == 0.f) {
+        ptx::st_relaxed(&st[2 * g], pack_word((p.epoch << 2) | kTagPrefix, total.a));
+    } else {
+        ptx::st_relaxed(&st[2 * g + 1], pack_word((p.epoch << 2) | kTagAgg, total.b));
+        ptx::st_relaxed(&st[2 * g], pack_word((p.epoch << 2) | kTagAgg, total.a));
+    }
+}
+
+__device__ __forceinline__ void publish_inclusive(const Params &p, int64_t g, float v)
+{
+    if (g == p.withhold_tile) return;
+    ptx::st_relaxed(&p.states[2 * g], pack_word((p.epoch << 2) | kTagPrefix, v));
+}
+
+// Decoupled look-back, reading side (one thread per warp): the value
+// entering tile g (position j > 0 of its row) from its scan-order
+// predecessor, i.e. A at the step just outside the tile.  (w0, w1) are the
+// predecessor's state words as fetched when the tile started.  Walks back
+// through aggregates until an inclusive value, a zero decay, or the row's
+// first tile; every wait is bounded.
+__device__ inline float lookback_read(const Params &p, int64_t g, int64_t j, unsigned long long w0,
+                                      unsigned long long w1)
+{
+    const unsigned long long *st = p.states;
     const uint32_t tagA = (p.epoch << 2) | kTagAgg;
     const uint32_t tagP = (p.epoch << 2) | kTagPrefix;
-    if (j == 0 || total.b == 0.f) {
-        // the inclusive value does not depend on anything before the tile
-        ptx::st_relaxed(&st[2 * g], pack_word(tagP, total.a));
-        if (j == 0) return 0.f;
-    } else {
-        ptx::st_relaxed(&st[2 * g + 1], pack_word(tagA, total.b));
-        ptx::st_relaxed(&st[2 * g], pack_word(tagA, total.a));
-    }
     Pair acc{0.f, 1.f};
     int64_t k = g - p.N;
     int64_t left = j;  // predecessors not yet folded in
-    float carry = 0.f;
     uint64_t waited_since = 0;
     uint32_t nap = 32;
     bool fresh = true;  // (w0, w1) hold a probe of tile k
@@ -221,17 +239,11 @@ __device__ inline float lookback(const Params &p, int64_t g, int64_t j, Pair tot
         }
         fresh = false;
         const uint32_t tag = static_cast<uint32_t>(w0 >> 32);
-        if (tag == tagP) {
-            carry = fmaf(acc.b, __uint_as_float(static_cast<uint32_t>(w0)), acc.a);
-            break;
-        }
+        if (tag == tagP) return fmaf(acc.b, __uint_as_float(static_cast<uint32_t>(w0)), acc.a);
         if (tag == tagA && static_cast<uint32_t>(w1 >> 32) == tagA) {
             acc = compose(acc, Pair{__uint_as_float(static_cast<uint32_t>(w0)),
                                     __uint_as_float(static_cast<uint32_t>(w1))});
-            if (acc.b == 0.f || --left == 0) {
-                carry = acc.a;
-                break;
-            }
+            if (acc.b == 0.f || --left == 0) return acc.a;
             k -= p.N;
             waited_since = 0;
             nap = 32;
@@ -242,14 +254,11 @@ __device__ inline float lookback(const Params &p, int64_t g, int64_t j, Pair tot
             waited_since = now;
         } else if (now - waited_since > p.spin_limit_ns) {
             record_error(p, RLSCAN_ERR_TIMEOUT, static_cast<uint32_t>(g));
-            carry = __int_as_float(0x7fc00000);
-            break;
+            return __int_as_float(0x7fc00000);
         }
         __nanosleep(nap);
         if (nap < 512) nap <<= 1;
     }
-    if (total.b != 0.f) ptx::st_relaxed(&st[2 * g], pack_word(tagP, fmaf(total.b, carry, total.a)));
-    return carry;
 }
 
 template <bool FWD>
@@ -287,11 +296,10 @@ __device__ __forceinline__ Pair warp_exclusive_from(Pair inc, int lane)
     return ex;
 }
 
-// Where this thread's ITEMS steps sit in a tile: row, first step, number of
-// valid steps (kv) and the index of the row's boundary step in the range
-// (kb; -1 if none).
+// Where this thread's ITEMS steps sit in a tile: number of valid steps (kv)
+// and the index of the row's boundary step within the range (kb; -1 if
+// none).  `col` is the thread's first column within the tile's row segment.
 struct ThreadSpan {
-    int64_t row, t_first;
     int kv, kb;
 };
 
@@ -299,13 +307,15 @@ template <bool FWD, int ITEMS>
 __device__ __forceinline__ ThreadSpan thread_span(const Params &p, const TileGeo &tg, int rit, int col)
 {
     ThreadSpan sp;
-    sp.row = tg.row0 + rit;
-    sp.t_first = tg.t0 + col;
     const bool row_ok = rit < tg.nrows;
-    const int64_t rem = p.T - sp.t_first;
-    sp.kv = row_ok ? static_cast<int>(rem < 0 ? 0 : (rem > ITEMS ? ITEMS : rem)) : 0;
-    const int64_t d = FWD ? -sp.t_first : (p.T - 1 - sp.t_first);
-    sp.kb = (row_ok && d >= 0 && d < ITEMS) ? static_cast<int>(d) : -1;
+    const int rem = tg.len - col;
+    sp.kv = row_ok ? (rem < 0 ? 0 : (rem > ITEMS ? ITEMS : rem)) : 0;
+    sp.kb = -1;
+    // only a packed tile or a row's first tile in scan order holds the boundary
+    if (row_ok && (p.packed || tg.j == 0)) {
+        const int d = FWD ? -col : (tg.len - 1 - col);
+        if (d >= 0 && d < ITEMS) sp.kb = d;
+    }
     return sp;
 }
 
@@ -314,8 +324,9 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
 {
     constexpr int NIN = E::NIN, NOUT = E::NOUT;
     constexpr int TILE = THREADS * ITEMS, AST = TILE + 8, WARPS = THREADS / 32;
-    constexpr int PRODUCER = THREADS - 32;  // lane 0 of the last warp
+    constexpr int PRODUCER = THREADS - 32;          // lane 0 of the last warp
     constexpr bool FWD = E::FWD;
+    constexpr int PUB_WARP = FWD ? WARPS - 1 : 0;   // warp holding the tile's last element in scan order
     static_assert(STAGES >= 2, "the ring needs two stages");
     static_assert(ITEMS % 4 == 0, "items per thread are moved as float4");
     static_assert(TILE >= kMinTile, "workspace sizing assumes tiles of at least kMinTile");
@@ -324,9 +335,7 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
     __shared__ __align__(8) uint64_t mbar[STAGES];
     __shared__ int64_t tile_ids[STAGES];
     __shared__ TileGeo s_geo[STAGES];
-    __shared__ Pair wexcl[WARPS];
-    __shared__ Pair wagg[WARPS];
-    __shared__ float s_carry;
+    __shared__ Pair wagg[2][WARPS];  // warp aggregates, double-buffered by tile parity
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -352,10 +361,15 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
         }
     };
 
+    ptx::pdl_trigger_dependents();
     if (tid == PRODUCER) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) ptx::mbar_init(&mbar[s], 1);
         ptx::fence_mbar_init();
+    }
+    // nothing global is touched before the previous kernel has completed
+    ptx::pdl_wait_prerequisites();
+    if (tid == PRODUCER) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) fill_slot(s, next_tile());
     }
@@ -369,9 +383,9 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
     // its range; fetched one tile ahead so its latency is hidden.
     auto load_row_scalar = [&](int s) -> float {
         if (!E::ROWSCALAR || p.rowscalar == nullptr || tile_ids[s] >= p.num_tiles) return 0.f;
-        const ThreadSpan sp = thread_span<FWD, ITEMS>(p, s_geo[s], rit, col);
-        if (sp.kb < 0) return 0.f;
-        return __ldg(p.rowscalar + sp.row * p.rowscalar_stride);
+        const TileGeo tg = s_geo[s];
+        if (thread_span<FWD, ITEMS>(p, tg, rit, col).kb < 0) return 0.f;
+        return __ldg(p.rowscalar + (tg.row0 + rit) * p.rowscalar_stride);
     };
     float rsc_next = load_row_scalar(0);
     uint32_t lost_stages = 0, lost_parity = 0;  // waits that timed out (thread 0)
@@ -383,6 +397,7 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
         const TileGeo tg = s_geo[s];
         const float rsc = rsc_next;
         float *stage = smem + s * NIN * AST;
+        const bool chained = !p.packed && tg.j > 0;  // needs its predecessor's value
 
         // the ticket for the refill of this slot, drawn early (its latency
         // overlaps this tile's work)
@@ -390,14 +405,14 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
         if (tid == PRODUCER) refill = next_tile();
         // predecessor state for the look-back, also fetched early
         unsigned long long pw0 = 0, pw1 = 0;
-        if (tid == 0 && !p.packed && tg.j > 0) {
+        if (chained && lane == 0) {
             pw0 = ptx::ld_relaxed(&p.states[2 * (g - p.N)]);
             pw1 = ptx::ld_relaxed(&p.states[2 * (g - p.N) + 1]);
         }
 
         if (tma) {
             const uint32_t parity = static_cast<uint32_t>((it / STAGES) & 1);
-            if (!wait_phase(&mbar[s], parity, p.spin_limit_ns) && tid == 0) {
+            if (!wait_phase(&mbar[s], parity, p.copy_limit_ns) && tid == 0) {
                 lost_stages |= 1u << s;
                 lost_parity = (lost_parity & ~(1u << s)) | (parity << s);
                 record_error(p, RLSCAN_ERR_TIMEOUT, 0x80000000u | static_cast<uint32_t>(s));
@@ -458,27 +473,41 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
         }
         const Pair inc = warp_inclusive<FWD>(agg, lane);
         const Pair ex = warp_exclusive_from<FWD>(inc, lane);
-        if (lane == (FWD ? 31 : 0)) wagg[warp] = inc;
-        __syncthreads();  // every thread has its inputs in registers: the stage is free
+        Pair *wa = wagg[it & 1];
+        if (lane == (FWD ? 31 : 0)) wa[warp] = inc;
+        __syncthreads();  // warp aggregates visible; every input is in registers: the stage is free
 
         if (tid == PRODUCER) fill_slot(s, refill);
         rsc_next = load_row_scalar((it + 1) % STAGES);
 
-        if (warp == 0) {
-            const Pair w = lane < WARPS ? wagg[lane] : Pair{0.f, 1.f};
-            const Pair winc = warp_inclusive<FWD>(w, lane);
-            const Pair wex = warp_exclusive_from<FWD>(winc, lane);
-            if (lane < WARPS) wexcl[lane] = wex;
-            Pair total;
-            total.a = __shfl_sync(0xffffffffu, winc.a, FWD ? 31 : 0);
-            total.b = __shfl_sync(0xffffffffu, winc.b, FWD ? 31 : 0);
-            if (lane == 0) s_carry = p.packed ? 0.f : lookback(p, g, tg.j, total, pw0, pw1);
+        // map entering this warp's range from the warps before it in scan order
+        Pair we{0.f, 1.f};
+        if (FWD) {
+#pragma unroll
+            for (int w2 = 0; w2 < WARPS - 1; ++w2)
+                if (w2 < warp) we = compose(wa[w2], we);
+        } else {
+#pragma unroll
+            for (int w2 = WARPS - 1; w2 > 0; --w2)
+                if (w2 > warp) we = compose(wa[w2], we);
         }
-        __syncthreads();
+        // value entering the tile
+        float carry = 0.f;
+        if (chained || (!p.packed && warp == PUB_WARP)) {
+            if (warp == PUB_WARP && lane == 0)
+                publish_first(p, g, tg.j, compose(wa[PUB_WARP], we));
+            if (chained) {
+                if (lane == 0) carry = lookback_read(p, g, tg.j, pw0, pw1);
+                carry = __shfl_sync(0xffffffffu, carry, 0);
+                if (warp == PUB_WARP && lane == 0) {
+                    const Pair total = compose(wa[PUB_WARP], we);
+                    if (total.b != 0.f) publish_inclusive(p, g, fmaf(total.b, carry, total.a));
+                }
+            }
+        }
 
         // exact value entering this thread's range, then its serial recurrence
-        const Pair we = wexcl[warp];
-        const float x_in = fmaf(ex.b, fmaf(we.b, s_carry, we.a), ex.a);
+        const float x_in = fmaf(ex.b, fmaf(we.b, carry, we.a), ex.a);
         float A[ITEMS];
         {
             float v = x_in;
@@ -501,7 +530,7 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
         else E::template post<ITEMS, true>(x, xn, sp.kb, p, rsc, A, x_in, keep, o);
 
         if (sp.kv > 0) {
-            const int64_t off = sp.row * p.rs + sp.t_first;
+            const int64_t off = (tg.row0 + rit) * p.rs + tg.t0 + col;
             if (tma) {
 #pragma unroll
                 for (int q = 0; q < NOUT; ++q) {
@@ -527,7 +556,7 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
     // bounded wait before the shared memory is released.
     if (lost_stages != 0 && tid == 0) {
         for (int s = 0; s < STAGES; ++s)
-            if ((lost_stages >> s) & 1u) wait_phase(&mbar[s], (lost_parity >> s) & 1u, p.spin_limit_ns);
+            if ((lost_stages >> s) & 1u) wait_phase(&mbar[s], (lost_parity >> s) & 1u, p.copy_limit_ns);
     }
     if (p.dynamic) {
         __syncthreads();  // every ticket this CTA will draw has been drawn
