@@ -99,7 +99,7 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
                                      static_cast<int>(smem)) != cudaSuccess)
                 return RLSCAN_ERR_CUDA;
             int occ = 0, sms = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, S::THREADS, smem) != cudaSuccess ||
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, block_threads<S::THREADS>(), smem) != cudaSuccess ||
                 cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
                 return RLSCAN_ERR_CUDA;
             blocks_per_sm[dev] = occ > 0 ? occ : 1;
@@ -110,7 +110,7 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
     const int64_t grid = p.num_tiles < slots ? p.num_tiles : slots;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(S::THREADS);
+    cfg.blockDim = dim3(block_threads<S::THREADS>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

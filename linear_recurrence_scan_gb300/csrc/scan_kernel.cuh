@@ -39,12 +39,14 @@
 //  * Launched with programmatic stream serialization: the next kernel may be
 //    scheduled while this one drains, and this one touches global memory
 //    only after griddepcontrol.wait (previous kernel complete and visible).
-//  * Roles: the last warp's lane 0 draws tickets and issues the copies.
-//    One CTA barrier per tile: after it each warp composes the aggregates of
-//    the warps before it (double-buffered in shared memory) and, for a
-//    chained tile, its lane 0 reads the predecessor states itself; the warp
-//    holding the tile's last element in scan order publishes.  A stage is
-//    refilled as soon as every thread has read it into registers.
+//  * Roles (warp specialisation): lane 0 of an extra producer warp draws
+//    tickets and issues the copies, gated per stage by an "empty" mbarrier
+//    that the compute warps arrive on; the compute warps wait on the stage's
+//    "full" mbarrier.  The compute warps share one named barrier per tile:
+//    after it each warp composes the aggregates of the warps before it
+//    (double-buffered in shared memory) and, for a chained tile, its lane 0
+//    reads the predecessor states itself; the warp holding the tile's last
+//    element in scan order publishes.
 //  * Every wait (mbarrier phase, predecessor state) is bounded in time; on
 //    expiry the kernel records RLSCAN_ERR_TIMEOUT in the workspace, uses NaN
 //    for the missing value and carries on, so it always terminates.
@@ -160,11 +162,11 @@ __device__ void issue_tile_copies(const Params &p, const TileGeo &tg, float *sta
 }
 
 // Element-wise cooperative load of one tile (any alignment), same layout.
-template <class E, int THREADS, int TILE, int AST>
-__device__ void load_tile_elementwise(const Params &p, const TileGeo &tg, float *stage)
+template <class E, int TILE, int AST>
+__device__ void load_tile_elementwise(const Params &p, const TileGeo &tg, float *stage, int nthreads)
 {
     const int total = tg.nrows * p.C;
-    for (int e = threadIdx.x; e < total; e += THREADS) {
+    for (int e = threadIdx.x; e < total; e += nthreads) {
         const int i = e / p.C;
         const int c = e - i * p.C;
         if (c < tg.len) {
@@ -319,20 +321,31 @@ __device__ __forceinline__ ThreadSpan thread_span(const Params &p, const TileGeo
     return sp;
 }
 
+// Block = THREADS compute threads + one producer warp.
+template <int THREADS>
+constexpr int block_threads() { return THREADS + 32; }
+#ifndef RLSCAN_MIN_BLOCKS
+#define RLSCAN_MIN_BLOCKS 3
+#endif
+template <int THREADS>
+constexpr int min_blocks() { return RLSCAN_MIN_BLOCKS; }
+
 template <class E, int THREADS, int ITEMS, int STAGES>
-__global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ Params p)
+__global__ void __launch_bounds__(block_threads<THREADS>(), min_blocks<THREADS>())
+scan_kernel(const __grid_constant__ Params p)
 {
     constexpr int NIN = E::NIN, NOUT = E::NOUT;
     constexpr int TILE = THREADS * ITEMS, AST = TILE + 8, WARPS = THREADS / 32;
-    constexpr int PRODUCER = THREADS - 32;          // lane 0 of the last warp
     constexpr bool FWD = E::FWD;
     constexpr int PUB_WARP = FWD ? WARPS - 1 : 0;   // warp holding the tile's last element in scan order
+    constexpr int COMPUTE_BAR = 1;                  // named barrier of the compute warps
     static_assert(STAGES >= 2, "the ring needs two stages");
     static_assert(ITEMS % 4 == 0, "items per thread are moved as float4");
     static_assert(TILE >= kMinTile, "workspace sizing assumes tiles of at least kMinTile");
 
     extern __shared__ __align__(128) float smem[];
-    __shared__ __align__(8) uint64_t mbar[STAGES];
+    __shared__ __align__(8) uint64_t full_bar[STAGES];   // stage data (and tile id) ready
+    __shared__ __align__(8) uint64_t empty_bar[STAGES];  // every compute warp is done reading it
     __shared__ int64_t tile_ids[STAGES];
     __shared__ TileGeo s_geo[STAGES];
     __shared__ Pair wagg[2][WARPS];  // warp aggregates, double-buffered by tile parity
@@ -341,68 +354,89 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
     const int lane = tid & 31, warp = tid >> 5;
     const bool tma = p.tma != 0;
 
-    // Tile sequence: an atomic ticket when tiles depend on each other, a
-    // static stride otherwise.  Only the producer thread draws.
-    int64_t static_next = blockIdx.x;
-    auto next_tile = [&]() -> int64_t {
-        if (p.dynamic)
-            return static_cast<int64_t>(atomicAdd(reinterpret_cast<unsigned long long *>(p.hdr), 1ull));
-        const int64_t t = static_next;
-        static_next += gridDim.x;
-        return t;
-    };
-    // producer: record tile g in ring slot s and start its copies
-    auto fill_slot = [&](int s, int64_t g) {
-        tile_ids[s] = g;
-        if (g < p.num_tiles) {
-            const TileGeo tg = decode_tile<FWD, TILE>(p, g);
-            s_geo[s] = tg;
-            if (tma) issue_tile_copies<E, TILE, AST>(p, tg, smem + s * NIN * AST, &mbar[s]);
-        }
-    };
-
     ptx::pdl_trigger_dependents();
-    if (tid == PRODUCER) {
+    if (tid == 0) {
 #pragma unroll
-        for (int s = 0; s < STAGES; ++s) ptx::mbar_init(&mbar[s], 1);
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(&full_bar[s], 1);
+            ptx::mbar_init(&empty_bar[s], WARPS);
+        }
         ptx::fence_mbar_init();
     }
     // nothing global is touched before the previous kernel has completed
     ptx::pdl_wait_prerequisites();
-    if (tid == PRODUCER) {
-#pragma unroll
-        for (int s = 0; s < STAGES; ++s) fill_slot(s, next_tile());
-    }
     __syncthreads();
+
+    if (warp == WARPS) {
+        // Producer (lane 0 of the extra warp): for ring slot s of iteration
+        // it, wait until every compute warp has released the slot (iteration
+        // it - STAGES), draw the next ticket, record the tile and start its
+        // copies.  An exhausted ticket completes the slot's phase
+        // without data, which tells the compute warps to stop.  Tickets are
+        // drawn just before their copies can start, so tiles are processed
+        // in close to ticket order.
+        if (lane == 0) {
+            int64_t static_next = blockIdx.x;
+            for (int it = 0;; ++it) {
+                const int s = it % STAGES;
+                if (it >= STAGES &&
+                    !wait_phase(&empty_bar[s], static_cast<uint32_t>((it / STAGES - 1) & 1),
+                                p.spin_limit_ns + p.copy_limit_ns))
+                    record_error(p, RLSCAN_ERR_TIMEOUT, 0x40000000u | static_cast<uint32_t>(s));
+                int64_t g;
+                if (p.dynamic) {
+                    g = static_cast<int64_t>(atomicAdd(reinterpret_cast<unsigned long long *>(p.hdr), 1ull));
+                } else {
+                    g = static_next;
+                    static_next += gridDim.x;
+                }
+                tile_ids[s] = g;
+                if (g >= p.num_tiles) {
+                    ptx::mbar_arrive(&full_bar[s]);
+                    break;
+                }
+                const TileGeo tg = decode_tile<FWD, TILE>(p, g);
+                s_geo[s] = tg;
+                if (tma) issue_tile_copies<E, TILE, AST>(p, tg, smem + s * NIN * AST, &full_bar[s]);
+                else ptx::mbar_arrive(&full_bar[s]);
+            }
+        }
+    } else {
 
     const int li = tid * ITEMS;
     const int rit = p.packed ? li / p.C : 0;
     const int col = p.packed ? li - rit * p.C : li;
 
     // Row scalar of this thread's row when the row's boundary step falls in
-    // its range; fetched one tile ahead so its latency is hidden.
+    // its range.  Fetched one tile ahead when that tile is already known
+    // (its slot's phase has completed), so the latency is hidden.
     auto load_row_scalar = [&](int s) -> float {
-        if (!E::ROWSCALAR || p.rowscalar == nullptr || tile_ids[s] >= p.num_tiles) return 0.f;
+        if (tile_ids[s] >= p.num_tiles) return 0.f;
         const TileGeo tg = s_geo[s];
         if (thread_span<FWD, ITEMS>(p, tg, rit, col).kb < 0) return 0.f;
         return __ldg(p.rowscalar + (tg.row0 + rit) * p.rowscalar_stride);
     };
-    float rsc_next = load_row_scalar(0);
+    constexpr bool kRowScalar = E::ROWSCALAR;
+    const bool use_rsc = kRowScalar && p.rowscalar != nullptr;
+    float rsc_next = 0.f;
+    bool rsc_ready = false;
     uint32_t lost_stages = 0, lost_parity = 0;  // waits that timed out (thread 0)
 
     for (int it = 0;; ++it) {
         const int s = it % STAGES;
+        const uint32_t parity = static_cast<uint32_t>((it / STAGES) & 1);
+        if (!wait_phase(&full_bar[s], parity, p.copy_limit_ns) && tid == 0) {
+            lost_stages |= 1u << s;
+            lost_parity = (lost_parity & ~(1u << s)) | (parity << s);
+            record_error(p, RLSCAN_ERR_TIMEOUT, 0x80000000u | static_cast<uint32_t>(s));
+        }
         const int64_t g = tile_ids[s];
         if (g >= p.num_tiles) break;
         const TileGeo tg = s_geo[s];
-        const float rsc = rsc_next;
+        const float rsc = !use_rsc ? 0.f : (rsc_ready ? rsc_next : load_row_scalar(s));
         float *stage = smem + s * NIN * AST;
         const bool chained = !p.packed && tg.j > 0;  // needs its predecessor's value
 
-        // the ticket for the refill of this slot, drawn early (its latency
-        // overlaps this tile's work)
-        int64_t refill = 0;
-        if (tid == PRODUCER) refill = next_tile();
         // predecessor state for the look-back, also fetched early
         unsigned long long pw0 = 0, pw1 = 0;
         if (chained && lane == 0) {
@@ -410,16 +444,9 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
             pw1 = ptx::ld_relaxed(&p.states[2 * (g - p.N) + 1]);
         }
 
-        if (tma) {
-            const uint32_t parity = static_cast<uint32_t>((it / STAGES) & 1);
-            if (!wait_phase(&mbar[s], parity, p.copy_limit_ns) && tid == 0) {
-                lost_stages |= 1u << s;
-                lost_parity = (lost_parity & ~(1u << s)) | (parity << s);
-                record_error(p, RLSCAN_ERR_TIMEOUT, 0x80000000u | static_cast<uint32_t>(s));
-            }
-        } else {
-            load_tile_elementwise<E, THREADS, TILE, AST>(p, tg, stage);
-            __syncthreads();
+        if (!tma) {
+            load_tile_elementwise<E, TILE, AST>(p, tg, stage, THREADS);
+            ptx::named_barrier(COMPUTE_BAR, THREADS);
         }
 
         const ThreadSpan sp = thread_span<FWD, ITEMS>(p, tg, rit, col);
@@ -475,10 +502,14 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
         const Pair ex = warp_exclusive_from<FWD>(inc, lane);
         Pair *wa = wagg[it & 1];
         if (lane == (FWD ? 31 : 0)) wa[warp] = inc;
-        __syncthreads();  // warp aggregates visible; every input is in registers: the stage is free
+        ptx::named_barrier(COMPUTE_BAR, THREADS);  // warp aggregates visible
+        if (lane == 0) ptx::mbar_arrive(&empty_bar[s]);  // every input is in registers: the slot is free
 
-        if (tid == PRODUCER) fill_slot(s, refill);
-        rsc_next = load_row_scalar((it + 1) % STAGES);
+        if (use_rsc) {
+            const int s1 = (it + 1) % STAGES;
+            rsc_ready = ptx::mbar_test_wait(&full_bar[s1], static_cast<uint32_t>(((it + 1) / STAGES) & 1));
+            if (rsc_ready) rsc_next = load_row_scalar(s1);
+        }
 
         // map entering this warp's range from the warps before it in scan order
         Pair we{0.f, 1.f};
@@ -556,11 +587,12 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ P
     // bounded wait before the shared memory is released.
     if (lost_stages != 0 && tid == 0) {
         for (int s = 0; s < STAGES; ++s)
-            if ((lost_stages >> s) & 1u) wait_phase(&mbar[s], (lost_parity >> s) & 1u, p.copy_limit_ns);
+            if ((lost_stages >> s) & 1u) wait_phase(&full_bar[s], (lost_parity >> s) & 1u, p.copy_limit_ns);
     }
+    }  // compute warps
     if (p.dynamic) {
         __syncthreads();  // every ticket this CTA will draw has been drawn
-        if (tid == PRODUCER) {
+        if (tid == THREADS) {
             __threadfence();
             const uint32_t done = atomicAdd(&p.hdr[kHdrExit], 1u);
             if (done == gridDim.x - 1) {  // last CTA out: re-arm the ticket for the next call
