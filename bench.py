@@ -49,7 +49,10 @@ def _cfg_workloads():
         "gae_returns_4096x1024": dict(
             desc="GAE + discounted returns + TD(lambda) returns, last_value bootstrap, no truncations",
             N=4096, T=1024, gen=lambda N, T: synthetic.config_batch(1, N=N, T=T),
-            estimators=[("gae", 16, c1), ("discounted_returns", 12, c1), ("lambda_returns", 16, c1)]),
+            estimators=[("gae", 16, c1), ("discounted_returns", 12, c1), ("lambda_returns", 16, c1)],
+            # the step's three outputs from one kernel: r, v, term read once,
+            # advantages, lambda-returns, discounted returns written
+            fused=("gae_returns", 24, c1)),
         "gae_8x128": dict(
             desc="GAE with truncations and 2-D bootstrap", N=8, T=128,
             gen=lambda N, T: synthetic.config_batch(0, N=N, T=T),
@@ -95,6 +98,7 @@ IO = {
                 [], 2),
     "eligibility_traces": (["gradients", "trace_dones"], [], 1),
     "episodic_prefix_sum": (["inputs", "prefix_dones"], [], 1),
+    "gae_returns": (["rewards", "values", "terminateds"], ["last_value"], 3),
 }
 
 
@@ -118,12 +122,14 @@ def _measured_peak():
 
 
 def _ncu_traffic(kernel, workload):
-    """DRAM bytes per launch recorded under profiles/ for this kernel and
-    workload, if taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch that an ncu capture recorded for this kernel and
+    workload (profiles/traffic.md, a fenced JSON block), if the capture was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
     try:
         with open(path) as f:
-            rec = json.load(f)
+            text = f.read()
+        rec = json.loads(text.split("```json", 1)[1].split("```", 1)[0])
     except Exception:
         return None
     e = rec.get(f"{kernel}@{workload}")
@@ -239,6 +245,11 @@ def _launcher(name, c, bufs, outs, N, T, ws, wsn, stream):
     if name == "episodic_prefix_sum":
         return lambda: lib.rlscan_episodic_prefix_sum(b["inputs"], b["prefix_dones"], None, 1, N,
                                                       T, T, o[0], ws, wsn, stream)
+    if name == "gae_returns":
+        return lambda: lib.rlscan_gae_returns(b["rewards"], b["values"], b["terminateds"], None,
+                                              None, b["last_value"], N, T, T, g,
+                                              float(c["lambda_"]), o[0], o[1], o[2], ws, wsn,
+                                              stream)
     raise KeyError(name)
 
 
@@ -271,6 +282,9 @@ def _public_call(name, c, t):
         return [Lb.compute_eligibility_traces(t["gradients"], t["trace_dones"], g, c["lambda_"])]
     if name == "episodic_prefix_sum":
         return [Lb.compute_episodic_prefix_sum(t["inputs"], t["prefix_dones"], None, "starts_at")]
+    if name == "gae_returns":
+        return list(Lb.compute_gae_and_returns(t["rewards"], t["values"], t["terminateds"], None, g,
+                                               c["lambda_"], None, t["last_value"]))
     raise KeyError(name)
 
 
@@ -284,10 +298,14 @@ def run_ours(args, wl_name, rank, world, local_rank):
     N, T = wl["N"], wl["T"]
     batch = wl["gen"](N, T)
     names = [e[0] for e in wl["estimators"]]
-    need_in = sorted({k for n in names for k in IO[n][0] + IO[n][1]})
+    fused = wl.get("fused")
+    # the step: one fused kernel when the workload has one, else each estimator
+    step_kernels = [fused] if fused else list(wl["estimators"])
+    all_kernels = step_kernels + ([e for e in wl["estimators"]] if fused else [])
+    need_in = sorted({k for (n, _, _) in all_kernels for k in IO[n][0] + IO[n][1]})
     host = {k: batch[k] for k in need_in}
     set_bytes = sum(v.nbytes for v in host.values()) + sum(
-        IO[n][2] * N * T * 4 for n in names)
+        IO[n][2] * N * T * 4 for (n, _, _) in step_kernels)
     n_sets = 1 if set_bytes > 4 * L2_BYTES else min(16, max(2, math.ceil(4 * L2_BYTES / set_bytes)))
     stream = torch.cuda.current_stream(dev)
     sh = ctypes.c_void_p(stream.cuda_stream)
@@ -301,67 +319,78 @@ def run_ours(args, wl_name, rank, world, local_rank):
     sets = []
     for _ in range(n_sets):
         bufs = {k: torch.from_numpy(v).to(dev) for k, v in host.items()}
-        calls = []
-        for (name, bps, c) in wl["estimators"]:
+        calls = {}
+        for (name, bps, c) in all_kernels:
             outs = [torch.empty((N, T), dtype=torch.float32, device=dev) for _ in range(IO[name][2])]
-            calls.append((name, _launcher(name, c, bufs, outs, N, T, ws, wsn, sh), outs))
-        sets.append((bufs, calls))
+            calls[name] = _launcher(name, c, bufs, outs, N, T, ws, wsn, sh)
+        sets.append(calls)
     torch.cuda.synchronize()
 
-    def step(i, evs=None):
-        _, calls = sets[i % n_sets]
-        for j, (name, fn, _) in enumerate(calls):
+    def run(kernels, i, evs=None):
+        calls = sets[i % n_sets]
+        for j, (name, _, _) in enumerate(kernels):
             if evs is not None:
                 evs[j][0].record(stream)
-            st = fn()
+            st = calls[name]()
             if st != 0:
                 raise _native.RlscanError(st, name)
             if evs is not None:
                 evs[j][1].record(stream)
 
+    def timed(kernels, K, offset):
+        """K steps of `kernels`, one event pair per kernel launch, plus one
+        pair around the whole region; barrier + synchronize on both sides."""
+        kev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in kernels]
+               for _ in range(K)]
+        t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        t0e.record(stream)
+        for i in range(K):
+            run(kernels, offset + i, kev[i])
+        t1e.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        per = {n: [kev[i][j][0].elapsed_time(kev[i][j][1]) for i in range(K)]
+               for j, (n, _, _) in enumerate(kernels)}
+        return t0e.elapsed_time(t1e) / K, per, wall
+
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
     for i in range(args.warmup):
-        step(i)
+        run(step_kernels, i)
     torch.cuda.synchronize()
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
     K = args.steps
-    kev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in names] for _ in range(K)]
-    t0e = torch.cuda.Event(enable_timing=True)
-    t1e = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    t0e.record(stream)
-    for i in range(K):
-        step(args.warmup + i, kev[i])
-    t1e.record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    if dist is not None:
-        dist.barrier()
-    total_ms = t0e.elapsed_time(t1e)
-    per_kernel = {n: [kev[i][j][0].elapsed_time(kev[i][j][1]) for i in range(K)]
-                  for j, n in enumerate(names)}
-    ms_step = max_over_ranks(total_ms / K)
+    ms_step, per_kernel, wall = timed(step_kernels, K, args.warmup)
+    ms_step = max_over_ranks(ms_step)
+    per_est_times = per_kernel
+    if fused:  # the estimators one kernel each, for the per-estimator figures
+        for i in range(args.warmup):
+            run(wl["estimators"], i)
+        _, per_est_times, _ = timed(wl["estimators"], K, args.warmup)
 
-    # e2e through the public API: pinned host inputs -> device, three calls,
-    # results back to pinned host memory, every step
-    pinned = {k: torch.from_numpy(v).pin_memory() for k, v in host.items()}
-    dbufs = {k: torch.empty(v.shape, dtype=torch.float32, device=dev) for k, v in host.items()}
+    # e2e through the public API: pinned host inputs -> device, the step's
+    # call(s), results back to pinned host memory, every step
+    e2e_in = sorted({k for (n, _, _) in step_kernels for k in IO[n][0] + IO[n][1]})
+    pinned = {k: torch.from_numpy(host[k]).pin_memory() for k in e2e_in}
+    dbufs = {k: torch.empty(v.shape, dtype=torch.float32, device=dev) for k, v in pinned.items()}
     out_host = [torch.empty((N, T), dtype=torch.float32).pin_memory()
-                for n in names for _ in range(IO[n][2])]
-    h2d = sum(v.nbytes for v in host.values())
+                for (n, _, _) in step_kernels for _ in range(IO[n][2])]
+    h2d = sum(v.numel() * 4 for v in pinned.values())
     d2h = sum(o.numel() * 4 for o in out_host)
 
     def e2e_step():
         for k in pinned:
             dbufs[k].copy_(pinned[k], non_blocking=True)
         outs = []
-        for (name, _, c) in wl["estimators"]:
+        for (name, _, c) in step_kernels:
             outs += _public_call(name, c, dbufs)
         for o, hbuf in zip(outs, out_host):
             hbuf.copy_(o, non_blocking=True)
@@ -377,20 +406,19 @@ def run_ours(args, wl_name, rank, world, local_rank):
 
     steps_per_call = N * T
     peak, peak_kind = _measured_peak()
-    per_est = {}
-    dominant, dom_total = None, -1.0
-    for (name, bps, _) in wl["estimators"]:
-        ts = np.array(per_kernel[name])
+
+    def kernel_stats(name, bps, ts):
+        ts = np.array(ts)
         avg_us = float(ts.mean() * 1e3)
         gbs = bps * steps_per_call / (avg_us * 1e-6) / 1e9
-        per_est[name] = {"us_mean": round(avg_us, 2), "us_median": round(float(np.median(ts)) * 1e3, 2),
-                         "env_steps_per_s": steps_per_call / (avg_us * 1e-6),
-                         "bytes_per_env_step": bps, "gb_per_s": round(gbs, 1),
-                         "frac_of_measured_hbm": round(gbs / peak, 4),
-                         "frac_of_nominal_8tbs": round(gbs / 8000.0, 4)}
-        if ts.sum() > dom_total:
-            dominant, dom_total = name, float(ts.sum())
-    d = per_est[dominant]
+        return {"us_mean": round(avg_us, 2), "us_median": round(float(np.median(ts)) * 1e3, 2),
+                "env_steps_per_s": steps_per_call / (avg_us * 1e-6), "bytes_per_env_step": bps,
+                "gb_per_s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
+                "frac_of_nominal_8tbs": round(gbs / 8000.0, 4)}
+    per_est = {n: kernel_stats(n, bps, per_est_times[n]) for (n, bps, _) in wl["estimators"]}
+    step_stats = {n: kernel_stats(n, bps, per_kernel[n]) for (n, bps, _) in step_kernels}
+    dominant = max(step_kernels, key=lambda e: sum(per_kernel[e[0]]))[0]
+    d = step_stats[dominant]
     result = {
         "metric": "env-steps/sec and achieved HBM GB/s (% of GB300 peak) per estimator, 1 GPU",
         "value": world * steps_per_call / (ms_step * 1e-3),
@@ -400,9 +428,12 @@ def run_ours(args, wl_name, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl_name, "description": wl["desc"], "num_envs": N, "seq_len": T,
-                   "estimators": names, "parallelism": f"rows, {world} independent batch(es)",
+                   "estimators": names,
+                   "step_kernels": [n for (n, _, _) in step_kernels],
+                   "parallelism": f"rows, {world} independent batch(es)",
                    "l2": f"{n_sets} rotating input sets of {set_bytes / 1e6:.0f} MB "
                          f"({n_sets * set_bytes / 1e6:.0f} MB > 129 MB L2)"},
+        "step": step_stats,
         "per_estimator": per_est,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": d["gb_per_s"], "peak": peak,
                      "peak_source": peak_kind, "unit": "GB/s", "frac": d["frac_of_measured_hbm"],
@@ -411,7 +442,7 @@ def run_ours(args, wl_name, rank, world, local_rank):
         "e2e": {"value": world * steps_per_call / e2e_s, "unit": "env-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "pinned host -> device copies, public compute_* API, results -> pinned host"},
-        "gpu_launches": K * len(names),
+        "gpu_launches": K * len(step_kernels),
         "wall_s_timed": round(wall, 4),
         "clocks": clocks,
     }

@@ -132,6 +132,35 @@ rlscan_status rlscan_gae(const float *rewards, const float *values, const float 
                          void *ws, size_t ws_bytes, rlscan_stream_t stream);
 
 /*
+ * GAE, lambda-returns and discounted returns from one read of the buffer.
+ * The rl-triton paper's planned fused post-scan extensions (Sec. 9.3); the
+ * returns tutorial's identity that lambda-returns are the GAE targets
+ * (Sec. 6); API reference compute_gae / compute_lambda_returns /
+ * compute_discounted_returns for each output.
+ *   advantages         = rlscan_gae on the same arguments
+ *   lambda_returns     = advantages + values: TD(lambda) returns whose
+ *                        V(s_{t+1}) is the successor value rlscan_gae uses
+ *                        (values[t+1]; the bootstrap at truncated steps and
+ *                        at the window end), i.e. rlscan_lambda_returns with
+ *                        next_values built that way
+ *   discounted_returns = rlscan_discounted_returns on the same rewards,
+ *                        flags and bootstrap (carry bs_{T-1})
+ * One kernel runs both recurrences (beta = gamma lambda (1 - done) and
+ * gamma (1 - done)) over a single pass of the inputs.
+ * Inputs : as rlscan_gae.
+ * Outputs: advantages, lambda_returns, discounted_returns [N,T], each
+ *          nullable, at least one non-NULL.
+ * Errors : as rlscan_gae; RLSCAN_ERR_NULL when every output is NULL.
+ */
+rlscan_status rlscan_gae_returns(const float *rewards, const float *values,
+                                 const float *terminateds, const float *truncateds,
+                                 const float *bootstrap_values, const float *last_value,
+                                 int64_t N, int64_t T, int64_t row_stride, float gamma,
+                                 float lambda, float *advantages, float *lambda_returns,
+                                 float *discounted_returns, void *ws, size_t ws_bytes,
+                                 rlscan_stream_t stream);
+
+/*
  * GAE without any device allocation, for callers that cannot allocate.
  * The rl-triton pages have no counterpart: this is a deployment variant of
  * rlscan_gae.  Some callers may not allocate device memory when they call
@@ -142,8 +171,8 @@ rlscan_status rlscan_gae(const float *rewards, const float *values, const float 
  * cross-block carries; this entry point takes it from a 4 MiB buffer built
  * into the library (each GPU that loads the library keeps it until the
  * process exits) instead of a caller workspace.  That covers shapes with
- * rlscan_workspace_bytes(N, T) <= 4 MiB, i.e. N * ceil(T / 1024) <= 262140
- * (e.g. 64 rows of 4M steps); larger shapes return RLSCAN_ERR_SCRATCH_LIMIT
+ * rlscan_workspace_bytes(N, T) <= 4 MiB, i.e. N * ceil(T / 1024) <= 131070
+ * (e.g. 32 rows of 4M steps); larger shapes return RLSCAN_ERR_SCRATCH_LIMIT
  * before any device work.  Same arguments and results as rlscan_gae, minus
  * the workspace.  The first call on a device looks up the buffer's address
  * and zeroes it on `stream`; make that first call before any stream

@@ -47,6 +47,7 @@ SIGNATURES = {
     "rlscan_workspace_status": ([_P, _SZ, _P], _I),
     "rlscan_gae": ([_P] * 6 + [_I64] * 3 + [_F, _F, _P, _P, _SZ, _P], _I),
     "rlscan_gae_noalloc": ([_P] * 6 + [_I64] * 3 + [_F, _F, _P, _P], _I),
+    "rlscan_gae_returns": ([_P] * 6 + [_I64] * 3 + [_F, _F, _P, _P, _P, _P, _SZ, _P], _I),
     "rlscan_vtrace": ([_P] * 8 + [_I64] * 3 + [_F, _F, _F, _P, _P, _P, _SZ, _P], _I),
     "rlscan_retrace": ([_P] * 7 + [_I64] * 3 + [_F] * 4 + [_P, _P, _P, _SZ, _P], _I),
     "rlscan_lambda_returns": ([_P] * 6 + [_I64] * 3 + [_F, _F, _P, _P, _SZ, _P], _I),

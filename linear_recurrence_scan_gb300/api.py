@@ -14,7 +14,7 @@ import torch
 from . import _native
 
 __all__ = [
-    "compute_gae", "compute_vtrace", "compute_retrace_from_probs", "compute_lambda_returns",
+    "compute_gae", "compute_gae_and_returns", "compute_vtrace", "compute_retrace_from_probs", "compute_lambda_returns",
     "compute_discounted_returns", "compute_eligibility_traces", "compute_episodic_prefix_sum",
     "linear_scan", "workspace_status",
 ]
@@ -162,6 +162,36 @@ def compute_gae(rewards, values, terminateds, truncateds=None, gamma=0.99, lambd
         c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma), float(lambda_),
         _vp(out), ws, wsn, s), "rlscan_gae")
     return out
+
+
+def compute_gae_and_returns(rewards, values, terminateds, truncateds=None, gamma=0.99,
+                            lambda_=0.95, bootstrap_values=None, last_value=None,
+                            outputs=("advantages", "lambda_returns", "discounted_returns")):
+    """GAE advantages, lambda-returns (= advantages + values) and discounted
+    returns from one pass over the inputs (one fused kernel).  ``outputs``
+    selects which are produced; returns them as a tuple in that order."""
+    known = ("advantages", "lambda_returns", "discounted_returns")
+    if not outputs or any(o not in known for o in outputs):
+        raise ValueError(f"outputs must be a non-empty subset of {known}")
+    c = _Call("rewards", rewards)
+    c.mat("values", values)
+    c.mat("terminateds", terminateds)
+    c.mat("truncateds", truncateds, False)
+    c.mat("bootstrap_values", bootstrap_values, False)
+    c.vec("last_value", last_value)
+    if last_value is not None and bootstrap_values is not None:
+        raise ValueError("pass either last_value or bootstrap_values, not both")
+    if last_value is not None and truncateds is not None:
+        raise ValueError("last_value cannot be combined with truncateds; use bootstrap_values")
+    outs = c.finish(len(outputs))
+    by_name = dict(zip(outputs, outs))
+    ws, wsn, s = _ws_for(c)
+    _native.check(_native.lib().rlscan_gae_returns(
+        c.m("rewards"), c.m("values"), c.m("terminateds"), c.m("truncateds"),
+        c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma), float(lambda_),
+        _vp(by_name.get("advantages")), _vp(by_name.get("lambda_returns")),
+        _vp(by_name.get("discounted_returns")), ws, wsn, s), "rlscan_gae_returns")
+    return tuple(outs)
 
 
 def compute_vtrace(log_pi_target, log_pi_behavior, values, rewards, terminateds, truncateds=None,

@@ -10,6 +10,8 @@
 //
 // Interface (all static, I = items per thread):
 //   NIN, NOUT       number of [N,T] inputs and outputs
+//   K               affine recurrences solved per step (1, or 2 for the
+//                   fused GAE + returns estimator)
 //   FWD             true for forward-in-time recurrences
 //   HALO            bit j set: input j is also read one step outside the
 //                   thread's range (t+1 backward, t-1 forward)
@@ -21,12 +23,12 @@
 //       inputs); EDGE: the row's boundary step (t = T-1 backward, t = 0
 //       forward) is element kb of the range (otherwise kb is ignored and the
 //       boundary tests compile away); rsc = this row's scalar (only
-//       meaningful when EDGE).
-//   boundary(x, k, rsc, p)
-//       value folded in at the row boundary element k: A_T (backward) or
-//       A_{-1} (forward); the kernel sets a_k += b_k * value, b_k = 0.
+//       meaningful when EDGE).  Writes a[s][k], b[s][k] for each scan s < K.
+//   boundary(x, k, rsc, p, bv)
+//       values folded in at the row boundary element k, one per scan: A_T
+//       (backward) or A_{-1} (forward); the kernel sets a += b * bv, b = 0.
 //   post<I, EDGE>(x, xn, kb, p, rsc, A, A_after, keep, o)
-//       A[k] = scan result at the k-th step; A_after = result at the step
+//       A[s][k] = scan s at the k-th step; A_after[s] = scan s at the step
 //       after the range (backward only; used for successor targets).
 #pragma once
 
@@ -46,6 +48,7 @@ template <bool TRUNC, bool BS2D>
 struct GAE {
     static_assert(TRUNC || !BS2D, "2-D bootstrap is read only with truncation flags");
     static constexpr int NIN = 3 + TRUNC + BS2D, NOUT = 1;
+    static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = false, ROWSCALAR = !BS2D;
     static constexpr unsigned HALO = 1u << 1;
     static constexpr int TR = 3, BS = 3 + TRUNC;
@@ -53,7 +56,7 @@ struct GAE {
 
     template <int I, bool EDGE>
     __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
-                                  const Params &p, float rsc, float (&a)[I], float (&b)[I], Keep<I> &)
+                                  const Params &p, float rsc, float (&a)[K][I], float (&b)[K][I], Keep<I> &)
     {
         const float g = p.c0, gl = p.c0 * p.c1;
 #pragma unroll
@@ -73,18 +76,18 @@ struct GAE {
                 vn = last ? rsc : vnext;
                 done = term;
             }
-            a[k] = fmaf(g * (1.f - term), vn, x[0][k]) - x[1][k];
-            b[k] = gl * (1.f - done);
+            a[0][k] = fmaf(g * (1.f - term), vn, x[0][k]) - x[1][k];
+            b[0][k] = gl * (1.f - done);
         }
     }
     template <int I>
-    __device__ static float boundary(const float (&)[NIN][I], int, float, const Params &) { return 0.f; }
+    __device__ static void boundary(const float (&)[NIN][I], int, float, const Params &, float (&bv)[K]) { bv[0] = 0.f; }
     template <int I, bool EDGE>
     __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int, const Params &,
-                                float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
+                                float, const float (&A)[K][I], const float (&)[K], const Keep<I> &, float (&o)[NOUT][I])
     {
 #pragma unroll
-        for (int k = 0; k < I; ++k) o[0][k] = A[k];
+        for (int k = 0; k < I; ++k) o[0][k] = A[0][k];
     }
 };
 
@@ -98,6 +101,7 @@ template <bool TRUNC, bool BS2D>
 struct VTrace {
     static_assert(TRUNC || !BS2D, "2-D bootstrap is read only with truncation flags");
     static constexpr int NIN = 5 + TRUNC + BS2D, NOUT = 2;
+    static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = false, ROWSCALAR = !BS2D;
     static constexpr unsigned HALO = 1u << 2;
     static constexpr int TR = 5, BS = 5 + TRUNC;
@@ -119,7 +123,7 @@ struct VTrace {
 
     template <int I, bool EDGE>
     __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
-                                  const Params &p, float rsc, float (&a)[I], float (&b)[I], Keep<I> &keep)
+                                  const Params &p, float rsc, float (&a)[K][I], float (&b)[K][I], Keep<I> &keep)
     {
         const float g = p.c0;
 #pragma unroll
@@ -132,26 +136,26 @@ struct VTrace {
             float done;
             if constexpr (TRUNC) done = done_of(term, x[TR][k]);
             else done = term;
-            a[k] = rho * (fmaf(g * (1.f - term), vn, x[3][k]) - x[2][k]);
-            b[k] = g * c * (1.f - done);
+            a[0][k] = rho * (fmaf(g * (1.f - term), vn, x[3][k]) - x[2][k]);
+            b[0][k] = g * c * (1.f - done);
             keep.rho[k] = rho;
         }
     }
     template <int I>
-    __device__ static float boundary(const float (&)[NIN][I], int, float, const Params &) { return 0.f; }
+    __device__ static void boundary(const float (&)[NIN][I], int, float, const Params &, float (&bv)[K]) { bv[0] = 0.f; }
     template <int I, bool EDGE>
     __device__ static void post(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
-                                const Params &p, float rsc, const float (&A)[I], float A_after,
+                                const Params &p, float rsc, const float (&A)[K][I], const float (&A_after)[K],
                                 const Keep<I> &keep, float (&o)[NOUT][I])
     {
         const float g = p.c0;
 #pragma unroll
         for (int k = 0; k < I; ++k) {
             const bool last = (EDGE && k == kb);
-            const float vs_next = (k + 1 < I) ? A[k + 1] + x[2][k + 1] : A_after + xn[2];
+            const float vs_next = (k + 1 < I) ? A[0][k + 1] + x[2][k + 1] : A_after[0] + xn[2];
             const float nvs = successor<I>(x, k, last, vs_next, rsc);
             const float term = x[4][k];
-            o[0][k] = A[k] + x[2][k];
+            o[0][k] = A[0][k] + x[2][k];
             o[1][k] = keep.rho[k] * (fmaf(g * (1.f - term), nvs, x[3][k]) - x[2][k]);
         }
     }
@@ -167,13 +171,14 @@ struct VTrace {
 template <bool TRUNC>
 struct Retrace {
     static constexpr int NIN = 6 + TRUNC, NOUT = 2;
+    static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = false, ROWSCALAR = false;
     static constexpr unsigned HALO = (1u << 0) | (1u << 1) | (1u << 2);
     template <int I> struct Keep { float rho[I]; };
 
     template <int I, bool EDGE>
     __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
-                                  const Params &p, float, float (&a)[I], float (&b)[I], Keep<I> &keep)
+                                  const Params &p, float, float (&a)[K][I], float (&b)[K][I], Keep<I> &keep)
     {
         const float g = p.c0, lam = p.c1;
         float c[I + 1];
@@ -192,24 +197,24 @@ struct Retrace {
             if constexpr (TRUNC) done = done_of(term, x[6][k]);
             else done = term;
             const float cn = last ? 0.f : c[k + 1];
-            a[k] = fmaf(g * (1.f - term), x[3][k], x[4][k]) - x[2][k];
-            b[k] = g * cn * (1.f - done);
+            a[0][k] = fmaf(g * (1.f - term), x[3][k], x[4][k]) - x[2][k];
+            b[0][k] = g * cn * (1.f - done);
         }
     }
     template <int I>
-    __device__ static float boundary(const float (&)[NIN][I], int, float, const Params &) { return 0.f; }
+    __device__ static void boundary(const float (&)[NIN][I], int, float, const Params &, float (&bv)[K]) { bv[0] = 0.f; }
     template <int I, bool EDGE>
     __device__ static void post(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
-                                const Params &p, float, const float (&A)[I], float A_after,
+                                const Params &p, float, const float (&A)[K][I], const float (&A_after)[K],
                                 const Keep<I> &keep, float (&o)[NOUT][I])
     {
         const float g = p.c0;
 #pragma unroll
         for (int k = 0; k < I; ++k) {
             const bool last = (EDGE && k == kb);
-            const float qn = last ? 0.f : ((k + 1 < I) ? A[k + 1] + x[2][k + 1] : A_after + xn[2]);
+            const float qn = last ? 0.f : ((k + 1 < I) ? A[0][k + 1] + x[2][k + 1] : A_after[0] + xn[2]);
             const float term = x[5][k];
-            o[0][k] = A[k] + x[2][k];
+            o[0][k] = A[0][k] + x[2][k];
             o[1][k] = keep.rho[k] * (fmaf(g * (1.f - term), qn, x[4][k]) - x[2][k]);
         }
     }
@@ -224,6 +229,7 @@ template <bool TRUNC, bool BS2D>
 struct LambdaReturns {
     static_assert(TRUNC || !BS2D, "2-D bootstrap is read only with truncation flags");
     static constexpr int NIN = 3 + TRUNC + BS2D, NOUT = 1;
+    static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = false, ROWSCALAR = !BS2D;
     static constexpr unsigned HALO = 0;
     static constexpr int TR = 3, BS = 3 + TRUNC;
@@ -231,7 +237,7 @@ struct LambdaReturns {
 
     template <int I, bool EDGE>
     __device__ static void coeffs(const float (&x)[NIN][I], const float (&)[NIN], int kb,
-                                  const Params &p, float rsc, float (&a)[I], float (&b)[I], Keep<I> &)
+                                  const Params &p, float rsc, float (&a)[K][I], float (&b)[K][I], Keep<I> &)
     {
         const float g = p.c0, gl = p.c0 * p.c1, g1l = p.c0 * (1.f - p.c1);
 #pragma unroll
@@ -244,27 +250,27 @@ struct LambdaReturns {
                 if constexpr (BS2D) bs = x[BS][k];
                 else bs = last ? rsc : 0.f;
                 const float nd = 1.f - done_of(term, tr);
-                a[k] = fmaf(g * tr, bs, fmaf(g1l * nd, x[1][k], x[0][k]));
-                b[k] = gl * nd;
+                a[0][k] = fmaf(g * tr, bs, fmaf(g1l * nd, x[1][k], x[0][k]));
+                b[0][k] = gl * nd;
             } else {
                 const float nd = 1.f - term;
-                a[k] = fmaf(g1l * nd, x[1][k], x[0][k]);
-                b[k] = gl * nd;
+                a[0][k] = fmaf(g1l * nd, x[1][k], x[0][k]);
+                b[0][k] = gl * nd;
             }
         }
     }
     template <int I>
-    __device__ static float boundary(const float (&x)[NIN][I], int k, float rsc, const Params &)
+    __device__ static void boundary(const float (&x)[NIN][I], int k, float rsc, const Params &, float (&bv)[K])
     {
-        if constexpr (BS2D) return x[BS][k];
-        else return rsc;
+        if constexpr (BS2D) bv[0] = x[BS][k];
+        else bv[0] = rsc;
     }
     template <int I, bool EDGE>
     __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int, const Params &,
-                                float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
+                                float, const float (&A)[K][I], const float (&)[K], const Keep<I> &, float (&o)[NOUT][I])
     {
 #pragma unroll
-        for (int k = 0; k < I; ++k) o[0][k] = A[k];
+        for (int k = 0; k < I; ++k) o[0][k] = A[0][k];
     }
 };
 
@@ -275,6 +281,7 @@ template <bool TRUNC, bool BS2D>
 struct Discounted {
     static_assert(TRUNC || !BS2D, "2-D bootstrap is read only with truncation flags");
     static constexpr int NIN = 2 + TRUNC + BS2D, NOUT = 1;
+    static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = false, ROWSCALAR = !BS2D;
     static constexpr unsigned HALO = 0;
     static constexpr int TR = 2, BS = 2 + TRUNC;
@@ -282,7 +289,7 @@ struct Discounted {
 
     template <int I, bool EDGE>
     __device__ static void coeffs(const float (&x)[NIN][I], const float (&)[NIN], int kb,
-                                  const Params &p, float rsc, float (&a)[I], float (&b)[I], Keep<I> &)
+                                  const Params &p, float rsc, float (&a)[K][I], float (&b)[K][I], Keep<I> &)
     {
         const float g = p.c0;
 #pragma unroll
@@ -294,26 +301,26 @@ struct Discounted {
                 float bs;
                 if constexpr (BS2D) bs = x[BS][k];
                 else bs = last ? rsc : 0.f;
-                a[k] = fmaf(g * tr, bs, x[0][k]);
-                b[k] = g * (1.f - done_of(term, tr));
+                a[0][k] = fmaf(g * tr, bs, x[0][k]);
+                b[0][k] = g * (1.f - done_of(term, tr));
             } else {
-                a[k] = x[0][k];
-                b[k] = g * (1.f - term);
+                a[0][k] = x[0][k];
+                b[0][k] = g * (1.f - term);
             }
         }
     }
     template <int I>
-    __device__ static float boundary(const float (&x)[NIN][I], int k, float rsc, const Params &)
+    __device__ static void boundary(const float (&x)[NIN][I], int k, float rsc, const Params &, float (&bv)[K])
     {
-        if constexpr (BS2D) return x[BS][k];
-        else return rsc;
+        if constexpr (BS2D) bv[0] = x[BS][k];
+        else bv[0] = rsc;
     }
     template <int I, bool EDGE>
     __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int, const Params &,
-                                float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
+                                float, const float (&A)[K][I], const float (&)[K], const Keep<I> &, float (&o)[NOUT][I])
     {
 #pragma unroll
-        for (int k = 0; k < I; ++k) o[0][k] = A[k];
+        for (int k = 0; k < I; ++k) o[0][k] = A[0][k];
     }
 };
 
@@ -322,31 +329,32 @@ struct Discounted {
 // d_{-1} = 0, A_{-1} = seed.  Inputs: 0 gradients, 1 dones.
 struct Eligibility {
     static constexpr int NIN = 2, NOUT = 1;
+    static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = true, ROWSCALAR = true;
     static constexpr unsigned HALO = 1u << 1;
     template <int I> struct Keep {};
 
     template <int I, bool EDGE>
     __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
-                                  const Params &p, float, float (&a)[I], float (&b)[I], Keep<I> &)
+                                  const Params &p, float, float (&a)[K][I], float (&b)[K][I], Keep<I> &)
     {
         const float gl = p.c0 * p.c1;
 #pragma unroll
         for (int k = 0; k < I; ++k) {
             float dprev = (k > 0) ? x[1][k - 1] : xn[1];
             if (EDGE && k == kb) dprev = 0.f;
-            a[k] = x[0][k];
-            b[k] = gl * (1.f - dprev);
+            a[0][k] = x[0][k];
+            b[0][k] = gl * (1.f - dprev);
         }
     }
     template <int I>
-    __device__ static float boundary(const float (&)[NIN][I], int, float rsc, const Params &) { return rsc; }
+    __device__ static void boundary(const float (&)[NIN][I], int, float rsc, const Params &, float (&bv)[K]) { bv[0] = rsc; }
     template <int I, bool EDGE>
     __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int, const Params &,
-                                float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
+                                float, const float (&A)[K][I], const float (&)[K], const Keep<I> &, float (&o)[NOUT][I])
     {
 #pragma unroll
-        for (int k = 0; k < I; ++k) o[0][k] = A[k];
+        for (int k = 0; k < I; ++k) o[0][k] = A[0][k];
     }
 };
 
@@ -356,13 +364,14 @@ struct Eligibility {
 template <bool STARTS_AT>
 struct Prefix {
     static constexpr int NIN = 2, NOUT = 1;
+    static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = true, ROWSCALAR = true;
     static constexpr unsigned HALO = STARTS_AT ? 0u : (1u << 1);
     template <int I> struct Keep {};
 
     template <int I, bool EDGE>
     __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
-                                  const Params &, float, float (&a)[I], float (&b)[I], Keep<I> &)
+                                  const Params &, float, float (&a)[K][I], float (&b)[K][I], Keep<I> &)
     {
 #pragma unroll
         for (int k = 0; k < I; ++k) {
@@ -373,18 +382,18 @@ struct Prefix {
                 d = (k > 0) ? x[1][k - 1] : xn[1];
                 if (EDGE && k == kb) d = 0.f;
             }
-            a[k] = x[0][k];
-            b[k] = 1.f - d;
+            a[0][k] = x[0][k];
+            b[0][k] = 1.f - d;
         }
     }
     template <int I>
-    __device__ static float boundary(const float (&)[NIN][I], int, float rsc, const Params &) { return rsc; }
+    __device__ static void boundary(const float (&)[NIN][I], int, float rsc, const Params &, float (&bv)[K]) { bv[0] = rsc; }
     template <int I, bool EDGE>
     __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int, const Params &,
-                                float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
+                                float, const float (&A)[K][I], const float (&)[K], const Keep<I> &, float (&o)[NOUT][I])
     {
 #pragma unroll
-        for (int k = 0; k < I; ++k) o[0][k] = A[k];
+        for (int k = 0; k < I; ++k) o[0][k] = A[0][k];
     }
 };
 
@@ -393,28 +402,100 @@ struct Prefix {
 template <bool FORWARD>
 struct Linear {
     static constexpr int NIN = 2, NOUT = 1;
+    static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = FORWARD, ROWSCALAR = true;
     static constexpr unsigned HALO = 0;
     template <int I> struct Keep {};
 
     template <int I, bool EDGE>
     __device__ static void coeffs(const float (&x)[NIN][I], const float (&)[NIN], int,
-                                  const Params &, float, float (&a)[I], float (&b)[I], Keep<I> &)
+                                  const Params &, float, float (&a)[K][I], float (&b)[K][I], Keep<I> &)
     {
 #pragma unroll
         for (int k = 0; k < I; ++k) {
-            a[k] = x[0][k];
-            b[k] = x[1][k];
+            a[0][k] = x[0][k];
+            b[0][k] = x[1][k];
         }
     }
     template <int I>
-    __device__ static float boundary(const float (&)[NIN][I], int, float rsc, const Params &) { return rsc; }
+    __device__ static void boundary(const float (&)[NIN][I], int, float rsc, const Params &, float (&bv)[K]) { bv[0] = rsc; }
     template <int I, bool EDGE>
     __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int, const Params &,
-                                float, const float (&A)[I], float, const Keep<I> &, float (&o)[NOUT][I])
+                                float, const float (&A)[K][I], const float (&)[K], const Keep<I> &, float (&o)[NOUT][I])
     {
 #pragma unroll
-        for (int k = 0; k < I; ++k) o[0][k] = A[k];
+        for (int k = 0; k < I; ++k) o[0][k] = A[0][k];
+    }
+};
+
+// ---------------------------------------------------------------------------
+// GAE together with lambda-returns and discounted returns from one read.
+// Scan 0 is GAE (alpha = r + gamma (1-term) Vn - V, beta = gamma lambda
+// (1-done), A_T = 0); lambda-returns are A + V (the identity the returns
+// tutorial states for lambda-returns as GAE targets, Sec. 6; it equals the
+// TD(lambda) recurrence with V(s_{t+1}) taken from `values` and the
+// bootstrap); scan 1 is the discounted return (alpha = r + gamma trunc bs,
+// beta = gamma (1-done), G_T = bs_{T-1}).
+// Inputs as GAE: 0 rewards, 1 values, 2 terminateds, [3 truncateds], [3+TRUNC bootstrap].
+// Outputs: 0 advantages, 1 lambda-returns, 2 discounted returns (each may be null).
+template <bool TRUNC, bool BS2D>
+struct GAEReturns {
+    static_assert(TRUNC || !BS2D, "2-D bootstrap is read only with truncation flags");
+    static constexpr int NIN = 3 + TRUNC + BS2D, NOUT = 3;
+    static constexpr int K = 2;
+    static constexpr bool FWD = false, ROWSCALAR = !BS2D;
+    static constexpr unsigned HALO = 1u << 1;
+    static constexpr int TR = 3, BS = 3 + TRUNC;
+    template <int I> struct Keep {};
+
+    template <int I, bool EDGE>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
+                                  const Params &p, float rsc, float (&a)[K][I], float (&b)[K][I], Keep<I> &)
+    {
+        const float g = p.c0, gl = p.c0 * p.c1;
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            const bool last = (EDGE && k == kb);
+            const float vnext = (k + 1 < I) ? x[1][k + 1] : xn[1];
+            const float term = x[2][k];
+            float vn, done, ret_alpha;
+            if constexpr (TRUNC) {
+                const float tr = x[TR][k];
+                float bs;
+                if constexpr (BS2D) bs = x[BS][k];
+                else bs = last ? rsc : 0.f;
+                vn = last ? bs : fmaf(1.f - tr, vnext, bs);
+                done = done_of(term, tr);
+                ret_alpha = fmaf(g * tr, bs, x[0][k]);
+            } else {
+                vn = last ? rsc : vnext;
+                done = term;
+                ret_alpha = x[0][k];
+            }
+            a[0][k] = fmaf(g * (1.f - term), vn, x[0][k]) - x[1][k];
+            b[0][k] = gl * (1.f - done);
+            a[1][k] = ret_alpha;
+            b[1][k] = g * (1.f - done);
+        }
+    }
+    template <int I>
+    __device__ static void boundary(const float (&x)[NIN][I], int k, float rsc, const Params &, float (&bv)[K])
+    {
+        bv[0] = 0.f;
+        if constexpr (BS2D) bv[1] = x[BS][k];
+        else bv[1] = rsc;
+    }
+    template <int I, bool EDGE>
+    __device__ static void post(const float (&x)[NIN][I], const float (&)[NIN], int, const Params &,
+                                float, const float (&A)[K][I], const float (&)[K], const Keep<I> &,
+                                float (&o)[NOUT][I])
+    {
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            o[0][k] = A[0][k];
+            o[1][k] = A[0][k] + x[1][k];
+            o[2][k] = A[1][k];
+        }
     }
 };
 

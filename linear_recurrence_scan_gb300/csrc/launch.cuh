@@ -71,7 +71,7 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
         p.R = 1;
         p.tiles_per_row = (p.T + TILE - 1) / TILE;
         p.num_tiles = p.N * p.tiles_per_row;
-        const size_t need = kHeaderBytes + kStateBytes * static_cast<size_t>(p.num_tiles);
+        const size_t need = kHeaderBytes + kStateBytes * E::K * static_cast<size_t>(p.num_tiles);
         if (ws == nullptr || ws_bytes < need || !aligned16(ws)) return RLSCAN_ERR_WORKSPACE;
         p.dynamic = 1;
         p.hdr = static_cast<uint32_t *>(ws);
@@ -81,7 +81,7 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
 
     bool tma = (p.T % 4 == 0) && (p.rs % 4 == 0);
     for (int j = 0; j < E::NIN; ++j) tma = tma && aligned16(p.in[j]);
-    for (int q = 0; q < E::NOUT; ++q) tma = tma && aligned16(p.out[q]);
+    for (int q = 0; q < E::NOUT; ++q) tma = tma && (p.out[q] == nullptr || aligned16(p.out[q]));
     p.tma = tma ? 1 : 0;
     p.spin_limit_ns = spin_limit_ns();
     p.copy_limit_ns = 2000000000ull;  // bulk copies land in microseconds; never cut short

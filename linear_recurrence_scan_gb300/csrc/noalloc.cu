@@ -32,8 +32,9 @@
 
 namespace {
 
-// Header + 262,140 tile states of at least 1024 steps each: enough for, e.g.,
-// 64 rows of 4M steps or 4096 rows of 64K steps.
+// Header + 16 bytes per (tile of at least 1024 steps, scan), sized by
+// rlscan_workspace_bytes: N * ceil(T / 1024) <= 131,070, e.g. 32 rows of 4M
+// steps or 2048 rows of 64K steps.
 constexpr size_t kScratchBytes = size_t(4) << 20;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];

@@ -13,13 +13,15 @@ namespace rlscan {
 
 constexpr int kMaxIn = 8;
 
-// Workspace layout: a 64-byte header followed by one 16-byte state per tile.
+// Workspace layout: a 64-byte header followed by one 16-byte state per tile
+// and scan (an estimator solves up to kMaxScans recurrences per step).
 //   bytes  0.. 7  u64 tile ticket (dynamic tile ids, reset by the last CTA)
 //   bytes  8..11  u32 count of CTAs that finished (reset by the last CTA)
 //   bytes 12..15  u32 first error code recorded on the device (0 = none)
 //   bytes 16..19  u32 detail of that error (tile index / stage)
 constexpr size_t kHeaderBytes = 64;
 constexpr size_t kStateBytes = 16;
+constexpr int kMaxScans = 2;
 enum HeaderWord : int { kHdrExit = 2, kHdrError = 3, kHdrDetail = 4 };
 
 // Smallest tile (elements per row segment) any kernel uses; the workspace
@@ -28,7 +30,7 @@ constexpr int kMinTile = 1024;
 
 struct Params {
     const float *in[kMaxIn];   // [N, rs] inputs, order defined by the estimator
-    float *out[2];             // [N, rs] outputs
+    float *out[3];             // [N, rs] outputs (optional ones may be null)
     const float *rowscalar;    // per-row scalar (bootstrap / carry / seed), nullable
     int64_t rowscalar_stride;  // elements between consecutive rows' scalars
     int64_t N, T, rs;
@@ -52,6 +54,7 @@ struct Params {
 
 // Launchers (one translation unit per estimator family).
 rlscan_status launch_gae(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
+rlscan_status launch_gae_returns(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_vtrace(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_retrace(bool trunc, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_lambda_returns(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);

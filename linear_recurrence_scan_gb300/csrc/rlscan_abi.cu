@@ -184,7 +184,7 @@ RLSCAN_API size_t rlscan_workspace_bytes(int64_t N, int64_t T)
 {
     if (N <= 0 || T <= 0 || T <= kMinTile) return 0;
     const int64_t tiles = N * ((T + kMinTile - 1) / kMinTile);
-    return kHeaderBytes + kStateBytes * static_cast<size_t>(tiles);
+    return kHeaderBytes + kStateBytes * kMaxScans * static_cast<size_t>(tiles);
 }
 
 RLSCAN_API rlscan_status rlscan_workspace_init(void *ws, size_t ws_bytes, rlscan_stream_t stream)
@@ -248,6 +248,53 @@ RLSCAN_API rlscan_status rlscan_gae(const float *rewards, const float *values, c
         p.rowscalar_stride = row_stride;
     }
     return launch_gae(false, false, p, ws, ws_bytes, cs(stream));
+}
+
+RLSCAN_API rlscan_status rlscan_gae_returns(const float *rewards, const float *values,
+                                            const float *terminateds, const float *truncateds,
+                                            const float *bootstrap_values, const float *last_value,
+                                            int64_t N, int64_t T, int64_t row_stride, float gamma,
+                                            float lambda, float *advantages, float *lambda_returns,
+                                            float *discounted_returns, void *ws, size_t ws_bytes,
+                                            rlscan_stream_t stream)
+{
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!rewards || !values || !terminateds) return RLSCAN_ERR_NULL;
+    if (!advantages && !lambda_returns && !discounted_returns) return RLSCAN_ERR_NULL;
+    if (bootstrap_values && last_value) return RLSCAN_ERR_ARG_CONFLICT;
+    if (last_value && truncateds) return RLSCAN_ERR_ARG_CONFLICT;
+    for (const float *o : {static_cast<const float *>(advantages), static_cast<const float *>(lambda_returns),
+                           static_cast<const float *>(discounted_returns)}) {
+        if (o == nullptr) continue;
+        if (same_as_any(o, {rewards, values, terminateds, truncateds, bootstrap_values, last_value}))
+            return RLSCAN_ERR_ARG_CONFLICT;
+    }
+    if ((advantages && (advantages == lambda_returns || advantages == discounted_returns)) ||
+        (lambda_returns && lambda_returns == discounted_returns))
+        return RLSCAN_ERR_ARG_CONFLICT;
+    RLSCAN_TRY(run_checks(terminateds, truncateds, bootstrap_values, N, T, row_stride, cs(stream)));
+    Params p = base_params(N, T, row_stride);
+    p.c0 = gamma;
+    p.c1 = lambda;
+    p.out[0] = advantages;
+    p.out[1] = lambda_returns;
+    p.out[2] = discounted_returns;
+    p.in[0] = rewards;
+    p.in[1] = values;
+    p.in[2] = terminateds;
+    if (truncateds) {
+        p.in[3] = truncateds;
+        p.in[4] = bootstrap_values;
+        return launch_gae_returns(true, bootstrap_values != nullptr, p, ws, ws_bytes, cs(stream));
+    }
+    if (last_value) {
+        p.rowscalar = last_value;
+    } else if (bootstrap_values) {
+        p.rowscalar = bootstrap_values + (T - 1);
+        p.rowscalar_stride = row_stride;
+    }
+    return launch_gae_returns(false, false, p, ws, ws_bytes, cs(stream));
 }
 
 RLSCAN_API rlscan_status rlscan_vtrace(const float *log_pi_target, const float *log_pi_behavior,

@@ -195,35 +195,41 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, uint6
     }
 }
 
-// Decoupled look-back, publishing side (one thread per tile): the tile's
-// aggregate map `total`, or directly its inclusive value when that does not
-// depend on anything before the tile (first tile of the row, or b == 0).
-__device__ __forceinline__ void publish_first(const Params &p, int64_t g, int64_t j, Pair total)
+// Decoupled look-back.  Tile g holds one 16-byte state per scan it solves
+// (K of them, slot g * K + scan): two 64-bit words, each a 32-bit tag
+// (call epoch << 2 | kind) beside a float payload.
+//
+// Publishing side (one thread per tile and scan): the tile's aggregate map
+// `total`, or directly its inclusive value when that does not depend on
+// anything before the tile (first tile of the row, or b == 0).
+__device__ __forceinline__ void publish_first(const Params &p, int64_t slot, int64_t g, int64_t j,
+                                              Pair total)
 {
     if (g == p.withhold_tile) return;  // test hook: successors must time out
     unsigned long long *st = p.states;
     if (j == 0 || total.b == 0.f) {
-        ptx::st_relaxed(&st[2 * g], pack_word((p.epoch << 2) | kTagPrefix, total.a));
+        ptx::st_relaxed(&st[2 * slot], pack_word((p.epoch << 2) | kTagPrefix, total.a));
     } else {
-        ptx::st_relaxed(&st[2 * g + 1], pack_word((p.epoch << 2) | kTagAgg, total.b));
-        ptx::st_relaxed(&st[2 * g], pack_word((p.epoch << 2) | kTagAgg, total.a));
+        ptx::st_relaxed(&st[2 * slot + 1], pack_word((p.epoch << 2) | kTagAgg, total.b));
+        ptx::st_relaxed(&st[2 * slot], pack_word((p.epoch << 2) | kTagAgg, total.a));
     }
 }
 
-__device__ __forceinline__ void publish_inclusive(const Params &p, int64_t g, float v)
+__device__ __forceinline__ void publish_inclusive(const Params &p, int64_t slot, int64_t g, float v)
 {
     if (g == p.withhold_tile) return;
-    ptx::st_relaxed(&p.states[2 * g], pack_word((p.epoch << 2) | kTagPrefix, v));
+    ptx::st_relaxed(&p.states[2 * slot], pack_word((p.epoch << 2) | kTagPrefix, v));
 }
 
-// Decoupled look-back, reading side (one thread per warp): the value
-// entering tile g (position j > 0 of its row) from its scan-order
-// predecessor, i.e. A at the step just outside the tile.  (w0, w1) are the
+// Reading side (one thread per warp and scan): the value entering tile g
+// (position j > 0 of its row) from its scan-order predecessor, i.e. A at the
+// step just outside the tile, for scan `sc` of K.  (w0, w1) are the
 // predecessor's state words as fetched when the tile started.  Walks back
 // through aggregates until an inclusive value, a zero decay, or the row's
 // first tile; every wait is bounded.
-__device__ inline float lookback_read(const Params &p, int64_t g, int64_t j, unsigned long long w0,
-                                      unsigned long long w1)
+template <int K>
+__device__ inline float lookback_read(const Params &p, int64_t g, int64_t j, int sc,
+                                      unsigned long long w0, unsigned long long w1)
 {
     const unsigned long long *st = p.states;
     const uint32_t tagA = (p.epoch << 2) | kTagAgg;
@@ -236,8 +242,8 @@ __device__ inline float lookback_read(const Params &p, int64_t g, int64_t j, uns
     bool fresh = true;  // (w0, w1) hold a probe of tile k
     for (;;) {
         if (!fresh) {
-            w0 = ptx::ld_relaxed(&st[2 * k]);
-            w1 = ptx::ld_relaxed(&st[2 * k + 1]);
+            w0 = ptx::ld_relaxed(&st[2 * (k * K + sc)]);
+            w1 = ptx::ld_relaxed(&st[2 * (k * K + sc) + 1]);
         }
         fresh = false;
         const uint32_t tag = static_cast<uint32_t>(w0 >> 32);
@@ -327,16 +333,17 @@ constexpr int block_threads() { return THREADS + 32; }
 #ifndef RLSCAN_MIN_BLOCKS
 #define RLSCAN_MIN_BLOCKS 3
 #endif
-template <int THREADS>
-constexpr int min_blocks() { return RLSCAN_MIN_BLOCKS; }
+template <int K>
+constexpr int min_blocks() { return K > 1 ? 2 : RLSCAN_MIN_BLOCKS; }  // two scans need more registers
 
 template <class E, int THREADS, int ITEMS, int STAGES>
-__global__ void __launch_bounds__(block_threads<THREADS>(), min_blocks<THREADS>())
+__global__ void __launch_bounds__(block_threads<THREADS>(), min_blocks<E::K>())
 scan_kernel(const __grid_constant__ Params p)
 {
-    constexpr int NIN = E::NIN, NOUT = E::NOUT;
+    constexpr int NIN = E::NIN, NOUT = E::NOUT, K = E::K;
     constexpr int TILE = THREADS * ITEMS, AST = TILE + 8, WARPS = THREADS / 32;
     constexpr bool FWD = E::FWD;
+    static_assert(K >= 1 && K <= kMaxScans, "scans per step");
     constexpr int PUB_WARP = FWD ? WARPS - 1 : 0;   // warp holding the tile's last element in scan order
     constexpr int COMPUTE_BAR = 1;                  // named barrier of the compute warps
     static_assert(STAGES >= 2, "the ring needs two stages");
@@ -348,7 +355,7 @@ scan_kernel(const __grid_constant__ Params p)
     __shared__ __align__(8) uint64_t empty_bar[STAGES];  // every compute warp is done reading it
     __shared__ int64_t tile_ids[STAGES];
     __shared__ TileGeo s_geo[STAGES];
-    __shared__ Pair wagg[2][WARPS];  // warp aggregates, double-buffered by tile parity
+    __shared__ Pair wagg[2][WARPS][K];  // warp aggregates per scan, double-buffered by tile parity
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -437,11 +444,13 @@ scan_kernel(const __grid_constant__ Params p)
         float *stage = smem + s * NIN * AST;
         const bool chained = !p.packed && tg.j > 0;  // needs its predecessor's value
 
-        // predecessor state for the look-back, also fetched early
+        // predecessor states for the look-back (lane sc < K reads scan sc),
+        // fetched early so their latency overlaps the tile's work
         unsigned long long pw0 = 0, pw1 = 0;
-        if (chained && lane == 0) {
-            pw0 = ptx::ld_relaxed(&p.states[2 * (g - p.N)]);
-            pw1 = ptx::ld_relaxed(&p.states[2 * (g - p.N) + 1]);
+        if (chained && lane < K) {
+            const int64_t slot = (g - p.N) * K + lane;
+            pw0 = ptx::ld_relaxed(&p.states[2 * slot]);
+            pw1 = ptx::ld_relaxed(&p.states[2 * slot + 1]);
         }
 
         if (!tma) {
@@ -468,7 +477,7 @@ scan_kernel(const __grid_constant__ Params p)
             xn[j] = ((E::HALO >> j) & 1u) ? (FWD ? src[j * AST - 1] : src[j * AST + ITEMS]) : 0.f;
         }
 
-        float a[ITEMS], b[ITEMS];
+        float a[K][ITEMS], b[K][ITEMS];
         typename E::template Keep<ITEMS> keep;
         if (!edge) {
             E::template coeffs<ITEMS, false>(x, xn, -1, p, rsc, a, b, keep);
@@ -476,33 +485,45 @@ scan_kernel(const __grid_constant__ Params p)
             E::template coeffs<ITEMS, true>(x, xn, sp.kb, p, rsc, a, b, keep);
 #pragma unroll
             for (int k = 0; k < ITEMS; ++k) {
-                if (k == sp.kb) {  // fold the row's boundary value; sever
-                    a[k] = fmaf(b[k], E::template boundary<ITEMS>(x, k, rsc, p), a[k]);
-                    b[k] = 0.f;
+                if (k == sp.kb) {  // fold the row's boundary values; sever
+                    float bv[K];
+                    E::template boundary<ITEMS>(x, k, rsc, p, bv);
+#pragma unroll
+                    for (int sc = 0; sc < K; ++sc) {
+                        a[sc][k] = fmaf(b[sc][k], bv[sc], a[sc][k]);
+                        b[sc][k] = 0.f;
+                    }
                 }
                 if (k >= sp.kv) {  // outside the data: identity map
-                    a[k] = 0.f;
-                    b[k] = 1.f;
+#pragma unroll
+                    for (int sc = 0; sc < K; ++sc) {
+                        a[sc][k] = 0.f;
+                        b[sc][k] = 1.f;
+                    }
                 }
             }
         }
 
-        // thread aggregate, in scan order
-        Pair agg;
-        if (FWD) {
-            agg = Pair{a[0], b[0]};
+        // per scan: thread aggregate in scan order, warp scan
+        Pair ex[K];
+        Pair(*wa)[K] = wagg[it & 1];
 #pragma unroll
-            for (int k = 1; k < ITEMS; ++k) agg = compose(Pair{a[k], b[k]}, agg);
-        } else {
-            agg = Pair{a[ITEMS - 1], b[ITEMS - 1]};
+        for (int sc = 0; sc < K; ++sc) {
+            Pair agg;
+            if (FWD) {
+                agg = Pair{a[sc][0], b[sc][0]};
 #pragma unroll
-            for (int k = ITEMS - 2; k >= 0; --k) agg = compose(Pair{a[k], b[k]}, agg);
+                for (int k = 1; k < ITEMS; ++k) agg = compose(Pair{a[sc][k], b[sc][k]}, agg);
+            } else {
+                agg = Pair{a[sc][ITEMS - 1], b[sc][ITEMS - 1]};
+#pragma unroll
+                for (int k = ITEMS - 2; k >= 0; --k) agg = compose(Pair{a[sc][k], b[sc][k]}, agg);
+            }
+            const Pair inc = warp_inclusive<FWD>(agg, lane);
+            ex[sc] = warp_exclusive_from<FWD>(inc, lane);
+            if (lane == (FWD ? 31 : 0)) wa[warp][sc] = inc;
         }
-        const Pair inc = warp_inclusive<FWD>(agg, lane);
-        const Pair ex = warp_exclusive_from<FWD>(inc, lane);
-        Pair *wa = wagg[it & 1];
-        if (lane == (FWD ? 31 : 0)) wa[warp] = inc;
-        ptx::named_barrier(COMPUTE_BAR, THREADS);  // warp aggregates visible
+        ptx::named_barrier(COMPUTE_BAR, THREADS);        // warp aggregates visible
         if (lane == 0) ptx::mbar_arrive(&empty_bar[s]);  // every input is in registers: the slot is free
 
         if (use_rsc) {
@@ -512,47 +533,67 @@ scan_kernel(const __grid_constant__ Params p)
         }
 
         // map entering this warp's range from the warps before it in scan order
-        Pair we{0.f, 1.f};
-        if (FWD) {
+        Pair we[K];
 #pragma unroll
-            for (int w2 = 0; w2 < WARPS - 1; ++w2)
-                if (w2 < warp) we = compose(wa[w2], we);
-        } else {
+        for (int sc = 0; sc < K; ++sc) {
+            we[sc] = Pair{0.f, 1.f};
+            if (FWD) {
 #pragma unroll
-            for (int w2 = WARPS - 1; w2 > 0; --w2)
-                if (w2 > warp) we = compose(wa[w2], we);
+                for (int w2 = 0; w2 < WARPS - 1; ++w2)
+                    if (w2 < warp) we[sc] = compose(wa[w2][sc], we[sc]);
+            } else {
+#pragma unroll
+                for (int w2 = WARPS - 1; w2 > 0; --w2)
+                    if (w2 > warp) we[sc] = compose(wa[w2][sc], we[sc]);
+            }
         }
-        // value entering the tile
-        float carry = 0.f;
-        if (chained || (!p.packed && warp == PUB_WARP)) {
-            if (warp == PUB_WARP && lane == 0)
-                publish_first(p, g, tg.j, compose(wa[PUB_WARP], we));
+        // value entering the tile, per scan: publish this tile's aggregates
+        // first, then walk the K chains in parallel (lane sc walks scan sc)
+        float carry[K];
+#pragma unroll
+        for (int sc = 0; sc < K; ++sc) carry[sc] = 0.f;
+        if (!p.packed) {
+            if (warp == PUB_WARP && lane == 0) {
+#pragma unroll
+                for (int sc = 0; sc < K; ++sc)
+                    publish_first(p, g * K + sc, g, tg.j, compose(wa[PUB_WARP][sc], we[sc]));
+            }
             if (chained) {
-                if (lane == 0) carry = lookback_read(p, g, tg.j, pw0, pw1);
-                carry = __shfl_sync(0xffffffffu, carry, 0);
+                float mine = 0.f;
+                if (lane < K) mine = lookback_read<K>(p, g, tg.j, lane, pw0, pw1);
+#pragma unroll
+                for (int sc = 0; sc < K; ++sc) carry[sc] = __shfl_sync(0xffffffffu, mine, sc);
                 if (warp == PUB_WARP && lane == 0) {
-                    const Pair total = compose(wa[PUB_WARP], we);
-                    if (total.b != 0.f) publish_inclusive(p, g, fmaf(total.b, carry, total.a));
+#pragma unroll
+                    for (int sc = 0; sc < K; ++sc) {
+                        const Pair total = compose(wa[PUB_WARP][sc], we[sc]);
+                        if (total.b != 0.f)
+                            publish_inclusive(p, g * K + sc, g, fmaf(total.b, carry[sc], total.a));
+                    }
                 }
             }
         }
+        // exact value entering this thread's range
+        float x_in[K];
+#pragma unroll
+        for (int sc = 0; sc < K; ++sc) x_in[sc] = fmaf(ex[sc].b, fmaf(we[sc].b, carry[sc], we[sc].a), ex[sc].a);
 
-        // exact value entering this thread's range, then its serial recurrence
-        const float x_in = fmaf(ex.b, fmaf(we.b, carry, we.a), ex.a);
-        float A[ITEMS];
-        {
-            float v = x_in;
+        // serial recurrence of each scan from its exact incoming value
+        float A[K][ITEMS];
+#pragma unroll
+        for (int sc = 0; sc < K; ++sc) {
+            float v = x_in[sc];
             if (FWD) {
 #pragma unroll
                 for (int k = 0; k < ITEMS; ++k) {
-                    v = fmaf(b[k], v, a[k]);
-                    A[k] = v;
+                    v = fmaf(b[sc][k], v, a[sc][k]);
+                    A[sc][k] = v;
                 }
             } else {
 #pragma unroll
                 for (int k = ITEMS - 1; k >= 0; --k) {
-                    v = fmaf(b[k], v, a[k]);
-                    A[k] = v;
+                    v = fmaf(b[sc][k], v, a[sc][k]);
+                    A[sc][k] = v;
                 }
             }
         }
@@ -562,19 +603,17 @@ scan_kernel(const __grid_constant__ Params p)
 
         if (sp.kv > 0) {
             const int64_t off = (tg.row0 + rit) * p.rs + tg.t0 + col;
-            if (tma) {
 #pragma unroll
-                for (int q = 0; q < NOUT; ++q) {
+            for (int q = 0; q < NOUT; ++q) {
+                if (NOUT > 1 && p.out[q] == nullptr) continue;  // optional output
+                if (tma) {
 #pragma unroll
                     for (int k = 0; k < ITEMS; k += 4) {
                         if (k < sp.kv)
                             *reinterpret_cast<float4 *>(p.out[q] + off + k) =
                                 make_float4(o[q][k], o[q][k + 1], o[q][k + 2], o[q][k + 3]);
                     }
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < NOUT; ++q) {
+                } else {
 #pragma unroll
                     for (int k = 0; k < ITEMS; ++k)
                         if (k < sp.kv) p.out[q][off + k] = o[q][k];

@@ -64,6 +64,22 @@ def test_config1_gae_returns_4096x1024():
                                       l, None, b["last_value"]), "config 1 lambda returns")
 
 
+def test_config1_fused_gae_returns_4096x1024():
+    """The fused kernel on the same workload matches all three oracles."""
+    c = synthetic.CONFIGS[1]
+    b = synthetic.config_batch(1)
+    g, l = c["gamma"], c["lambda_"]
+    adv, lam, disc = L().compute_gae_and_returns(dev(b["rewards"]), dev(b["values"]),
+                                                 dev(b["terminateds"]), None, g, l, None,
+                                                 dev(b["last_value"]))
+    assert_disc(adv, oracle.gae(b["rewards"], b["values"], b["terminateds"], None, g, l, None,
+                                b["last_value"]), "fused gae")
+    assert_disc(lam, oracle.lambda_returns(b["rewards"], b["next_values"], b["terminateds"], None,
+                                           g, l, None, b["last_value"]), "fused lambda returns")
+    assert_disc(disc, oracle.discounted_returns(b["rewards"], b["terminateds"], None, g, None,
+                                                b["last_value"]), "fused discounted")
+
+
 def _vtrace(b, c):
     args = (c["gamma"], c["rho_bar"], c["c_bar"])
     ref = oracle.vtrace(b["log_pi_target"], b["log_pi_behavior"], b["values"], b["rewards"],

@@ -124,6 +124,36 @@ def test_gae(N, T, rs, variant):
     assert_disc(got, ref, "gae")
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("N,T,rs", SHAPES, ids=IDS)
+def test_gae_and_returns_fused(N, T, rs, variant):
+    """One kernel, three outputs: GAE, lambda-returns = GAE + V, discounted
+    returns on the same rewards, flags and bootstrap."""
+    c, _ = make_case(11, N, T, variant)
+    adv = oracle.gae(c["r"], c["v"], c["term"], c["trunc"], 0.99, 0.95, c["bs"], c["last"])
+    disc = oracle.discounted_returns(c["r"], c["term"], c["trunc"], 0.99, c["bs"], c["last"])
+    got = L().compute_gae_and_returns(to_dev(c["r"], rs), to_dev(c["v"], rs), to_dev(c["term"], rs),
+                                      to_dev(c["trunc"], rs), 0.99, 0.95, to_dev(c["bs"], rs),
+                                      to_dev(c["last"]))
+    assert_disc(got[0], adv, "fused advantages")
+    assert_disc(got[1], adv + c["v"].astype(np.float64), "fused lambda returns")
+    assert_disc(got[2], disc, "fused discounted returns")
+
+
+@pytest.mark.parametrize("outputs", [("discounted_returns",), ("lambda_returns", "advantages")])
+def test_gae_and_returns_output_subsets(outputs):
+    c, _ = make_case(12, 5, 3000, "last_value")
+    ref = {"advantages": oracle.gae(c["r"], c["v"], c["term"], None, 0.99, 0.95, None, c["last"])}
+    ref["lambda_returns"] = ref["advantages"] + c["v"].astype(np.float64)
+    ref["discounted_returns"] = oracle.discounted_returns(c["r"], c["term"], None, 0.99, None,
+                                                          c["last"])
+    got = L().compute_gae_and_returns(to_dev(c["r"]), to_dev(c["v"]), to_dev(c["term"]), None,
+                                      0.99, 0.95, None, to_dev(c["last"]), outputs=outputs)
+    assert len(got) == len(outputs)
+    for name, t in zip(outputs, got):
+        assert_disc(t, ref[name], name)
+
+
 @pytest.mark.parametrize("variant", VARIANTS + ["trunc_last"])
 @pytest.mark.parametrize("N,T,rs", SHAPES, ids=IDS)
 def test_vtrace(N, T, rs, variant):
