@@ -352,6 +352,7 @@ scan_kernel(const __grid_constant__ Params p)
 
     extern __shared__ __align__(128) float smem[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];   // stage data (and tile id) ready
+    __shared__ __align__(8) uint64_t meta_bar[STAGES];   // tile id and geometry recorded
     __shared__ __align__(8) uint64_t empty_bar[STAGES];  // every compute warp is done reading it
     __shared__ int64_t tile_ids[STAGES];
     __shared__ TileGeo s_geo[STAGES];
@@ -366,6 +367,7 @@ scan_kernel(const __grid_constant__ Params p)
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&full_bar[s], 1);
+            ptx::mbar_init(&meta_bar[s], 1);
             ptx::mbar_init(&empty_bar[s], WARPS);
         }
         ptx::fence_mbar_init();
@@ -399,11 +401,13 @@ scan_kernel(const __grid_constant__ Params p)
                 }
                 tile_ids[s] = g;
                 if (g >= p.num_tiles) {
+                    ptx::mbar_arrive(&meta_bar[s]);
                     ptx::mbar_arrive(&full_bar[s]);
                     break;
                 }
                 const TileGeo tg = decode_tile<FWD, TILE>(p, g);
                 s_geo[s] = tg;
+                ptx::mbar_arrive(&meta_bar[s]);  // the tile is known before its data lands
                 if (tma) issue_tile_copies<E, TILE, AST>(p, tg, smem + s * NIN * AST, &full_bar[s]);
                 else ptx::mbar_arrive(&full_bar[s]);
             }
@@ -415,8 +419,9 @@ scan_kernel(const __grid_constant__ Params p)
     const int col = p.packed ? li - rit * p.C : li;
 
     // Row scalar of this thread's row when the row's boundary step falls in
-    // its range.  Fetched one tile ahead when that tile is already known
-    // (its slot's phase has completed), so the latency is hidden.
+    // its range.  Fetched one tile ahead once that tile is known (its slot's
+    // meta phase has completed; its data may still be in flight), so the
+    // latency is hidden.
     auto load_row_scalar = [&](int s) -> float {
         if (tile_ids[s] >= p.num_tiles) return 0.f;
         const TileGeo tg = s_geo[s];
@@ -528,7 +533,7 @@ scan_kernel(const __grid_constant__ Params p)
 
         if (use_rsc) {
             const int s1 = (it + 1) % STAGES;
-            rsc_ready = ptx::mbar_test_wait(&full_bar[s1], static_cast<uint32_t>(((it + 1) / STAGES) & 1));
+            rsc_ready = ptx::mbar_test_wait(&meta_bar[s1], static_cast<uint32_t>(((it + 1) / STAGES) & 1));
             if (rsc_ready) rsc_next = load_row_scalar(s1);
         }
 
