@@ -29,13 +29,16 @@ namespace rlscan {
 #ifndef RLSCAN_MAX_STAGES
 #define RLSCAN_MAX_STAGES 4
 #endif
+#ifndef RLSCAN_THREADS_2048
+#define RLSCAN_THREADS_2048 256
+#endif
 
 template <class E>
 struct Shape {
     static constexpr int BYTES_PER_STEP = 4 * (E::NIN + E::NOUT);
     static constexpr int TILE_RAW = RLSCAN_TILE_BYTES_TARGET / BYTES_PER_STEP;
     static constexpr int TILE = TILE_RAW >= 3072 ? 4096 : (TILE_RAW >= 1536 ? 2048 : 1024);
-    static constexpr int THREADS = TILE >= 2048 ? 256 : 128;
+    static constexpr int THREADS = TILE >= 4096 ? 256 : (TILE >= 2048 ? RLSCAN_THREADS_2048 : 128);
     static constexpr int ITEMS = TILE / THREADS;
     static constexpr int STAGE_BYTES = E::NIN * (TILE + 8) * 4;
     static constexpr int RAW = (RLSCAN_SMEM_BUDGET_KB * 1024) / STAGE_BYTES;
