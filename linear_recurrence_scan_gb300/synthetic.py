@@ -25,6 +25,14 @@ Sec. 7, and the caller-side conventions of the API reference):
                 log_pi_target = log_pi_behavior + N(0, 0.5^2).
 * ``retrace``   rewards, Q(s_t,a_t), E_pi[Q(s_{t+1},.)] ~ N(0,1);
                 mu(a_t|s_t) ~ U(0.05, 1); pi(a_t|s_t) = mu * exp(N(0, 0.5^2)).
+* ``retrace_actions``  the full action-space form of the retrace recipe with
+                A actions (4 on the pages' Retrace benchmarks): target
+                probabilities softmax(z), z ~ N(0,1)^A per step; behaviour
+                probabilities softmax(z + N(0, 0.5^2)^A); the taken action
+                drawn from the behaviour probabilities (inverse CDF of a
+                uniform draw) as int64; action_probs_behavior = the behaviour
+                probability of that action; Q(s_t,a_t), Q(s_{t+1},a) for
+                every a, rewards ~ N(0,1); flags as for ``retrace``.
 * ``long_rows`` episode starts F ~ Bernoulli(p_start); prefix-sum inputs are
                 integers uniform in [0, 9] stored as float32 with
                 dones = F ("starts_at"); eligibility-trace dones mark the step
@@ -41,7 +49,7 @@ _TENSOR_IDS = {
     "log_ratio": 8, "q_values": 9, "expected_next_q": 10, "mu_taken": 11,
     "pi_log_ratio": 12, "episode_starts": 13, "inputs": 14, "gradients": 15,
     "alpha": 16, "beta": 17, "carry": 18, "seed_values": 19, "beta_zero": 20,
-    "action_logits": 21, "next_q_all": 22, "actions": 23,
+    "action_logits": 21, "next_q_all": 22, "actions": 23, "behavior_logit_noise": 24,
 }
 
 # The five workloads used by the tests and the benchmark.  Shapes and
@@ -156,6 +164,33 @@ def retrace_batch(N, T, seed=0, config_id=3, p_term=0.001, p_trunc=0.0):
     return dict(pi_taken=pi, mu_taken=mu,
                 q_values=normal(seed, config_id, "q_values", (N, T)),
                 expected_next_q=normal(seed, config_id, "expected_next_q", (N, T)),
+                rewards=normal(seed, config_id, "rewards", (N, T)),
+                terminateds=term, truncateds=trunc)
+
+
+def _softmax(z):
+    z = z - z.max(axis=-1, keepdims=True)
+    e = np.exp(z)
+    return (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+
+
+def retrace_actions_batch(N, T, A=4, seed=0, config_id=3, p_term=0.001, p_trunc=0.0):
+    term, trunc = _flags(N, T, seed, config_id, p_term, p_trunc)
+    z = normal(seed, config_id, "action_logits", (N, T, A))
+    target = _softmax(z)
+    z += normal(seed, config_id, "behavior_logit_noise", (N, T, A), std=0.5)
+    behavior = _softmax(z)
+    del z
+    u = stream(seed, config_id, "actions").random((N, T), dtype=np.float32)
+    cdf = np.cumsum(behavior, axis=-1)
+    actions = np.minimum((u[..., None] >= cdf).sum(axis=-1), A - 1).astype(np.int64)
+    del cdf
+    mu = np.take_along_axis(behavior, actions[..., None], axis=-1)[..., 0]
+    del behavior
+    return dict(action_probs_target=target, action_probs_behavior=np.ascontiguousarray(mu),
+                q_values=normal(seed, config_id, "q_values", (N, T)),
+                next_q_values_all=normal(seed, config_id, "next_q_all", (N, T, A)),
+                actions=actions,
                 rewards=normal(seed, config_id, "rewards", (N, T)),
                 terminateds=term, truncateds=trunc)
 

@@ -61,6 +61,7 @@ _SIGNATURES = {
     "oracle_gae": [_I64] * 5 + [_P] * 6 + [_D, _D, _P],
     "oracle_vtrace": [_I64] * 5 + [_P] * 8 + [_D, _D, _D, _P, _P],
     "oracle_retrace": [_I64] * 5 + [_P] * 7 + [_D, _D, _D, _D, _P, _P],
+    "oracle_retrace_actions": [_I64] * 6 + [_P] * 8 + [_D, _D, _D, _D, _P, _P],
     "oracle_lambda_returns": [_I64] * 5 + [_P] * 6 + [_D, _D, _P],
     "oracle_discounted_returns": [_I64] * 5 + [_P] * 5 + [_D, _P],
     "oracle_eligibility_traces": [_I64] * 5 + [_P] * 3 + [_D, _D, _P],
@@ -116,7 +117,7 @@ class Oracle:
         for name, argtypes in _SIGNATURES.items():
             fn = getattr(lib, name)
             fn.argtypes = argtypes
-            fn.restype = None
+            fn.restype = _I64 if name == "oracle_retrace_actions" else None
         self._lib = lib
 
     def gae(self, rewards, values, terminateds, truncateds=None, gamma=0.99, lambda_=0.95,
@@ -155,6 +156,34 @@ class Oracle:
                                c.mat(expected_next_q, "expected_next_q"), c.mat(rewards, "rewards"),
                                c.mat(terminateds, "terminateds"), c.mat(truncateds, "truncateds"),
                                gamma, lambda_, c_bar, rho_bar, qret.ctypes.data, adv.ctypes.data)
+        return qret, adv
+
+    def retrace_actions(self, action_probs_target, action_probs_behavior, q_values,
+                        next_q_values_all, actions, rewards, terminateds, truncateds=None,
+                        gamma=0.99, lambda_=1.0, c_bar=1.0, rho_bar=1.0, rows=None):
+        """Retrace(lambda) targets and advantages from the full action-space
+        inputs ([N,T,A] target probabilities and successor Q-values, int64
+        actions), in the argument order of the API's compute_retrace."""
+        c = _Rows(rewards)
+        probs = np.ascontiguousarray(action_probs_target, dtype=np.float32)
+        nq = np.ascontiguousarray(next_q_values_all, dtype=np.float32)
+        if probs.ndim != 3 or probs.shape[:2] != (c.N, c.T) or nq.shape != probs.shape:
+            raise ValueError("action_probs_target and next_q_values_all must be [N, T, A]")
+        acts = np.asarray(actions)
+        if acts.shape != (c.N, c.T) or acts.dtype.kind not in "iu":
+            raise ValueError("actions must be an integer [N, T] array")
+        acts = np.ascontiguousarray(acts, dtype=np.int64)
+        c.keep += [probs, nq, acts]
+        qret, adv = c.out(), c.out()
+        head = c.head(rows)
+        bad = self._lib.oracle_retrace_actions(
+            head[0], head[1], probs.shape[2], head[2], head[3], head[4], probs.ctypes.data,
+            c.mat(action_probs_behavior, "action_probs_behavior"), c.mat(q_values, "q_values"),
+            nq.ctypes.data, acts.ctypes.data, c.mat(rewards, "rewards"),
+            c.mat(terminateds, "terminateds"), c.mat(truncateds, "truncateds"),
+            gamma, lambda_, c_bar, rho_bar, qret.ctypes.data, adv.ctypes.data)
+        if bad:
+            raise ValueError(f"{bad} action indices outside [0, {probs.shape[2]})")
         return qret, adv
 
     def lambda_returns(self, rewards, next_values, terminateds, truncateds=None, gamma=0.99,
@@ -234,6 +263,10 @@ def vtrace(*args, **kwargs):
 
 def retrace(*args, **kwargs):
     return default().retrace(*args, **kwargs)
+
+
+def retrace_actions(*args, **kwargs):
+    return default().retrace_actions(*args, **kwargs)
 
 
 def lambda_returns(*args, **kwargs):

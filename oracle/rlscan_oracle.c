@@ -177,6 +177,35 @@ void oracle_vtrace(int64_t N, int64_t T, int64_t rs, int64_t row_begin, int64_t 
  *   adv_t  = rho_t (r_t + gamma (1-term_t) Qret_{t+1} - Q_t),  Qret_T = 0
  * truncateds may be NULL (all zero).
  */
+/*
+ * One row of the Retrace recurrence above, with the taken action's target
+ * probability pi_t and the expected successor value EQ_t given in double.
+ */
+static void retrace_row(int64_t T, int64_t row, int64_t rs, const double *pi, const double *eq,
+                        const float *mu, const float *q, const float *r, const float *term,
+                        const float *trunc, double gamma, double lam, double c_bar,
+                        double rho_bar, double *qret, double *adv)
+{
+    double D_next = 0.0;
+    for (int64_t t = T - 1; t >= 0; --t) {
+        double c_next = 0.0;
+        if (t < T - 1)
+            c_next = lam * min2(c_bar, pi[t + 1] / AT(mu, row, t + 1, rs));
+        double te = AT(term, row, t, rs);
+        double tr = trunc ? AT(trunc, row, t, rs) : 0.0;
+        double delta = AT(r, row, t, rs) + gamma * (1.0 - te) * eq[t] - AT(q, row, t, rs);
+        double D = delta + gamma * c_next * (1.0 - done_flag(te, tr)) * D_next;
+        qret[t] = AT(q, row, t, rs) + D;
+        D_next = D;
+    }
+    for (int64_t t = 0; t < T; ++t) {
+        double rho = min2(rho_bar, pi[t] / AT(mu, row, t, rs));
+        double te = AT(term, row, t, rs);
+        double qn = (t < T - 1) ? qret[t + 1] : 0.0;
+        adv[t] = rho * (AT(r, row, t, rs) + gamma * (1.0 - te) * qn - AT(q, row, t, rs));
+    }
+}
+
 void oracle_retrace(int64_t N, int64_t T, int64_t rs, int64_t row_begin, int64_t row_end,
                     const float *pi, const float *mu, const float *q, const float *eq,
                     const float *r, const float *term, const float *trunc,
@@ -184,29 +213,69 @@ void oracle_retrace(int64_t N, int64_t T, int64_t rs, int64_t row_begin, int64_t
                     double *qret_out, double *adv_out)
 {
     (void)N;
+    double *pi_d = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    double *eq_d = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
     for (int64_t row = row_begin; row < row_end; ++row) {
-        double *qret = qret_out + row * T;
-        double *adv = adv_out + row * T;
-        double D_next = 0.0;
-        for (int64_t t = T - 1; t >= 0; --t) {
-            double c_next = 0.0;
-            if (t < T - 1)
-                c_next = lam * min2(c_bar, AT(pi, row, t + 1, rs) / AT(mu, row, t + 1, rs));
-            double te = AT(term, row, t, rs);
-            double tr = trunc ? AT(trunc, row, t, rs) : 0.0;
-            double delta = AT(r, row, t, rs) + gamma * (1.0 - te) * AT(eq, row, t, rs)
-                           - AT(q, row, t, rs);
-            double D = delta + gamma * c_next * (1.0 - done_flag(te, tr)) * D_next;
-            qret[t] = AT(q, row, t, rs) + D;
-            D_next = D;
-        }
         for (int64_t t = 0; t < T; ++t) {
-            double rho = min2(rho_bar, AT(pi, row, t, rs) / AT(mu, row, t, rs));
-            double te = AT(term, row, t, rs);
-            double qn = (t < T - 1) ? qret[t + 1] : 0.0;
-            adv[t] = rho * (AT(r, row, t, rs) + gamma * (1.0 - te) * qn - AT(q, row, t, rs));
+            pi_d[t] = AT(pi, row, t, rs);
+            eq_d[t] = AT(eq, row, t, rs);
         }
+        retrace_row(T, row, rs, pi_d, eq_d, mu, q, r, term, trunc, gamma, lam, c_bar, rho_bar,
+                    qret_out + row * T, adv_out + row * T);
     }
+    free(pi_d);
+    free(eq_d);
+}
+
+/*
+ * Retrace(lambda) from the full action-space inputs -- [API] compute_retrace
+ * (its signature: action_probs_target and next_q_values_all [N,T,A],
+ * actions int64 [N,T], action_probs_behavior the behaviour probability of
+ * the taken action; its unfused branch reduces the action dimension first).
+ *   EQ_t = sum_a pi_target[t,a] * Qnext[t,a]     (a = 0 .. A-1 in order;
+ *          the target weights are those stored at the same step t, as the
+ *          API's reduction multiplies the two [N,T,A] tensors element-wise)
+ *   pi_t = pi_target[t, actions[t]]
+ * then the recurrence of oracle_retrace with mu_t = action_probs_behavior[t].
+ * The [N,T,A] arrays are dense (row stride T*A); actions and the [N,T] arrays
+ * have row stride rs.  Returns the number of steps whose action index lies
+ * outside [0, A); their rows are left unwritten.
+ */
+int64_t oracle_retrace_actions(int64_t N, int64_t T, int64_t A, int64_t rs, int64_t row_begin,
+                               int64_t row_end, const float *probs, const float *mu,
+                               const float *q, const float *next_q_all, const int64_t *actions,
+                               const float *r, const float *term, const float *trunc,
+                               double gamma, double lam, double c_bar, double rho_bar,
+                               double *qret_out, double *adv_out)
+{
+    (void)N;
+    int64_t bad = 0;
+    double *pi_d = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    double *eq_d = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    for (int64_t row = row_begin; row < row_end; ++row) {
+        int64_t row_bad = 0;
+        for (int64_t t = 0; t < T; ++t) {
+            const float *pt = probs + (row * T + t) * A;
+            const float *qt = next_q_all + (row * T + t) * A;
+            double s = 0.0;
+            for (int64_t a = 0; a < A; ++a) s += (double)pt[a] * (double)qt[a];
+            eq_d[t] = s;
+            int64_t at = actions[row * rs + t];
+            if (at < 0 || at >= A) {
+                ++row_bad;
+                pi_d[t] = 0.0;
+            } else {
+                pi_d[t] = (double)pt[at];
+            }
+        }
+        bad += row_bad;
+        if (row_bad == 0)
+            retrace_row(T, row, rs, pi_d, eq_d, mu, q, r, term, trunc, gamma, lam, c_bar,
+                        rho_bar, qret_out + row * T, adv_out + row * T);
+    }
+    free(pi_d);
+    free(eq_d);
+    return bad;
 }
 
 /*

@@ -587,6 +587,115 @@ def check_severing_and_continuation(orc):
     _close(part, full[:, k:], tol=0.0, what="prefix continuation")
 
 
+# --------------------------------------------------------------------------
+# Retrace from the full action-space inputs ([N,T,A] probabilities and
+# successor Q-values, int64 actions)
+# --------------------------------------------------------------------------
+
+GOLDEN_RETRACE_ACTIONS = os.path.join(os.path.dirname(__file__), "golden",
+                                      "retrace_actions_worked.json")
+
+
+def _retrace_actions_inputs(rng, N, T, A, dyadic):
+    if dyadic:  # every product and sum below is exact in float32 and float64
+        probs = _f32(rng.integers(0, 9, (N, T, A)) / 8.0)
+        nq = _f32(rng.integers(-8, 9, (N, T, A)))
+    else:
+        w = rng.random((N, T, A)) + 0.05
+        probs = _f32(w / w.sum(-1, keepdims=True))
+        nq = _f32(rng.standard_normal((N, T, A)))
+    acts = rng.integers(0, A, (N, T)).astype(np.int64)
+    mu = _f32(rng.uniform(0.1, 1.0, (N, T)))
+    q = _f32(rng.standard_normal((N, T)))
+    r = _f32(rng.standard_normal((N, T)))
+    term, trunc = _flags(rng, N, T, 0.1, 0.1)
+    return probs, nq, acts, mu, q, r, term, trunc
+
+
+def check_retrace_actions_golden(orc):
+    """The hand-worked two-action example (API reference, compute_retrace)."""
+    with open(GOLDEN_RETRACE_ACTIONS) as f:
+        c = json.load(f)
+    i, p = c["inputs"], c["params"]
+    qret, adv = orc.retrace_actions(
+        _f32(i["action_probs_target"]), _f32(i["action_probs_behavior"]), _f32(i["q_values"]),
+        _f32(i["next_q_values_all"]), np.asarray(i["actions"], np.int64), _f32(i["rewards"]),
+        _f32(i["terminateds"]), None, p["gamma"], p["lambda_"], p["c_bar"], p["rho_bar"])
+    _close(qret, c["expected"]["retrace_targets"], tol=0.0, what="retrace actions golden Q_ret")
+    _close(adv, c["expected"]["advantages"], tol=0.0, what="retrace actions golden advantages")
+
+
+def check_retrace_actions_reduction(orc):
+    """The action dimension enters only through the library gather
+    pi_t = take_along_axis(pi_target, actions) and the library contraction
+    EQ_t = einsum(pi_target[t,:], Qnext[t,:]) at the same step: with
+    binary-fraction inputs both are exact, and the result must equal Retrace
+    on those per-step values bit for bit."""
+    rng = np.random.default_rng(21)
+    N, T, A, g, l = 4, 37, 5, 0.9, 0.8
+    probs, nq, acts, mu, q, r, term, trunc = _retrace_actions_inputs(rng, N, T, A, True)
+    pi = np.take_along_axis(probs, acts[..., None], axis=-1)[..., 0]
+    eq = np.einsum("nta,nta->nt", probs.astype(np.float64), nq.astype(np.float64))
+    assert np.array_equal(_f32(eq).astype(np.float64), eq)
+    for tr in (None, trunc):
+        want = orc.retrace(pi, mu, q, _f32(eq), r, term, tr, g, l, 1.0, 0.9)
+        got = orc.retrace_actions(probs, mu, q, nq, acts, r, term, tr, g, l, 1.0, 0.9)
+        _close(got[0], want[0], tol=0.0, what="retrace actions targets vs gathered inputs")
+        _close(got[1], want[1], tol=0.0, what="retrace actions advantages vs gathered inputs")
+
+
+def check_retrace_actions_relabelling(orc):
+    """Renaming the actions by a permutation (columns of both [N,T,A] arrays
+    and the action indices together) leaves every output unchanged."""
+    rng = np.random.default_rng(22)
+    N, T, A, g, l = 3, 29, 4, 0.95, 0.9
+    probs, nq, acts, mu, q, r, term, trunc = _retrace_actions_inputs(rng, N, T, A, False)
+    sigma = np.array([2, 0, 3, 1])
+    inv = np.argsort(sigma)
+    base = orc.retrace_actions(probs, mu, q, nq, acts, r, term, trunc, g, l, 1.0, 1.0)
+    perm = orc.retrace_actions(np.ascontiguousarray(probs[..., inv]), mu, q,
+                               np.ascontiguousarray(nq[..., inv]), sigma[acts], r, term, trunc,
+                               g, l, 1.0, 1.0)
+    _close(perm[0], base[0], tol=1e-12, what="retrace actions relabelled targets")
+    _close(perm[1], base[1], tol=1e-12, what="retrace actions relabelled advantages")
+
+
+def check_retrace_actions_one_hot(orc):
+    """A deterministic target policy (one-hot on action b_t) with mu = 1:
+    EQ_t = Qnext[t, b_t], the traces are c_t = lambda [a_t = b_t] and rho_t =
+    [a_t = b_t], and Delta_t is the telescoped sum
+    sum_{k>=t} gamma^{k-t} prod_{i=t+1}^{k} c_i (1 - done_{i-1}) delta_k
+    (Retrace tutorial Sec. 2) with delta_k = r_k + gamma (1-term_k) EQ_k - Q_k."""
+    rng = np.random.default_rng(23)
+    N, T, A, g, l = 3, 19, 3, 0.9, 0.7
+    b = rng.integers(0, A, (N, T))
+    acts = np.where(rng.random((N, T)) < 0.7, b, rng.integers(0, A, (N, T))).astype(np.int64)
+    probs = _f32(np.eye(A)[b])
+    nq = _f32(rng.standard_normal((N, T, A)))
+    mu = np.ones((N, T), np.float32)
+    q = _f32(rng.standard_normal((N, T)))
+    r = _f32(rng.standard_normal((N, T)))
+    term, trunc = _flags(rng, N, T, 0.1, 0.1)
+    qret, adv = orc.retrace_actions(probs, mu, q, nq, acts, r, term, trunc, g, l, 1.0, 1.0)
+    hit = (acts == b).astype(np.float64)
+    eqv = np.take_along_axis(_d64(nq), b[..., None], axis=-1)[..., 0]
+    delta = _d64(r) + g * (1.0 - _d64(term)) * eqv - _d64(q)
+    done = np.minimum(1.0, _d64(term) + _d64(trunc))
+    want = np.zeros((N, T))
+    for n in range(N):
+        for t in range(T):
+            acc, prod = 0.0, 1.0
+            for k in range(t, T):
+                if k > t:
+                    prod *= l * hit[n, k] * (1.0 - done[n, k - 1])
+                acc += g ** (k - t) * prod * delta[n, k]
+            want[n, t] = acc
+    _close(qret - _d64(q), want, what="retrace one-hot telescoped sum")
+    qn = np.concatenate([qret[:, 1:], np.zeros((N, 1))], axis=1)
+    _close(adv, hit * (_d64(r) + g * (1.0 - _d64(term)) * qn - _d64(q)),
+           what="retrace one-hot advantages")
+
+
 ALL_CHECKS = [
     check_golden,
     check_brute_force,
@@ -599,6 +708,10 @@ ALL_CHECKS = [
     check_forward_scans,
     check_appendix_a_polynomial,
     check_severing_and_continuation,
+    check_retrace_actions_golden,
+    check_retrace_actions_reduction,
+    check_retrace_actions_relabelling,
+    check_retrace_actions_one_hot,
 ]
 
 

@@ -50,16 +50,28 @@ MUTANTS = {
         "double nvs = continuation(vrow, t, T, trunc, bs, last_value, row, rs);"),
     # Retrace: trace weight c_t instead of c_{t+1}
     "retrace_no_index_shift": (
-        "c_next = lam * min2(c_bar, AT(pi, row, t + 1, rs) / AT(mu, row, t + 1, rs));",
-        "c_next = lam * min2(c_bar, AT(pi, row, t, rs) / AT(mu, row, t, rs));"),
+        "c_next = lam * min2(c_bar, pi[t + 1] / AT(mu, row, t + 1, rs));",
+        "c_next = lam * min2(c_bar, pi[t] / AT(mu, row, t, rs));"),
     # Retrace: lambda dropped from c
     "retrace_drop_lambda": (
-        "c_next = lam * min2(c_bar, AT(pi, row, t + 1, rs) / AT(mu, row, t + 1, rs));",
-        "c_next = min2(c_bar, AT(pi, row, t + 1, rs) / AT(mu, row, t + 1, rs));"),
+        "c_next = lam * min2(c_bar, pi[t + 1] / AT(mu, row, t + 1, rs));",
+        "c_next = min2(c_bar, pi[t + 1] / AT(mu, row, t + 1, rs));"),
     # Retrace: advantage not gated by termination
     "retrace_adv_gate": (
         "adv[t] = rho * (AT(r, row, t, rs) + gamma * (1.0 - te) * qn - AT(q, row, t, rs));",
         "adv[t] = rho * (AT(r, row, t, rs) + gamma * qn - AT(q, row, t, rs));"),
+    # Retrace front end: successor Q weighted with the next step's probabilities
+    "retrace_actions_next_step_weights": (
+        "for (int64_t a = 0; a < A; ++a) s += (double)pt[a] * (double)qt[a];",
+        "for (int64_t a = 0; a < A; ++a) s += (double)(t + 1 < T ? pt + A : pt)[a] * (double)qt[a];"),
+    # Retrace front end: taken-action probability gathered from the Q-values
+    "retrace_actions_gather_q": (
+        "pi_d[t] = (double)pt[at];",
+        "pi_d[t] = (double)qt[at];"),
+    # Retrace front end: action index mirrored
+    "retrace_actions_gather_index": (
+        "pi_d[t] = (double)pt[at];",
+        "pi_d[t] = (double)pt[A - 1 - at];"),
     # TD(lambda): (1 - lambda) weight replaced by lambda
     "td_value_weight": (
         "double G = AT(r, row, t, rs) + gamma * (1.0 - lam) * nd * AT(nv, row, t, rs)",
