@@ -65,6 +65,13 @@ def _cfg_workloads():
             desc="Retrace(lambda) on per-step inputs, no truncations", N=1024, T=16384,
             gen=lambda N, T: synthetic.config_batch(3, N=N, T=T),
             estimators=[("retrace", 32, c3)]),
+        "retrace_actions_1024x16384x4": dict(
+            desc="Retrace(lambda) from [N,T,A] target probabilities and successor Q-values with "
+                 "int64 actions (A = 4), reduced in-kernel, no truncations",
+            N=1024, T=16384,
+            gen=lambda N, T: synthetic.retrace_actions_batch(N, T, 4, 0, 3, c3["p_term"], 0.0),
+            # 2 x [N,T,4] f32 + int64 action + 4 [N,T] f32 in, 2 [N,T] f32 out
+            estimators=[("retrace_actions", 64, c3)]),
         "long_rows_64x1048576": dict(
             desc="eligibility traces + episodic prefix sum (starts_at, integer inputs)",
             N=64, T=1 << 20, gen=lambda N, T: synthetic.config_batch(4, N=N, T=T),
@@ -96,6 +103,8 @@ IO = {
                 "truncateds", "bootstrap_values"], [], 2),
     "retrace": (["pi_taken", "mu_taken", "q_values", "expected_next_q", "rewards", "terminateds"],
                 [], 2),
+    "retrace_actions": (["action_probs_target", "action_probs_behavior", "q_values",
+                         "next_q_values_all", "actions", "rewards", "terminateds"], [], 2),
     "eligibility_traces": (["gradients", "trace_dones"], [], 1),
     "episodic_prefix_sum": (["inputs", "prefix_dones"], [], 1),
     "gae_returns": (["rewards", "values", "terminateds"], ["last_value"], 3),
@@ -238,6 +247,13 @@ def _launcher(name, c, bufs, outs, N, T, ws, wsn, stream):
                                           b["expected_next_q"], b["rewards"], b["terminateds"],
                                           None, N, T, T, g, float(c["lambda_"]), float(c["c_bar"]),
                                           float(c["rho_bar"]), o[0], o[1], ws, wsn, stream)
+    if name == "retrace_actions":
+        A = bufs["action_probs_target"].shape[2]
+        return lambda: lib.rlscan_retrace_actions(
+            b["action_probs_target"], b["action_probs_behavior"], b["q_values"],
+            b["next_q_values_all"], b["actions"], b["rewards"], b["terminateds"], None, N, T, A, T,
+            T * A, g, float(c["lambda_"]), float(c["c_bar"]), float(c["rho_bar"]), o[0], o[1], ws,
+            wsn, stream)
     if name == "eligibility_traces":
         return lambda: lib.rlscan_eligibility_traces(b["gradients"], b["trace_dones"], None, N, T,
                                                      T, g, float(c["lambda_"]), o[0], ws, wsn,
@@ -278,6 +294,11 @@ def _public_call(name, c, t):
                                                   t["expected_next_q"], t["rewards"],
                                                   t["terminateds"], None, g, c["lambda_"],
                                                   c["c_bar"], c["rho_bar"]))
+    if name == "retrace_actions":
+        return list(Lb.compute_retrace(t["action_probs_target"], t["action_probs_behavior"],
+                                       t["q_values"], t["next_q_values_all"], t["actions"],
+                                       t["rewards"], t["terminateds"], None, g, c["lambda_"],
+                                       c["c_bar"], c["rho_bar"]))
     if name == "eligibility_traces":
         return [Lb.compute_eligibility_traces(t["gradients"], t["trace_dones"], g, c["lambda_"])]
     if name == "episodic_prefix_sum":
@@ -380,10 +401,10 @@ def run_ours(args, wl_name, rank, world, local_rank):
     # call(s), results back to pinned host memory, every step
     e2e_in = sorted({k for (n, _, _) in step_kernels for k in IO[n][0] + IO[n][1]})
     pinned = {k: torch.from_numpy(host[k]).pin_memory() for k in e2e_in}
-    dbufs = {k: torch.empty(v.shape, dtype=torch.float32, device=dev) for k, v in pinned.items()}
+    dbufs = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pinned.items()}
     out_host = [torch.empty((N, T), dtype=torch.float32).pin_memory()
                 for (n, _, _) in step_kernels for _ in range(IO[n][2])]
-    h2d = sum(v.numel() * 4 for v in pinned.values())
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = sum(o.numel() * 4 for o in out_host)
 
     def e2e_step():
@@ -474,6 +495,11 @@ def _oracle_call(name, c, b):
         return oracle.retrace(b["pi_taken"], b["mu_taken"], b["q_values"], b["expected_next_q"],
                               b["rewards"], b["terminateds"], None, g, c["lambda_"], c["c_bar"],
                               c["rho_bar"])
+    if name == "retrace_actions":
+        return oracle.retrace_actions(b["action_probs_target"], b["action_probs_behavior"],
+                                      b["q_values"], b["next_q_values_all"], b["actions"],
+                                      b["rewards"], b["terminateds"], None, g, c["lambda_"],
+                                      c["c_bar"], c["rho_bar"])
     if name == "eligibility_traces":
         return oracle.eligibility_traces(b["gradients"], b["trace_dones"], g, c["lambda_"])
     if name == "episodic_prefix_sum":

@@ -237,6 +237,46 @@ rlscan_status rlscan_retrace(const float *pi_taken, const float *mu_taken, const
                              void *ws, size_t ws_bytes, rlscan_stream_t stream);
 
 /*
+ * Retrace(lambda) targets and advantages from the full action-space inputs,
+ * the argument set of the rl-triton API reference's compute_retrace
+ * (action_probs_target and next_q_values_all [N,T,A], actions int64 [N,T]).
+ * The action dimension is reduced inside the kernel, per step:
+ *   EQ_t = sum_a pi_target[t,a] * next_q_values_all[t,a]      (a = 0 .. A-1)
+ *   pi_t = pi_target[t, actions[t]]
+ * then the recurrence of rlscan_retrace with mu_t = action_probs_behavior[t].
+ * The target weights are those stored at the same step t: the API's
+ * reduction multiplies the two [N,T,A] tensors element-wise (its
+ * mathematical text weights Q(s_{t+1},.) with pi(.|s_{t+1}); a caller who
+ * wants that stores pi(.|s_{t+1}) at step t).
+ * Layout : action_probs_target and next_q_values_all are float32 [N,T,A]
+ *          with element (n,t,a) at n * action_row_stride + t * A + a
+ *          (action_row_stride >= T * A, the same for both); actions is int64
+ *          [N,T] and every float32 [N,T] argument has row stride row_stride.
+ * Inputs : action_probs_target, action_probs_behavior, q_values,
+ *          next_q_values_all, actions, rewards, terminateds; truncateds
+ *          nullable (zero).
+ * Outputs: retrace_targets, advantages [N,T].
+ * An action outside [0, A) makes pi_t NaN (its row's outputs are then NaN
+ * up to the row start); with RLSCAN_CHECKS=1 such a call returns
+ * RLSCAN_ERR_INVALID_INPUT instead.
+ * Errors : RLSCAN_ERR_ARG_VALUE when A < 1 or A > 65536; RLSCAN_ERR_SHAPE
+ *          when action_row_stride < T * A.
+ * The [N,T,A] rows are staged into shared memory with bulk copies when they
+ * are 16-byte aligned (action_row_stride a multiple of 4) and a 1024-step
+ * tile of them fits the ring (A <= 9); otherwise the kernel reads them from
+ * global memory.  Both give the same results.
+ */
+rlscan_status rlscan_retrace_actions(const float *action_probs_target,
+                                     const float *action_probs_behavior, const float *q_values,
+                                     const float *next_q_values_all, const int64_t *actions,
+                                     const float *rewards, const float *terminateds,
+                                     const float *truncateds, int64_t N, int64_t T, int64_t A,
+                                     int64_t row_stride, int64_t action_row_stride,
+                                     float gamma, float lambda, float c_bar, float rho_bar,
+                                     float *retrace_targets, float *advantages,
+                                     void *ws, size_t ws_bytes, rlscan_stream_t stream);
+
+/*
  * TD(lambda) returns.
  * rl-triton API reference, compute_lambda_returns; rl-triton paper Table 1
  * row "TD(lambda)" and Sec. 3.3.4; "Returns and Eligibility Traces with

@@ -50,6 +50,7 @@ SIGNATURES = {
     "rlscan_gae_returns": ([_P] * 6 + [_I64] * 3 + [_F, _F, _P, _P, _P, _P, _SZ, _P], _I),
     "rlscan_vtrace": ([_P] * 8 + [_I64] * 3 + [_F, _F, _F, _P, _P, _P, _SZ, _P], _I),
     "rlscan_retrace": ([_P] * 7 + [_I64] * 3 + [_F] * 4 + [_P, _P, _P, _SZ, _P], _I),
+    "rlscan_retrace_actions": ([_P] * 8 + [_I64] * 5 + [_F] * 4 + [_P, _P, _P, _SZ, _P], _I),
     "rlscan_lambda_returns": ([_P] * 6 + [_I64] * 3 + [_F, _F, _P, _P, _SZ, _P], _I),
     "rlscan_discounted_returns": ([_P] * 5 + [_I64] * 3 + [_F, _P, _P, _SZ, _P], _I),
     "rlscan_eligibility_traces": ([_P] * 3 + [_I64] * 3 + [_F, _F, _P, _P, _SZ, _P], _I),

@@ -14,7 +14,8 @@ import torch
 from . import _native
 
 __all__ = [
-    "compute_gae", "compute_gae_and_returns", "compute_vtrace", "compute_retrace_from_probs", "compute_lambda_returns",
+    "compute_gae", "compute_gae_and_returns", "compute_vtrace", "compute_retrace",
+    "compute_retrace_from_probs", "compute_lambda_returns",
     "compute_discounted_returns", "compute_eligibility_traces", "compute_episodic_prefix_sum",
     "linear_scan", "workspace_status",
 ]
@@ -216,6 +217,64 @@ def compute_vtrace(log_pi_target, log_pi_behavior, values, rewards, terminateds,
         c.N, c.T, c.rs, float(gamma), float(rho_bar), float(c_bar), _vp(vs), _vp(adv),
         ws, wsn, s), "rlscan_vtrace")
     return vs, adv
+
+
+def compute_retrace(action_probs_target, action_probs_behavior, q_values, next_q_values_all,
+                    actions, rewards, terminateds, truncateds=None, gamma=0.99, lambda_=1.0,
+                    c_bar=1.0, rho_bar=1.0):
+    """Retrace(lambda) (targets, advantages) from the full action-space inputs
+    (rl-triton API reference, compute_retrace): action_probs_target and
+    next_q_values_all [N,T,A] float32, actions [N,T] int64, the other
+    arguments [N,T] float32.  The action dimension is reduced inside the
+    kernel: E_pi[Q'] with the target probabilities of the same step, and
+    pi(a_t|s_t) gathered at ``actions``."""
+    c = _Call("rewards", rewards)
+    for name, t in (("action_probs_behavior", action_probs_behavior), ("q_values", q_values),
+                    ("rewards", rewards), ("terminateds", terminateds)):
+        c.mat(name, t)
+    c.mat("truncateds", truncateds, False)
+    if not isinstance(actions, torch.Tensor) or actions.dtype != torch.int64:
+        raise TypeError("actions must be an int64 torch.Tensor")
+    if not actions.is_cuda or actions.device != c.device:
+        raise ValueError(f"actions must be on {c.device}")
+    if tuple(actions.shape) != (c.N, c.T):
+        raise ValueError(f"actions shape {tuple(actions.shape)} != {(c.N, c.T)}")
+    wide = []
+    for name, t in (("action_probs_target", action_probs_target),
+                    ("next_q_values_all", next_q_values_all)):
+        if not isinstance(t, torch.Tensor) or t.dim() != 3:
+            raise ValueError(f"{name} must be a [num_envs, seq_len, num_actions] tensor")
+        _check(name, t, (c.N, c.T, t.shape[2]), c.device)
+        wide.append(t)
+    A = wide[0].shape[2]
+    if wide[1].shape[2] != A:
+        raise ValueError("action_probs_target and next_q_values_all differ in num_actions")
+    qret, adv = c.finish(2)
+    # actions share the float arrays' row stride; the [N,T,A] pair shares one
+    # row stride of its own with unit inner strides
+    acts = actions
+    if c.N > 1 and acts.stride(0) != c.rs or (c.T > 1 and acts.stride(1) != 1):
+        acts = torch.empty_strided((c.N, c.T), (c.rs, 1), dtype=torch.int64, device=c.device)
+        acts.copy_(actions)
+
+    def inner_ok(t):
+        return (A <= 1 or t.stride(2) == 1) and (c.T <= 1 or t.stride(1) == A)
+    ars = c.T * A
+    if all(inner_ok(t) for t in wide) and (c.N <= 1 or len({t.stride(0) for t in wide}) == 1):
+        if c.N > 1:
+            ars = wide[0].stride(0)
+    else:
+        ars = -1
+    if ars < c.T * A:
+        wide = [t.contiguous() for t in wide]
+        ars = c.T * A
+    ws, wsn, s = _ws_for(c)
+    _native.check(_native.lib().rlscan_retrace_actions(
+        _vp(wide[0]), c.m("action_probs_behavior"), c.m("q_values"), _vp(wide[1]), _vp(acts),
+        c.m("rewards"), c.m("terminateds"), c.m("truncateds"), c.N, c.T, A, c.rs, ars,
+        float(gamma), float(lambda_), float(c_bar), float(rho_bar), _vp(qret), _vp(adv),
+        ws, wsn, s), "rlscan_retrace_actions")
+    return qret, adv
 
 
 def compute_retrace_from_probs(pi_taken, mu_taken, q_values, expected_next_q, rewards,

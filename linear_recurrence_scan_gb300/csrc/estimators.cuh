@@ -33,12 +33,17 @@
 #pragma once
 
 #include "params.cuh"
+#include "ptx.cuh"
 
 namespace rlscan {
 namespace est {
 
 // done_t = min(1, terminated_t + truncated_t)
 __device__ __forceinline__ float done_of(float term, float trunc) { return fminf(1.f, term + trunc); }
+
+// min(clip, x) that keeps a NaN x (fminf would return the clip), so an
+// undefined ratio such as 0/0 shows in the outputs instead of being clipped
+__device__ __forceinline__ float clip_above(float clip, float x) { return clip < x ? clip : x; }
 
 // ---------------------------------------------------------------------------
 // GAE: alpha = r + gamma (1-term) Vn - V, beta = gamma lambda (1-done), A_T = 0.
@@ -130,7 +135,7 @@ struct VTrace {
         for (int k = 0; k < I; ++k) {
             const bool last = (EDGE && k == kb);
             const float ratio = expf(x[0][k] - x[1][k]);
-            const float rho = fminf(p.c1, ratio), c = fminf(p.c2, ratio);
+            const float rho = clip_above(p.c1, ratio), c = clip_above(p.c2, ratio);
             const float term = x[4][k];
             const float vn = successor<I>(x, k, last, (k + 1 < I) ? x[2][k + 1] : xn[2], rsc);
             float done;
@@ -185,10 +190,10 @@ struct Retrace {
 #pragma unroll
         for (int k = 0; k < I; ++k) {
             const float ratio = x[0][k] / x[1][k];
-            c[k] = lam * fminf(p.c2, ratio);
-            keep.rho[k] = fminf(p.c3, ratio);
+            c[k] = lam * clip_above(p.c2, ratio);
+            keep.rho[k] = clip_above(p.c3, ratio);
         }
-        c[I] = lam * fminf(p.c2, xn[0] / xn[1]);
+        c[I] = lam * clip_above(p.c2, xn[0] / xn[1]);
 #pragma unroll
         for (int k = 0; k < I; ++k) {
             const bool last = (EDGE && k == kb);
@@ -216,6 +221,98 @@ struct Retrace {
             const float term = x[5][k];
             o[0][k] = A[0][k] + x[2][k];
             o[1][k] = keep.rho[k] * (fmaf(g * (1.f - term), qn, x[4][k]) - x[2][k]);
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Retrace from the full action-space inputs (API reference, compute_retrace
+// signature): the narrow inputs of Retrace above, except that pi (0) and
+// EQ (3) are not read from global memory.  prepass() derives them per step
+// from three wide arrays staged beside the narrow ones:
+//   wide 0  target probabilities pi(.|s_t)     A words per step
+//   wide 1  successor values Q(s_{t+1}, .)     A words per step
+//   wide 2  int64 action a_t                   2 words per step
+//   EQ_t = sum_a pi(a|s_t) Q(s_{t+1}, a)   (weights of the same step t, as
+//          the API's reduction multiplies the two [N,T,A] tensors)
+//   pi_t = pi(a_t|s_t), NaN when a_t lies outside [0, A)
+// Inputs (narrow): 1 mu, 2 q, 4 rewards, 5 terminateds, [6 truncateds].
+template <bool TRUNC>
+struct RetraceActions : Retrace<TRUNC> {
+    static constexpr int NWIDE = 3;
+    static constexpr unsigned DERIVED = (1u << 0) | (1u << 3);
+    static constexpr int PI = 0, EQ = 3;
+
+    __host__ __device__ static int wide_words(int w, int A) { return w < 2 ? A : 2; }
+
+    // Fill the derived arrays of one tile (pi_out / eq_out: their stage
+    // slots, data from offset 4).  Step e of the tile (packed: row e / C,
+    // column e % C; long rows: e < len, plus e = len for the step after the
+    // tile) is read from the stage's wide region `wsm` when `staged`, else
+    // from global memory.  Consecutive threads take consecutive steps, so
+    // the wide rows are read without bank conflicts (shared) or coalesced
+    // (global).  The derived slots overlay the wide region, so when staged
+    // every thread reads all its steps before any thread writes (named
+    // barrier BAR of the THREADS compute threads).
+    template <int TILE, int AST, int THREADS, int BAR, class Geo>
+    __device__ static void prepass(const Params &p, const Geo &tg, float *pi_out, float *eq_out,
+                                   const float *wsm, bool staged, int tid)
+    {
+        constexpr int MAXK = TILE / THREADS + 1;
+        const int A = p.A;
+        const int total = p.packed ? tg.nrows * p.C : tg.len + ((tg.t0 + tg.len < p.T) ? 1 : 0);
+        const float *sp = wsm;
+        const float *sq = wsm + (TILE + 4) * A;
+        const long long *sa = reinterpret_cast<const long long *>(wsm + 2 * (TILE + 4) * A);
+        const float nan = __int_as_float(0x7fc00000);
+        float pv[MAXK], ev[MAXK];
+#pragma unroll
+        for (int k = 0; k < MAXK; ++k) {
+            const int e = tid + k * THREADS;
+            pv[k] = 0.f;
+            ev[k] = 0.f;
+            if (e >= total) continue;
+            int i = 0, c = e;
+            if (p.packed) {
+                i = e / p.C;
+                c = e - i * p.C;
+                if (c >= tg.len) continue;
+            }
+            if (staged && A == 4) {
+                const float4 u = *reinterpret_cast<const float4 *>(sp + 4 * e);
+                const float4 v = *reinterpret_cast<const float4 *>(sq + 4 * e);
+                const long long a = sa[e];
+                const int ai = static_cast<int>(a);
+                ev[k] = fmaf(u.w, v.w, fmaf(u.z, v.z, fmaf(u.y, v.y, u.x * v.x)));
+                const float pk = ai == 0 ? u.x : (ai == 1 ? u.y : (ai == 2 ? u.z : u.w));
+                pv[k] = static_cast<unsigned long long>(a) < 4ull ? pk : nan;
+                continue;
+            }
+            const float *pr, *nq;
+            long long a;
+            if (staged) {
+                pr = sp + e * A;
+                nq = sq + e * A;
+                a = sa[e];
+            } else {
+                const int64_t row = tg.row0 + i, t = tg.t0 + c;
+                pr = static_cast<const float *>(p.wide[0]) + row * p.wide_rs[0] + t * A;
+                nq = static_cast<const float *>(p.wide[1]) + row * p.wide_rs[1] + t * A;
+                a = __ldg(reinterpret_cast<const long long *>(p.wide[2]) + (row * p.wide_rs[2] >> 1) + t);
+            }
+            float eq = 0.f;
+            for (int q = 0; q < A; ++q) eq = fmaf(pr[q], nq[q], eq);
+            ev[k] = eq;
+            pv[k] = (a >= 0 && a < A) ? pr[a] : nan;
+        }
+        if (staged) ptx::named_barrier(BAR, THREADS);
+#pragma unroll
+        for (int k = 0; k < MAXK; ++k) {
+            const int e = tid + k * THREADS;
+            if (e < total) {
+                pi_out[4 + e] = pv[k];
+                eq_out[4 + e] = ev[k];
+            }
         }
     }
 };

@@ -32,17 +32,29 @@ namespace rlscan {
 #ifndef RLSCAN_THREADS_2048
 #define RLSCAN_THREADS_2048 256
 #endif
+// Estimators with wide inputs (several words per step, e.g. [N,T,A]) move
+// far more bytes per step: 1024-step tiles, and a ring of WIDE_STAGES stages
+// whose size depends on the runtime width (one CTA per SM at A = 4).
+#ifndef RLSCAN_WIDE_THREADS
+#define RLSCAN_WIDE_THREADS 256
+#endif
+#ifndef RLSCAN_WIDE_STAGES
+#define RLSCAN_WIDE_STAGES 2
+#endif
 
 template <class E>
 struct Shape {
+    static constexpr bool WIDE = WideOf<E>::NWIDE > 0;
     static constexpr int BYTES_PER_STEP = 4 * (E::NIN + E::NOUT);
     static constexpr int TILE_RAW = RLSCAN_TILE_BYTES_TARGET / BYTES_PER_STEP;
-    static constexpr int TILE = TILE_RAW >= 3072 ? 4096 : (TILE_RAW >= 1536 ? 2048 : 1024);
-    static constexpr int THREADS = TILE >= 4096 ? 256 : (TILE >= 2048 ? RLSCAN_THREADS_2048 : 128);
+    static constexpr int TILE = WIDE ? 1024 : (TILE_RAW >= 3072 ? 4096 : (TILE_RAW >= 1536 ? 2048 : 1024));
+    static constexpr int THREADS = WIDE ? RLSCAN_WIDE_THREADS
+                                        : (TILE >= 4096 ? 256 : (TILE >= 2048 ? RLSCAN_THREADS_2048 : 128));
     static constexpr int ITEMS = TILE / THREADS;
-    static constexpr int STAGE_BYTES = E::NIN * (TILE + 8) * 4;
+    static constexpr int STAGE_BYTES = E::NIN * (TILE + 8) * 4;  // narrow arrays
     static constexpr int RAW = (RLSCAN_SMEM_BUDGET_KB * 1024) / STAGE_BYTES;
-    static constexpr int STAGES = RAW < 2 ? 2 : (RAW > RLSCAN_MAX_STAGES ? RLSCAN_MAX_STAGES : RAW);
+    static constexpr int STAGES = WIDE ? RLSCAN_WIDE_STAGES
+                                       : (RAW < 2 ? 2 : (RAW > RLSCAN_MAX_STAGES ? RLSCAN_MAX_STAGES : RAW));
     static_assert(TILE == THREADS * ITEMS, "tile shape");
 };
 
@@ -56,7 +68,7 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
     using S = Shape<E>;
     constexpr int TILE = S::TILE;
     auto kernel = scan_kernel<E, S::THREADS, S::ITEMS, S::STAGES>;
-    const size_t smem = static_cast<size_t>(S::STAGES) * S::STAGE_BYTES;
+    size_t smem = static_cast<size_t>(S::STAGES) * S::STAGE_BYTES;
 
     if (p.T <= TILE) {
         p.packed = 1;
@@ -92,24 +104,65 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RLSCAN_ERR_CUDA;
+    // per device: SM count, dynamic shared memory a CTA may opt into (the
+    // device limit less the kernel's static shared memory), and resident
+    // CTAs for the last dynamic size (fixed per instantiation, except for
+    // wide inputs, whose stage size depends on the width)
     static std::mutex mu;
     static int blocks_per_sm[kMaxDevices];
     static int sm_count[kMaxDevices];
+    static size_t max_dyn[kMaxDevices];
+    static size_t occ_smem[kMaxDevices];
+    size_t dyn_limit = 0;
+    {
+    std::lock_guard<std::mutex> lock(mu);
+    if (sm_count[dev] == 0) {
+        int sms = 0, optin = 0;
+        cudaFuncAttributes fa;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa, kernel) != cudaSuccess)
+            return RLSCAN_ERR_CUDA;
+        const size_t dyn = static_cast<size_t>(optin) > fa.sharedSizeBytes ? optin - fa.sharedSizeBytes : 0;
+        if (dyn < smem) return RLSCAN_ERR_CUDA;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(S::WIDE ? dyn : smem)) != cudaSuccess)
+            return RLSCAN_ERR_CUDA;
+        max_dyn[dev] = dyn;
+        sm_count[dev] = sms > 0 ? sms : 1;
+    }
+    dyn_limit = max_dyn[dev];
+    }
+    if constexpr (S::WIDE) {
+        // stage the wide arrays when they are aligned and the ring fits
+        int64_t wide_floats = 0;
+        bool wide_ok = tma;
+        for (int w = 0; w < WideOf<E>::NWIDE; ++w) {
+            wide_floats += static_cast<int64_t>(TILE + 4) * p.wide_words[w];
+            wide_ok = wide_ok && aligned16(p.wide[w]) && (p.wide_rs[w] % 4 == 0);
+        }
+        // copied narrow arrays, then the wide region, which the derived
+        // arrays overlay (they need a region of their own when not staged)
+        const int64_t copied = static_cast<int64_t>(narrow_copied<E>()) * (TILE + 8);
+        const int64_t derived = static_cast<int64_t>(E::NIN - narrow_copied<E>()) * (TILE + 8);
+        const int64_t staged_floats = copied + (wide_floats > derived ? wide_floats : derived);
+        wide_ok = wide_ok && static_cast<size_t>(S::STAGES) * staged_floats * 4 <= dyn_limit;
+        p.wide_staged = wide_ok ? 1 : 0;
+        p.stage_floats = static_cast<int32_t>(wide_ok ? staged_floats : copied + derived);
+        smem = static_cast<size_t>(S::STAGES) * p.stage_floats * 4;
+    }
+    int64_t slots = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (sm_count[dev] == 0) {
-            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem)) != cudaSuccess)
-                return RLSCAN_ERR_CUDA;
-            int occ = 0, sms = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, block_threads<S::THREADS>(), smem) != cudaSuccess ||
-                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        if (occ_smem[dev] != smem) {
+            int occ = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, block_threads<S::THREADS>(), smem) != cudaSuccess)
                 return RLSCAN_ERR_CUDA;
             blocks_per_sm[dev] = occ > 0 ? occ : 1;
-            sm_count[dev] = sms > 0 ? sms : 1;
+            occ_smem[dev] = smem;
         }
+        slots = static_cast<int64_t>(sm_count[dev]) * blocks_per_sm[dev];
     }
-    const int64_t slots = static_cast<int64_t>(sm_count[dev]) * blocks_per_sm[dev];
     const int64_t grid = p.num_tiles < slots ? p.num_tiles : slots;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));

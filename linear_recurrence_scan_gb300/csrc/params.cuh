@@ -12,6 +12,7 @@
 namespace rlscan {
 
 constexpr int kMaxIn = 8;
+constexpr int kMaxWide = 3;  // staged arrays with several 4-byte words per step
 
 // Workspace layout: a 64-byte header followed by one 16-byte state per tile
 // and scan (an estimator solves up to kMaxScans recurrences per step).
@@ -50,6 +51,15 @@ struct Params {
     uint64_t spin_limit_ns;    // bound on every look-back wait
     uint64_t copy_limit_ns;    // bound on every wait for a bulk copy
     int64_t withhold_tile;     // test hook: this tile never publishes (-1: none)
+
+    // wide inputs (several 4-byte words per step, e.g. [N, T, A] arrays),
+    // used only by estimators that declare them
+    const void *wide[kMaxWide];
+    int64_t wide_rs[kMaxWide];    // row stride in 4-byte words
+    int32_t wide_words[kMaxWide]; // 4-byte words per step
+    int32_t wide_staged;          // 1: copied into the stage; 0: read from global memory
+    int32_t stage_floats;         // floats per ring stage (narrow and wide regions)
+    int32_t A;                    // number of actions
 };
 
 // Launchers (one translation unit per estimator family).
@@ -57,6 +67,7 @@ rlscan_status launch_gae(bool trunc, bool bs2d, Params p, void *ws, size_t ws_by
 rlscan_status launch_gae_returns(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_vtrace(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_retrace(bool trunc, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
+rlscan_status launch_retrace_actions(bool trunc, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_lambda_returns(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_discounted(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_eligibility(Params p, void *ws, size_t ws_bytes, cudaStream_t s);

@@ -121,6 +121,41 @@ rlscan_status run_checks(const float *term, const float *trunc, const float *bs,
     return flags ? RLSCAN_ERR_INVALID_INPUT : RLSCAN_OK;
 }
 
+// Every action index in [0, A) (compute_retrace gathers pi_target at it).
+__global__ void check_actions(const long long *actions, int64_t N, int64_t T, int64_t rs, int64_t A)
+{
+    uint32_t bad = 0;
+    const int64_t total = N * T;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row = i / T, t = i - row * T;
+        const long long a = actions[row * rs + t];
+        if (a < 0 || a >= A) bad = 4u;
+    }
+    if (bad) atomicOr(&g_check_flags, bad);
+}
+
+rlscan_status run_action_checks(const int64_t *actions, int64_t N, int64_t T, int64_t rs, int64_t A,
+                                cudaStream_t stream)
+{
+    if (!checks_enabled()) return RLSCAN_OK;
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_check_flags, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice,
+                                stream) != cudaSuccess)
+        return RLSCAN_ERR_CUDA;
+    int64_t blocks = (N * T + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    check_actions<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        reinterpret_cast<const long long *>(actions), N, T, rs, A);
+    uint32_t flags = 0;
+    if (cudaGetLastError() != cudaSuccess ||
+        cudaMemcpyFromSymbolAsync(&flags, g_check_flags, sizeof(flags), 0, cudaMemcpyDeviceToHost,
+                                  stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return RLSCAN_ERR_CUDA;
+    return flags ? RLSCAN_ERR_INVALID_INPUT : RLSCAN_OK;
+}
+
 inline rlscan_status check_shape(int64_t N, int64_t T, int64_t rs)
 {
     if (N < 0 || T < 0 || rs < T) return RLSCAN_ERR_SHAPE;
@@ -376,6 +411,53 @@ RLSCAN_API rlscan_status rlscan_retrace(const float *pi_taken, const float *mu_t
     p.in[5] = terminateds;
     p.in[6] = truncateds;
     return launch_retrace(truncateds != nullptr, p, ws, ws_bytes, cs(stream));
+}
+
+RLSCAN_API rlscan_status rlscan_retrace_actions(const float *action_probs_target,
+                                                const float *action_probs_behavior,
+                                                const float *q_values, const float *next_q_values_all,
+                                                const int64_t *actions, const float *rewards,
+                                                const float *terminateds, const float *truncateds,
+                                                int64_t N, int64_t T, int64_t A, int64_t row_stride,
+                                                int64_t action_row_stride, float gamma, float lambda,
+                                                float c_bar, float rho_bar, float *retrace_targets,
+                                                float *advantages, void *ws, size_t ws_bytes,
+                                                rlscan_stream_t stream)
+{
+    if (A < 1 || A > 65536) return RLSCAN_ERR_ARG_VALUE;
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (action_row_stride < T * A) return RLSCAN_ERR_SHAPE;
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!action_probs_target || !action_probs_behavior || !q_values || !next_q_values_all || !actions ||
+        !rewards || !terminateds || !retrace_targets || !advantages)
+        return RLSCAN_ERR_NULL;
+    for (const float *o : {static_cast<const float *>(retrace_targets), static_cast<const float *>(advantages)})
+        if (same_as_any(o, {action_probs_target, action_probs_behavior, q_values, next_q_values_all,
+                            actions, rewards, terminateds, truncateds}))
+            return RLSCAN_ERR_ARG_CONFLICT;
+    if (retrace_targets == advantages) return RLSCAN_ERR_ARG_CONFLICT;
+    RLSCAN_TRY(run_checks(terminateds, truncateds, nullptr, N, T, row_stride, cs(stream)));
+    RLSCAN_TRY(run_action_checks(actions, N, T, row_stride, A, cs(stream)));
+    Params p = base_params(N, T, row_stride);
+    p.c0 = gamma;
+    p.c1 = lambda;
+    p.c2 = c_bar;
+    p.c3 = rho_bar;
+    p.out[0] = retrace_targets;
+    p.out[1] = advantages;
+    p.in[1] = action_probs_behavior;
+    p.in[2] = q_values;
+    p.in[4] = rewards;
+    p.in[5] = terminateds;
+    p.in[6] = truncateds;
+    p.A = static_cast<int32_t>(A);
+    p.wide[0] = action_probs_target;
+    p.wide[1] = next_q_values_all;
+    p.wide[2] = actions;
+    p.wide_rs[0] = action_row_stride;
+    p.wide_rs[1] = action_row_stride;
+    p.wide_rs[2] = 2 * row_stride;
+    return launch_retrace_actions(truncateds != nullptr, p, ws, ws_bytes, cs(stream));
 }
 
 RLSCAN_API rlscan_status rlscan_lambda_returns(const float *rewards, const float *next_values,

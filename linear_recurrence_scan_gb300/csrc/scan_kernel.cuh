@@ -53,6 +53,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 
 #include "estimators.cuh"
 #include "params.cuh"
@@ -63,6 +64,42 @@ namespace rlscan {
 struct Pair {
     float a, b;
 };
+
+// Wide inputs of an estimator (none unless it declares NWIDE / DERIVED):
+// NWIDE arrays of several words per step staged after the narrow arrays,
+// and the narrow arrays (bit mask) that prepass() derives from them instead
+// of reading global memory.
+template <class E, class = void>
+struct WideOf {
+    static constexpr int NWIDE = 0;
+    static constexpr unsigned DERIVED = 0u;
+};
+template <class E>
+struct WideOf<E, std::void_t<decltype(E::NWIDE)>> {
+    static constexpr int NWIDE = E::NWIDE;
+    static constexpr unsigned DERIVED = E::DERIVED;
+};
+
+// Shared-memory slot of narrow input j within a stage: the copied arrays
+// first, in input order, then the derived ones.  The wide region starts
+// after the copied arrays and overlays the derived slots: prepass() reads
+// the wide rows, then writes the derived values over them.
+template <class E>
+__host__ __device__ constexpr int narrow_copied()
+{
+    int n = 0;
+    for (int j = 0; j < E::NIN; ++j) n += ((WideOf<E>::DERIVED >> j) & 1u) ? 0 : 1;
+    return n;
+}
+template <class E>
+__host__ __device__ constexpr int slot_of(int j)
+{
+    constexpr unsigned D = WideOf<E>::DERIVED;
+    const bool derived = (D >> j) & 1u;
+    int below = 0;
+    for (int i = 0; i < j; ++i) below += (((D >> i) & 1u) != 0) == derived ? 1 : 0;
+    return derived ? narrow_copied<E>() + below : below;
+}
 
 // outer o inner: x -> outer.a + outer.b * (inner.a + inner.b * x)
 __device__ __forceinline__ Pair compose(Pair outer, Pair inner)
@@ -120,23 +157,46 @@ __device__ __forceinline__ TileGeo decode_tile(const Params &p, int64_t g)
 // Issue the bulk copies of one tile into `stage` (called by one thread).
 // Array j of the stage occupies AST floats; its data start at offset 4, the
 // step before the tile at offset 3 and the step after it at offset 4+TILE.
+// Wide array w (when staged) follows the narrow arrays and occupies
+// (TILE + 4) * words floats: step e of the tile at e * words, the step after
+// the tile right behind the last one.
 template <class E, int TILE, int AST>
 __device__ void issue_tile_copies(const Params &p, const TileGeo &tg, float *stage, uint64_t *bar)
 {
+    constexpr int NW = WideOf<E>::NWIDE;
+    constexpr unsigned DER = WideOf<E>::DERIVED;
+    const bool wide = NW > 0 && p.wide_staged;
+    float *wsm = stage + narrow_copied<E>() * AST;
     if (p.packed) {
-        if (p.rs == p.T && p.C == p.T) {  // rows contiguous in global and in shared memory
-            const uint32_t nb = static_cast<uint32_t>(tg.nrows * p.T * 4);
-            ptx::mbar_arrive_expect_tx(bar, nb * E::NIN);
+        bool contig = p.rs == p.T && p.C == p.T;  // rows contiguous in global and in shared memory
+#pragma unroll
+        for (int w = 0; w < NW; ++w) contig = contig && (!wide || p.wide_rs[w] == p.T * p.wide_words[w]);
+        const int copies = contig ? 1 : tg.nrows;
+        const int64_t steps = contig ? static_cast<int64_t>(tg.nrows) * p.T : p.T;
+        const uint32_t nb = static_cast<uint32_t>(steps * 4);
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int j = 0; j < E::NIN; ++j)
+            if (!((DER >> j) & 1u)) bytes += nb;
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+            if (wide) bytes += nb * static_cast<uint32_t>(p.wide_words[w]);
+        ptx::mbar_arrive_expect_tx(bar, bytes * static_cast<uint32_t>(copies));
+        for (int i = 0; i < copies; ++i) {
 #pragma unroll
             for (int j = 0; j < E::NIN; ++j)
-                ptx::bulk_g2s(stage + j * AST + 4, p.in[j] + tg.row0 * p.rs, nb, bar);
-        } else {
-            const uint32_t nb = static_cast<uint32_t>(p.T * 4);
-            ptx::mbar_arrive_expect_tx(bar, nb * E::NIN * tg.nrows);
-            for (int i = 0; i < tg.nrows; ++i) {
+                if (!((DER >> j) & 1u))
+                    ptx::bulk_g2s(stage + slot_of<E>(j) * AST + 4 + i * p.C, p.in[j] + (tg.row0 + i) * p.rs, nb, bar);
+            if (wide) {
+                float *dst = wsm;
 #pragma unroll
-                for (int j = 0; j < E::NIN; ++j)
-                    ptx::bulk_g2s(stage + j * AST + 4 + i * p.C, p.in[j] + (tg.row0 + i) * p.rs, nb, bar);
+                for (int w = 0; w < NW; ++w) {
+                    const int W = p.wide_words[w];
+                    ptx::bulk_g2s(dst + static_cast<int64_t>(i) * p.C * W,
+                                  static_cast<const float *>(p.wide[w]) + (tg.row0 + i) * p.wide_rs[w],
+                                  nb * static_cast<uint32_t>(W), bar);
+                    dst += (TILE + 4) * W;
+                }
             }
         }
         return;
@@ -152,19 +212,37 @@ __device__ void issue_tile_copies(const Params &p, const TileGeo &tg, float *sta
             if (!E::FWD && hi[j] < p.T) hi[j] += 4;   // next step (T % 4 == 0 keeps it in the row)
             if (E::FWD && lo[j] > 0) lo[j] -= 4;      // previous step
         }
-        bytes += static_cast<uint32_t>((hi[j] - lo[j]) * 4);
+        if (!((DER >> j) & 1u)) bytes += static_cast<uint32_t>((hi[j] - lo[j]) * 4);
+    }
+    // wide arrays: the tile and, backward, the four steps after it
+    const int64_t whi = (!E::FWD && tg.t0 + tg.len < p.T) ? tg.t0 + tg.len + 4 : tg.t0 + tg.len;
+    if (wide) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) bytes += static_cast<uint32_t>((whi - tg.t0) * 4 * p.wide_words[w]);
     }
     ptx::mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
     for (int j = 0; j < E::NIN; ++j)
-        ptx::bulk_g2s(stage + j * AST + 4 + (lo[j] - tg.t0), p.in[j] + base + lo[j],
-                      static_cast<uint32_t>((hi[j] - lo[j]) * 4), bar);
+        if (!((DER >> j) & 1u))
+            ptx::bulk_g2s(stage + slot_of<E>(j) * AST + 4 + (lo[j] - tg.t0), p.in[j] + base + lo[j],
+                          static_cast<uint32_t>((hi[j] - lo[j]) * 4), bar);
+    if (wide) {
+        float *dst = wsm;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const int W = p.wide_words[w];
+            ptx::bulk_g2s(dst, static_cast<const float *>(p.wide[w]) + tg.row0 * p.wide_rs[w] + tg.t0 * W,
+                          static_cast<uint32_t>((whi - tg.t0) * 4 * W), bar);
+            dst += (TILE + 4) * W;
+        }
+    }
 }
 
 // Element-wise cooperative load of one tile (any alignment), same layout.
 template <class E, int TILE, int AST>
 __device__ void load_tile_elementwise(const Params &p, const TileGeo &tg, float *stage, int nthreads)
 {
+    constexpr unsigned DER = WideOf<E>::DERIVED;
     const int total = tg.nrows * p.C;
     for (int e = threadIdx.x; e < total; e += nthreads) {
         const int i = e / p.C;
@@ -172,15 +250,16 @@ __device__ void load_tile_elementwise(const Params &p, const TileGeo &tg, float 
         if (c < tg.len) {
             const int64_t src = (tg.row0 + i) * p.rs + tg.t0 + c;
 #pragma unroll
-            for (int j = 0; j < E::NIN; ++j) stage[j * AST + 4 + e] = __ldg(p.in[j] + src);
+            for (int j = 0; j < E::NIN; ++j)
+                if (!((DER >> j) & 1u)) stage[slot_of<E>(j) * AST + 4 + e] = __ldg(p.in[j] + src);
         }
     }
     if (!p.packed && threadIdx.x < E::NIN) {
         const int j = threadIdx.x;
-        if ((E::HALO >> j) & 1u) {
+        if (((E::HALO & ~DER) >> j) & 1u) {
             const int64_t base = tg.row0 * p.rs;
-            if (!E::FWD && tg.t0 + tg.len < p.T) stage[j * AST + 4 + TILE] = __ldg(p.in[j] + base + tg.t0 + tg.len);
-            if (E::FWD && tg.t0 > 0) stage[j * AST + 3] = __ldg(p.in[j] + base + tg.t0 - 1);
+            if (!E::FWD && tg.t0 + tg.len < p.T) stage[slot_of<E>(j) * AST + 4 + TILE] = __ldg(p.in[j] + base + tg.t0 + tg.len);
+            if (E::FWD && tg.t0 > 0) stage[slot_of<E>(j) * AST + 3] = __ldg(p.in[j] + base + tg.t0 - 1);
         }
     }
 }
@@ -333,11 +412,13 @@ constexpr int block_threads() { return THREADS + 32; }
 #ifndef RLSCAN_MIN_BLOCKS
 #define RLSCAN_MIN_BLOCKS 3
 #endif
-template <int K>
-constexpr int min_blocks() { return K > 1 ? 2 : RLSCAN_MIN_BLOCKS; }  // two scans need more registers
+// Two scans need more registers; two CTAs per SM is the most the wide
+// stages leave room for.
+template <class E>
+constexpr int min_blocks() { return (WideOf<E>::NWIDE > 0 || E::K > 1) ? 2 : RLSCAN_MIN_BLOCKS; }
 
 template <class E, int THREADS, int ITEMS, int STAGES>
-__global__ void __launch_bounds__(block_threads<THREADS>(), min_blocks<E::K>())
+__global__ void __launch_bounds__(block_threads<THREADS>(), min_blocks<E>())
 scan_kernel(const __grid_constant__ Params p)
 {
     constexpr int NIN = E::NIN, NOUT = E::NOUT, K = E::K;
@@ -349,6 +430,8 @@ scan_kernel(const __grid_constant__ Params p)
     static_assert(STAGES >= 2, "the ring needs two stages");
     static_assert(ITEMS % 4 == 0, "items per thread are moved as float4");
     static_assert(TILE >= kMinTile, "workspace sizing assumes tiles of at least kMinTile");
+    constexpr int NWIDE = WideOf<E>::NWIDE;
+    static_assert(NWIDE == 0 || !FWD, "wide inputs are staged for backward recurrences only");
 
     extern __shared__ __align__(128) float smem[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];   // stage data (and tile id) ready
@@ -361,6 +444,7 @@ scan_kernel(const __grid_constant__ Params p)
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const bool tma = p.tma != 0;
+    const int SST = NWIDE > 0 ? p.stage_floats : NIN * AST;  // floats per ring stage
 
     ptx::pdl_trigger_dependents();
     if (tid == 0) {
@@ -408,7 +492,7 @@ scan_kernel(const __grid_constant__ Params p)
                 const TileGeo tg = decode_tile<FWD, TILE>(p, g);
                 s_geo[s] = tg;
                 ptx::mbar_arrive(&meta_bar[s]);  // the tile is known before its data lands
-                if (tma) issue_tile_copies<E, TILE, AST>(p, tg, smem + s * NIN * AST, &full_bar[s]);
+                if (tma) issue_tile_copies<E, TILE, AST>(p, tg, smem + s * SST, &full_bar[s]);
                 else ptx::mbar_arrive(&full_bar[s]);
             }
         }
@@ -446,7 +530,7 @@ scan_kernel(const __grid_constant__ Params p)
         if (g >= p.num_tiles) break;
         const TileGeo tg = s_geo[s];
         const float rsc = !use_rsc ? 0.f : (rsc_ready ? rsc_next : load_row_scalar(s));
-        float *stage = smem + s * NIN * AST;
+        float *stage = smem + s * SST;
         const bool chained = !p.packed && tg.j > 0;  // needs its predecessor's value
 
         // predecessor states for the look-back (lane sc < K reads scan sc),
@@ -462,6 +546,13 @@ scan_kernel(const __grid_constant__ Params p)
             load_tile_elementwise<E, TILE, AST>(p, tg, stage, THREADS);
             ptx::named_barrier(COMPUTE_BAR, THREADS);
         }
+        if constexpr (NWIDE > 0) {  // derive the per-step inputs from the wide arrays
+            E::template prepass<TILE, AST, THREADS, COMPUTE_BAR>(p, tg, stage + slot_of<E>(E::PI) * AST,
+                                                                 stage + slot_of<E>(E::EQ) * AST,
+                                                                 stage + narrow_copied<E>() * AST,
+                                                                 tma && p.wide_staged, tid);
+            ptx::named_barrier(COMPUTE_BAR, THREADS);
+        }
 
         const ThreadSpan sp = thread_span<FWD, ITEMS>(p, tg, rit, col);
         const bool edge = sp.kb >= 0 || sp.kv < ITEMS;
@@ -473,13 +564,13 @@ scan_kernel(const __grid_constant__ Params p)
         for (int j = 0; j < NIN; ++j) {
 #pragma unroll
             for (int k = 0; k < ITEMS; k += 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(src + j * AST + k);
+                const float4 v = *reinterpret_cast<const float4 *>(src + slot_of<E>(j) * AST + k);
                 x[j][k] = v.x;
                 x[j][k + 1] = v.y;
                 x[j][k + 2] = v.z;
                 x[j][k + 3] = v.w;
             }
-            xn[j] = ((E::HALO >> j) & 1u) ? (FWD ? src[j * AST - 1] : src[j * AST + ITEMS]) : 0.f;
+            xn[j] = ((E::HALO >> j) & 1u) ? (FWD ? src[slot_of<E>(j) * AST - 1] : src[slot_of<E>(j) * AST + ITEMS]) : 0.f;
         }
 
         float a[K][ITEMS], b[K][ITEMS];

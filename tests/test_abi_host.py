@@ -99,6 +99,31 @@ def test_enum_and_null_validation(lib):
     assert lib.rlscan_workspace_init(ctypes.c_void_p(8), 64, None) == 5
 
 
+def retrace_actions(lib, **kw):
+    a = dict(probs=1, mu=2, q=3, nq=4, acts=5, r=6, term=7, trunc=P, N=2, T=4, A=4, rs=4, ars=16,
+             qret=10, adv=11)
+    a.update(kw)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x * 256)
+    return lib.rlscan_retrace_actions(vp(a["probs"]), vp(a["mu"]), vp(a["q"]), vp(a["nq"]),
+                                      vp(a["acts"]), vp(a["r"]), vp(a["term"]), vp(a["trunc"]),
+                                      a["N"], a["T"], a["A"], a["rs"], a["ars"], 0.99, 1.0, 1.0,
+                                      1.0, vp(a["qret"]), vp(a["adv"]), None, 0, None)
+
+
+def test_retrace_actions_validation(lib):
+    assert retrace_actions(lib, A=0) == 4
+    assert retrace_actions(lib, A=65537, ars=4 * 65537) == 4
+    assert retrace_actions(lib, ars=15) == 2                     # [N,T,A] rows overlap
+    assert retrace_actions(lib, rs=3) == 2
+    assert retrace_actions(lib, N=0) == 0                        # no-op, no CUDA call
+    assert retrace_actions(lib, acts=None) == 1
+    assert retrace_actions(lib, nq=None) == 1
+    assert retrace_actions(lib, adv=None) == 1
+    assert retrace_actions(lib, adv=10) == 3                     # outputs alias
+    assert retrace_actions(lib, qret=4) == 3                     # output aliases an input
+    assert retrace_actions(lib, adv=5) == 3
+
+
 def test_python_layer_rejects_cpu_and_wrong_dtype():
     import torch
     import linear_recurrence_scan_gb300 as L
@@ -109,3 +134,6 @@ def test_python_layer_rejects_cpu_and_wrong_dtype():
         L.compute_episodic_prefix_sum(x, x, boundary="middle")
     with pytest.raises(ValueError, match="direction"):
         L.linear_scan(x, x, direction="sideways")
+    with pytest.raises(ValueError, match="CUDA"):
+        L.compute_retrace(torch.zeros(2, 4, 3), x, x, torch.zeros(2, 4, 3),
+                          torch.zeros(2, 4, dtype=torch.int64), x, x)
