@@ -347,22 +347,18 @@ def run_ours(args, wl_name, rank, world, local_rank):
         sets.append(calls)
     torch.cuda.synchronize()
 
-    def run(kernels, i, evs=None):
+    def run(kernels, i):
         calls = sets[i % n_sets]
-        for j, (name, _, _) in enumerate(kernels):
-            if evs is not None:
-                evs[j][0].record(stream)
+        for (name, _, _) in kernels:
             st = calls[name]()
             if st != 0:
                 raise _native.RlscanError(st, name)
-            if evs is not None:
-                evs[j][1].record(stream)
 
-    def timed(kernels, K, offset):
-        """K steps of `kernels`, one event pair per kernel launch, plus one
-        pair around the whole region; barrier + synchronize on both sides."""
-        kev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in kernels]
-               for _ in range(K)]
+    def region(kernels, K, offset):
+        """K steps of `kernels` back to back on the stream, one CUDA event
+        pair around the whole region (none between launches, which would
+        serialise them); barrier + synchronize on both sides.  Returns ms
+        per step and the host wall time of the region."""
         t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             import torch.distributed as dist
@@ -371,16 +367,22 @@ def run_ours(args, wl_name, rank, world, local_rank):
         wall0 = time.perf_counter()
         t0e.record(stream)
         for i in range(K):
-            run(kernels, offset + i, kev[i])
+            run(kernels, offset + i)
         t1e.record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
-        per = {n: [kev[i][j][0].elapsed_time(kev[i][j][1]) for i in range(K)]
-               for j, (n, _, _) in enumerate(kernels)}
-        return t0e.elapsed_time(t1e) / K, per, wall
+        return t0e.elapsed_time(t1e) / K, wall
+
+    def launch_durations(kernels, K):
+        """Average device duration of each kernel: K launches of that kernel
+        alone, back to back, timed as one region, three times."""
+        out = {}
+        for e in kernels:
+            out[e[0]] = [region([e], K, args.warmup + r * K)[0] for r in range(3)]
+        return out
 
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -389,13 +391,16 @@ def run_ours(args, wl_name, rank, world, local_rank):
         run(step_kernels, i)
     torch.cuda.synchronize()
     K = args.steps
-    ms_step, per_kernel, wall = timed(step_kernels, K, args.warmup)
+    ms_step, wall = region(step_kernels, K, args.warmup)
     ms_step = max_over_ranks(ms_step)
+    # per-launch durations of the step's kernels (the step itself when it is one kernel)
+    per_kernel = ({step_kernels[0][0]: [ms_step]} if len(step_kernels) == 1
+                  else launch_durations(step_kernels, K))
     per_est_times = per_kernel
     if fused:  # the estimators one kernel each, for the per-estimator figures
         for i in range(args.warmup):
             run(wl["estimators"], i)
-        _, per_est_times, _ = timed(wl["estimators"], K, args.warmup)
+        per_est_times = launch_durations(wl["estimators"], K)
 
     # e2e through the public API: pinned host inputs -> device, the step's
     # call(s), results back to pinned host memory, every step
@@ -464,6 +469,8 @@ def run_ours(args, wl_name, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "pinned host -> device copies, public compute_* API, results -> pinned host"},
         "gpu_launches": K * len(step_kernels),
+        "timing": "CUDA events around K back-to-back steps (no events between launches); "
+                  "per-kernel durations from K back-to-back launches of that kernel alone",
         "wall_s_timed": round(wall, 4),
         "clocks": clocks,
     }

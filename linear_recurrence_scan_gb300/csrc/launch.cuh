@@ -41,6 +41,18 @@ namespace rlscan {
 #ifndef RLSCAN_WIDE_STAGES
 #define RLSCAN_WIDE_STAGES 2
 #endif
+// Long rows with several tiles of each row in flight finish every tile
+// after the next tile's first half (deferred look-back); the pending tile
+// keeps its stage, so the ring needs at least three.  RLSCAN_DEFER_MODE:
+// -1 decide from the shape (several tiles of each row in flight, and the
+// deeper ring keeps three CTAs per SM or as many as before), 0 never,
+// 1 whenever rows span several tiles.
+#ifndef RLSCAN_DEFER_STAGES
+#define RLSCAN_DEFER_STAGES 3
+#endif
+#ifndef RLSCAN_DEFER_MODE
+#define RLSCAN_DEFER_MODE -1
+#endif
 
 template <class E>
 struct Shape {
@@ -53,22 +65,98 @@ struct Shape {
     static constexpr int ITEMS = TILE / THREADS;
     static constexpr int STAGE_BYTES = E::NIN * (TILE + 8) * 4;  // narrow arrays
     static constexpr int RAW = (RLSCAN_SMEM_BUDGET_KB * 1024) / STAGE_BYTES;
-    static constexpr int STAGES = WIDE ? RLSCAN_WIDE_STAGES
-                                       : (RAW < 2 ? 2 : (RAW > RLSCAN_MAX_STAGES ? RLSCAN_MAX_STAGES : RAW));
+    // ring of an immediate-finish launch, and of a deferred one
+    static constexpr int SHORT_STAGES = WIDE ? RLSCAN_WIDE_STAGES
+                                             : (RAW < 2 ? 2 : (RAW > RLSCAN_MAX_STAGES ? RLSCAN_MAX_STAGES : RAW));
+    static constexpr int DEFER_STAGES = (WIDE || RLSCAN_DEFER_STAGES < 3) ? 0
+                                        : (RLSCAN_DEFER_STAGES > SHORT_STAGES ? RLSCAN_DEFER_STAGES : SHORT_STAGES);
     static_assert(TILE == THREADS * ITEMS, "tile shape");
 };
 
 constexpr int kMaxDevices = 64;
 
+#define RLSCAN_LAUNCH_TRY(expr)                 \
+    do {                                        \
+        const rlscan_status st_ = (expr);       \
+        if (st_ != RLSCAN_OK) return st_;       \
+    } while (0)
+
 inline bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// Per-device launch facts of one kernel: SM count, the dynamic shared
+// memory a CTA may opt into (the device limit less the kernel's static
+// shared memory), and resident CTAs for the last dynamic size used.
+struct KernelFacts {
+    std::mutex mu;
+    int sm_count[kMaxDevices] = {};
+    size_t max_dyn[kMaxDevices] = {};
+    int blocks_per_sm[kMaxDevices] = {};
+    size_t occ_smem[kMaxDevices] = {};
+};
+
+template <class Kernel>
+rlscan_status kernel_facts(KernelFacts &f, Kernel kernel, int dev, int threads, size_t largest, bool opt_in_max,
+                           size_t smem, size_t *dyn_limit, int64_t *slots)
+{
+    std::lock_guard<std::mutex> lock(f.mu);
+    if (f.sm_count[dev] == 0) {
+        int sms = 0, optin = 0;
+        cudaFuncAttributes fa;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa, kernel) != cudaSuccess)
+            return RLSCAN_ERR_CUDA;
+        const size_t dyn = static_cast<size_t>(optin) > fa.sharedSizeBytes ? optin - fa.sharedSizeBytes : 0;
+        if (dyn < largest) return RLSCAN_ERR_CUDA;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(opt_in_max ? dyn : largest)) != cudaSuccess)
+            return RLSCAN_ERR_CUDA;
+        f.max_dyn[dev] = dyn;
+        f.sm_count[dev] = sms > 0 ? sms : 1;
+    }
+    if (dyn_limit != nullptr) *dyn_limit = f.max_dyn[dev];
+    if (slots != nullptr) {
+        if (f.occ_smem[dev] != smem) {
+            int occ = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem) != cudaSuccess)
+                return RLSCAN_ERR_CUDA;
+            f.blocks_per_sm[dev] = occ > 0 ? occ : 1;
+            f.occ_smem[dev] = smem;
+        }
+        *slots = static_cast<int64_t>(f.sm_count[dev]) * f.blocks_per_sm[dev];
+    }
+    return RLSCAN_OK;
+}
+
+template <class Kernel>
+rlscan_status launch_kernel(Kernel kernel, const Params &p, int64_t grid, int threads, size_t smem,
+                            cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) {
+        cudaGetLastError();
+        return RLSCAN_ERR_CUDA;
+    }
+    return cudaGetLastError() == cudaSuccess ? RLSCAN_OK : RLSCAN_ERR_CUDA;
+}
 
 template <class E>
 rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stream)
 {
     using S = Shape<E>;
     constexpr int TILE = S::TILE;
-    auto kernel = scan_kernel<E, S::THREADS, S::ITEMS, S::STAGES>;
-    size_t smem = static_cast<size_t>(S::STAGES) * S::STAGE_BYTES;
+    constexpr int BT = block_threads<S::THREADS>();
+    auto kernel = scan_kernel<E, S::THREADS, S::ITEMS, S::SHORT_STAGES, false>;
+    size_t smem = static_cast<size_t>(S::SHORT_STAGES) * S::STAGE_BYTES;
 
     if (p.T <= TILE) {
         p.packed = 1;
@@ -104,35 +192,9 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RLSCAN_ERR_CUDA;
-    // per device: SM count, dynamic shared memory a CTA may opt into (the
-    // device limit less the kernel's static shared memory), and resident
-    // CTAs for the last dynamic size (fixed per instantiation, except for
-    // wide inputs, whose stage size depends on the width)
-    static std::mutex mu;
-    static int blocks_per_sm[kMaxDevices];
-    static int sm_count[kMaxDevices];
-    static size_t max_dyn[kMaxDevices];
-    static size_t occ_smem[kMaxDevices];
+    static KernelFacts facts;
     size_t dyn_limit = 0;
-    {
-    std::lock_guard<std::mutex> lock(mu);
-    if (sm_count[dev] == 0) {
-        int sms = 0, optin = 0;
-        cudaFuncAttributes fa;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-            cudaFuncGetAttributes(&fa, kernel) != cudaSuccess)
-            return RLSCAN_ERR_CUDA;
-        const size_t dyn = static_cast<size_t>(optin) > fa.sharedSizeBytes ? optin - fa.sharedSizeBytes : 0;
-        if (dyn < smem) return RLSCAN_ERR_CUDA;
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(S::WIDE ? dyn : smem)) != cudaSuccess)
-            return RLSCAN_ERR_CUDA;
-        max_dyn[dev] = dyn;
-        sm_count[dev] = sms > 0 ? sms : 1;
-    }
-    dyn_limit = max_dyn[dev];
-    }
+    RLSCAN_LAUNCH_TRY(kernel_facts(facts, kernel, dev, BT, smem, S::WIDE, smem, &dyn_limit, nullptr));
     if constexpr (S::WIDE) {
         // stage the wide arrays when they are aligned and the ring fits
         int64_t wide_floats = 0;
@@ -146,39 +208,32 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
         const int64_t copied = static_cast<int64_t>(narrow_copied<E>()) * (TILE + 8);
         const int64_t derived = static_cast<int64_t>(E::NIN - narrow_copied<E>()) * (TILE + 8);
         const int64_t staged_floats = copied + (wide_floats > derived ? wide_floats : derived);
-        wide_ok = wide_ok && static_cast<size_t>(S::STAGES) * staged_floats * 4 <= dyn_limit;
+        wide_ok = wide_ok && static_cast<size_t>(S::SHORT_STAGES) * staged_floats * 4 <= dyn_limit;
         p.wide_staged = wide_ok ? 1 : 0;
         p.stage_floats = static_cast<int32_t>(wide_ok ? staged_floats : copied + derived);
-        smem = static_cast<size_t>(S::STAGES) * p.stage_floats * 4;
+        smem = static_cast<size_t>(S::SHORT_STAGES) * p.stage_floats * 4;
     }
     int64_t slots = 0;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (occ_smem[dev] != smem) {
-            int occ = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, block_threads<S::THREADS>(), smem) != cudaSuccess)
-                return RLSCAN_ERR_CUDA;
-            blocks_per_sm[dev] = occ > 0 ? occ : 1;
-            occ_smem[dev] = smem;
+    RLSCAN_LAUNCH_TRY(kernel_facts(facts, kernel, dev, BT, smem, S::WIDE, smem, nullptr, &slots));
+
+    // Deferred finishing when several tiles of each row are in flight at
+    // once (their look-backs would otherwise wait on one another).
+    if constexpr (S::DEFER_STAGES >= 3) {
+        const bool want = !p.packed && (RLSCAN_DEFER_MODE == 1 ||
+                                        (RLSCAN_DEFER_MODE < 0 && slots * S::SHORT_STAGES >= 2 * p.N));
+        if (want) {
+            auto dkernel = scan_kernel<E, S::THREADS, S::ITEMS, S::DEFER_STAGES, true>;
+            static KernelFacts dfacts;
+            const size_t dsmem = static_cast<size_t>(S::DEFER_STAGES) * S::STAGE_BYTES;
+            int64_t dslots = 0;
+            RLSCAN_LAUNCH_TRY(kernel_facts(dfacts, dkernel, dev, BT, dsmem, false, dsmem, nullptr, &dslots));
+            // only while the deeper ring keeps three CTAs per SM resident (or
+            // as many as the immediate kernel); forced: always
+            if (RLSCAN_DEFER_MODE == 1 || dslots >= slots || dslots >= 3 * static_cast<int64_t>(facts.sm_count[dev]))
+                return launch_kernel(dkernel, p, p.num_tiles < dslots ? p.num_tiles : dslots, BT, dsmem, stream);
         }
-        slots = static_cast<int64_t>(sm_count[dev]) * blocks_per_sm[dev];
     }
-    const int64_t grid = p.num_tiles < slots ? p.num_tiles : slots;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(block_threads<S::THREADS>());
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) {
-        cudaGetLastError();
-        return RLSCAN_ERR_CUDA;
-    }
-    return cudaGetLastError() == cudaSuccess ? RLSCAN_OK : RLSCAN_ERR_CUDA;
+    return launch_kernel(kernel, p, p.num_tiles < slots ? p.num_tiles : slots, BT, smem, stream);
 }
 
 }  // namespace rlscan

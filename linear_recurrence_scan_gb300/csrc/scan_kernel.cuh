@@ -414,11 +414,18 @@ constexpr int block_threads() { return THREADS + 32; }
 #endif
 // Two scans need more registers; two CTAs per SM is the most the wide
 // stages leave room for.
-template <class E>
-constexpr int min_blocks() { return (WideOf<E>::NWIDE > 0 || E::K > 1) ? 2 : RLSCAN_MIN_BLOCKS; }
+#ifndef RLSCAN_DEFER_MIN_BLOCKS
+#define RLSCAN_DEFER_MIN_BLOCKS 0  // 0: as the immediate-finish kernel
+#endif
+template <class E, bool DEFER>
+constexpr int min_blocks()
+{
+    return (DEFER && RLSCAN_DEFER_MIN_BLOCKS > 0) ? RLSCAN_DEFER_MIN_BLOCKS
+                                                 : ((WideOf<E>::NWIDE > 0 || E::K > 1) ? 2 : RLSCAN_MIN_BLOCKS);
+}
 
-template <class E, int THREADS, int ITEMS, int STAGES>
-__global__ void __launch_bounds__(block_threads<THREADS>(), min_blocks<E>())
+template <class E, int THREADS, int ITEMS, int STAGES, bool DEFER>
+__global__ void __launch_bounds__(block_threads<THREADS>(), min_blocks<E, DEFER>())
 scan_kernel(const __grid_constant__ Params p)
 {
     constexpr int NIN = E::NIN, NOUT = E::NOUT, K = E::K;
@@ -445,6 +452,8 @@ scan_kernel(const __grid_constant__ Params p)
     const int lane = tid & 31, warp = tid >> 5;
     const bool tma = p.tma != 0;
     const int SST = NWIDE > 0 ? p.stage_floats : NIN * AST;  // floats per ring stage
+    constexpr int NST = STAGES;                                // ring stages
+    static_assert(!DEFER || STAGES >= 3, "a deferred tile holds its stage: the ring needs three");
 
     ptx::pdl_trigger_dependents();
     if (tid == 0) {
@@ -463,17 +472,17 @@ scan_kernel(const __grid_constant__ Params p)
     if (warp == WARPS) {
         // Producer (lane 0 of the extra warp): for ring slot s of iteration
         // it, wait until every compute warp has released the slot (iteration
-        // it - STAGES), draw the next ticket, record the tile and start its
-        // copies.  An exhausted ticket completes the slot's phase
-        // without data, which tells the compute warps to stop.  Tickets are
-        // drawn just before their copies can start, so tiles are processed
-        // in close to ticket order.
+        // it - STAGES), draw the next ticket, record the tile and start its copies.  An
+        // exhausted ticket completes the slot's phase without data, which
+        // tells the compute warps to stop.  Tickets are drawn just before
+        // their copies can start, so tiles are processed in close to ticket
+        // order.
         if (lane == 0) {
             int64_t static_next = blockIdx.x;
             for (int it = 0;; ++it) {
-                const int s = it % STAGES;
-                if (it >= STAGES &&
-                    !wait_phase(&empty_bar[s], static_cast<uint32_t>((it / STAGES - 1) & 1),
+                const int s = it % NST;
+                if (it >= NST &&
+                    !wait_phase(&empty_bar[s], static_cast<uint32_t>((it / NST - 1) & 1),
                                 p.spin_limit_ns + p.copy_limit_ns))
                     record_error(p, RLSCAN_ERR_TIMEOUT, 0x40000000u | static_cast<uint32_t>(s));
                 int64_t g;
@@ -518,14 +527,169 @@ scan_kernel(const __grid_constant__ Params p)
     bool rsc_ready = false;
     uint32_t lost_stages = 0, lost_parity = 0;  // waits that timed out (thread 0)
 
+    using Keep = typename E::template Keep<ITEMS>;
+
+    // inputs of this thread's ITEMS steps, plus the neighbour step
+    auto load_inputs = [&](const float *stage, float (&x)[NIN][ITEMS], float (&xn)[NIN]) {
+        const float *src = stage + 4 + li;
+#pragma unroll
+        for (int j = 0; j < NIN; ++j) {
+            const float *aj = src + slot_of<E>(j) * AST;
+#pragma unroll
+            for (int k = 0; k < ITEMS; k += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(aj + k);
+                x[j][k] = v.x;
+                x[j][k + 1] = v.y;
+                x[j][k + 2] = v.z;
+                x[j][k + 3] = v.w;
+            }
+            xn[j] = ((E::HALO >> j) & 1u) ? (FWD ? aj[-1] : aj[ITEMS]) : 0.f;
+        }
+    };
+
+    // coefficients of the thread's steps: the row's boundary values folded
+    // in (and the recurrence severed) there, the identity map outside the data
+    auto make_coeffs = [&](const float (&x)[NIN][ITEMS], const float (&xn)[NIN], const ThreadSpan &sp, float rsc,
+                           float (&a)[K][ITEMS], float (&b)[K][ITEMS], Keep &keep) {
+        const bool edge = sp.kb >= 0 || sp.kv < ITEMS;
+        if (!edge) {
+            E::template coeffs<ITEMS, false>(x, xn, -1, p, rsc, a, b, keep);
+            return;
+        }
+        E::template coeffs<ITEMS, true>(x, xn, sp.kb, p, rsc, a, b, keep);
+#pragma unroll
+        for (int k = 0; k < ITEMS; ++k) {
+            if (k == sp.kb) {
+                float bv[K];
+                E::template boundary<ITEMS>(x, k, rsc, p, bv);
+#pragma unroll
+                for (int sc = 0; sc < K; ++sc) {
+                    a[sc][k] = fmaf(b[sc][k], bv[sc], a[sc][k]);
+                    b[sc][k] = 0.f;
+                }
+            }
+            if (k >= sp.kv) {
+#pragma unroll
+                for (int sc = 0; sc < K; ++sc) {
+                    a[sc][k] = 0.f;
+                    b[sc][k] = 1.f;
+                }
+            }
+        }
+    };
+
+    // serial recurrence of each scan from its exact incoming value, the
+    // estimator's outputs, and the stores
+    auto finish = [&](const float (&x)[NIN][ITEMS], const float (&xn)[NIN], const float (&a)[K][ITEMS],
+                      const float (&b)[K][ITEMS], const Keep &keep, const ThreadSpan &sp, const TileGeo &tg,
+                      float rsc, const float (&x_in)[K]) {
+        float A[K][ITEMS];
+#pragma unroll
+        for (int sc = 0; sc < K; ++sc) {
+            float v = x_in[sc];
+            if (FWD) {
+#pragma unroll
+                for (int k = 0; k < ITEMS; ++k) {
+                    v = fmaf(b[sc][k], v, a[sc][k]);
+                    A[sc][k] = v;
+                }
+            } else {
+#pragma unroll
+                for (int k = ITEMS - 1; k >= 0; --k) {
+                    v = fmaf(b[sc][k], v, a[sc][k]);
+                    A[sc][k] = v;
+                }
+            }
+        }
+        float o[NOUT][ITEMS];
+        const bool edge = sp.kb >= 0 || sp.kv < ITEMS;
+        if (!edge) E::template post<ITEMS, false>(x, xn, -1, p, rsc, A, x_in, keep, o);
+        else E::template post<ITEMS, true>(x, xn, sp.kb, p, rsc, A, x_in, keep, o);
+        if (sp.kv > 0) {
+            const int64_t off = (tg.row0 + rit) * p.rs + tg.t0 + col;
+#pragma unroll
+            for (int q = 0; q < NOUT; ++q) {
+                if (NOUT > 1 && p.out[q] == nullptr) continue;  // optional output
+                if (tma) {
+#pragma unroll
+                    for (int k = 0; k < ITEMS; k += 4) {
+                        if (k < sp.kv)
+                            *reinterpret_cast<float4 *>(p.out[q] + off + k) =
+                                make_float4(o[q][k], o[q][k + 1], o[q][k + 2], o[q][k + 3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < ITEMS; ++k)
+                        if (k < sp.kv) p.out[q][off + k] = o[q][k];
+                }
+            }
+        }
+    };
+
+    // Value entering a chained tile per scan (lane sc < K walks scan sc from
+    // the prefetched predecessor words), broadcast to the warp; the
+    // publishing warp then publishes the tile's inclusive values.
+    auto carry_in = [&](int64_t g, int64_t j, const Pair (&total)[K], unsigned long long w0,
+                        unsigned long long w1, float (&carry)[K]) {
+        float mine = 0.f;
+        if (lane < K) mine = lookback_read<K>(p, g, j, lane, w0, w1);
+#pragma unroll
+        for (int sc = 0; sc < K; ++sc) carry[sc] = __shfl_sync(0xffffffffu, mine, sc);
+        if (warp == PUB_WARP && lane == 0) {
+#pragma unroll
+            for (int sc = 0; sc < K; ++sc)
+                if (total[sc].b != 0.f) publish_inclusive(p, g * K + sc, g, fmaf(total[sc].b, carry[sc], total[sc].a));
+        }
+    };
+
+    // Deferred finishing (long rows with several tiles of a row in flight):
+    // a tile's look-back, rescan and stores run after the next tile's first
+    // half, so the predecessors have had that long to publish.  The pending
+    // tile keeps its stage (inputs are re-read from it) until it is done.
+    constexpr bool defer = DEFER;
+    bool pend = false;
+    int ps = 0;
+    int64_t pg = 0;
+    float prsc = 0.f;
+    Pair pex[K], pwe[K], ptot[K];
+    unsigned long long pw0 = 0, pw1 = 0;
+    auto finish_pending = [&]() {
+        const TileGeo tg = decode_tile<FWD, TILE>(p, pg);
+        float carry[K];
+#pragma unroll
+        for (int sc = 0; sc < K; ++sc) carry[sc] = 0.f;
+        if (tg.j > 0) carry_in(pg, tg.j, ptot, pw0, pw1, carry);
+        const ThreadSpan sp = thread_span<FWD, ITEMS>(p, tg, rit, col);
+        float x[NIN][ITEMS], xn[NIN];
+        load_inputs(smem + ps * SST, x, xn);
+        float a[K][ITEMS], b[K][ITEMS];
+        Keep keep;
+        make_coeffs(x, xn, sp, prsc, a, b, keep);
+        float x_in[K];
+#pragma unroll
+        for (int sc = 0; sc < K; ++sc) x_in[sc] = fmaf(pex[sc].b, fmaf(pwe[sc].b, carry[sc], pwe[sc].a), pex[sc].a);
+        finish(x, xn, a, b, keep, sp, tg, prsc, x_in);
+        if (lane == 0) ptx::mbar_arrive(&empty_bar[ps]);  // the pending tile's stage is free
+        pend = false;
+    };
+    auto prefetch_pending = [&]() {  // first predecessor state of the pending tile
+        const int64_t j = pg / p.N;
+        if (j > 0 && lane < K) {
+            const int64_t slot = (pg - p.N) * K + lane;
+            pw0 = ptx::ld_relaxed(&p.states[2 * slot]);
+            pw1 = ptx::ld_relaxed(&p.states[2 * slot + 1]);
+        }
+    };
+
     for (int it = 0;; ++it) {
-        const int s = it % STAGES;
-        const uint32_t parity = static_cast<uint32_t>((it / STAGES) & 1);
+        const int s = it % NST;
+        const uint32_t parity = static_cast<uint32_t>((it / NST) & 1);
         if (!wait_phase(&full_bar[s], parity, p.copy_limit_ns) && tid == 0) {
             lost_stages |= 1u << s;
             lost_parity = (lost_parity & ~(1u << s)) | (parity << s);
             record_error(p, RLSCAN_ERR_TIMEOUT, 0x80000000u | static_cast<uint32_t>(s));
         }
+        if (pend) prefetch_pending();
         const int64_t g = tile_ids[s];
         if (g >= p.num_tiles) break;
         const TileGeo tg = s_geo[s];
@@ -533,13 +697,13 @@ scan_kernel(const __grid_constant__ Params p)
         float *stage = smem + s * SST;
         const bool chained = !p.packed && tg.j > 0;  // needs its predecessor's value
 
-        // predecessor states for the look-back (lane sc < K reads scan sc),
-        // fetched early so their latency overlaps the tile's work
-        unsigned long long pw0 = 0, pw1 = 0;
-        if (chained && lane < K) {
+        // predecessor states for an immediate look-back (lane sc < K reads
+        // scan sc), fetched early so their latency overlaps the tile's work
+        unsigned long long cw0 = 0, cw1 = 0;
+        if (!defer && chained && lane < K) {
             const int64_t slot = (g - p.N) * K + lane;
-            pw0 = ptx::ld_relaxed(&p.states[2 * slot]);
-            pw1 = ptx::ld_relaxed(&p.states[2 * slot + 1]);
+            cw0 = ptx::ld_relaxed(&p.states[2 * slot]);
+            cw1 = ptx::ld_relaxed(&p.states[2 * slot + 1]);
         }
 
         if (!tma) {
@@ -555,50 +719,11 @@ scan_kernel(const __grid_constant__ Params p)
         }
 
         const ThreadSpan sp = thread_span<FWD, ITEMS>(p, tg, rit, col);
-        const bool edge = sp.kb >= 0 || sp.kv < ITEMS;
-
-        // inputs of this thread's ITEMS steps, plus the neighbour step
         float x[NIN][ITEMS], xn[NIN];
-        const float *src = stage + 4 + li;
-#pragma unroll
-        for (int j = 0; j < NIN; ++j) {
-#pragma unroll
-            for (int k = 0; k < ITEMS; k += 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(src + slot_of<E>(j) * AST + k);
-                x[j][k] = v.x;
-                x[j][k + 1] = v.y;
-                x[j][k + 2] = v.z;
-                x[j][k + 3] = v.w;
-            }
-            xn[j] = ((E::HALO >> j) & 1u) ? (FWD ? src[slot_of<E>(j) * AST - 1] : src[slot_of<E>(j) * AST + ITEMS]) : 0.f;
-        }
-
+        load_inputs(stage, x, xn);
         float a[K][ITEMS], b[K][ITEMS];
-        typename E::template Keep<ITEMS> keep;
-        if (!edge) {
-            E::template coeffs<ITEMS, false>(x, xn, -1, p, rsc, a, b, keep);
-        } else {
-            E::template coeffs<ITEMS, true>(x, xn, sp.kb, p, rsc, a, b, keep);
-#pragma unroll
-            for (int k = 0; k < ITEMS; ++k) {
-                if (k == sp.kb) {  // fold the row's boundary values; sever
-                    float bv[K];
-                    E::template boundary<ITEMS>(x, k, rsc, p, bv);
-#pragma unroll
-                    for (int sc = 0; sc < K; ++sc) {
-                        a[sc][k] = fmaf(b[sc][k], bv[sc], a[sc][k]);
-                        b[sc][k] = 0.f;
-                    }
-                }
-                if (k >= sp.kv) {  // outside the data: identity map
-#pragma unroll
-                    for (int sc = 0; sc < K; ++sc) {
-                        a[sc][k] = 0.f;
-                        b[sc][k] = 1.f;
-                    }
-                }
-            }
-        }
+        Keep keep;
+        make_coeffs(x, xn, sp, rsc, a, b, keep);
 
         // per scan: thread aggregate in scan order, warp scan
         Pair ex[K];
@@ -619,12 +744,13 @@ scan_kernel(const __grid_constant__ Params p)
             ex[sc] = warp_exclusive_from<FWD>(inc, lane);
             if (lane == (FWD ? 31 : 0)) wa[warp][sc] = inc;
         }
-        ptx::named_barrier(COMPUTE_BAR, THREADS);        // warp aggregates visible
-        if (lane == 0) ptx::mbar_arrive(&empty_bar[s]);  // every input is in registers: the slot is free
+        ptx::named_barrier(COMPUTE_BAR, THREADS);  // warp aggregates visible
+        // every input is in registers: unless the tile is finished later, the slot is free
+        if (!defer && lane == 0) ptx::mbar_arrive(&empty_bar[s]);
 
         if (use_rsc) {
-            const int s1 = (it + 1) % STAGES;
-            rsc_ready = ptx::mbar_test_wait(&meta_bar[s1], static_cast<uint32_t>(((it + 1) / STAGES) & 1));
+            const int s1 = (it + 1) % NST;
+            rsc_ready = ptx::mbar_test_wait(&meta_bar[s1], static_cast<uint32_t>(((it + 1) / NST) & 1));
             if (rsc_ready) rsc_next = load_row_scalar(s1);
         }
 
@@ -643,86 +769,48 @@ scan_kernel(const __grid_constant__ Params p)
                     if (w2 > warp) we[sc] = compose(wa[w2][sc], we[sc]);
             }
         }
-        // value entering the tile, per scan: publish this tile's aggregates
-        // first, then walk the K chains in parallel (lane sc walks scan sc)
-        float carry[K];
+        if (!p.packed && warp == PUB_WARP && lane == 0) {
 #pragma unroll
-        for (int sc = 0; sc < K; ++sc) carry[sc] = 0.f;
-        if (!p.packed) {
-            if (warp == PUB_WARP && lane == 0) {
+            for (int sc = 0; sc < K; ++sc) publish_first(p, g * K + sc, g, tg.j, compose(wa[PUB_WARP][sc], we[sc]));
+        }
+
+        if (!defer) {
+            float carry[K];
 #pragma unroll
-                for (int sc = 0; sc < K; ++sc)
-                    publish_first(p, g * K + sc, g, tg.j, compose(wa[PUB_WARP][sc], we[sc]));
-            }
+            for (int sc = 0; sc < K; ++sc) carry[sc] = 0.f;
             if (chained) {
-                float mine = 0.f;
-                if (lane < K) mine = lookback_read<K>(p, g, tg.j, lane, pw0, pw1);
+                Pair total[K];
 #pragma unroll
-                for (int sc = 0; sc < K; ++sc) carry[sc] = __shfl_sync(0xffffffffu, mine, sc);
-                if (warp == PUB_WARP && lane == 0) {
-#pragma unroll
-                    for (int sc = 0; sc < K; ++sc) {
-                        const Pair total = compose(wa[PUB_WARP][sc], we[sc]);
-                        if (total.b != 0.f)
-                            publish_inclusive(p, g * K + sc, g, fmaf(total.b, carry[sc], total.a));
-                    }
-                }
+                for (int sc = 0; sc < K; ++sc) total[sc] = compose(wa[PUB_WARP][sc], we[sc]);
+                carry_in(g, tg.j, total, cw0, cw1, carry);
             }
-        }
-        // exact value entering this thread's range
-        float x_in[K];
+            float x_in[K];
 #pragma unroll
-        for (int sc = 0; sc < K; ++sc) x_in[sc] = fmaf(ex[sc].b, fmaf(we[sc].b, carry[sc], we[sc].a), ex[sc].a);
-
-        // serial recurrence of each scan from its exact incoming value
-        float A[K][ITEMS];
+            for (int sc = 0; sc < K; ++sc) x_in[sc] = fmaf(ex[sc].b, fmaf(we[sc].b, carry[sc], we[sc].a), ex[sc].a);
+            finish(x, xn, a, b, keep, sp, tg, rsc, x_in);
+        } else {
+            if (pend) finish_pending();
+            pend = true;
+            ps = s;
+            pg = g;
+            prsc = rsc;
 #pragma unroll
-        for (int sc = 0; sc < K; ++sc) {
-            float v = x_in[sc];
-            if (FWD) {
-#pragma unroll
-                for (int k = 0; k < ITEMS; ++k) {
-                    v = fmaf(b[sc][k], v, a[sc][k]);
-                    A[sc][k] = v;
-                }
-            } else {
-#pragma unroll
-                for (int k = ITEMS - 1; k >= 0; --k) {
-                    v = fmaf(b[sc][k], v, a[sc][k]);
-                    A[sc][k] = v;
-                }
-            }
-        }
-        float o[NOUT][ITEMS];
-        if (!edge) E::template post<ITEMS, false>(x, xn, -1, p, rsc, A, x_in, keep, o);
-        else E::template post<ITEMS, true>(x, xn, sp.kb, p, rsc, A, x_in, keep, o);
-
-        if (sp.kv > 0) {
-            const int64_t off = (tg.row0 + rit) * p.rs + tg.t0 + col;
-#pragma unroll
-            for (int q = 0; q < NOUT; ++q) {
-                if (NOUT > 1 && p.out[q] == nullptr) continue;  // optional output
-                if (tma) {
-#pragma unroll
-                    for (int k = 0; k < ITEMS; k += 4) {
-                        if (k < sp.kv)
-                            *reinterpret_cast<float4 *>(p.out[q] + off + k) =
-                                make_float4(o[q][k], o[q][k + 1], o[q][k + 2], o[q][k + 3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < ITEMS; ++k)
-                        if (k < sp.kv) p.out[q][off + k] = o[q][k];
-                }
+            for (int sc = 0; sc < K; ++sc) {
+                pex[sc] = ex[sc];
+                pwe[sc] = we[sc];
+                // the aggregate map, kept for the publishing warp (wagg is
+                // reused two tiles later, possibly before this tile is done)
+                ptot[sc] = compose(wa[PUB_WARP][sc], we[sc]);
             }
         }
     }
+    if (pend) finish_pending();
 
     // A copy whose wait timed out may still be landing: give it one more
     // bounded wait before the shared memory is released.
     if (lost_stages != 0 && tid == 0) {
-        for (int s = 0; s < STAGES; ++s)
-            if ((lost_stages >> s) & 1u) wait_phase(&full_bar[s], (lost_parity >> s) & 1u, p.copy_limit_ns);
+        for (int s2 = 0; s2 < NST; ++s2)
+            if ((lost_stages >> s2) & 1u) wait_phase(&full_bar[s2], (lost_parity >> s2) & 1u, p.copy_limit_ns);
     }
     }  // compute warps
     if (p.dynamic) {
