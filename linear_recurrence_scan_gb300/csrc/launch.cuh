@@ -21,7 +21,7 @@ namespace rlscan {
 // the defaults: short kernels prefer a shallow ring (more CTAs per SM, and
 // every CTA's first tile arrives sooner).  The macros exist for such sweeps.
 #ifndef RLSCAN_TILE_BYTES_TARGET
-#define RLSCAN_TILE_BYTES_TARGET 40960
+#define RLSCAN_TILE_BYTES_TARGET 30000
 #endif
 #ifndef RLSCAN_SMEM_BUDGET_KB
 #define RLSCAN_SMEM_BUDGET_KB 64
