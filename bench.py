@@ -53,6 +53,12 @@ def _cfg_workloads():
             # the step's three outputs from one kernel: r, v, term read once,
             # advantages, lambda-returns, discounted returns written
             fused=("gae_returns", 24, c1)),
+        "gae_normalized_4096x1024": dict(
+            desc="GAE advantages normalised over the batch (fused moments + in-place pass) "
+                 "and TD(lambda) returns, last_value bootstrap, no truncations",
+            N=4096, T=1024, gen=lambda N, T: synthetic.config_batch(1, N=N, T=T),
+            # r, v, term read once; normalised advantages and lambda-returns written
+            estimators=[("gae_normalized", 20, c1)]),
         "gae_8x128": dict(
             desc="GAE with truncations and 2-D bootstrap", N=8, T=128,
             gen=lambda N, T: synthetic.config_batch(0, N=N, T=T),
@@ -108,7 +114,10 @@ IO = {
     "eligibility_traces": (["gradients", "trace_dones"], [], 1),
     "episodic_prefix_sum": (["inputs", "prefix_dones"], [], 1),
     "gae_returns": (["rewards", "values", "terminateds"], ["last_value"], 3),
+    "gae_normalized": (["rewards", "values", "terminateds"], ["last_value"], 2),
 }
+# kernels one call launches (default 1)
+LAUNCHES = {"gae_normalized": 2}
 
 
 def _csrc_hash():
@@ -261,6 +270,11 @@ def _launcher(name, c, bufs, outs, N, T, ws, wsn, stream):
     if name == "episodic_prefix_sum":
         return lambda: lib.rlscan_episodic_prefix_sum(b["inputs"], b["prefix_dones"], None, 1, N,
                                                       T, T, o[0], ws, wsn, stream)
+    if name == "gae_normalized":
+        return lambda: lib.rlscan_gae_normalized(b["rewards"], b["values"], b["terminateds"], None,
+                                                 None, b["last_value"], N, T, T, g,
+                                                 float(c["lambda_"]), 1e-8, o[0], o[1], None, None,
+                                                 ws, wsn, stream)
     if name == "gae_returns":
         return lambda: lib.rlscan_gae_returns(b["rewards"], b["values"], b["terminateds"], None,
                                               None, b["last_value"], N, T, T, g,
@@ -303,6 +317,10 @@ def _public_call(name, c, t):
         return [Lb.compute_eligibility_traces(t["gradients"], t["trace_dones"], g, c["lambda_"])]
     if name == "episodic_prefix_sum":
         return [Lb.compute_episodic_prefix_sum(t["inputs"], t["prefix_dones"], None, "starts_at")]
+    if name == "gae_normalized":
+        return list(Lb.compute_gae_normalized(t["rewards"], t["values"], t["terminateds"], None, g,
+                                              c["lambda_"], None, t["last_value"], 1e-8,
+                                              outputs=("advantages", "lambda_returns")))
     if name == "gae_returns":
         return list(Lb.compute_gae_and_returns(t["rewards"], t["values"], t["terminateds"], None, g,
                                                c["lambda_"], None, t["last_value"]))
@@ -331,7 +349,7 @@ def run_ours(args, wl_name, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     sh = ctypes.c_void_p(stream.cuda_stream)
     lib = _native.lib()
-    wsn = lib.rlscan_workspace_bytes(N, T)
+    wsn = max(lib.rlscan_workspace_bytes(N, T), lib.rlscan_gae_normalized_workspace_bytes(N, T))
     ws = None
     if wsn:
         ws_t = torch.empty(wsn, dtype=torch.uint8, device=dev)
@@ -468,7 +486,7 @@ def run_ours(args, wl_name, rank, world, local_rank):
         "e2e": {"value": world * steps_per_call / e2e_s, "unit": "env-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "pinned host -> device copies, public compute_* API, results -> pinned host"},
-        "gpu_launches": K * len(step_kernels),
+        "gpu_launches": K * sum(LAUNCHES.get(n, 1) for (n, _, _) in step_kernels),
         "timing": "CUDA events around K back-to-back steps (no events between launches); "
                   "per-kernel durations from K back-to-back launches of that kernel alone",
         "wall_s_timed": round(wall, 4),
@@ -507,6 +525,15 @@ def _oracle_call(name, c, b):
                                       b["q_values"], b["next_q_values_all"], b["actions"],
                                       b["rewards"], b["terminateds"], None, g, c["lambda_"],
                                       c["c_bar"], c["rho_bar"])
+    if name == "gae_normalized":
+        adv = oracle.gae(b["rewards"], b["values"], b["terminateds"], None, g, c["lambda_"], None,
+                         b["last_value"])
+        nv = np.zeros_like(b["values"])
+        nv[:, :-1] = b["values"][:, 1:]
+        nv[:, -1] = b["last_value"]
+        return (oracle.normalize_advantages(adv, 1e-8)[0],
+                oracle.lambda_returns(b["rewards"], nv, b["terminateds"], None, g, c["lambda_"],
+                                      None, b["last_value"]))
     if name == "eligibility_traces":
         return oracle.eligibility_traces(b["gradients"], b["trace_dones"], g, c["lambda_"])
     if name == "episodic_prefix_sum":

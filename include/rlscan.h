@@ -188,6 +188,39 @@ rlscan_status rlscan_gae_noalloc(const float *rewards, const float *values,
                                  float lambda, float *advantages, rlscan_stream_t stream);
 
 /*
+ * GAE with its advantages normalised over the whole batch, fused with the
+ * returns.  rl-triton paper Sec. 9.3 plans "fused advantage normalization";
+ * it is read here as the usual per-batch whitening
+ *   adv_t <- (A_t - mean) / (std + eps)
+ * with mean and the unbiased (n - 1) standard deviation of all N*T raw GAE
+ * advantages A_t of the call (rlscan_gae's values).  The scan kernel also
+ * accumulates the batch moments (sum and sum of squares, per CTA in double
+ * precision); a second kernel, ordered after it on `stream`, combines the
+ * per-CTA sums in CTA order and normalises the advantages in place.
+ * lambda_returns (A_t + V_t) and discounted_returns are computed from the
+ * RAW advantages, as in rlscan_gae_returns.
+ * Inputs : as rlscan_gae_returns; eps >= 0 (else RLSCAN_ERR_ARG_VALUE).
+ * Outputs: advantages [N,T] (normalised; required); lambda_returns,
+ *          discounted_returns [N,T] nullable; moments: nullable device
+ *          float[2] receiving (mean, std) of the raw advantages.
+ * Workspace: always needed, rlscan_gae_normalized_workspace_bytes(N, T)
+ *          bytes, 16-byte aligned, zeroed once by rlscan_workspace_init
+ *          (the usual look-back workspace followed by the moments region);
+ *          otherwise RLSCAN_ERR_WORKSPACE.
+ * With N*T == 1 the standard deviation is undefined and the output is NaN.
+ */
+size_t rlscan_gae_normalized_workspace_bytes(int64_t N, int64_t T);
+
+rlscan_status rlscan_gae_normalized(const float *rewards, const float *values,
+                                    const float *terminateds, const float *truncateds,
+                                    const float *bootstrap_values, const float *last_value,
+                                    int64_t N, int64_t T, int64_t row_stride, float gamma,
+                                    float lambda, float eps, float *advantages,
+                                    float *lambda_returns, float *discounted_returns,
+                                    float *moments, void *ws, size_t ws_bytes,
+                                    rlscan_stream_t stream);
+
+/*
  * V-trace targets and advantages.
  * rl-triton API reference, compute_vtrace; rl-triton paper Table 1 row
  * "V-Trace" and Sec. 3.3.2.

@@ -9,7 +9,8 @@ if it has not been built).
 __version__ = "0.1.0"
 
 _API = {
-    "compute_gae", "compute_gae_and_returns", "compute_vtrace", "compute_retrace",
+    "compute_gae", "compute_gae_and_returns", "compute_gae_normalized", "compute_vtrace",
+    "compute_retrace",
     "compute_retrace_from_probs", "compute_lambda_returns",
     "compute_discounted_returns", "compute_eligibility_traces", "compute_episodic_prefix_sum",
     "linear_scan", "workspace_status",

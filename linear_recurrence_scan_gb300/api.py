@@ -14,7 +14,8 @@ import torch
 from . import _native
 
 __all__ = [
-    "compute_gae", "compute_gae_and_returns", "compute_vtrace", "compute_retrace",
+    "compute_gae", "compute_gae_and_returns", "compute_gae_normalized", "compute_vtrace",
+    "compute_retrace",
     "compute_retrace_from_probs", "compute_lambda_returns",
     "compute_discounted_returns", "compute_eligibility_traces", "compute_episodic_prefix_sum",
     "linear_scan", "workspace_status",
@@ -193,6 +194,43 @@ def compute_gae_and_returns(rewards, values, terminateds, truncateds=None, gamma
         _vp(by_name.get("advantages")), _vp(by_name.get("lambda_returns")),
         _vp(by_name.get("discounted_returns")), ws, wsn, s), "rlscan_gae_returns")
     return tuple(outs)
+
+
+def compute_gae_normalized(rewards, values, terminateds, truncateds=None, gamma=0.99,
+                           lambda_=0.95, bootstrap_values=None, last_value=None, eps=1e-8,
+                           outputs=("advantages", "lambda_returns"), return_moments=False):
+    """GAE advantages normalised over the whole batch, (A - mean) / (std + eps)
+    with the unbiased standard deviation, fused with the returns (which use
+    the raw advantages).  ``outputs`` selects from "advantages" (normalised,
+    always produced), "lambda_returns" and "discounted_returns"; returns them
+    as a tuple in that order, followed by a CUDA float tensor (mean, std) of
+    the raw advantages when ``return_moments``."""
+    known = ("advantages", "lambda_returns", "discounted_returns")
+    if "advantages" not in outputs or any(o not in known for o in outputs):
+        raise ValueError(f"outputs must include 'advantages' and be a subset of {known}")
+    c = _Call("rewards", rewards)
+    c.mat("values", values)
+    c.mat("terminateds", terminateds)
+    c.mat("truncateds", truncateds, False)
+    c.mat("bootstrap_values", bootstrap_values, False)
+    c.vec("last_value", last_value)
+    if last_value is not None and bootstrap_values is not None:
+        raise ValueError("pass either last_value or bootstrap_values, not both")
+    if last_value is not None and truncateds is not None:
+        raise ValueError("last_value cannot be combined with truncateds; use bootstrap_values")
+    outs = c.finish(len(outputs))
+    by_name = dict(zip(outputs, outs))
+    moments = torch.empty(2, dtype=torch.float32, device=c.device) if return_moments else None
+    s = c.stream()
+    need = _native.lib().rlscan_gae_normalized_workspace_bytes(c.N, c.T)
+    ws, wsn = _workspace(c.device, s, need)
+    _native.check(_native.lib().rlscan_gae_normalized(
+        c.m("rewards"), c.m("values"), c.m("terminateds"), c.m("truncateds"),
+        c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma), float(lambda_),
+        float(eps), _vp(by_name["advantages"]), _vp(by_name.get("lambda_returns")),
+        _vp(by_name.get("discounted_returns")), _vp(moments), ws, wsn, s),
+        "rlscan_gae_normalized")
+    return tuple(outs) + ((moments,) if return_moments else ())
 
 
 def compute_vtrace(log_pi_target, log_pi_behavior, values, rewards, terminateds, truncateds=None,

@@ -596,5 +596,12 @@ struct GAEReturns {
     }
 };
 
+// GAE + returns whose kernel also accumulates the batch moments (sum and
+// sum of squares) of the advantages, output 0, for their normalisation.
+template <bool TRUNC, bool BS2D>
+struct GAEReturnsMoments : GAEReturns<TRUNC, BS2D> {
+    static constexpr bool MOMENTS = true;
+};
+
 }  // namespace est
 }  // namespace rlscan

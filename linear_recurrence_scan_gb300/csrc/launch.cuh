@@ -150,7 +150,7 @@ rlscan_status launch_kernel(Kernel kernel, const Params &p, int64_t grid, int th
 }
 
 template <class E>
-rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stream)
+rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stream, int64_t *grid_out = nullptr)
 {
     using S = Shape<E>;
     constexpr int TILE = S::TILE;
@@ -229,11 +229,18 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
             RLSCAN_LAUNCH_TRY(kernel_facts(dfacts, dkernel, dev, BT, dsmem, false, dsmem, nullptr, &dslots));
             // only while the deeper ring keeps three CTAs per SM resident (or
             // as many as the immediate kernel); forced: always
-            if (RLSCAN_DEFER_MODE == 1 || dslots >= slots || dslots >= 3 * static_cast<int64_t>(facts.sm_count[dev]))
-                return launch_kernel(dkernel, p, p.num_tiles < dslots ? p.num_tiles : dslots, BT, dsmem, stream);
+            if (MomentsOf<E>::value && dslots > kMaxMomentCtas) dslots = kMaxMomentCtas;
+            if (RLSCAN_DEFER_MODE == 1 || dslots >= slots || dslots >= 3 * static_cast<int64_t>(facts.sm_count[dev])) {
+                const int64_t grid = p.num_tiles < dslots ? p.num_tiles : dslots;
+                if (grid_out != nullptr) *grid_out = grid;
+                return launch_kernel(dkernel, p, grid, BT, dsmem, stream);
+            }
         }
     }
-    return launch_kernel(kernel, p, p.num_tiles < slots ? p.num_tiles : slots, BT, smem, stream);
+    if (MomentsOf<E>::value && slots > kMaxMomentCtas) slots = kMaxMomentCtas;  // one moments slot per CTA
+    const int64_t grid = p.num_tiles < slots ? p.num_tiles : slots;
+    if (grid_out != nullptr) *grid_out = grid;
+    return launch_kernel(kernel, p, grid, BT, smem, stream);
 }
 
 }  // namespace rlscan

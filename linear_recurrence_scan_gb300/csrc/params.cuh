@@ -25,6 +25,12 @@ constexpr size_t kStateBytes = 16;
 constexpr int kMaxScans = 2;
 enum HeaderWord : int { kHdrExit = 2, kHdrError = 3, kHdrDetail = 4 };
 
+// Batch moments of the advantages (normalising entry point): after the
+// header and tile states, at a 256-byte boundary, one 16-byte slot per CTA
+// of the scan kernel: its sum and sum of squares, each a float pair (hi, lo).
+constexpr int kMaxMomentCtas = 4096;
+constexpr size_t kMomentBytes = 16 * static_cast<size_t>(kMaxMomentCtas);
+
 // Smallest tile (elements per row segment) any kernel uses; the workspace
 // size query is computed with it, so it covers every entry point.
 constexpr int kMinTile = 1024;
@@ -60,11 +66,18 @@ struct Params {
     int32_t wide_staged;          // 1: copied into the stage; 0: read from global memory
     int32_t stage_floats;         // floats per ring stage (narrow and wide regions)
     int32_t A;                    // number of actions
+
+    // batch moments of output 0 (estimators that declare MOMENTS)
+    float *mom_part;              // [gridDim.x][4] per-CTA sum and sum of squares, each a float pair
 };
 
 // Launchers (one translation unit per estimator family).
 rlscan_status launch_gae(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_gae_returns(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
+rlscan_status launch_gae_moments(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s,
+                                 int64_t *grid);
+rlscan_status launch_normalize(float *x, int64_t N, int64_t T, int64_t rs, const float *parts, int64_t nparts,
+                               float eps, float *moments_out, cudaStream_t s);
 rlscan_status launch_vtrace(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_retrace(bool trunc, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_retrace_actions(bool trunc, Params p, void *ws, size_t ws_bytes, cudaStream_t s);

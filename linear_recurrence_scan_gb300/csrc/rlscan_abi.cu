@@ -222,6 +222,14 @@ RLSCAN_API size_t rlscan_workspace_bytes(int64_t N, int64_t T)
     return kHeaderBytes + kStateBytes * kMaxScans * static_cast<size_t>(tiles);
 }
 
+RLSCAN_API size_t rlscan_gae_normalized_workspace_bytes(int64_t N, int64_t T)
+{
+    if (N <= 0 || T <= 0) return 0;
+    size_t scan = rlscan_workspace_bytes(N, T);
+    if (scan < kHeaderBytes) scan = kHeaderBytes;
+    return (scan + 255) / 256 * 256 + kMomentBytes;
+}
+
 RLSCAN_API rlscan_status rlscan_workspace_init(void *ws, size_t ws_bytes, rlscan_stream_t stream)
 {
     if (ws == nullptr) return RLSCAN_ERR_NULL;
@@ -330,6 +338,64 @@ RLSCAN_API rlscan_status rlscan_gae_returns(const float *rewards, const float *v
         p.rowscalar_stride = row_stride;
     }
     return launch_gae_returns(false, false, p, ws, ws_bytes, cs(stream));
+}
+
+RLSCAN_API rlscan_status rlscan_gae_normalized(const float *rewards, const float *values,
+                                               const float *terminateds, const float *truncateds,
+                                               const float *bootstrap_values, const float *last_value,
+                                               int64_t N, int64_t T, int64_t row_stride, float gamma,
+                                               float lambda, float eps, float *advantages,
+                                               float *lambda_returns, float *discounted_returns,
+                                               float *moments, void *ws, size_t ws_bytes,
+                                               rlscan_stream_t stream)
+{
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!rewards || !values || !terminateds || !advantages) return RLSCAN_ERR_NULL;
+    if (!(eps >= 0.f)) return RLSCAN_ERR_ARG_VALUE;
+    if (bootstrap_values && last_value) return RLSCAN_ERR_ARG_CONFLICT;
+    if (last_value && truncateds) return RLSCAN_ERR_ARG_CONFLICT;
+    for (const float *o : {static_cast<const float *>(advantages), static_cast<const float *>(lambda_returns),
+                           static_cast<const float *>(discounted_returns), static_cast<const float *>(moments)}) {
+        if (o == nullptr) continue;
+        if (same_as_any(o, {rewards, values, terminateds, truncateds, bootstrap_values, last_value}))
+            return RLSCAN_ERR_ARG_CONFLICT;
+    }
+    if (advantages == lambda_returns || advantages == discounted_returns || advantages == moments ||
+        (lambda_returns && (lambda_returns == discounted_returns || lambda_returns == moments)) ||
+        (discounted_returns && discounted_returns == moments))
+        return RLSCAN_ERR_ARG_CONFLICT;
+    const size_t need = rlscan_gae_normalized_workspace_bytes(N, T);
+    if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u) != 0)
+        return RLSCAN_ERR_WORKSPACE;
+    RLSCAN_TRY(run_checks(terminateds, truncateds, bootstrap_values, N, T, row_stride, cs(stream)));
+    Params p = base_params(N, T, row_stride);
+    p.c0 = gamma;
+    p.c1 = lambda;
+    p.out[0] = advantages;
+    p.out[1] = lambda_returns;
+    p.out[2] = discounted_returns;
+    p.in[0] = rewards;
+    p.in[1] = values;
+    p.in[2] = terminateds;
+    p.mom_part = reinterpret_cast<float *>(static_cast<char *>(ws) + (need - kMomentBytes));
+    int64_t grid = 0;
+    rlscan_status st;
+    if (truncateds) {
+        p.in[3] = truncateds;
+        p.in[4] = bootstrap_values;
+        st = launch_gae_moments(true, bootstrap_values != nullptr, p, ws, ws_bytes, cs(stream), &grid);
+    } else {
+        if (last_value) {
+            p.rowscalar = last_value;
+        } else if (bootstrap_values) {
+            p.rowscalar = bootstrap_values + (T - 1);
+            p.rowscalar_stride = row_stride;
+        }
+        st = launch_gae_moments(false, false, p, ws, ws_bytes, cs(stream), &grid);
+    }
+    if (st != RLSCAN_OK) return st;
+    return launch_normalize(advantages, N, T, row_stride, p.mom_part, grid, eps, moments, cs(stream));
 }
 
 RLSCAN_API rlscan_status rlscan_vtrace(const float *log_pi_target, const float *log_pi_behavior,

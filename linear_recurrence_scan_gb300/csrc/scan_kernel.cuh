@@ -55,6 +55,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "dfloat.cuh"
 #include "estimators.cuh"
 #include "params.cuh"
 #include "ptx.cuh"
@@ -78,6 +79,16 @@ template <class E>
 struct WideOf<E, std::void_t<decltype(E::NWIDE)>> {
     static constexpr int NWIDE = E::NWIDE;
     static constexpr unsigned DERIVED = E::DERIVED;
+};
+
+// Estimators whose kernel accumulates the batch moments of output 0.
+template <class E, class = void>
+struct MomentsOf {
+    static constexpr bool value = false;
+};
+template <class E>
+struct MomentsOf<E, std::void_t<decltype(E::MOMENTS)>> {
+    static constexpr bool value = E::MOMENTS;
 };
 
 // Shared-memory slot of narrow input j within a stage: the copied arrays
@@ -417,15 +428,18 @@ constexpr int block_threads() { return THREADS + 32; }
 #ifndef RLSCAN_DEFER_MIN_BLOCKS
 #define RLSCAN_DEFER_MIN_BLOCKS 0  // 0: as the immediate-finish kernel
 #endif
-template <class E, bool DEFER>
+template <class E, bool DEFER, int THREADS>
 constexpr int min_blocks()
 {
+    // small two-scan CTAs: keep four resident (the ring allows it)
     return (DEFER && RLSCAN_DEFER_MIN_BLOCKS > 0) ? RLSCAN_DEFER_MIN_BLOCKS
-                                                 : ((WideOf<E>::NWIDE > 0 || E::K > 1) ? 2 : RLSCAN_MIN_BLOCKS);
+           : (WideOf<E>::NWIDE > 0) ? 2
+           : (E::K > 1) ? (THREADS <= 128 && !DEFER ? 4 : 2)
+           : RLSCAN_MIN_BLOCKS;
 }
 
 template <class E, int THREADS, int ITEMS, int STAGES, bool DEFER>
-__global__ void __launch_bounds__(block_threads<THREADS>(), min_blocks<E, DEFER>())
+__global__ void __launch_bounds__(block_threads<THREADS>(), min_blocks<E, DEFER, THREADS>())
 scan_kernel(const __grid_constant__ Params p)
 {
     constexpr int NIN = E::NIN, NOUT = E::NOUT, K = E::K;
@@ -528,6 +542,10 @@ scan_kernel(const __grid_constant__ Params p)
     uint32_t lost_stages = 0, lost_parity = 0;  // waits that timed out (thread 0)
 
     using Keep = typename E::template Keep<ITEMS>;
+    constexpr bool MOM = MomentsOf<E>::value;
+    // this thread's share of the batch moments: a float sum per tile, carried
+    // across tiles (and combined across the CTA and the grid) as float pairs
+    DF mom_s{0.f, 0.f}, mom_q{0.f, 0.f};
 
     // inputs of this thread's ITEMS steps, plus the neighbour step
     auto load_inputs = [&](const float *stage, float (&x)[NIN][ITEMS], float (&xn)[NIN]) {
@@ -605,6 +623,18 @@ scan_kernel(const __grid_constant__ Params p)
         const bool edge = sp.kb >= 0 || sp.kv < ITEMS;
         if (!edge) E::template post<ITEMS, false>(x, xn, -1, p, rsc, A, x_in, keep, o);
         else E::template post<ITEMS, true>(x, xn, sp.kb, p, rsc, A, x_in, keep, o);
+        if constexpr (MOM) {  // this tile's share of the batch moments of output 0
+            float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+            for (int k = 0; k < ITEMS; ++k) {
+                if (k < sp.kv) {
+                    s1 += o[0][k];
+                    s2 = fmaf(o[0][k], o[0][k], s2);
+                }
+            }
+            mom_s = df_add(mom_s, DF{s1, 0.f});
+            mom_q = df_add(mom_q, DF{s2, 0.f});
+        }
         if (sp.kv > 0) {
             const int64_t off = (tg.row0 + rit) * p.rs + tg.t0 + col;
 #pragma unroll
@@ -805,6 +835,31 @@ scan_kernel(const __grid_constant__ Params p)
         }
     }
     if (pend) finish_pending();
+
+    if constexpr (MOM) {
+        // CTA total of the moments (float pairs), delivered to this CTA's
+        // slot; the normalising pass combines the slots after this kernel
+        __shared__ DF s_mom[WARPS][2];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            mom_s = df_add(mom_s, df_shfl_down(mom_s, o));
+            mom_q = df_add(mom_q, df_shfl_down(mom_q, o));
+        }
+        if (lane == 0) {
+            s_mom[warp][0] = mom_s;
+            s_mom[warp][1] = mom_q;
+        }
+        ptx::named_barrier(COMPUTE_BAR, THREADS);
+        if (tid == 0) {
+            DF cs{0.f, 0.f}, cq{0.f, 0.f};
+            for (int w2 = 0; w2 < WARPS; ++w2) {
+                cs = df_add(cs, s_mom[w2][0]);
+                cq = df_add(cq, s_mom[w2][1]);
+            }
+            *reinterpret_cast<float4 *>(p.mom_part + 4 * static_cast<int64_t>(blockIdx.x)) =
+                make_float4(cs.hi, cs.lo, cq.hi, cq.lo);
+        }
+    }
 
     // A copy whose wait timed out may still be landing: give it one more
     // bounded wait before the shared memory is released.

@@ -244,6 +244,20 @@ class Oracle:
         return out
 
 
+def normalize_advantages(advantages, eps=1e-8):
+    """Per-batch whitening of advantages (rl-triton paper Sec. 9.3, "fused
+    advantage normalization", read as (A - mean) / (std + eps) over all N*T
+    values with the unbiased standard deviation).  Two passes in float64:
+    the mean, then the sum of squared deviations.  Returns the normalised
+    array and (mean, std)."""
+    a = np.asarray(advantages, dtype=np.float64)
+    n = a.size
+    mean = a.sum() / n
+    dev = a - mean
+    std = np.sqrt((dev * dev).sum() / (n - 1)) if n > 1 else float("nan")
+    return dev / (std + eps), (float(mean), float(std))
+
+
 def default() -> Oracle:
     """The oracle built from ``oracle/rlscan_oracle.c`` (compiled on first use)."""
     global _default

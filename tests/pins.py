@@ -696,6 +696,45 @@ def check_retrace_actions_one_hot(orc):
            what="retrace one-hot advantages")
 
 
+# --------------------------------------------------------------------------
+# advantage normalisation (per-batch whitening)
+# --------------------------------------------------------------------------
+
+def check_normalize_against_stdlib(orc, normalize=None):
+    """(A - mean) / (std + eps) with the unbiased standard deviation, against
+    Python's statistics.fmean / statistics.stdev (an independent
+    implementation), for several shapes and eps."""
+    import statistics
+    normalize = normalize or _normalize_of(orc)
+    rng = np.random.default_rng(31)
+    for shape, eps in (((1, 2), 0.0), ((3, 7), 1e-8), ((4, 33), 0.5), ((2, 100), 1e-3)):
+        x = rng.standard_normal(shape) * 3.0 + 1.5
+        vals = [float(v) for v in x.ravel()]
+        mean, sd = statistics.fmean(vals), statistics.stdev(vals)
+        got, (gm, gs) = normalize(x, eps)
+        _close(gm, mean, tol=1e-12, what="normalize mean")
+        _close(gs, sd, tol=1e-12, what="normalize std")
+        _close(got, (x - mean) / (sd + eps), tol=1e-12, what="normalized values")
+
+
+def check_normalize_invariants(orc, normalize=None):
+    """With eps = 0 the result has mean 0 and unbiased standard deviation 1,
+    and is unchanged by a positive affine map of the inputs."""
+    normalize = normalize or _normalize_of(orc)
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((5, 40))
+    y, _ = normalize(x, 0.0)
+    _close(y.mean(), 0.0, tol=1e-12, what="normalized mean")
+    _close(y.std(ddof=1), 1.0, tol=1e-12, what="normalized std")
+    z, _ = normalize(2.5 * x - 7.0, 0.0)
+    _close(z, y, tol=1e-10, what="normalization affine invariance")
+
+
+def _normalize_of(orc):
+    import oracle
+    return getattr(orc, "normalize_advantages", oracle.normalize_advantages)
+
+
 ALL_CHECKS = [
     check_golden,
     check_brute_force,
@@ -712,6 +751,8 @@ ALL_CHECKS = [
     check_retrace_actions_reduction,
     check_retrace_actions_relabelling,
     check_retrace_actions_one_hot,
+    check_normalize_against_stdlib,
+    check_normalize_invariants,
 ]
 
 

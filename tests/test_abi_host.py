@@ -124,6 +124,27 @@ def test_retrace_actions_validation(lib):
     assert retrace_actions(lib, adv=5) == 3
 
 
+def test_gae_normalized_validation(lib):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x * 256)
+    need = lib.rlscan_gae_normalized_workspace_bytes(2, 4)
+    assert need >= 64 + 16 * 4096 and lib.rlscan_gae_normalized_workspace_bytes(0, 4) == 0
+    # look-back part of the workspace (rounded to 256 bytes) before the moments region
+    assert (lib.rlscan_gae_normalized_workspace_bytes(64, 1 << 20) - need
+            == (lib.rlscan_workspace_bytes(64, 1 << 20) + 255) // 256 * 256 - 256)
+
+    def call(adv=10, eps=1e-8, ws=20, wsn=None, moments=None):
+        return lib.rlscan_gae_normalized(vp(1), vp(2), vp(3), None, None, None, 2, 4, 4, 0.99,
+                                         0.95, eps, vp(adv), None, None, vp(moments), vp(ws),
+                                         need if wsn is None else wsn, None)
+    assert call(adv=None) == 1
+    assert call(eps=-1.0) == 4
+    assert call(eps=float("nan")) == 4
+    assert call(ws=None) == 5
+    assert call(wsn=need - 1) == 5
+    assert call(moments=10) == 3                                  # moments alias the advantages
+    assert call(adv=2) == 3                                       # output aliases an input
+
+
 def test_python_layer_rejects_cpu_and_wrong_dtype():
     import torch
     import linear_recurrence_scan_gb300 as L

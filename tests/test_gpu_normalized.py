@@ -1,0 +1,117 @@
+"""GAE with batch-normalised advantages (fused moments + in-place
+normalisation) against the float64 oracle: gae() then
+normalize_advantages().  The returns are compared with their own oracles
+(they use the raw advantages).
+
+Tolerances: normalised advantages and returns |gpu - ref| <= 1e-4 + 1e-5 |ref|;
+the reported (mean, std) within 1e-5 relative (+1e-6 absolute for the mean).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_recurrence_scan_gb300 import synthetic
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from linear_recurrence_scan_gb300 import build
+    build.build()
+
+
+def L():
+    import linear_recurrence_scan_gb300 as lib
+    return lib
+
+
+def dev(a, rs=None):
+    if a is None:
+        return None
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if rs is not None and a.ndim == 2 and rs != a.shape[1]:
+        big = torch.zeros((a.shape[0], rs), dtype=torch.float32)
+        big[:, : a.shape[1]] = t
+        return big.to(DEV)[:, : a.shape[1]]
+    return t.to(DEV)
+
+
+def assert_disc(gpu, ref, what):
+    g = gpu.double().cpu().numpy()
+    err = np.abs(g - ref)
+    bad = ~(err <= 1e-4 + 1e-5 * np.abs(ref))
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} off, first {i}: "
+                             f"gpu {g[i]!r} ref {ref[i]!r}")
+
+
+# (N, T, row stride or None, mode): packed, one tile, look-back, deferred
+# look-back (few long rows), element-wise staging, strided rows
+CASES = [
+    (8, 128, None, "last"), (5, 37, None, "last"), (6, 1024, None, "last"),
+    (3, 3000, None, "last"), (2, 40000, None, "2d"), (64, 1 << 16, None, "last"),
+    (5, 100, 104, "2d"), (5, 100, 103, "last"), (4096, 1024, None, "last"),
+]
+IDS = [f"{n}x{t}" + (f"_rs{rs}" if rs else "") + f"_{m}" for n, t, rs, m in CASES]
+
+
+@pytest.mark.parametrize("case", CASES, ids=IDS)
+def test_normalized_parity(case):
+    N, T, rs, mode = case
+    b = synthetic.gae_batch(N, T, 3, 51, 0.01, 0.005 if mode == "2d" else 0.0, mode)
+    g, lam, eps = 0.99, 0.95, 1e-8
+    trunc = b["truncateds"]
+    bs, last = b["bootstrap_values"], b["last_value"]
+    raw = oracle.gae(b["rewards"], b["values"], b["terminateds"], trunc, g, lam, bs, last)
+    want, (mean, sd) = oracle.normalize_advantages(raw, eps)
+    adv, lret, disc, mom = L().compute_gae_normalized(
+        dev(b["rewards"], rs), dev(b["values"], rs), dev(b["terminateds"], rs), dev(trunc, rs), g,
+        lam, dev(bs, rs), dev(last), eps,
+        outputs=("advantages", "lambda_returns", "discounted_returns"), return_moments=True)
+    assert_disc(adv, want, "normalized advantages")
+    m = mom.double().cpu().numpy()
+    assert abs(m[0] - mean) <= 1e-6 + 1e-5 * abs(mean), (m, mean)
+    assert abs(m[1] - sd) <= 1e-5 * sd, (m, sd)
+    nv = np.zeros_like(b["values"])
+    nv[:, :-1] = b["values"][:, 1:]
+    if mode == "last":
+        nv[:, -1] = b["last_value"]
+        lam_ref = oracle.lambda_returns(b["rewards"], nv, b["terminateds"], None, g, lam, None, last)
+        disc_ref = oracle.discounted_returns(b["rewards"], b["terminateds"], None, g, None, last)
+        assert_disc(lret, lam_ref, "lambda returns")
+        assert_disc(disc, disc_ref, "discounted returns")
+    else:
+        assert_disc(lret, raw + b["values"].astype(np.float64), "lambda returns = raw A + V")
+        disc_ref = oracle.discounted_returns(b["rewards"], b["terminateds"], trunc, g, bs, None)
+        assert_disc(disc, disc_ref, "discounted returns")
+
+
+def test_repeated_and_interleaved_calls():
+    """The per-call moments counter re-arms itself: repeated calls, and calls
+    interleaved with other entry points on the same workspace, agree."""
+    N, T = 64, 1 << 14
+    b = synthetic.gae_batch(N, T, 4, 52, 0.01, 0.0, "last")
+    args = [dev(b[k]) for k in ("rewards", "values", "terminateds")]
+    first = L().compute_gae_normalized(*args, None, 0.99, 0.95, None, dev(b["last_value"]))[0]
+    for _ in range(3):
+        L().compute_gae(*args, None, 0.99, 0.95, None, dev(b["last_value"]))
+        again = L().compute_gae_normalized(*args, None, 0.99, 0.95, None, dev(b["last_value"]))[0]
+        torch.testing.assert_close(again, first, rtol=1e-6, atol=1e-6)
+
+
+def test_single_value_gives_nan():
+    x = torch.ones(1, 1, device=DEV)
+    adv, = L().compute_gae_normalized(x, x, torch.zeros(1, 1, device=DEV), outputs=("advantages",))
+    assert torch.isnan(adv).all()
+
+
+def test_eps_must_be_non_negative():
+    from linear_recurrence_scan_gb300 import _native
+    x = torch.ones(2, 4, device=DEV)
+    with pytest.raises(_native.RlscanError):
+        L().compute_gae_normalized(x, x, torch.zeros(2, 4, device=DEV), eps=-1.0)

@@ -124,3 +124,31 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     lib = oracle.build(force=True, src=str(mutated), out=str(tmp_path / "libmutant.so"))
     failing = pins.failing_checks(oracle.Oracle(lib))
     assert failing, f"no pin caught the planted mistake {name}"
+
+
+# The normalisation is numpy code in oracle/__init__.py: plant mistakes in a
+# copy of that function's source and run the normalisation pins on it.
+NORMALIZE_MUTANTS = {
+    "biased_std": ("/ (n - 1)", "/ n"),
+    "eps_in_variance": ("return dev / (std + eps)", "return dev / np.sqrt(std * std + eps)"),
+    "mean_not_removed": ("return dev / (std + eps)", "return a / (std + eps)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(NORMALIZE_MUTANTS))
+def test_normalize_pins_catch_planted_mistake(name):
+    import inspect
+    import numpy as np
+    old, new = NORMALIZE_MUTANTS[name]
+    src = inspect.getsource(oracle.normalize_advantages)
+    assert src.count(old) == 1, f"mutation site for {name} not unique/absent"
+    ns = {"np": np}
+    exec(src.replace(old, new), ns)
+    fn = ns["normalize_advantages"]
+    caught = False
+    for chk in (pins.check_normalize_against_stdlib, pins.check_normalize_invariants):
+        try:
+            chk(None, fn)
+        except AssertionError:
+            caught = True
+    assert caught, f"no pin caught the planted mistake {name}"
