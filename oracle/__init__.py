@@ -59,6 +59,7 @@ _P = ctypes.c_void_p
 
 _SIGNATURES = {
     "oracle_gae": [_I64] * 5 + [_P] * 6 + [_D, _D, _P],
+    "oracle_gae_masked": [_I64] * 5 + [_P] * 7 + [_D, _D, _P],
     "oracle_vtrace": [_I64] * 5 + [_P] * 8 + [_D, _D, _D, _P, _P],
     "oracle_retrace": [_I64] * 5 + [_P] * 7 + [_D, _D, _D, _D, _P, _P],
     "oracle_retrace_actions": [_I64] * 6 + [_P] * 8 + [_D, _D, _D, _D, _P, _P],
@@ -129,6 +130,20 @@ class Oracle:
                            c.mat(terminateds, "terminateds"), c.mat(truncateds, "truncateds"),
                            c.mat(bootstrap_values, "bootstrap_values"),
                            c.vec(last_value, "last_value"), gamma, lambda_, out.ctypes.data)
+        return out
+
+    def gae_masked(self, rewards, values, terminateds, mask, truncateds=None, gamma=0.99,
+                   lambda_=0.95, bootstrap_values=None, last_value=None, rows=None):
+        """GAE with observation-skip masking (float64): masked steps carry
+        the next step's advantage unchanged."""
+        c = _Rows(rewards)
+        out = c.out()
+        self._lib.oracle_gae_masked(*c.head(rows), c.mat(rewards, "rewards"),
+                                    c.mat(values, "values"), c.mat(terminateds, "terminateds"),
+                                    c.mat(truncateds, "truncateds"),
+                                    c.mat(bootstrap_values, "bootstrap_values"),
+                                    c.vec(last_value, "last_value"), c.mat(mask, "mask"), gamma,
+                                    lambda_, out.ctypes.data)
         return out
 
     def vtrace(self, log_pi_target, log_pi_behavior, values, rewards, terminateds, truncateds=None,
@@ -269,6 +284,10 @@ def default() -> Oracle:
 
 def gae(*args, **kwargs):
     return default().gae(*args, **kwargs)
+
+
+def gae_masked(*args, **kwargs):
+    return default().gae_masked(*args, **kwargs)
 
 
 def vtrace(*args, **kwargs):

@@ -117,6 +117,44 @@ void oracle_gae(int64_t N, int64_t T, int64_t rs, int64_t row_begin, int64_t row
 }
 
 /*
+ * GAE with observation-skip masking -- [PAPER] Sec. 9.3 (planned extension:
+ * "observation-skip masking that carries the recurrence across masked
+ * tokens (beta_t = 1)").  Reading: a masked step (mask_t = 0) contributes
+ * nothing and hands the value through, A_t = A_{t+1}; an unmasked step is
+ * the GAE step of oracle_gae, unchanged (its successor value is V_next_t as
+ * defined there).  mask is float 0/1.
+ */
+void oracle_gae_masked(int64_t N, int64_t T, int64_t rs, int64_t row_begin, int64_t row_end,
+                       const float *r, const float *v, const float *term, const float *trunc,
+                       const float *bs, const float *last_value, const float *mask,
+                       double gamma, double lam, double *adv)
+{
+    (void)N;
+    double *vrow = (double *)malloc((size_t)(T > 0 ? T : 1) * sizeof(double));
+    if (!vrow) return;
+    for (int64_t row = row_begin; row < row_end; ++row) {
+        double *out = adv + row * T;
+        for (int64_t t = 0; t < T; ++t) vrow[t] = AT(v, row, t, rs);
+        double carry = 0.0;  /* A_{t+1} */
+        for (int64_t t = T - 1; t >= 0; --t) {
+            double A;
+            if (AT(mask, row, t, rs) == 0.0) {
+                A = carry;
+            } else {
+                double vnext = continuation(vrow, t, T, trunc, bs, last_value, row, rs);
+                double te = AT(term, row, t, rs);
+                double tr = trunc ? AT(trunc, row, t, rs) : 0.0;
+                double td = AT(r, row, t, rs) + gamma * (1.0 - te) * vnext - vrow[t];
+                A = td + gamma * lam * (1.0 - done_flag(te, tr)) * carry;
+            }
+            out[t] = A;
+            carry = A;
+        }
+    }
+    free(vrow);
+}
+
+/*
  * V-trace -- [API] compute_vtrace (docstring and unfused branch);
  * [PAPER] Table 1 row "V-Trace", Sec. 3.3.2.
  *   ratio_t = exp(log_pi_target_t - log_pi_behavior_t)

@@ -697,6 +697,57 @@ def check_retrace_actions_one_hot(orc):
 
 
 # --------------------------------------------------------------------------
+# observation-skip masking (GAE)
+# --------------------------------------------------------------------------
+
+def check_gae_masked(orc):
+    """Observation-skip GAE (paper Sec. 9.3: the recurrence is carried across
+    masked tokens, beta = 1): an all-ones mask is plain GAE; an all-zeros
+    mask gives zero; a hand-worked case; and brute force -- for an unmasked
+    step, A_t = sum over unmasked k >= t of (prod over unmasked j in [t, k)
+    of gamma lambda (1 - done_j)) delta_k, with delta from the paper's
+    successor rule; a masked step holds the next unmasked step's value (0
+    past the last one)."""
+    rng = np.random.default_rng(41)
+    N, T, g, l = 4, 29, 0.93, 0.8
+    r = _f32(rng.standard_normal((N, T)))
+    v = _f32(rng.standard_normal((N, T)))
+    term, trunc = _flags(rng, N, T, 0.1, 0.1)
+    bs = _conforming_bs(rng, term, trunc)
+    ones = np.ones((N, T), np.float32)
+    _close(orc.gae_masked(r, v, term, ones, trunc, g, l, bs), orc.gae(r, v, term, trunc, g, l, bs),
+           tol=0.0, what="all-ones mask = GAE")
+    _close(orc.gae_masked(r, v, term, 0 * ones, trunc, g, l, bs), np.zeros((N, T)), tol=0.0,
+           what="all-zeros mask")
+    # hand-worked: r = (1,2,3,4), V = 0, no flags, mask (1,0,1,0), gamma 0.5,
+    # lambda 1: A_3 = 0 (masked, past the end), A_2 = 3, A_1 = A_2 = 3,
+    # A_0 = 1 + 0.5 * 3 = 2.5
+    hw = orc.gae_masked(_f32([[1, 2, 3, 4]]), _f32([[0, 0, 0, 0]]), _f32([[0, 0, 0, 0]]),
+                        _f32([[1, 0, 1, 0]]), None, 0.5, 1.0)
+    _close(hw, [[2.5, 3.0, 3.0, 0.0]], tol=0.0, what="masked hand-worked")
+    for tr, b, last in ((None, None, _f32(rng.standard_normal(N))), (trunc, bs, None)):
+        mask = (rng.random((N, T)) < 0.6).astype(np.float32)
+        got = orc.gae_masked(r, v, term, mask, tr, g, l, b, last)
+        nxt = _table1_next(_d64(v), tr, b, last, T)
+        delta = _d64(r) + g * (1 - _d64(term)) * nxt - _d64(v)
+        done = np.minimum(1.0, _d64(term) + _d64(tr, (N, T)))
+        want = np.zeros((N, T))
+        for n in range(N):
+            for t in range(T):
+                t0 = t
+                while t0 < T and mask[n, t0] == 0:
+                    t0 += 1
+                acc, prod = 0.0, 1.0
+                for k in range(t0, T):
+                    if mask[n, k] == 0:
+                        continue
+                    acc += prod * delta[n, k]
+                    prod *= g * l * (1 - done[n, k])
+                want[n, t] = acc
+        _close(got, want, what="masked GAE brute force")
+
+
+# --------------------------------------------------------------------------
 # advantage normalisation (per-batch whitening)
 # --------------------------------------------------------------------------
 
@@ -751,6 +802,7 @@ ALL_CHECKS = [
     check_retrace_actions_reduction,
     check_retrace_actions_relabelling,
     check_retrace_actions_one_hot,
+    check_gae_masked,
     check_normalize_against_stdlib,
     check_normalize_invariants,
 ]

@@ -72,6 +72,18 @@ MUTANTS = {
     "retrace_actions_gather_index": (
         "pi_d[t] = (double)pt[at];",
         "pi_d[t] = (double)pt[A - 1 - at];"),
+    # masked GAE: a masked step resets instead of carrying
+    "masked_reset": (
+        "            if (AT(mask, row, t, rs) == 0.0) {\n                A = carry;",
+        "            if (AT(mask, row, t, rs) == 0.0) {\n                A = 0.0;"),
+    # masked GAE: the carry across a masked step is discounted
+    "masked_discounted_carry": (
+        "            if (AT(mask, row, t, rs) == 0.0) {\n                A = carry;",
+        "            if (AT(mask, row, t, rs) == 0.0) {\n                A = gamma * lam * carry;"),
+    # masked GAE: mask ignored
+    "masked_ignored": (
+        "            if (AT(mask, row, t, rs) == 0.0) {\n                A = carry;",
+        "            if (AT(mask, row, t, rs) == 2.0) {\n                A = carry;"),
     # TD(lambda): (1 - lambda) weight replaced by lambda
     "td_value_weight": (
         "double G = AT(r, row, t, rs) + gamma * (1.0 - lam) * nd * AT(nv, row, t, rs)",
