@@ -59,6 +59,12 @@ def _cfg_workloads():
             N=4096, T=1024, gen=lambda N, T: synthetic.config_batch(1, N=N, T=T),
             # r, v, term read once; normalised advantages and lambda-returns written
             estimators=[("gae_normalized", 20, c1)]),
+        "gae_masked_4096x8192": dict(
+            desc="token-level GAE with observation-skip masking on LLM rollouts (masked prompt, "
+                 "tool observations and padding; outcome reward on the last response token)",
+            N=4096, T=8192, gen=lambda N, T: synthetic.llm_tokens_batch(N, T),
+            # r, v, term, mask read once; advantages written
+            estimators=[("gae_masked", 20, dict(gamma=1.0, lambda_=0.95))]),
         "gae_8x128": dict(
             desc="GAE with truncations and 2-D bootstrap", N=8, T=128,
             gen=lambda N, T: synthetic.config_batch(0, N=N, T=T),
@@ -115,6 +121,7 @@ IO = {
     "episodic_prefix_sum": (["inputs", "prefix_dones"], [], 1),
     "gae_returns": (["rewards", "values", "terminateds"], ["last_value"], 3),
     "gae_normalized": (["rewards", "values", "terminateds"], ["last_value"], 2),
+    "gae_masked": (["rewards", "values", "terminateds", "mask"], [], 1),
 }
 # kernels one call launches (default 1)
 LAUNCHES = {"gae_normalized": 2}
@@ -270,6 +277,10 @@ def _launcher(name, c, bufs, outs, N, T, ws, wsn, stream):
     if name == "episodic_prefix_sum":
         return lambda: lib.rlscan_episodic_prefix_sum(b["inputs"], b["prefix_dones"], None, 1, N,
                                                       T, T, o[0], ws, wsn, stream)
+    if name == "gae_masked":
+        return lambda: lib.rlscan_gae_masked(b["rewards"], b["values"], b["terminateds"], None, None,
+                                             None, b["mask"], N, T, T, g, float(c["lambda_"]), o[0],
+                                             ws, wsn, stream)
     if name == "gae_normalized":
         return lambda: lib.rlscan_gae_normalized(b["rewards"], b["values"], b["terminateds"], None,
                                                  None, b["last_value"], N, T, T, g,
@@ -317,6 +328,9 @@ def _public_call(name, c, t):
         return [Lb.compute_eligibility_traces(t["gradients"], t["trace_dones"], g, c["lambda_"])]
     if name == "episodic_prefix_sum":
         return [Lb.compute_episodic_prefix_sum(t["inputs"], t["prefix_dones"], None, "starts_at")]
+    if name == "gae_masked":
+        return [Lb.compute_gae(t["rewards"], t["values"], t["terminateds"], None, g, c["lambda_"],
+                               mask=t["mask"])]
     if name == "gae_normalized":
         return list(Lb.compute_gae_normalized(t["rewards"], t["values"], t["terminateds"], None, g,
                                               c["lambda_"], None, t["last_value"], 1e-8,
@@ -525,6 +539,9 @@ def _oracle_call(name, c, b):
                                       b["q_values"], b["next_q_values_all"], b["actions"],
                                       b["rewards"], b["terminateds"], None, g, c["lambda_"],
                                       c["c_bar"], c["rho_bar"])
+    if name == "gae_masked":
+        return oracle.gae_masked(b["rewards"], b["values"], b["terminateds"], b["mask"], None, g,
+                                 c["lambda_"])
     if name == "gae_normalized":
         adv = oracle.gae(b["rewards"], b["values"], b["terminateds"], None, g, c["lambda_"], None,
                          b["last_value"])

@@ -132,6 +132,26 @@ rlscan_status rlscan_gae(const float *rewards, const float *values, const float 
                          void *ws, size_t ws_bytes, rlscan_stream_t stream);
 
 /*
+ * GAE with observation-skip masking.  rl-triton paper Sec. 9.3 plans
+ * "observation-skip masking that carries the recurrence across masked
+ * tokens (beta_t = 1)"; read here as: at a masked step (mask_t = 0) the
+ * advantage is handed through unchanged, A_t = A_{t+1} (alpha_t = 0,
+ * beta_t = 1); an unmasked step is the GAE step of rlscan_gae unchanged,
+ * including its successor value Vn_t (the stored V_{t+1}, or the bootstrap
+ * rule there).  Past the last unmasked step of a row the value is 0.
+ *   A_t = m_t delta_t + (m_t gamma lambda (1 - done_t) + 1 - m_t) A_{t+1}
+ * For token-level LLM rollouts, mask = 1 on the policy's (response) tokens
+ * and 0 on prompt, observation or padding tokens.
+ * Inputs : as rlscan_gae, plus mask [N,T] float32 0/1 (required).
+ * Outputs: advantages [N,T] (masked steps hold the next unmasked value).
+ */
+rlscan_status rlscan_gae_masked(const float *rewards, const float *values, const float *terminateds,
+                                const float *truncateds, const float *bootstrap_values,
+                                const float *last_value, const float *mask, int64_t N, int64_t T,
+                                int64_t row_stride, float gamma, float lambda, float *advantages,
+                                void *ws, size_t ws_bytes, rlscan_stream_t stream);
+
+/*
  * GAE, lambda-returns and discounted returns from one read of the buffer.
  * The rl-triton paper's planned fused post-scan extensions (Sec. 9.3); the
  * returns tutorial's identity that lambda-returns are the GAE targets

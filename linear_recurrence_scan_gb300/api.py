@@ -145,13 +145,17 @@ def workspace_status(device=None):
 # estimators (rl-triton API reference signatures)
 
 def compute_gae(rewards, values, terminateds, truncateds=None, gamma=0.99, lambda_=0.95,
-                bootstrap_values=None, last_value=None):
-    """GAE advantages [num_envs, seq_len] (rl-triton API reference, compute_gae)."""
+                bootstrap_values=None, last_value=None, mask=None):
+    """GAE advantages [num_envs, seq_len] (rl-triton API reference, compute_gae).
+    ``mask`` (an addition, float 0/1 [num_envs, seq_len]) selects
+    observation-skip masking: masked steps carry the next step's advantage
+    unchanged (beta = 1), unmasked steps are plain GAE steps."""
     c = _Call("rewards", rewards)
     c.mat("values", values)
     c.mat("terminateds", terminateds)
     c.mat("truncateds", truncateds, False)
     c.mat("bootstrap_values", bootstrap_values, False)
+    c.mat("mask", mask, False)
     c.vec("last_value", last_value)
     if last_value is not None and bootstrap_values is not None:
         raise ValueError("pass either last_value or bootstrap_values, not both")
@@ -159,6 +163,12 @@ def compute_gae(rewards, values, terminateds, truncateds=None, gamma=0.99, lambd
         raise ValueError("last_value cannot be combined with truncateds; use bootstrap_values")
     (out,) = c.finish(1)
     ws, wsn, s = _ws_for(c)
+    if mask is not None:
+        _native.check(_native.lib().rlscan_gae_masked(
+            c.m("rewards"), c.m("values"), c.m("terminateds"), c.m("truncateds"),
+            c.m("bootstrap_values"), c.v("last_value"), c.m("mask"), c.N, c.T, c.rs,
+            float(gamma), float(lambda_), _vp(out), ws, wsn, s), "rlscan_gae_masked")
+        return out
     _native.check(_native.lib().rlscan_gae(
         c.m("rewards"), c.m("values"), c.m("terminateds"), c.m("truncateds"),
         c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma), float(lambda_),

@@ -97,6 +97,44 @@ struct GAE {
 };
 
 // ---------------------------------------------------------------------------
+// GAE with observation-skip masking (rl-triton paper Sec. 9.3: the
+// recurrence is carried across masked tokens, beta = 1): the GAE map of an
+// unmasked step, and the identity map (alpha = 0, beta = 1) at a masked one:
+//   alpha = m alpha_GAE,  beta = m beta_GAE + (1 - m),  m = mask_t in {0, 1}.
+// Inputs: those of GAE<TRUNC, BS2D>, then the mask.
+template <bool TRUNC, bool BS2D>
+struct GAEMasked : GAE<TRUNC, BS2D> {
+    using Base = GAE<TRUNC, BS2D>;
+    static constexpr int NIN = Base::NIN + 1, MASK = Base::NIN;
+    template <int I> struct Keep {};
+
+    template <int I, bool EDGE>
+    __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
+                                  const Params &p, float rsc, float (&a)[1][I], float (&b)[1][I], Keep<I> &)
+    {
+        const float(&xb)[Base::NIN][I] = reinterpret_cast<const float(&)[Base::NIN][I]>(x);
+        const float(&xnb)[Base::NIN] = reinterpret_cast<const float(&)[Base::NIN]>(xn);
+        typename Base::template Keep<I> kb_unused;
+        Base::template coeffs<I, EDGE>(xb, xnb, kb, p, rsc, a, b, kb_unused);
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            const float m = x[MASK][k];
+            a[0][k] *= m;
+            b[0][k] = fmaf(m, b[0][k], 1.f - m);
+        }
+    }
+    template <int I>
+    __device__ static void boundary(const float (&)[NIN][I], int, float, const Params &, float (&bv)[1]) { bv[0] = 0.f; }
+    template <int I, bool EDGE>
+    __device__ static void post(const float (&)[NIN][I], const float (&)[NIN], int, const Params &,
+                                float, const float (&A)[1][I], const float (&)[1], const Keep<I> &, float (&o)[1][I])
+    {
+#pragma unroll
+        for (int k = 0; k < I; ++k) o[0][k] = A[0][k];
+    }
+};
+
+// ---------------------------------------------------------------------------
 // V-trace: ratio = exp(lpt - lpb), rho = min(rho_bar, ratio), c = min(c_bar, ratio);
 // alpha = rho (r + gamma (1-term) Vn - V), beta = gamma c (1-done), D_T = 0;
 // vs = D + V, adv = rho (r + gamma (1-term) vsn - V).

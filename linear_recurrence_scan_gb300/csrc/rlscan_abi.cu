@@ -293,6 +293,48 @@ RLSCAN_API rlscan_status rlscan_gae(const float *rewards, const float *values, c
     return launch_gae(false, false, p, ws, ws_bytes, cs(stream));
 }
 
+RLSCAN_API rlscan_status rlscan_gae_masked(const float *rewards, const float *values,
+                                           const float *terminateds, const float *truncateds,
+                                           const float *bootstrap_values, const float *last_value,
+                                           const float *mask, int64_t N, int64_t T, int64_t row_stride,
+                                           float gamma, float lambda, float *advantages, void *ws,
+                                           size_t ws_bytes, rlscan_stream_t stream)
+{
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!rewards || !values || !terminateds || !mask || !advantages) return RLSCAN_ERR_NULL;
+    if (bootstrap_values && last_value) return RLSCAN_ERR_ARG_CONFLICT;
+    if (last_value && truncateds) return RLSCAN_ERR_ARG_CONFLICT;
+    if (same_as_any(advantages, {rewards, values, terminateds, truncateds, bootstrap_values, last_value, mask}))
+        return RLSCAN_ERR_ARG_CONFLICT;
+    RLSCAN_TRY(run_checks(terminateds, truncateds, bootstrap_values, N, T, row_stride, cs(stream)));
+    Params p = base_params(N, T, row_stride);
+    p.c0 = gamma;
+    p.c1 = lambda;
+    p.out[0] = advantages;
+    p.in[0] = rewards;
+    p.in[1] = values;
+    p.in[2] = terminateds;
+    if (truncateds) {
+        p.in[3] = truncateds;
+        if (bootstrap_values) {
+            p.in[4] = bootstrap_values;
+            p.in[5] = mask;
+        } else {
+            p.in[4] = mask;
+        }
+        return launch_gae_masked(true, bootstrap_values != nullptr, p, ws, ws_bytes, cs(stream));
+    }
+    p.in[3] = mask;
+    if (last_value) {
+        p.rowscalar = last_value;
+    } else if (bootstrap_values) {
+        p.rowscalar = bootstrap_values + (T - 1);
+        p.rowscalar_stride = row_stride;
+    }
+    return launch_gae_masked(false, false, p, ws, ws_bytes, cs(stream));
+}
+
 RLSCAN_API rlscan_status rlscan_gae_returns(const float *rewards, const float *values,
                                             const float *terminateds, const float *truncateds,
                                             const float *bootstrap_values, const float *last_value,

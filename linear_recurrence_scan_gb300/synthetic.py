@@ -33,6 +33,14 @@ Sec. 7, and the caller-side conventions of the API reference):
                 uniform draw) as int64; action_probs_behavior = the behaviour
                 probability of that action; Q(s_t,a_t), Q(s_{t+1},a) for
                 every a, rewards ~ N(0,1); flags as for ``retrace``.
+* ``llm_tokens``  token-level rollouts of an LLM policy, one response per
+                row: a masked prompt of U[64, 512) tokens, a response whose
+                length is U[T/4, T - prompt] tokens in which tool-call
+                observations (masked) start with probability 1/256 per token
+                and last U[16, 128) tokens, then masked padding; values
+                ~ N(0,1) on response tokens (0 elsewhere); the outcome
+                reward ~ N(0,1) on the last response token, which is also
+                terminated; mask = 1 on the policy's response tokens.
 * ``long_rows`` episode starts F ~ Bernoulli(p_start); prefix-sum inputs are
                 integers uniform in [0, 9] stored as float32 with
                 dones = F ("starts_at"); eligibility-trace dones mark the step
@@ -50,6 +58,7 @@ _TENSOR_IDS = {
     "pi_log_ratio": 12, "episode_starts": 13, "inputs": 14, "gradients": 15,
     "alpha": 16, "beta": 17, "carry": 18, "seed_values": 19, "beta_zero": 20,
     "action_logits": 21, "next_q_all": 22, "actions": 23, "behavior_logit_noise": 24,
+    "prompt_len": 25, "response_len": 26, "obs_starts": 27, "obs_len": 28, "outcome": 29,
 }
 
 # The five workloads used by the tests and the benchmark.  Shapes and
@@ -193,6 +202,32 @@ def retrace_actions_batch(N, T, A=4, seed=0, config_id=3, p_term=0.001, p_trunc=
                 actions=actions,
                 rewards=normal(seed, config_id, "rewards", (N, T)),
                 terminateds=term, truncateds=trunc)
+
+
+def llm_tokens_batch(N, T, seed=0, config_id=6):
+    prompt = stream(seed, config_id, "prompt_len").integers(64, 512, N)
+    prompt = np.minimum(prompt, T // 2)
+    lo = np.maximum(1, T // 4)
+    resp = stream(seed, config_id, "response_len").integers(0, 1 << 30, N)
+    resp = lo + resp % np.maximum(1, T - prompt - lo + 1)
+    end = np.minimum(prompt + resp, T)                     # first padding token
+    t = np.arange(T)[None, :]
+    response = (t >= prompt[:, None]) & (t < end[:, None])
+    obs = np.zeros((N, T), dtype=bool)
+    starts = stream(seed, config_id, "obs_starts").random((N, T), dtype=np.float32) < 1.0 / 256
+    lens = stream(seed, config_id, "obs_len").integers(16, 128, (N, T))
+    rows, cols = np.nonzero(starts & response)
+    for r, c in zip(rows, cols):
+        obs[r, c:c + lens[r, c]] = True
+    mask = (response & ~obs).astype(np.float32)
+    values = np.where(response, normal(seed, config_id, "values", (N, T)), np.float32(0))
+    rewards = np.zeros((N, T), np.float32)
+    term = np.zeros((N, T), np.float32)
+    last = np.maximum(end - 1, 0)
+    outcome = normal(seed, config_id, "outcome", (N,))
+    rewards[np.arange(N), last] = outcome
+    term[np.arange(N), last] = 1.0
+    return dict(rewards=rewards, values=values.astype(np.float32), terminateds=term, mask=mask)
 
 
 def long_rows_batch(N, T, seed=0, config_id=4, p_start=1e-4):
