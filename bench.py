@@ -65,6 +65,18 @@ def _cfg_workloads():
             N=4096, T=8192, gen=lambda N, T: synthetic.llm_tokens_batch(N, T),
             # r, v, term, mask read once; advantages written
             estimators=[("gae_masked", 20, dict(gamma=1.0, lambda_=0.95))]),
+        "gae_compact_4096x1024": dict(
+            desc="GAE on compact storage: bfloat16 rewards and values, uint8 flags, float32 "
+                 "advantages (float32 arithmetic), last_value bootstrap",
+            N=4096, T=1024, gen=lambda N, T: synthetic.compact(synthetic.config_batch(1, N=N, T=T)),
+            # 2 + 2 + 1 bytes read, 4 written
+            estimators=[("gae_compact", 9, c1)]),
+        "gae_returns_compact_4096x1024": dict(
+            desc="GAE + discounted returns + TD(lambda) returns on compact storage: bfloat16 "
+                 "values in and out, uint8 flags (float32 arithmetic), last_value bootstrap",
+            N=4096, T=1024, gen=lambda N, T: synthetic.compact(synthetic.config_batch(1, N=N, T=T)),
+            # 2 + 2 + 1 bytes read, 3 x 2 written
+            estimators=[("gae_returns_compact", 11, c1)]),
         "gae_8x128": dict(
             desc="GAE with truncations and 2-D bootstrap", N=8, T=128,
             gen=lambda N, T: synthetic.config_batch(0, N=N, T=T),
@@ -122,7 +134,12 @@ IO = {
     "gae_returns": (["rewards", "values", "terminateds"], ["last_value"], 3),
     "gae_normalized": (["rewards", "values", "terminateds"], ["last_value"], 2),
     "gae_masked": (["rewards", "values", "terminateds", "mask"], [], 1),
+    "gae_compact": (["rewards", "values", "terminateds"], ["last_value"], 1),
+    "gae_returns_compact": (["rewards", "values", "terminateds"], ["last_value"], 3),
 }
+# output element bytes (default 4)
+OUT_BYTES = {"gae_returns_compact": 2}
+OUT_DTYPE = {"gae_returns_compact": "bf16"}
 # kernels one call launches (default 1)
 LAUNCHES = {"gae_normalized": 2}
 
@@ -277,6 +294,15 @@ def _launcher(name, c, bufs, outs, N, T, ws, wsn, stream):
     if name == "episodic_prefix_sum":
         return lambda: lib.rlscan_episodic_prefix_sum(b["inputs"], b["prefix_dones"], None, 1, N,
                                                       T, T, o[0], ws, wsn, stream)
+    if name == "gae_compact":
+        return lambda: lib.rlscan_gae_compact(b["rewards"], b["values"], b["terminateds"], None, None,
+                                              b["last_value"], N, T, T, g, float(c["lambda_"]), 0,
+                                              o[0], ws, wsn, stream)
+    if name == "gae_returns_compact":
+        return lambda: lib.rlscan_gae_returns_compact(b["rewards"], b["values"], b["terminateds"],
+                                                      None, None, b["last_value"], N, T, T, g,
+                                                      float(c["lambda_"]), 1, o[0], o[1], o[2], ws,
+                                                      wsn, stream)
     if name == "gae_masked":
         return lambda: lib.rlscan_gae_masked(b["rewards"], b["values"], b["terminateds"], None, None,
                                              None, b["mask"], N, T, T, g, float(c["lambda_"]), o[0],
@@ -292,6 +318,19 @@ def _launcher(name, c, bufs, outs, N, T, ws, wsn, stream):
                                               float(c["lambda_"]), o[0], o[1], o[2], ws, wsn,
                                               stream)
     raise KeyError(name)
+
+
+def _bf16(t):
+    """A device tensor of bfloat16 bits (uint16 storage) viewed as bfloat16."""
+    import torch
+    return t.view(torch.bfloat16) if t.dtype == torch.uint16 else t
+
+
+def _decode(a):
+    """Compact host arrays as float32: bfloat16 bits -> float, uint8 -> float."""
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32)
+    return a.astype(np.float32)
 
 
 def _public_call(name, c, t):
@@ -331,6 +370,14 @@ def _public_call(name, c, t):
     if name == "gae_masked":
         return [Lb.compute_gae(t["rewards"], t["values"], t["terminateds"], None, g, c["lambda_"],
                                mask=t["mask"])]
+    if name == "gae_compact":
+        return [Lb.compute_gae(_bf16(t["rewards"]), _bf16(t["values"]), t["terminateds"], None, g,
+                               c["lambda_"], None, t["last_value"])]
+    if name == "gae_returns_compact":
+        import torch
+        return list(Lb.compute_gae_and_returns(_bf16(t["rewards"]), _bf16(t["values"]),
+                                               t["terminateds"], None, g, c["lambda_"], None,
+                                               t["last_value"], out_dtype=torch.bfloat16))
     if name == "gae_normalized":
         return list(Lb.compute_gae_normalized(t["rewards"], t["values"], t["terminateds"], None, g,
                                               c["lambda_"], None, t["last_value"], 1e-8,
@@ -358,7 +405,7 @@ def run_ours(args, wl_name, rank, world, local_rank):
     need_in = sorted({k for (n, _, _) in all_kernels for k in IO[n][0] + IO[n][1]})
     host = {k: batch[k] for k in need_in}
     set_bytes = sum(v.nbytes for v in host.values()) + sum(
-        IO[n][2] * N * T * 4 for (n, _, _) in step_kernels)
+        IO[n][2] * N * T * OUT_BYTES.get(n, 4) for (n, _, _) in step_kernels)
     n_sets = 1 if set_bytes > 4 * L2_BYTES else min(16, max(2, math.ceil(4 * L2_BYTES / set_bytes)))
     stream = torch.cuda.current_stream(dev)
     sh = ctypes.c_void_p(stream.cuda_stream)
@@ -374,7 +421,8 @@ def run_ours(args, wl_name, rank, world, local_rank):
         bufs = {k: torch.from_numpy(v).to(dev) for k, v in host.items()}
         calls = {}
         for (name, bps, c) in all_kernels:
-            outs = [torch.empty((N, T), dtype=torch.float32, device=dev) for _ in range(IO[name][2])]
+            odt = torch.bfloat16 if OUT_DTYPE.get(name) == "bf16" else torch.float32
+            outs = [torch.empty((N, T), dtype=odt, device=dev) for _ in range(IO[name][2])]
             calls[name] = _launcher(name, c, bufs, outs, N, T, ws, wsn, sh)
         sets.append(calls)
     torch.cuda.synchronize()
@@ -439,10 +487,11 @@ def run_ours(args, wl_name, rank, world, local_rank):
     e2e_in = sorted({k for (n, _, _) in step_kernels for k in IO[n][0] + IO[n][1]})
     pinned = {k: torch.from_numpy(host[k]).pin_memory() for k in e2e_in}
     dbufs = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pinned.items()}
-    out_host = [torch.empty((N, T), dtype=torch.float32).pin_memory()
+    out_host = [torch.empty((N, T), dtype=torch.bfloat16 if OUT_DTYPE.get(n) == "bf16"
+                            else torch.float32).pin_memory()
                 for (n, _, _) in step_kernels for _ in range(IO[n][2])]
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-    d2h = sum(o.numel() * 4 for o in out_host)
+    d2h = sum(o.numel() * o.element_size() for o in out_host)
 
     def e2e_step():
         for k in pinned:
@@ -484,7 +533,8 @@ def run_ours(args, wl_name, rank, world, local_rank):
         "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
+        "dtype": "f32" if not any(n.endswith("_compact") for n in names) else
+                 "f32 arithmetic on bf16 values / u8 flags", "data": "synthetic",
         "config": {"workload": wl_name, "description": wl["desc"], "num_envs": N, "seq_len": T,
                    "estimators": names,
                    "step_kernels": [n for (n, _, _) in step_kernels],
@@ -539,6 +589,14 @@ def _oracle_call(name, c, b):
                                       b["q_values"], b["next_q_values_all"], b["actions"],
                                       b["rewards"], b["terminateds"], None, g, c["lambda_"],
                                       c["c_bar"], c["rho_bar"])
+    if name in ("gae_compact", "gae_returns_compact"):
+        dec = {k: _decode(b[k]) for k in ("rewards", "values", "terminateds")}
+        adv = oracle.gae(dec["rewards"], dec["values"], dec["terminateds"], None, g, c["lambda_"],
+                         None, b["last_value"])
+        if name == "gae_compact":
+            return adv
+        return adv, oracle.discounted_returns(dec["rewards"], dec["terminateds"], None, g, None,
+                                              b["last_value"])
     if name == "gae_masked":
         return oracle.gae_masked(b["rewards"], b["values"], b["terminateds"], b["mask"], None, g,
                                  c["lambda_"])

@@ -75,6 +75,12 @@ typedef enum rlscan_status {
     RLSCAN_ERR_SCRATCH_LIMIT = 9  /* shape needs more scratch than rlscan_gae_noalloc's built-in buffer */
 } rlscan_status;
 
+typedef enum rlscan_dtype {
+    RLSCAN_F32 = 0,   /* float32 */
+    RLSCAN_BF16 = 1,  /* bfloat16 */
+    RLSCAN_U8 = 2     /* uint8 */
+} rlscan_dtype;
+
 typedef enum rlscan_boundary {
     RLSCAN_ENDS_AT = 0,   /* done[t] = 1: the segment ends at t, reset lands at t+1 */
     RLSCAN_STARTS_AT = 1  /* done[t] = 1: the segment starts at t, reset lands at t  */
@@ -239,6 +245,44 @@ rlscan_status rlscan_gae_normalized(const float *rewards, const float *values,
                                     float *lambda_returns, float *discounted_returns,
                                     float *moments, void *ws, size_t ws_bytes,
                                     rlscan_stream_t stream);
+
+/*
+ * GAE and fused GAE + returns on compact storage: rewards, values and
+ * bootstrap_values in bfloat16, terminateds and truncateds in uint8 (0/1),
+ * outputs in float32 or bfloat16 (out_dtype).  rl-triton paper Sec. 9.3
+ * plans bfloat16 I/O and Sec. 9.2 defers it "pending a precision-tradeoff
+ * analysis"; here the arithmetic stays float32: a bfloat16 value is the
+ * float32 with the same upper 16 bits, so every stored input is read
+ * exactly and the recurrence is the float32 one of rlscan_gae /
+ * rlscan_gae_returns on those values.  The only additional error is the
+ * rounding of bfloat16 outputs (to nearest even, at most 2^-9 relative).
+ * Bytes per step fall from 16 to 9 (GAE, float32 out) or 7 (bf16 out).
+ * Inputs : rewards, values [N,T] bf16; terminateds [N,T] u8; truncateds
+ *          [N,T] u8 nullable; bootstrap_values [N,T] bf16 nullable, only
+ *          with truncateds (without truncateds the window bootstrap is
+ *          last_value, float32 [N], nullable); otherwise
+ *          RLSCAN_ERR_ARG_CONFLICT.
+ * Outputs: rlscan_gae_compact: advantages; rlscan_gae_returns_compact:
+ *          advantages, lambda_returns, discounted_returns (nullable, at
+ *          least one), each [N,T] of out_dtype (RLSCAN_F32 or RLSCAN_BF16,
+ *          else RLSCAN_ERR_ARG_VALUE).
+ * Bulk copies need rows in whole 16-byte units (T and row_stride multiples
+ * of 16 for the uint8 flags); other shapes use element-wise loads.  The
+ * content checks of RLSCAN_CHECKS do not cover these entry points.
+ */
+rlscan_status rlscan_gae_compact(const void *rewards, const void *values, const void *terminateds,
+                                 const void *truncateds, const void *bootstrap_values,
+                                 const float *last_value, int64_t N, int64_t T, int64_t row_stride,
+                                 float gamma, float lambda, rlscan_dtype out_dtype, void *advantages,
+                                 void *ws, size_t ws_bytes, rlscan_stream_t stream);
+
+rlscan_status rlscan_gae_returns_compact(const void *rewards, const void *values,
+                                         const void *terminateds, const void *truncateds,
+                                         const void *bootstrap_values, const float *last_value,
+                                         int64_t N, int64_t T, int64_t row_stride, float gamma,
+                                         float lambda, rlscan_dtype out_dtype, void *advantages,
+                                         void *lambda_returns, void *discounted_returns, void *ws,
+                                         size_t ws_bytes, rlscan_stream_t stream);
 
 /*
  * V-trace targets and advantages.

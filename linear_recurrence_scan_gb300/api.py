@@ -29,13 +29,13 @@ def _vp(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _check(name, t, shape, device=None):
+def _check(name, t, shape, device=None, dtypes=(torch.float32,)):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be on CUDA")
-    if t.dtype != torch.float32:
-        raise TypeError(f"{name}: expected float32, got {t.dtype}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: expected {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} shape {tuple(t.shape)} != {tuple(shape)}")
     if device is not None and t.device != device:
@@ -47,8 +47,8 @@ class _Call:
     stride (making copies contiguous only when the strides differ), and
     allocates outputs with that stride."""
 
-    def __init__(self, ref_name, ref):
-        _check(ref_name, ref, ref.shape)
+    def __init__(self, ref_name, ref, dtypes=(torch.float32,)):
+        _check(ref_name, ref, ref.shape, dtypes=dtypes)
         if ref.dim() != 2:
             raise ValueError(f"{ref_name} must be [num_envs, seq_len]")
         self.N, self.T = ref.shape
@@ -56,12 +56,12 @@ class _Call:
         self.mats = {ref_name: ref}
         self.vecs = {}
 
-    def mat(self, name, t, required=True):
+    def mat(self, name, t, required=True, dtypes=(torch.float32,)):
         if t is None:
             if required:
                 raise ValueError(f"{name} is required")
             return
-        _check(name, t, (self.N, self.T), self.device)
+        _check(name, t, (self.N, self.T), self.device, dtypes)
         self.mats[name] = t
 
     def vec(self, name, t):
@@ -70,7 +70,7 @@ class _Call:
         _check(name, t, (self.N,), self.device)
         self.vecs[name] = t.contiguous()
 
-    def finish(self, n_out):
+    def finish(self, n_out, dtype=torch.float32):
         def unit_inner(t):
             return self.T <= 1 or t.stride(1) == 1
         strides = {t.stride(0) if self.N > 1 else max(self.T, 1) for t in self.mats.values()}
@@ -81,10 +81,10 @@ class _Call:
             rs = self.T
         self.rs = max(rs, self.T)
         if self.rs == self.T:
-            outs = [torch.empty((self.N, self.T), dtype=torch.float32, device=self.device)
+            outs = [torch.empty((self.N, self.T), dtype=dtype, device=self.device)
                     for _ in range(n_out)]
         else:
-            outs = [torch.empty_strided((self.N, self.T), (self.rs, 1), dtype=torch.float32,
+            outs = [torch.empty_strided((self.N, self.T), (self.rs, 1), dtype=dtype,
                                         device=self.device) for _ in range(n_out)]
         self.outs = outs
         return outs
@@ -144,12 +144,54 @@ def workspace_status(device=None):
 # ---------------------------------------------------------------------------
 # estimators (rl-triton API reference signatures)
 
+_BF16 = (torch.bfloat16,)
+_FLAG8 = (torch.uint8, torch.bool)
+_OUT_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+
+def _compact_call(rewards, values, terminateds, truncateds, bootstrap_values, last_value, n_out,
+                  out_dtype):
+    """Arguments of the compact-storage entry points: bf16 values, uint8 /
+    bool flags, float32 last_value; outputs of ``out_dtype``."""
+    if out_dtype not in _OUT_DTYPES:
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
+    c = _Call("rewards", rewards, _BF16)
+    c.mat("values", values, dtypes=_BF16)
+    c.mat("terminateds", terminateds, dtypes=_FLAG8)
+    c.mat("truncateds", truncateds, False, _FLAG8)
+    c.mat("bootstrap_values", bootstrap_values, False, _BF16)
+    c.vec("last_value", last_value)
+    if last_value is not None and bootstrap_values is not None:
+        raise ValueError("pass either last_value or bootstrap_values, not both")
+    if last_value is not None and truncateds is not None:
+        raise ValueError("last_value cannot be combined with truncateds; use bootstrap_values")
+    if bootstrap_values is not None and truncateds is None:
+        raise ValueError("compact storage: the window bootstrap is last_value (float32 [N])")
+    outs = c.finish(n_out, out_dtype)
+    return c, outs
+
+
 def compute_gae(rewards, values, terminateds, truncateds=None, gamma=0.99, lambda_=0.95,
-                bootstrap_values=None, last_value=None, mask=None):
+                bootstrap_values=None, last_value=None, mask=None, out_dtype=None):
     """GAE advantages [num_envs, seq_len] (rl-triton API reference, compute_gae).
     ``mask`` (an addition, float 0/1 [num_envs, seq_len]) selects
     observation-skip masking: masked steps carry the next step's advantage
-    unchanged (beta = 1), unmasked steps are plain GAE steps."""
+    unchanged (beta = 1), unmasked steps are plain GAE steps.
+    bfloat16 rewards select compact storage: values and bootstrap_values
+    bfloat16, flags uint8 or bool, last_value float32; ``out_dtype``
+    (float32 by default, or bfloat16) sets the output type."""
+    if isinstance(rewards, torch.Tensor) and rewards.dtype == torch.bfloat16:
+        if mask is not None:
+            raise ValueError("mask is not available with compact storage")
+        c, (out,) = _compact_call(rewards, values, terminateds, truncateds, bootstrap_values,
+                                  last_value, 1, out_dtype or torch.float32)
+        ws, wsn, s = _ws_for(c)
+        _native.check(_native.lib().rlscan_gae_compact(
+            c.m("rewards"), c.m("values"), c.m("terminateds"), c.m("truncateds"),
+            c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma),
+            float(lambda_), _OUT_DTYPES[out_dtype or torch.float32], _vp(out), ws, wsn, s),
+            "rlscan_gae_compact")
+        return out
     c = _Call("rewards", rewards)
     c.mat("values", values)
     c.mat("terminateds", terminateds)
@@ -178,13 +220,27 @@ def compute_gae(rewards, values, terminateds, truncateds=None, gamma=0.99, lambd
 
 def compute_gae_and_returns(rewards, values, terminateds, truncateds=None, gamma=0.99,
                             lambda_=0.95, bootstrap_values=None, last_value=None,
-                            outputs=("advantages", "lambda_returns", "discounted_returns")):
+                            outputs=("advantages", "lambda_returns", "discounted_returns"),
+                            out_dtype=None):
     """GAE advantages, lambda-returns (= advantages + values) and discounted
     returns from one pass over the inputs (one fused kernel).  ``outputs``
-    selects which are produced; returns them as a tuple in that order."""
+    selects which are produced; returns them as a tuple in that order.
+    bfloat16 rewards select compact storage (see compute_gae)."""
     known = ("advantages", "lambda_returns", "discounted_returns")
     if not outputs or any(o not in known for o in outputs):
         raise ValueError(f"outputs must be a non-empty subset of {known}")
+    if isinstance(rewards, torch.Tensor) and rewards.dtype == torch.bfloat16:
+        c, outs = _compact_call(rewards, values, terminateds, truncateds, bootstrap_values,
+                                last_value, len(outputs), out_dtype or torch.float32)
+        by_name = dict(zip(outputs, outs))
+        ws, wsn, s = _ws_for(c)
+        _native.check(_native.lib().rlscan_gae_returns_compact(
+            c.m("rewards"), c.m("values"), c.m("terminateds"), c.m("truncateds"),
+            c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma),
+            float(lambda_), _OUT_DTYPES[out_dtype or torch.float32],
+            _vp(by_name.get("advantages")), _vp(by_name.get("lambda_returns")),
+            _vp(by_name.get("discounted_returns")), ws, wsn, s), "rlscan_gae_returns_compact")
+        return tuple(outs)
     c = _Call("rewards", rewards)
     c.mat("values", values)
     c.mat("terminateds", terminateds)

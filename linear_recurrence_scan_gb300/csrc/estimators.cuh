@@ -53,6 +53,7 @@ template <bool TRUNC, bool BS2D>
 struct GAE {
     static_assert(TRUNC || !BS2D, "2-D bootstrap is read only with truncation flags");
     static constexpr int NIN = 3 + TRUNC + BS2D, NOUT = 1;
+    static constexpr unsigned FLAGS = (1u << 2) | (TRUNC ? (1u << 3) : 0u);  // 0/1 inputs
     static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = false, ROWSCALAR = !BS2D;
     static constexpr unsigned HALO = 1u << 1;
@@ -577,6 +578,7 @@ template <bool TRUNC, bool BS2D>
 struct GAEReturns {
     static_assert(TRUNC || !BS2D, "2-D bootstrap is read only with truncation flags");
     static constexpr int NIN = 3 + TRUNC + BS2D, NOUT = 3;
+    static constexpr unsigned FLAGS = (1u << 2) | (TRUNC ? (1u << 3) : 0u);  // 0/1 inputs
     static constexpr int K = 2;
     static constexpr bool FWD = false, ROWSCALAR = !BS2D;
     static constexpr unsigned HALO = 1u << 1;
@@ -639,6 +641,18 @@ struct GAEReturns {
 template <bool TRUNC, bool BS2D>
 struct GAEReturnsMoments : GAEReturns<TRUNC, BS2D> {
     static constexpr bool MOMENTS = true;
+};
+
+// Compact storage of an estimator's inputs and outputs: value inputs in
+// VB-byte elements (2: bfloat16), flag inputs (Base::FLAGS) in FB-byte
+// elements (1: uint8 0/1), outputs in OB-byte elements (4: float,
+// 2: bfloat16 rounded to nearest even).  The arithmetic is the base
+// estimator's, in float: a bf16 value is the float with the same upper 16
+// bits, so every stored input is read exactly.
+template <class Base, int VB, int FB, int OB>
+struct Compact : Base {
+    static constexpr int OUT_BYTES = OB;
+    __host__ __device__ static constexpr int in_bytes(int j) { return ((Base::FLAGS >> j) & 1u) ? FB : VB; }
 };
 
 }  // namespace est

@@ -57,13 +57,22 @@ namespace rlscan {
 template <class E>
 struct Shape {
     static constexpr bool WIDE = WideOf<E>::NWIDE > 0;
-    static constexpr int BYTES_PER_STEP = 4 * (E::NIN + E::NOUT);
+    static constexpr int in_sum()
+    {
+        int n = 0;
+        for (int j = 0; j < E::NIN; ++j) n += IoOf<E>::in(j);
+        return n;
+    }
+    static constexpr int BYTES_PER_STEP = in_sum() + IoOf<E>::OUT * E::NOUT;
     static constexpr int TILE_RAW = RLSCAN_TILE_BYTES_TARGET / BYTES_PER_STEP;
-    static constexpr int TILE = WIDE ? 1024 : (TILE_RAW >= 3072 ? 4096 : (TILE_RAW >= 1536 ? 2048 : 1024));
+    // compact storage moves few bytes per step: cap at 2048 (8 steps per
+    // thread) so the register budget of three CTAs per SM holds
+    static constexpr int TILE_BY_BYTES = TILE_RAW >= 3072 ? 4096 : (TILE_RAW >= 1536 ? 2048 : 1024);
+    static constexpr int TILE = WIDE ? 1024 : ((IoOf<E>::LOWP && TILE_BY_BYTES > 2048) ? 2048 : TILE_BY_BYTES);
     static constexpr int THREADS = WIDE ? RLSCAN_WIDE_THREADS
                                         : (TILE >= 4096 ? 256 : (TILE >= 2048 ? RLSCAN_THREADS_2048 : 128));
     static constexpr int ITEMS = TILE / THREADS;
-    static constexpr int STAGE_BYTES = E::NIN * (TILE + 8) * 4;  // narrow arrays
+    static constexpr int STAGE_BYTES = narrow_bytes<E, TILE>();  // narrow arrays
     static constexpr int RAW = (RLSCAN_SMEM_BUDGET_KB * 1024) / STAGE_BYTES;
     // ring of an immediate-finish launch, and of a deferred one
     static constexpr int SHORT_STAGES = WIDE ? RLSCAN_WIDE_STAGES
@@ -182,9 +191,16 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
         p.epoch = next_epoch();
     }
 
-    bool tma = (p.T % 4 == 0) && (p.rs % 4 == 0);
-    for (int j = 0; j < E::NIN; ++j) tma = tma && aligned16(p.in[j]);
-    for (int q = 0; q < E::NOUT; ++q) tma = tma && (p.out[q] == nullptr || aligned16(p.out[q]));
+    // bulk copies and vector stores: whole 16-byte units in every row
+    bool tma = true;
+    for (int j = 0; j < E::NIN; ++j) {
+        const int units = 16 / IoOf<E>::in(j);
+        tma = tma && (p.T % units == 0) && (p.rs % units == 0) && aligned16(p.in[j]);
+    }
+    for (int q = 0; q < E::NOUT; ++q) {
+        const int units = 16 / IoOf<E>::OUT;
+        tma = tma && (p.T % units == 0) && (p.rs % units == 0) && (p.out[q] == nullptr || aligned16(p.out[q]));
+    }
     p.tma = tma ? 1 : 0;
     p.spin_limit_ns = spin_limit_ns();
     p.copy_limit_ns = 2000000000ull;  // bulk copies land in microseconds; never cut short

@@ -79,6 +79,10 @@ rlscan_status launch_gae_moments(bool trunc, bool bs2d, Params p, void *ws, size
 rlscan_status launch_normalize(float *x, int64_t N, int64_t T, int64_t rs, const float *parts, int64_t nparts,
                                float eps, float *moments_out, cudaStream_t s);
 rlscan_status launch_gae_masked(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
+rlscan_status launch_gae_compact(bool trunc, bool bs2d, bool bf16_out, Params p, void *ws, size_t ws_bytes,
+                                 cudaStream_t s);
+rlscan_status launch_gae_returns_compact(bool trunc, bool bs2d, bool bf16_out, Params p, void *ws, size_t ws_bytes,
+                                         cudaStream_t s);
 rlscan_status launch_vtrace(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_retrace(bool trunc, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_retrace_actions(bool trunc, Params p, void *ws, size_t ws_bytes, cudaStream_t s);

@@ -440,6 +440,83 @@ RLSCAN_API rlscan_status rlscan_gae_normalized(const float *rewards, const float
     return launch_normalize(advantages, N, T, row_stride, p.mom_part, grid, eps, moments, cs(stream));
 }
 
+namespace {
+// Shared checks and parameter block of the compact-storage GAE entry points.
+rlscan_status compact_params(const void *rewards, const void *values, const void *terminateds,
+                             const void *truncateds, const void *bootstrap_values, const float *last_value,
+                             int64_t N, int64_t T, int64_t row_stride, float gamma, float lambda,
+                             rlscan_dtype out_dtype, std::initializer_list<const void *> outs, Params &p)
+{
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (out_dtype != RLSCAN_F32 && out_dtype != RLSCAN_BF16) return RLSCAN_ERR_ARG_VALUE;
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!rewards || !values || !terminateds) return RLSCAN_ERR_NULL;
+    if (bootstrap_values && last_value) return RLSCAN_ERR_ARG_CONFLICT;
+    if (last_value && truncateds) return RLSCAN_ERR_ARG_CONFLICT;
+    if (bootstrap_values && !truncateds) return RLSCAN_ERR_ARG_CONFLICT;  // window bootstrap: last_value
+    const void *o_prev = nullptr;
+    for (const void *o : outs) {
+        if (o == nullptr) continue;
+        if (same_as_any(o, {rewards, values, terminateds, truncateds, bootstrap_values, last_value}) || o == o_prev)
+            return RLSCAN_ERR_ARG_CONFLICT;
+        o_prev = o;
+    }
+    p = base_params(N, T, row_stride);
+    p.c0 = gamma;
+    p.c1 = lambda;
+    p.in[0] = static_cast<const float *>(rewards);
+    p.in[1] = static_cast<const float *>(values);
+    p.in[2] = static_cast<const float *>(terminateds);
+    if (truncateds) {
+        p.in[3] = static_cast<const float *>(truncateds);
+        p.in[4] = static_cast<const float *>(bootstrap_values);
+    } else {
+        p.rowscalar = last_value;
+    }
+    return RLSCAN_OK;
+}
+}  // namespace
+
+RLSCAN_API rlscan_status rlscan_gae_compact(const void *rewards, const void *values, const void *terminateds,
+                                            const void *truncateds, const void *bootstrap_values,
+                                            const float *last_value, int64_t N, int64_t T, int64_t row_stride,
+                                            float gamma, float lambda, rlscan_dtype out_dtype, void *advantages,
+                                            void *ws, size_t ws_bytes, rlscan_stream_t stream)
+{
+    if (N > 0 && T > 0 && advantages == nullptr) return RLSCAN_ERR_NULL;
+    Params p;
+    RLSCAN_TRY(compact_params(rewards, values, terminateds, truncateds, bootstrap_values, last_value, N, T,
+                              row_stride, gamma, lambda, out_dtype, {advantages}, p));
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    p.out[0] = static_cast<float *>(advantages);
+    return launch_gae_compact(truncateds != nullptr, bootstrap_values != nullptr, out_dtype == RLSCAN_BF16, p,
+                              ws, ws_bytes, cs(stream));
+}
+
+RLSCAN_API rlscan_status rlscan_gae_returns_compact(const void *rewards, const void *values,
+                                                    const void *terminateds, const void *truncateds,
+                                                    const void *bootstrap_values, const float *last_value,
+                                                    int64_t N, int64_t T, int64_t row_stride, float gamma,
+                                                    float lambda, rlscan_dtype out_dtype, void *advantages,
+                                                    void *lambda_returns, void *discounted_returns, void *ws,
+                                                    size_t ws_bytes, rlscan_stream_t stream)
+{
+    if (N > 0 && T > 0 && !advantages && !lambda_returns && !discounted_returns) return RLSCAN_ERR_NULL;
+    if ((advantages && (advantages == lambda_returns || advantages == discounted_returns)) ||
+        (lambda_returns && lambda_returns == discounted_returns))
+        return RLSCAN_ERR_ARG_CONFLICT;
+    Params p;
+    RLSCAN_TRY(compact_params(rewards, values, terminateds, truncateds, bootstrap_values, last_value, N, T,
+                              row_stride, gamma, lambda, out_dtype, {advantages, lambda_returns, discounted_returns},
+                              p));
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    p.out[0] = static_cast<float *>(advantages);
+    p.out[1] = static_cast<float *>(lambda_returns);
+    p.out[2] = static_cast<float *>(discounted_returns);
+    return launch_gae_returns_compact(truncateds != nullptr, bootstrap_values != nullptr, out_dtype == RLSCAN_BF16,
+                                      p, ws, ws_bytes, cs(stream));
+}
+
 RLSCAN_API rlscan_status rlscan_vtrace(const float *log_pi_target, const float *log_pi_behavior,
                             const float *values, const float *rewards, const float *terminateds,
                             const float *truncateds, const float *bootstrap_values,

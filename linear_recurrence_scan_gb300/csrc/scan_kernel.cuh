@@ -55,6 +55,8 @@
 #include <cstdint>
 #include <type_traits>
 
+#include <cuda_bf16.h>
+
 #include "dfloat.cuh"
 #include "estimators.cuh"
 #include "params.cuh"
@@ -79,6 +81,21 @@ template <class E>
 struct WideOf<E, std::void_t<decltype(E::NWIDE)>> {
     static constexpr int NWIDE = E::NWIDE;
     static constexpr unsigned DERIVED = E::DERIVED;
+};
+
+// Element sizes of an estimator's narrow inputs and outputs: 4-byte floats
+// unless it declares in_bytes(j) / OUT_BYTES (bf16 values, uint8 flags).
+template <class E, class = void>
+struct IoOf {
+    static constexpr bool LOWP = false;
+    __host__ __device__ static constexpr int in(int) { return 4; }
+    static constexpr int OUT = 4;
+};
+template <class E>
+struct IoOf<E, std::void_t<decltype(E::OUT_BYTES)>> {
+    static constexpr bool LOWP = true;
+    __host__ __device__ static constexpr int in(int j) { return E::in_bytes(j); }
+    static constexpr int OUT = E::OUT_BYTES;
 };
 
 // Estimators whose kernel accumulates the batch moments of output 0.
@@ -110,6 +127,56 @@ __host__ __device__ constexpr int slot_of(int j)
     int below = 0;
     for (int i = 0; i < j; ++i) below += (((D >> i) & 1u) != 0) == derived ? 1 : 0;
     return derived ? narrow_copied<E>() + below : below;
+}
+
+// Shared-memory region of narrow input j in a stage: 16 bytes for the step
+// before the tile, the tile's steps, 16 bytes for the step after it.
+// Regions follow one another in slot order; 4-byte inputs give the float
+// layout (TILE + 8) floats per array, data from float 4.
+template <class E, int TILE>
+__host__ __device__ constexpr int region_bytes(int j) { return TILE * IoOf<E>::in(j) + 32; }
+template <class E, int TILE>
+__host__ __device__ constexpr int region_off(int j)
+{
+    int off = 0;
+    for (int i = 0; i < E::NIN; ++i)
+        if (slot_of<E>(i) < slot_of<E>(j)) off += region_bytes<E, TILE>(i);
+    return off;
+}
+template <class E, int TILE>
+__host__ __device__ constexpr int narrow_bytes()
+{
+    int n = 0;
+    for (int i = 0; i < E::NIN; ++i) n += region_bytes<E, TILE>(i);
+    return n;
+}
+// step 0 of the tile in array j's region
+template <class E, int TILE>
+__device__ __forceinline__ char *elem0(float *stage, int j)
+{
+    return reinterpret_cast<char *>(stage) + region_off<E, TILE>(j) + 16;
+}
+template <class E, int TILE>
+__device__ __forceinline__ const char *elem0(const float *stage, int j)
+{
+    return reinterpret_cast<const char *>(stage) + region_off<E, TILE>(j) + 16;
+}
+
+// one stored element of `bytes` bytes as a float: bf16 (the upper half of a
+// float), uint8 (an integer 0..255) or float
+template <int BYTES>
+__device__ __forceinline__ float to_float(const char *ptr)
+{
+    if constexpr (BYTES == 4) return *reinterpret_cast<const float *>(ptr);
+    else if constexpr (BYTES == 2) return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short *>(ptr)) << 16);
+    else return static_cast<float>(*reinterpret_cast<const unsigned char *>(ptr));
+}
+template <int BYTES>
+__device__ __forceinline__ void copy_elem(char *dst, const char *src)
+{
+    if constexpr (BYTES == 4) *reinterpret_cast<float *>(dst) = __ldg(reinterpret_cast<const float *>(src));
+    else if constexpr (BYTES == 2) *reinterpret_cast<unsigned short *>(dst) = __ldg(reinterpret_cast<const unsigned short *>(src));
+    else *reinterpret_cast<unsigned char *>(dst) = __ldg(reinterpret_cast<const unsigned char *>(src));
 }
 
 // outer o inner: x -> outer.a + outer.b * (inner.a + inner.b * x)
@@ -166,8 +233,9 @@ __device__ __forceinline__ TileGeo decode_tile(const Params &p, int64_t g)
 }
 
 // Issue the bulk copies of one tile into `stage` (called by one thread).
-// Array j of the stage occupies AST floats; its data start at offset 4, the
-// step before the tile at offset 3 and the step after it at offset 4+TILE.
+// Narrow array j occupies region_bytes(j): its data start 16 bytes in, with
+// the 16 bytes before the tile in front and the 16 bytes after it behind
+// (the neighbour step of a HALO input: copies are whole 16-byte units).
 // Wide array w (when staged) follows the narrow arrays and occupies
 // (TILE + 4) * words floats: step e of the tile at e * words, the step after
 // the tile right behind the last one.
@@ -188,16 +256,21 @@ __device__ void issue_tile_copies(const Params &p, const TileGeo &tg, float *sta
         uint32_t bytes = 0;
 #pragma unroll
         for (int j = 0; j < E::NIN; ++j)
-            if (!((DER >> j) & 1u)) bytes += nb;
+            if (!((DER >> j) & 1u)) bytes += static_cast<uint32_t>(steps * IoOf<E>::in(j));
 #pragma unroll
         for (int w = 0; w < NW; ++w)
             if (wide) bytes += nb * static_cast<uint32_t>(p.wide_words[w]);
         ptx::mbar_arrive_expect_tx(bar, bytes * static_cast<uint32_t>(copies));
         for (int i = 0; i < copies; ++i) {
 #pragma unroll
-            for (int j = 0; j < E::NIN; ++j)
-                if (!((DER >> j) & 1u))
-                    ptx::bulk_g2s(stage + slot_of<E>(j) * AST + 4 + i * p.C, p.in[j] + (tg.row0 + i) * p.rs, nb, bar);
+            for (int j = 0; j < E::NIN; ++j) {
+                if (!((DER >> j) & 1u)) {
+                    const int eb = IoOf<E>::in(j);
+                    ptx::bulk_g2s(elem0<E, TILE>(stage, j) + static_cast<int64_t>(i) * p.C * eb,
+                                  reinterpret_cast<const char *>(p.in[j]) + (tg.row0 + i) * p.rs * eb,
+                                  static_cast<uint32_t>(steps * eb), bar);
+                }
+            }
             if (wide) {
                 float *dst = wsm;
 #pragma unroll
@@ -217,13 +290,14 @@ __device__ void issue_tile_copies(const Params &p, const TileGeo &tg, float *sta
     uint32_t bytes = 0;
 #pragma unroll
     for (int j = 0; j < E::NIN; ++j) {
+        const int halo = 16 / IoOf<E>::in(j);  // steps in 16 bytes
         lo[j] = tg.t0;
         hi[j] = tg.t0 + tg.len;
         if ((E::HALO >> j) & 1u) {
-            if (!E::FWD && hi[j] < p.T) hi[j] += 4;   // next step (T % 4 == 0 keeps it in the row)
-            if (E::FWD && lo[j] > 0) lo[j] -= 4;      // previous step
+            if (!E::FWD && hi[j] < p.T) hi[j] += halo;   // next step (T a multiple of halo keeps it in the row)
+            if (E::FWD && lo[j] > 0) lo[j] -= halo;      // previous step
         }
-        if (!((DER >> j) & 1u)) bytes += static_cast<uint32_t>((hi[j] - lo[j]) * 4);
+        if (!((DER >> j) & 1u)) bytes += static_cast<uint32_t>((hi[j] - lo[j]) * IoOf<E>::in(j));
     }
     // wide arrays: the tile and, backward, the four steps after it
     const int64_t whi = (!E::FWD && tg.t0 + tg.len < p.T) ? tg.t0 + tg.len + 4 : tg.t0 + tg.len;
@@ -233,10 +307,14 @@ __device__ void issue_tile_copies(const Params &p, const TileGeo &tg, float *sta
     }
     ptx::mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
-    for (int j = 0; j < E::NIN; ++j)
-        if (!((DER >> j) & 1u))
-            ptx::bulk_g2s(stage + slot_of<E>(j) * AST + 4 + (lo[j] - tg.t0), p.in[j] + base + lo[j],
-                          static_cast<uint32_t>((hi[j] - lo[j]) * 4), bar);
+    for (int j = 0; j < E::NIN; ++j) {
+        if (!((DER >> j) & 1u)) {
+            const int eb = IoOf<E>::in(j);
+            ptx::bulk_g2s(elem0<E, TILE>(stage, j) + (lo[j] - tg.t0) * eb,
+                          reinterpret_cast<const char *>(p.in[j]) + (base + lo[j]) * eb,
+                          static_cast<uint32_t>((hi[j] - lo[j]) * eb), bar);
+        }
+    }
     if (wide) {
         float *dst = wsm;
 #pragma unroll
@@ -247,6 +325,19 @@ __device__ void issue_tile_copies(const Params &p, const TileGeo &tg, float *sta
             dst += (TILE + 4) * W;
         }
     }
+}
+
+// Element e of array j's tile region (e = -1: the step before the tile,
+// e = TILE: the step after it) from global element `src`.
+template <class E, int TILE>
+__device__ __forceinline__ void load_elem(const Params &p, float *stage, int j, int e, int64_t src)
+{
+    const int eb = IoOf<E>::in(j);
+    char *dst = elem0<E, TILE>(stage, j) + static_cast<int64_t>(e) * eb;
+    const char *from = reinterpret_cast<const char *>(p.in[j]) + src * eb;
+    if (eb == 4) copy_elem<4>(dst, from);
+    else if (eb == 2) copy_elem<2>(dst, from);
+    else copy_elem<1>(dst, from);
 }
 
 // Element-wise cooperative load of one tile (any alignment), same layout.
@@ -262,15 +353,17 @@ __device__ void load_tile_elementwise(const Params &p, const TileGeo &tg, float 
             const int64_t src = (tg.row0 + i) * p.rs + tg.t0 + c;
 #pragma unroll
             for (int j = 0; j < E::NIN; ++j)
-                if (!((DER >> j) & 1u)) stage[slot_of<E>(j) * AST + 4 + e] = __ldg(p.in[j] + src);
+                if (!((DER >> j) & 1u)) load_elem<E, TILE>(p, stage, j, e, src);
         }
     }
-    if (!p.packed && threadIdx.x < E::NIN) {
-        const int j = threadIdx.x;
-        if (((E::HALO & ~DER) >> j) & 1u) {
-            const int64_t base = tg.row0 * p.rs;
-            if (!E::FWD && tg.t0 + tg.len < p.T) stage[slot_of<E>(j) * AST + 4 + TILE] = __ldg(p.in[j] + base + tg.t0 + tg.len);
-            if (E::FWD && tg.t0 > 0) stage[slot_of<E>(j) * AST + 3] = __ldg(p.in[j] + base + tg.t0 - 1);
+    if (!p.packed) {
+        const int64_t base = tg.row0 * p.rs;
+#pragma unroll
+        for (int j = 0; j < E::NIN; ++j) {
+            if (threadIdx.x == j && (((E::HALO & ~DER) >> j) & 1u)) {
+                if (!E::FWD && tg.t0 + tg.len < p.T) load_elem<E, TILE>(p, stage, j, TILE, base + tg.t0 + tg.len);
+                if (E::FWD && tg.t0 > 0) load_elem<E, TILE>(p, stage, j, -1, base + tg.t0 - 1);
+            }
         }
     }
 }
@@ -465,7 +558,8 @@ scan_kernel(const __grid_constant__ Params p)
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const bool tma = p.tma != 0;
-    const int SST = NWIDE > 0 ? p.stage_floats : NIN * AST;  // floats per ring stage
+    static_assert(!(IoOf<E>::LOWP && NWIDE > 0), "wide inputs are float only");
+    const int SST = NWIDE > 0 ? p.stage_floats : narrow_bytes<E, TILE>() / 4;  // floats per ring stage
     constexpr int NST = STAGES;                                // ring stages
     static_assert(!DEFER || STAGES >= 3, "a deferred tile holds its stage: the ring needs three");
 
@@ -549,19 +643,38 @@ scan_kernel(const __grid_constant__ Params p)
 
     // inputs of this thread's ITEMS steps, plus the neighbour step
     auto load_inputs = [&](const float *stage, float (&x)[NIN][ITEMS], float (&xn)[NIN]) {
-        const float *src = stage + 4 + li;
 #pragma unroll
         for (int j = 0; j < NIN; ++j) {
-            const float *aj = src + slot_of<E>(j) * AST;
+            const int eb = IoOf<E>::in(j);
+            const char *aj = elem0<E, TILE>(stage, j) + li * eb;
 #pragma unroll
             for (int k = 0; k < ITEMS; k += 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(aj + k);
-                x[j][k] = v.x;
-                x[j][k + 1] = v.y;
-                x[j][k + 2] = v.z;
-                x[j][k + 3] = v.w;
+                if (eb == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(aj + 4 * k);
+                    x[j][k] = v.x;
+                    x[j][k + 1] = v.y;
+                    x[j][k + 2] = v.z;
+                    x[j][k + 3] = v.w;
+                } else if (eb == 2) {  // four bf16: a float's upper 16 bits each
+                    const uint2 v = *reinterpret_cast<const uint2 *>(aj + 2 * k);
+                    x[j][k] = __uint_as_float(v.x << 16);
+                    x[j][k + 1] = __uint_as_float(v.x & 0xffff0000u);
+                    x[j][k + 2] = __uint_as_float(v.y << 16);
+                    x[j][k + 3] = __uint_as_float(v.y & 0xffff0000u);
+                } else {               // four uint8
+                    const uint32_t v = *reinterpret_cast<const uint32_t *>(aj + k);
+                    x[j][k] = static_cast<float>(v & 0xffu);
+                    x[j][k + 1] = static_cast<float>((v >> 8) & 0xffu);
+                    x[j][k + 2] = static_cast<float>((v >> 16) & 0xffu);
+                    x[j][k + 3] = static_cast<float>(v >> 24);
+                }
             }
-            xn[j] = ((E::HALO >> j) & 1u) ? (FWD ? aj[-1] : aj[ITEMS]) : 0.f;
+            float nb = 0.f;
+            if ((E::HALO >> j) & 1u) {
+                const char *q = FWD ? aj - eb : aj + ITEMS * eb;
+                nb = eb == 4 ? to_float<4>(q) : (eb == 2 ? to_float<2>(q) : to_float<1>(q));
+            }
+            xn[j] = nb;
         }
     };
 
@@ -640,7 +753,26 @@ scan_kernel(const __grid_constant__ Params p)
 #pragma unroll
             for (int q = 0; q < NOUT; ++q) {
                 if (NOUT > 1 && p.out[q] == nullptr) continue;  // optional output
-                if (tma) {
+                if constexpr (IoOf<E>::OUT == 2) {  // bf16, rounded to nearest even
+                    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out[q]) + off;
+                    if (tma) {
+#pragma unroll
+                        for (int k = 0; k < ITEMS; k += 4) {
+                            if (k < sp.kv) {
+                                const __nv_bfloat162 lo2 = __floats2bfloat162_rn(o[q][k], o[q][k + 1]);
+                                const __nv_bfloat162 hi2 = __floats2bfloat162_rn(o[q][k + 2], o[q][k + 3]);
+                                uint2 w;
+                                w.x = *reinterpret_cast<const uint32_t *>(&lo2);
+                                w.y = *reinterpret_cast<const uint32_t *>(&hi2);
+                                *reinterpret_cast<uint2 *>(dst + k) = w;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < ITEMS; ++k)
+                            if (k < sp.kv) dst[k] = __float2bfloat16_rn(o[q][k]);
+                    }
+                } else if (tma) {
 #pragma unroll
                     for (int k = 0; k < ITEMS; k += 4) {
                         if (k < sp.kv)

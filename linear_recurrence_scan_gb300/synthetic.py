@@ -230,6 +230,25 @@ def llm_tokens_batch(N, T, seed=0, config_id=6):
     return dict(rewards=rewards, values=values.astype(np.float32), terminateds=term, mask=mask)
 
 
+def compact(batch, values=("rewards", "values", "bootstrap_values"),
+            flags=("terminateds", "truncateds")):
+    """The same batch in compact storage: the named value arrays as the raw
+    bits of bfloat16 (uint16, rounded to nearest even by torch), the flags
+    as uint8; other arrays unchanged."""
+    import torch
+    out = {}
+    for k, v in batch.items():
+        if v is None:
+            out[k] = None
+        elif k in values:
+            out[k] = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        elif k in flags:
+            out[k] = v.astype(np.uint8)
+        else:
+            out[k] = v
+    return out
+
+
 def long_rows_batch(N, T, seed=0, config_id=4, p_start=1e-4):
     starts = bernoulli(seed, config_id, "episode_starts", (N, T), p_start)
     ends = np.zeros_like(starts)
