@@ -140,6 +140,10 @@ IO = {
 # output element bytes (default 4)
 OUT_BYTES = {"gae_returns_compact": 2}
 OUT_DTYPE = {"gae_returns_compact": "bf16"}
+# streams the end-to-end steps rotate over (copies of one step overlap
+# another's compute)
+E2E_STREAMS = 3
+
 # kernels one call launches (default 1)
 LAUNCHES = {"gae_normalized": 2}
 
@@ -483,30 +487,37 @@ def run_ours(args, wl_name, rank, world, local_rank):
         per_est_times = launch_durations(wl["estimators"], K)
 
     # e2e through the public API: pinned host inputs -> device, the step's
-    # call(s), results back to pinned host memory, every step
+    # call(s), results back to pinned host memory, every step.  Consecutive
+    # steps go to E2E_STREAMS streams in turn (each with its own device and
+    # host buffers), so one step's upload, another's compute and a third's
+    # download overlap, as a pipeline of rollout batches would run.
     e2e_in = sorted({k for (n, _, _) in step_kernels for k in IO[n][0] + IO[n][1]})
     pinned = {k: torch.from_numpy(host[k]).pin_memory() for k in e2e_in}
-    dbufs = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pinned.items()}
-    out_host = [torch.empty((N, T), dtype=torch.bfloat16 if OUT_DTYPE.get(n) == "bf16"
-                            else torch.float32).pin_memory()
-                for (n, _, _) in step_kernels for _ in range(IO[n][2])]
+    e2e_streams = [torch.cuda.Stream(dev) for _ in range(E2E_STREAMS)]
+    dsets = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pinned.items()}
+             for _ in range(E2E_STREAMS)]
+    hsets = [[torch.empty((N, T), dtype=torch.bfloat16 if OUT_DTYPE.get(n) == "bf16"
+                          else torch.float32).pin_memory()
+              for (n, _, _) in step_kernels for _ in range(IO[n][2])] for _ in range(E2E_STREAMS)]
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-    d2h = sum(o.numel() * o.element_size() for o in out_host)
+    d2h = sum(o.numel() * o.element_size() for o in hsets[0])
 
-    def e2e_step():
-        for k in pinned:
-            dbufs[k].copy_(pinned[k], non_blocking=True)
-        outs = []
-        for (name, _, c) in step_kernels:
-            outs += _public_call(name, c, dbufs)
-        for o, hbuf in zip(outs, out_host):
-            hbuf.copy_(o, non_blocking=True)
-    for _ in range(max(1, min(args.warmup, 3))):
-        e2e_step()
+    def e2e_step(i):
+        j = i % E2E_STREAMS
+        with torch.cuda.stream(e2e_streams[j]):
+            for k in pinned:
+                dsets[j][k].copy_(pinned[k], non_blocking=True)
+            outs = []
+            for (name, _, c) in step_kernels:
+                outs += _public_call(name, c, dsets[j])
+            for o, hbuf in zip(outs, hsets[j]):
+                hbuf.copy_(o, non_blocking=True)
+    for i in range(max(E2E_STREAMS, min(args.warmup, 3))):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0 = time.perf_counter()
-    for _ in range(K):
-        e2e_step()
+    for i in range(K):
+        e2e_step(i)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - e0) / K)
     clocks = sampler.stop()
@@ -549,7 +560,8 @@ def run_ours(args, wl_name, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": d["bytes_per_env_step"] * steps_per_call},
         "e2e": {"value": world * steps_per_call / e2e_s, "unit": "env-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "path": "pinned host -> device copies, public compute_* API, results -> pinned host"},
+                "path": "pinned host -> device copies, public compute_* API, results -> pinned host; "
+                        f"steps round-robin over {E2E_STREAMS} streams"},
         "gpu_launches": K * sum(LAUNCHES.get(n, 1) for (n, _, _) in step_kernels),
         "timing": "CUDA events around K back-to-back steps (no events between launches); "
                   "per-kernel durations from K back-to-back launches of that kernel alone",
