@@ -140,8 +140,8 @@ IO = {
 # output element bytes (default 4)
 OUT_BYTES = {"gae_returns_compact": 2}
 OUT_DTYPE = {"gae_returns_compact": "bf16"}
-# streams the end-to-end steps rotate over (copies of one step overlap
-# another's compute)
+# streams the end-to-end steps rotate over by default (copies of one step
+# overlap another's compute)
 E2E_STREAMS = 3
 
 # kernels one call launches (default 1)
@@ -493,18 +493,28 @@ def run_ours(args, wl_name, rank, world, local_rank):
     # download overlap, as a pipeline of rollout batches would run.
     e2e_in = sorted({k for (n, _, _) in step_kernels for k in IO[n][0] + IO[n][1]})
     pinned = {k: torch.from_numpy(host[k]).pin_memory() for k in e2e_in}
-    e2e_streams = [torch.cuda.Stream(dev) for _ in range(E2E_STREAMS)]
+    NS = max(1, args.e2e_streams)
+    e2e_streams = [torch.cuda.Stream(dev) for _ in range(NS)]
     dsets = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pinned.items()}
-             for _ in range(E2E_STREAMS)]
+             for _ in range(NS)]
     hsets = [[torch.empty((N, T), dtype=torch.bfloat16 if OUT_DTYPE.get(n) == "bf16"
                           else torch.float32).pin_memory()
-              for (n, _, _) in step_kernels for _ in range(IO[n][2])] for _ in range(E2E_STREAMS)]
+              for (n, _, _) in step_kernels for _ in range(IO[n][2])] for _ in range(NS)]
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = sum(o.numel() * o.element_size() for o in hsets[0])
 
+    zero_copy = args.e2e_mode == "zerocopy"
+
     def e2e_step(i):
-        j = i % E2E_STREAMS
+        j = i % NS
         with torch.cuda.stream(e2e_streams[j]):
+            if zero_copy:
+                # the public API on the pinned host tensors themselves: the
+                # kernel reads the inputs and writes the (pinned) outputs over
+                # the host link
+                for (name, _, c) in step_kernels:
+                    hsets[j] = _public_call(name, c, pinned)
+                return
             for k in pinned:
                 dsets[j][k].copy_(pinned[k], non_blocking=True)
             outs = []
@@ -512,7 +522,7 @@ def run_ours(args, wl_name, rank, world, local_rank):
                 outs += _public_call(name, c, dsets[j])
             for o, hbuf in zip(outs, hsets[j]):
                 hbuf.copy_(o, non_blocking=True)
-    for i in range(max(E2E_STREAMS, min(args.warmup, 3))):
+    for i in range(max(NS, min(args.warmup, 3))):
         e2e_step(i)
     torch.cuda.synchronize()
     e0 = time.perf_counter()
@@ -560,8 +570,11 @@ def run_ours(args, wl_name, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": d["bytes_per_env_step"] * steps_per_call},
         "e2e": {"value": world * steps_per_call / e2e_s, "unit": "env-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "path": "pinned host -> device copies, public compute_* API, results -> pinned host; "
-                        f"steps round-robin over {E2E_STREAMS} streams"},
+                "path": ("public compute_* API on pinned host tensors: the kernel reads the inputs "
+                         "and writes the pinned outputs over the host link (zero copy)"
+                         if zero_copy else
+                         "pinned host -> device copies, public compute_* API, results -> pinned host")
+                        + f"; steps round-robin over {NS} streams"},
         "gpu_launches": K * sum(LAUNCHES.get(n, 1) for (n, _, _) in step_kernels),
         "timing": "CUDA events around K back-to-back steps (no events between launches); "
                   "per-kernel durations from K back-to-back launches of that kernel alone",
@@ -737,6 +750,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gae_returns_4096x1024", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=E2E_STREAMS,
+                    help="streams the end-to-end steps rotate over")
+    ap.add_argument("--e2e-mode", choices=["zerocopy", "copies"], default="copies",
+                    help="end-to-end leg: kernels on the pinned host buffers, or explicit copies")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

@@ -17,8 +17,12 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - Pointers are DEVICE pointers owned by the caller.  The library never
- *    allocates, frees or retains them.
+ *  - Pointers are owned by the caller: device memory, or page-locked host
+ *    memory (cudaHostAlloc / cudaHostRegister), which the kernel reads and
+ *    writes in place over the host link with plain loads and stores (zero
+ *    copy; bulk asynchronous copies are used for device memory only).  The
+ *    workspace must be device memory.  The library never allocates, frees
+ *    or retains them.
  *  - [N,T] arrays are float32, row-major, element stride 1, row stride
  *    `row_stride` elements (row_stride >= T), the same stride for every
  *    [N,T] argument of a call, inputs and outputs alike.  [N] arrays are

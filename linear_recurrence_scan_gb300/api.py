@@ -1,8 +1,11 @@
 """PyTorch-facing functions with the rl-triton API reference's names and
-defaults.  Each one checks its arguments (CUDA residency, float32, shapes --
-the pages' always-on structural checks), allocates the outputs with torch,
-and makes exactly one librlscan call on the current CUDA stream.  There is no
-CPU path: a missing library or a non-CUDA tensor raises.
+defaults.  Each one checks its arguments (residency, dtypes, shapes -- the
+pages' always-on structural checks), allocates the outputs with torch, and
+makes exactly one librlscan call on the current CUDA stream.  Tensors live
+on the GPU, or in page-locked host memory, which the kernel reads and writes
+in place over the host link (outputs are then page-locked host tensors,
+ready once the stream has synchronised).  There is no CPU path: a missing
+library or an ordinary CPU tensor raises.
 """
 from __future__ import annotations
 
@@ -30,15 +33,17 @@ def _vp(t):
 
 
 def _check(name, t, shape, device=None, dtypes=(torch.float32,)):
+    """CUDA tensors on `device`, or page-locked host tensors (the kernel then
+    reads / writes them in place over the host link)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be on CUDA")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be on CUDA or in page-locked (pinned) host memory")
     if t.dtype not in dtypes:
         raise TypeError(f"{name}: expected {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} shape {tuple(t.shape)} != {tuple(shape)}")
-    if device is not None and t.device != device:
+    if device is not None and t.is_cuda and t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
@@ -52,7 +57,11 @@ class _Call:
         if ref.dim() != 2:
             raise ValueError(f"{ref_name} must be [num_envs, seq_len]")
         self.N, self.T = ref.shape
-        self.device = ref.device
+        # pinned host inputs: outputs in pinned host memory too, the work on
+        # the current CUDA device
+        self.host = not ref.is_cuda
+        self.device = (torch.device("cuda", torch.cuda.current_device()) if self.host
+                       else ref.device)
         self.mats = {ref_name: ref}
         self.vecs = {}
 
@@ -80,12 +89,12 @@ class _Call:
             self.mats = {k: t.contiguous() for k, t in self.mats.items()}
             rs = self.T
         self.rs = max(rs, self.T)
+        where = dict(device="cpu", pin_memory=True) if self.host else dict(device=self.device)
         if self.rs == self.T:
-            outs = [torch.empty((self.N, self.T), dtype=dtype, device=self.device)
-                    for _ in range(n_out)]
+            outs = [torch.empty((self.N, self.T), dtype=dtype, **where) for _ in range(n_out)]
         else:
-            outs = [torch.empty_strided((self.N, self.T), (self.rs, 1), dtype=dtype,
-                                        device=self.device) for _ in range(n_out)]
+            outs = [torch.empty_strided((self.N, self.T), (self.rs, 1), dtype=dtype, **where)
+                    for _ in range(n_out)]
         self.outs = outs
         return outs
 
@@ -339,8 +348,8 @@ def compute_retrace(action_probs_target, action_probs_behavior, q_values, next_q
     c.mat("truncateds", truncateds, False)
     if not isinstance(actions, torch.Tensor) or actions.dtype != torch.int64:
         raise TypeError("actions must be an int64 torch.Tensor")
-    if not actions.is_cuda or actions.device != c.device:
-        raise ValueError(f"actions must be on {c.device}")
+    if not (actions.is_pinned() or (actions.is_cuda and actions.device == c.device)):
+        raise ValueError(f"actions must be on {c.device} or in pinned host memory")
     if tuple(actions.shape) != (c.N, c.T):
         raise ValueError(f"actions shape {tuple(actions.shape)} != {(c.N, c.T)}")
     wide = []
@@ -359,7 +368,7 @@ def compute_retrace(action_probs_target, action_probs_behavior, q_values, next_q
     acts = actions
     if c.N > 1 and acts.stride(0) != c.rs or (c.T > 1 and acts.stride(1) != 1):
         acts = torch.empty_strided((c.N, c.T), (c.rs, 1), dtype=torch.int64, device=c.device)
-        acts.copy_(actions)
+        acts.copy_(actions, non_blocking=True)
 
     def inner_ok(t):
         return (A <= 1 or t.stride(2) == 1) and (c.T <= 1 or t.stride(1) == A)

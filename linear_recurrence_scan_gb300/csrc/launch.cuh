@@ -92,6 +92,20 @@ constexpr int kMaxDevices = 64;
 
 inline bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+// Page-locked host memory (cudaHostAlloc / cudaHostRegister): the kernel
+// reads and writes it in place over the host link (zero copy) with plain
+// loads and stores; bulk asynchronous copies are used for device memory only.
+inline bool host_memory(const void *ptr)
+{
+    if (ptr == nullptr) return false;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
 // Per-device launch facts of one kernel: SM count, the dynamic shared
 // memory a CTA may opt into (the device limit less the kernel's static
 // shared memory), and resident CTAs for the last dynamic size used.
@@ -201,6 +215,11 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
         const int units = 16 / IoOf<E>::OUT;
         tma = tma && (p.T % units == 0) && (p.rs % units == 0) && (p.out[q] == nullptr || aligned16(p.out[q]));
     }
+    p.vec = tma ? 1 : 0;
+    bool on_host = false;
+    for (int j = 0; j < E::NIN; ++j) on_host = on_host || host_memory(p.in[j]);
+    for (int w = 0; w < WideOf<E>::NWIDE; ++w) on_host = on_host || host_memory(p.wide[w]);
+    tma = tma && !on_host;
     p.tma = tma ? 1 : 0;
     p.spin_limit_ns = spin_limit_ns();
     p.copy_limit_ns = 2000000000ull;  // bulk copies land in microseconds; never cut short

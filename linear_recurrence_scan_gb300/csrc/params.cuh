@@ -50,6 +50,7 @@ struct Params {
     int32_t R;                 // rows per tile (packed) or 1
     int32_t packed;            // 1: tiles hold whole rows; 0: rows split into tiles
     int32_t tma;               // 1: bulk asynchronous copies; 0: element-wise loads
+    int32_t vec;               // 1: rows in whole 16-byte units: vector stores
     int32_t dynamic;           // 1: tile ids from the workspace ticket (look-back)
     uint32_t epoch;            // tag of this call's tile states (30 bits)
     unsigned long long *states;

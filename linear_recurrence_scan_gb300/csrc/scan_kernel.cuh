@@ -558,6 +558,7 @@ scan_kernel(const __grid_constant__ Params p)
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const bool tma = p.tma != 0;
+    const bool vec = p.vec != 0;
     static_assert(!(IoOf<E>::LOWP && NWIDE > 0), "wide inputs are float only");
     const int SST = NWIDE > 0 ? p.stage_floats : narrow_bytes<E, TILE>() / 4;  // floats per ring stage
     constexpr int NST = STAGES;                                // ring stages
@@ -755,7 +756,7 @@ scan_kernel(const __grid_constant__ Params p)
                 if (NOUT > 1 && p.out[q] == nullptr) continue;  // optional output
                 if constexpr (IoOf<E>::OUT == 2) {  // bf16, rounded to nearest even
                     __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out[q]) + off;
-                    if (tma) {
+                    if (vec) {
 #pragma unroll
                         for (int k = 0; k < ITEMS; k += 4) {
                             if (k < sp.kv) {
@@ -772,7 +773,7 @@ scan_kernel(const __grid_constant__ Params p)
                         for (int k = 0; k < ITEMS; ++k)
                             if (k < sp.kv) dst[k] = __float2bfloat16_rn(o[q][k]);
                     }
-                } else if (tma) {
+                } else if (vec) {
 #pragma unroll
                     for (int k = 0; k < ITEMS; k += 4) {
                         if (k < sp.kv)
