@@ -45,8 +45,9 @@
  *  - Workspace: rows longer than one kernel tile are scanned by several
  *    thread blocks that pass carries through a caller-provided workspace
  *    (decoupled look-back).  rlscan_workspace_bytes(N, T) gives the size
- *    that suffices for every entry point at that shape (0 when none needs
- *    one, in which case `ws` may be NULL).  A workspace must be zeroed once
+ *    that suffices for every entry point at that shape except the
+ *    normalising one (rlscan_gae_normalized_workspace_bytes); it is 0 for
+ *    T <= 512, where none needs one and `ws` may be NULL.  A workspace must be zeroed once
  *    with rlscan_workspace_init() before its first use; afterwards it needs
  *    no clearing between calls.  One workspace serves one call at a time:
  *    calls that use the same workspace must be ordered (same stream, or
@@ -101,9 +102,10 @@ int rlscan_version(void);
 /* Static description of a status code.  Never NULL. */
 const char *rlscan_status_string(rlscan_status status);
 
-/* Bytes of workspace that suffice for every entry point on an [N, T] buffer.
- * 0 when no entry point needs one at this shape.  Returns 0 for N <= 0 or
- * T <= 0. */
+/* Bytes of workspace that suffice for every entry point on an [N, T] buffer
+ * (except rlscan_gae_normalized, which has its own query): a 64-byte header
+ * and 32 bytes per 1024 steps of every row.  0 for T <= 512, where no entry
+ * point needs one, and for N <= 0 or T <= 0. */
 size_t rlscan_workspace_bytes(int64_t N, int64_t T);
 
 /* Zero a workspace of `ws_bytes` bytes (asynchronously on `stream`).  Call

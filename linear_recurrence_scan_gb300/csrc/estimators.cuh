@@ -279,6 +279,9 @@ struct Retrace {
 template <bool TRUNC>
 struct RetraceActions : Retrace<TRUNC> {
     static constexpr int NWIDE = 3;
+    // with truncation flags a 1024-step stage leaves room for one CTA per SM:
+    // 512-step tiles keep three
+    static constexpr int WIDE_TILE = TRUNC ? 512 : 1024;
     static constexpr unsigned DERIVED = (1u << 0) | (1u << 3);
     static constexpr int PI = 0, EQ = 3;
 

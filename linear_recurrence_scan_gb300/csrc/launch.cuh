@@ -54,6 +54,17 @@ namespace rlscan {
 #define RLSCAN_DEFER_MODE -1
 #endif
 
+// Tile of a wide-input estimator: 1024 steps unless it declares WIDE_TILE
+// (a smaller tile keeps two or three CTAs per SM when its stage is large).
+template <class E, class = void>
+struct WideTileOf {
+    static constexpr int value = 1024;
+};
+template <class E>
+struct WideTileOf<E, std::void_t<decltype(E::WIDE_TILE)>> {
+    static constexpr int value = E::WIDE_TILE;
+};
+
 template <class E>
 struct Shape {
     static constexpr bool WIDE = WideOf<E>::NWIDE > 0;
@@ -68,8 +79,9 @@ struct Shape {
     // compact storage moves few bytes per step: cap at 2048 (8 steps per
     // thread) so the register budget of three CTAs per SM holds
     static constexpr int TILE_BY_BYTES = TILE_RAW >= 3072 ? 4096 : (TILE_RAW >= 1536 ? 2048 : 1024);
-    static constexpr int TILE = WIDE ? 1024 : ((IoOf<E>::LOWP && TILE_BY_BYTES > 2048) ? 2048 : TILE_BY_BYTES);
-    static constexpr int THREADS = WIDE ? RLSCAN_WIDE_THREADS
+    static constexpr int TILE = WIDE ? WideTileOf<E>::value
+                                     : ((IoOf<E>::LOWP && TILE_BY_BYTES > 2048) ? 2048 : TILE_BY_BYTES);
+    static constexpr int THREADS = WIDE ? (TILE < 1024 ? 128 : RLSCAN_WIDE_THREADS)
                                         : (TILE >= 4096 ? 256 : (TILE >= 2048 ? RLSCAN_THREADS_2048 : 128));
     static constexpr int ITEMS = TILE / THREADS;
     static constexpr int STAGE_BYTES = narrow_bytes<E, TILE>();  // narrow arrays

@@ -31,9 +31,12 @@ enum HeaderWord : int { kHdrExit = 2, kHdrError = 3, kHdrDetail = 4 };
 constexpr int kMaxMomentCtas = 4096;
 constexpr size_t kMomentBytes = 16 * static_cast<size_t>(kMaxMomentCtas);
 
-// Smallest tile (elements per row segment) any kernel uses; the workspace
-// size query is computed with it, so it covers every entry point.
+// The workspace size query counts 1024-step tiles and kMaxScans scans per
+// tile: kernels with 1024-step or longer tiles fit it with up to kMaxScans
+// scans, 512-step tiles with one scan.  Rows of up to 512 steps never need
+// a workspace.
 constexpr int kMinTile = 1024;
+constexpr int kSmallestTile = 512;
 
 struct Params {
     const float *in[kMaxIn];   // [N, rs] inputs, order defined by the estimator

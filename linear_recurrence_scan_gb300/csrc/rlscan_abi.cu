@@ -217,7 +217,7 @@ RLSCAN_API const char *rlscan_status_string(rlscan_status status)
 
 RLSCAN_API size_t rlscan_workspace_bytes(int64_t N, int64_t T)
 {
-    if (N <= 0 || T <= 0 || T <= kMinTile) return 0;
+    if (N <= 0 || T <= 0 || T <= kSmallestTile) return 0;
     const int64_t tiles = N * ((T + kMinTile - 1) / kMinTile);
     return kHeaderBytes + kStateBytes * kMaxScans * static_cast<size_t>(tiles);
 }

@@ -543,7 +543,8 @@ scan_kernel(const __grid_constant__ Params p)
     constexpr int COMPUTE_BAR = 1;                  // named barrier of the compute warps
     static_assert(STAGES >= 2, "the ring needs two stages");
     static_assert(ITEMS % 4 == 0, "items per thread are moved as float4");
-    static_assert(TILE >= kMinTile, "workspace sizing assumes tiles of at least kMinTile");
+    static_assert(TILE >= kSmallestTile && K * (TILE >= kMinTile ? 1 : kMinTile / TILE) <= kMaxScans,
+                  "the workspace holds kMaxScans states per 1024 steps");
     constexpr int NWIDE = WideOf<E>::NWIDE;
     static_assert(NWIDE == 0 || !FWD, "wide inputs are staged for backward recurrences only");
 

@@ -49,7 +49,8 @@ def test_version_and_status_strings(lib):
 def test_workspace_bytes(lib):
     assert lib.rlscan_workspace_bytes(0, 100) == 0
     assert lib.rlscan_workspace_bytes(10, 0) == 0
-    assert lib.rlscan_workspace_bytes(4096, 1024) == 0            # one tile per row
+    assert lib.rlscan_workspace_bytes(4096, 512) == 0             # one tile per row for every kernel
+    assert lib.rlscan_workspace_bytes(4096, 1024) == 64 + 16 * 2 * 4096
     # header + 16 bytes per (1024-step tile, scan), two scans at most
     assert lib.rlscan_workspace_bytes(2, 1025) == 64 + 16 * 2 * 2 * 2
     assert lib.rlscan_workspace_bytes(64, 1 << 20) == 64 + 16 * 2 * 64 * 1024
