@@ -20,7 +20,9 @@ _API = {
 def __getattr__(name):
     if name in _API:
         from . import api
-        return getattr(api, name)
+        value = getattr(api, name)
+        globals()[name] = value  # later lookups skip this hook
+        return value
     raise AttributeError(name)
 
 

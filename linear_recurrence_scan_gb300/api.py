@@ -29,7 +29,8 @@ __all__ = [
 # marshalling helpers
 
 def _vp(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Address of a tensor's data for a ctypes void* argument (None: NULL)."""
+    return None if t is None else t.data_ptr()
 
 
 def _check(name, t, shape, device=None, dtypes=(torch.float32,)):
@@ -37,14 +38,25 @@ def _check(name, t, shape, device=None, dtypes=(torch.float32,)):
     reads / writes them in place over the host link)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not (t.is_cuda or t.is_pinned()):
+    cuda = t.is_cuda
+    if not (cuda or t.is_pinned()):
         raise ValueError(f"{name} must be on CUDA or in page-locked (pinned) host memory")
     if t.dtype not in dtypes:
         raise TypeError(f"{name}: expected {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
-    if tuple(t.shape) != tuple(shape):
+    if t.shape != shape:
         raise ValueError(f"{name} shape {tuple(t.shape)} != {tuple(shape)}")
-    if device is not None and t.is_cuda and t.device != device:
+    if device is not None and cuda and t.get_device() != device.index:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(device):
+    """The current CUDA stream of `device` as an integer handle."""
+    if _raw_stream is not None:
+        return _raw_stream(device.index)
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 class _Call:
@@ -53,15 +65,16 @@ class _Call:
     allocates outputs with that stride."""
 
     def __init__(self, ref_name, ref, dtypes=(torch.float32,)):
+        if not isinstance(ref, torch.Tensor) or ref.dim() != 2:
+            raise ValueError(f"{ref_name} must be a [num_envs, seq_len] tensor")
         _check(ref_name, ref, ref.shape, dtypes=dtypes)
-        if ref.dim() != 2:
-            raise ValueError(f"{ref_name} must be [num_envs, seq_len]")
         self.N, self.T = ref.shape
         # pinned host inputs: outputs in pinned host memory too, the work on
         # the current CUDA device
         self.host = not ref.is_cuda
         self.device = (torch.device("cuda", torch.cuda.current_device()) if self.host
                        else ref.device)
+        self.shape = ref.shape
         self.mats = {ref_name: ref}
         self.vecs = {}
 
@@ -70,7 +83,7 @@ class _Call:
             if required:
                 raise ValueError(f"{name} is required")
             return
-        _check(name, t, (self.N, self.T), self.device, dtypes)
+        _check(name, t, self.shape, self.device, dtypes)
         self.mats[name] = t
 
     def vec(self, name, t):
@@ -80,15 +93,17 @@ class _Call:
         self.vecs[name] = t.contiguous()
 
     def finish(self, n_out, dtype=torch.float32):
-        def unit_inner(t):
-            return self.T <= 1 or t.stride(1) == 1
-        strides = {t.stride(0) if self.N > 1 else max(self.T, 1) for t in self.mats.values()}
-        ok = all(unit_inner(t) for t in self.mats.values()) and len(strides) == 1
-        rs = strides.pop() if ok else self.T
-        if not ok or rs < self.T:
-            self.mats = {k: t.contiguous() for k, t in self.mats.items()}
-            rs = self.T
-        self.rs = max(rs, self.T)
+        mats = self.mats.values()
+        if all(t.is_contiguous() for t in mats):
+            self.rs = self.T
+        else:
+            strides = {t.stride(0) if self.N > 1 else max(self.T, 1) for t in mats}
+            ok = all(self.T <= 1 or t.stride(1) == 1 for t in mats) and len(strides) == 1
+            rs = strides.pop() if ok else self.T
+            if not ok or rs < self.T:
+                self.mats = {k: t.contiguous() for k, t in self.mats.items()}
+                rs = self.T
+            self.rs = max(rs, self.T)
         where = dict(device="cpu", pin_memory=True) if self.host else dict(device=self.device)
         if self.rs == self.T:
             outs = [torch.empty((self.N, self.T), dtype=dtype, **where) for _ in range(n_out)]
@@ -105,11 +120,12 @@ class _Call:
         return _vp(self.vecs.get(name))
 
     def stream(self):
-        return ctypes.c_void_p(torch.cuda.current_stream(self.device).cuda_stream)
+        return _stream_handle(self.device)
 
 
 _ws_lock = threading.Lock()
 _ws_cache = {}
+_ws_bytes_cache = {}
 
 
 def _workspace(device, stream_handle, nbytes):
@@ -117,23 +133,35 @@ def _workspace(device, stream_handle, nbytes):
     Calls on one stream are ordered, so they may share a workspace."""
     if nbytes == 0:
         return None, 0
-    key = (device.index, stream_handle.value)
-    with _ws_lock:
-        ws = _ws_cache.get(key)
-        if ws is None or ws.numel() < nbytes:
-            size = max(nbytes, 0 if ws is None else 2 * ws.numel())
-            size = (size + 255) // 256 * 256
-            ws = torch.empty(size, dtype=torch.uint8, device=device)
-            _native.check(_native.lib().rlscan_workspace_init(_vp(ws), size, stream_handle),
-                          "rlscan_workspace_init")
-            _ws_cache[key] = ws
-        return _vp(ws), ws.numel()
+    key = (device.index, stream_handle)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        with _ws_lock:
+            ws = _ws_cache.get(key)
+            if ws is None or ws.numel() < nbytes:
+                size = max(nbytes, 0 if ws is None else 2 * ws.numel())
+                size = (size + 255) // 256 * 256
+                ws = torch.empty(size, dtype=torch.uint8, device=device)
+                _native.check(_native.lib().rlscan_workspace_init(_vp(ws), size, stream_handle),
+                              "rlscan_workspace_init")
+                _ws_cache[key] = ws
+    return ws.data_ptr(), ws.numel()
+
+
+def _workspace_bytes(N, T):
+    key = (N, T)
+    n = _ws_bytes_cache.get(key)
+    if n is None:
+        n = _native.lib().rlscan_workspace_bytes(N, T)
+        if len(_ws_bytes_cache) > 4096:
+            _ws_bytes_cache.clear()
+        _ws_bytes_cache[key] = n
+    return n
 
 
 def _ws_for(c):
     s = c.stream()
-    need = _native.lib().rlscan_workspace_bytes(c.N, c.T)
-    p, n = _workspace(c.device, s, need)
+    p, n = _workspace(c.device, s, _workspace_bytes(c.N, c.T))
     return p, n, s
 
 
@@ -141,8 +169,8 @@ def workspace_status(device=None):
     """Synchronise the current stream and raise if a kernel recorded an
     error (a cross-block wait that timed out) in its workspace."""
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
-    s = ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
-    ws = _ws_cache.get((device.index, s.value))
+    s = _stream_handle(device)
+    ws = _ws_cache.get((device.index, s))
     if ws is None:
         torch.cuda.current_stream(device).synchronize()
         return

@@ -202,7 +202,6 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
         p.dynamic = 0;
         p.hdr = nullptr;
         p.states = nullptr;
-        p.epoch = 0;
     } else {
         p.packed = 0;
         p.C = TILE;
@@ -214,7 +213,6 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
         p.dynamic = 1;
         p.hdr = static_cast<uint32_t *>(ws);
         p.states = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
-        p.epoch = next_epoch();
     }
 
     // bulk copies and vector stores: whole 16-byte units in every row

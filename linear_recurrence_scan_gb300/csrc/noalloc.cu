@@ -79,8 +79,10 @@ extern "C" RLSCAN_API rlscan_status rlscan_gae_noalloc(
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
         const rlscan_status st = scratch_for_current_device(s, &ws);
         if (st != RLSCAN_OK) return st;
-        // ticket, exit count and error word start at zero for every call
-        if (cudaMemsetAsync(ws, 0, rlscan::kHeaderBytes, s) != cudaSuccess) return RLSCAN_ERR_CUDA;
+        // ticket, exit count and error words start at zero for every call;
+        // the epoch word (kHdrEpoch) is kept, so earlier calls' tile states
+        // stay stale
+        if (cudaMemsetAsync(ws, 0, rlscan::kHdrEpoch * sizeof(uint32_t), s) != cudaSuccess) return RLSCAN_ERR_CUDA;
         ws_bytes = kScratchBytes;
     }
     return rlscan_gae(rewards, values, terminateds, truncateds, bootstrap_values, last_value, N, T,

@@ -23,7 +23,8 @@ constexpr int kMaxWide = 3;  // staged arrays with several 4-byte words per step
 constexpr size_t kHeaderBytes = 64;
 constexpr size_t kStateBytes = 16;
 constexpr int kMaxScans = 2;
-enum HeaderWord : int { kHdrExit = 2, kHdrError = 3, kHdrDetail = 4 };
+//   bytes 20..23  u32 epoch: tag of the current call's tile states (advanced by the last CTA)
+enum HeaderWord : int { kHdrExit = 2, kHdrError = 3, kHdrDetail = 4, kHdrEpoch = 5 };
 
 // Batch moments of the advantages (normalising entry point): after the
 // header and tile states, at a 256-byte boundary, one 16-byte slot per CTA
@@ -55,7 +56,6 @@ struct Params {
     int32_t tma;               // 1: bulk asynchronous copies; 0: element-wise loads
     int32_t vec;               // 1: rows in whole 16-byte units: vector stores
     int32_t dynamic;           // 1: tile ids from the workspace ticket (look-back)
-    uint32_t epoch;            // tag of this call's tile states (30 bits)
     unsigned long long *states;
     uint32_t *hdr;
     uint64_t spin_limit_ns;    // bound on every look-back wait
@@ -97,7 +97,6 @@ rlscan_status launch_prefix(bool starts_at, Params p, void *ws, size_t ws_bytes,
 rlscan_status launch_linear(bool forward, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 
 // Host helpers shared by the launchers (rlscan_abi.cu).
-uint32_t next_epoch();
 uint64_t spin_limit_ns();
 int64_t withhold_tile();  // RLSCAN_TEST_WITHHOLD_TILE, -1 when unset
 bool pdl_enabled();  // programmatic dependent launch (RLSCAN_PDL=0 disables)

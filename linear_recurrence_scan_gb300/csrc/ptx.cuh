@@ -103,6 +103,13 @@ __device__ __forceinline__ void st_relaxed(unsigned long long *p, unsigned long 
 // was launched with programmatic serialization) be scheduled now, and wait
 // until the previous kernel has completed and its writes are visible.
 // Both are no-ops for kernels launched without the attribute.
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t *ptr)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void pdl_trigger_dependents()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

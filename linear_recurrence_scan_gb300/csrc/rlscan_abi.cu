@@ -4,7 +4,6 @@
 // which optional arguments are present (the pages' HAS_TRUNCATIONS /
 // HAS_BOOTSTRAP / HAS_SEED / BOUNDARY_ENDS_AT specialisations, paper
 // Sec. 4.2), and the workspace helpers.
-#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <initializer_list>
@@ -14,16 +13,6 @@
 #include "params.cuh"
 
 namespace rlscan {
-
-uint32_t next_epoch()
-{
-    static std::atomic<uint32_t> counter{0};
-    uint32_t e;
-    do {
-        e = (counter.fetch_add(1, std::memory_order_relaxed) + 1) & 0x3FFFFFFFu;
-    } while (e == 0);
-    return e;
-}
 
 uint64_t spin_limit_ns()
 {

@@ -380,28 +380,32 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, uint6
 
 // Decoupled look-back.  Tile g holds one 16-byte state per scan it solves
 // (K of them, slot g * K + scan): two 64-bit words, each a 32-bit tag
-// (call epoch << 2 | kind) beside a float payload.
+// (call epoch << 2 | kind) beside a float payload.  The epoch is a counter
+// in the workspace header: every CTA reads it at start, the last CTA out
+// advances it, so the next call on the workspace (a stream-ordered launch,
+// or a replay of a captured graph) sees the states of this one as stale.
 //
 // Publishing side (one thread per tile and scan): the tile's aggregate map
 // `total`, or directly its inclusive value when that does not depend on
 // anything before the tile (first tile of the row, or b == 0).
-__device__ __forceinline__ void publish_first(const Params &p, int64_t slot, int64_t g, int64_t j,
-                                              Pair total)
+__device__ __forceinline__ void publish_first(const Params &p, uint32_t epoch, int64_t slot, int64_t g,
+                                              int64_t j, Pair total)
 {
     if (g == p.withhold_tile) return;  // test hook: successors must time out
     unsigned long long *st = p.states;
     if (j == 0 || total.b == 0.f) {
-        ptx::st_relaxed(&st[2 * slot], pack_word((p.epoch << 2) | kTagPrefix, total.a));
+        ptx::st_relaxed(&st[2 * slot], pack_word((epoch << 2) | kTagPrefix, total.a));
     } else {
-        ptx::st_relaxed(&st[2 * slot + 1], pack_word((p.epoch << 2) | kTagAgg, total.b));
-        ptx::st_relaxed(&st[2 * slot], pack_word((p.epoch << 2) | kTagAgg, total.a));
+        ptx::st_relaxed(&st[2 * slot + 1], pack_word((epoch << 2) | kTagAgg, total.b));
+        ptx::st_relaxed(&st[2 * slot], pack_word((epoch << 2) | kTagAgg, total.a));
     }
 }
 
-__device__ __forceinline__ void publish_inclusive(const Params &p, int64_t slot, int64_t g, float v)
+__device__ __forceinline__ void publish_inclusive(const Params &p, uint32_t epoch, int64_t slot, int64_t g,
+                                                  float v)
 {
     if (g == p.withhold_tile) return;
-    ptx::st_relaxed(&p.states[2 * slot], pack_word((p.epoch << 2) | kTagPrefix, v));
+    ptx::st_relaxed(&p.states[2 * slot], pack_word((epoch << 2) | kTagPrefix, v));
 }
 
 // Reading side (one thread per warp and scan): the value entering tile g
@@ -411,12 +415,12 @@ __device__ __forceinline__ void publish_inclusive(const Params &p, int64_t slot,
 // through aggregates until an inclusive value, a zero decay, or the row's
 // first tile; every wait is bounded.
 template <int K>
-__device__ inline float lookback_read(const Params &p, int64_t g, int64_t j, int sc,
+__device__ inline float lookback_read(const Params &p, uint32_t epoch, int64_t g, int64_t j, int sc,
                                       unsigned long long w0, unsigned long long w1)
 {
     const unsigned long long *st = p.states;
-    const uint32_t tagA = (p.epoch << 2) | kTagAgg;
-    const uint32_t tagP = (p.epoch << 2) | kTagPrefix;
+    const uint32_t tagA = (epoch << 2) | kTagAgg;
+    const uint32_t tagP = (epoch << 2) | kTagPrefix;
     Pair acc{0.f, 1.f};
     int64_t k = g - p.N;
     int64_t left = j;  // predecessors not yet folded in
@@ -577,7 +581,10 @@ scan_kernel(const __grid_constant__ Params p)
     }
     // nothing global is touched before the previous kernel has completed
     ptx::pdl_wait_prerequisites();
+    __shared__ uint32_t s_epoch;
+    if (tid == 0) s_epoch = p.dynamic ? (ptx::ld_relaxed_u32(&p.hdr[kHdrEpoch]) & 0x3FFFFFFFu) : 0u;
     __syncthreads();
+    const uint32_t epoch = s_epoch;  // tag of this call's tile states
 
     if (warp == WARPS) {
         // Producer (lane 0 of the extra warp): for ring slot s of iteration
@@ -796,13 +803,14 @@ scan_kernel(const __grid_constant__ Params p)
     auto carry_in = [&](int64_t g, int64_t j, const Pair (&total)[K], unsigned long long w0,
                         unsigned long long w1, float (&carry)[K]) {
         float mine = 0.f;
-        if (lane < K) mine = lookback_read<K>(p, g, j, lane, w0, w1);
+        if (lane < K) mine = lookback_read<K>(p, epoch, g, j, lane, w0, w1);
 #pragma unroll
         for (int sc = 0; sc < K; ++sc) carry[sc] = __shfl_sync(0xffffffffu, mine, sc);
         if (warp == PUB_WARP && lane == 0) {
 #pragma unroll
             for (int sc = 0; sc < K; ++sc)
-                if (total[sc].b != 0.f) publish_inclusive(p, g * K + sc, g, fmaf(total[sc].b, carry[sc], total[sc].a));
+                if (total[sc].b != 0.f)
+                    publish_inclusive(p, epoch, g * K + sc, g, fmaf(total[sc].b, carry[sc], total[sc].a));
         }
     };
 
@@ -935,7 +943,8 @@ scan_kernel(const __grid_constant__ Params p)
         }
         if (!p.packed && warp == PUB_WARP && lane == 0) {
 #pragma unroll
-            for (int sc = 0; sc < K; ++sc) publish_first(p, g * K + sc, g, tg.j, compose(wa[PUB_WARP][sc], we[sc]));
+            for (int sc = 0; sc < K; ++sc)
+                publish_first(p, epoch, g * K + sc, g, tg.j, compose(wa[PUB_WARP][sc], we[sc]));
         }
 
         if (!defer) {
@@ -1007,9 +1016,10 @@ scan_kernel(const __grid_constant__ Params p)
         if (tid == THREADS) {
             __threadfence();
             const uint32_t done = atomicAdd(&p.hdr[kHdrExit], 1u);
-            if (done == gridDim.x - 1) {  // last CTA out: re-arm the ticket for the next call
+            if (done == gridDim.x - 1) {  // last CTA out: re-arm the ticket, advance the epoch
                 atomicExch(reinterpret_cast<unsigned long long *>(p.hdr), 0ull);
                 atomicExch(&p.hdr[kHdrExit], 0u);
+                atomicAdd(&p.hdr[kHdrEpoch], 1u);
                 __threadfence();
             }
         }
