@@ -49,7 +49,8 @@
  *    normalising one (rlscan_gae_normalized_workspace_bytes); it is 0 for
  *    T <= 512, where none needs one and `ws` may be NULL.  A workspace must be zeroed once
  *    with rlscan_workspace_init() before its first use; afterwards it needs
- *    no clearing between calls.  One workspace serves one call at a time:
+ *    no clearing between calls (the kernels keep a call counter in it, so
+ *    calls captured into a CUDA graph may be replayed).  One workspace serves one call at a time:
  *    calls that use the same workspace must be ordered (same stream, or
  *    synchronised).  Calls on different workspaces may run concurrently.
  *  - Arithmetic is float32 (exp via expf, IEEE division).
