@@ -85,6 +85,16 @@ def _cfg_workloads():
             desc="V-trace with truncations and 2-D bootstrap", N=2048, T=4096,
             gen=lambda N, T: synthetic.config_batch(2, N=N, T=T),
             estimators=[("vtrace", 36, c2)]),
+        "vtrace_4096x1024": dict(
+            desc="V-trace with truncations and 2-D bootstrap at the 4096 x 1024 shape "
+                 "(like-for-like with the GAE step)", N=4096, T=1024,
+            gen=lambda N, T: synthetic.vtrace_batch(N, T, 0, 2, c2["p_term"], c2["p_trunc"], "2d"),
+            estimators=[("vtrace", 36, c2)]),
+        "retrace_4096x1024": dict(
+            desc="Retrace(lambda) on per-step inputs at the 4096 x 1024 shape (like-for-like)",
+            N=4096, T=1024,
+            gen=lambda N, T: synthetic.retrace_batch(N, T, 0, 3, c3["p_term"], 0.0),
+            estimators=[("retrace", 32, c3)]),
         "retrace_1024x16384": dict(
             desc="Retrace(lambda) on per-step inputs, no truncations", N=1024, T=16384,
             gen=lambda N, T: synthetic.config_batch(3, N=N, T=T),
@@ -421,14 +431,19 @@ def run_ours(args, wl_name, rank, world, local_rank):
         _native.check(lib.rlscan_workspace_init(ctypes.c_void_p(ws_t.data_ptr()), wsn, sh), "init")
         ws = ctypes.c_void_p(ws_t.data_ptr())
     sets = []
+    keep = []  # every set's tensors stay allocated: the launchers hold raw pointers
     for _ in range(n_sets):
         bufs = {k: torch.from_numpy(v).to(dev) for k, v in host.items()}
+        keep.append(bufs)
         calls = {}
         for (name, bps, c) in all_kernels:
             odt = torch.bfloat16 if OUT_DTYPE.get(name) == "bf16" else torch.float32
             outs = [torch.empty((N, T), dtype=odt, device=dev) for _ in range(IO[name][2])]
+            keep.append(outs)
             calls[name] = _launcher(name, c, bufs, outs, N, T, ws, wsn, sh)
         sets.append(calls)
+    ptrs = [t.data_ptr() for group in keep for t in (group.values() if isinstance(group, dict) else group)]
+    assert len(ptrs) == len(set(ptrs)), "input sets must not share memory"
     torch.cuda.synchronize()
 
     def run(kernels, i):
@@ -576,8 +591,10 @@ def run_ours(args, wl_name, rank, world, local_rank):
                          "pinned host -> device copies, public compute_* API, results -> pinned host")
                         + f"; steps round-robin over {NS} streams"},
         "gpu_launches": K * sum(LAUNCHES.get(n, 1) for (n, _, _) in step_kernels),
+        "full_call_us": round(wall / K * 1e6, 2),
         "timing": "CUDA events around K back-to-back steps (no events between launches); "
-                  "per-kernel durations from K back-to-back launches of that kernel alone",
+                  "per-kernel durations from K back-to-back launches of that kernel alone; "
+                  "full_call_us: host wall time of the timed region per step",
         "wall_s_timed": round(wall, 4),
         "clocks": clocks,
     }
@@ -653,9 +670,11 @@ def _slice(batch, r0, r1):
     return out
 
 
-def oracle_time(wl_name, rows, threads, min_seconds=10.0, max_reps=10000):
+def oracle_time(wl_name, rows, threads, min_seconds=10.0, max_reps=10000, min_reps=3):
     """Time the oracle (as it is) on `rows` rows of the workload, rows split
-    across `threads` host threads.  Returns env-steps/s and the description."""
+    across `threads` host threads, for at least `min_reps` passes and
+    `min_seconds`.  Returns the env-steps/s of the best pass and the
+    description."""
     import oracle
     oracle.build()
     wl = WORKLOADS[wl_name]
@@ -672,16 +691,17 @@ def oracle_time(wl_name, rows, threads, min_seconds=10.0, max_reps=10000):
             for f in futs:
                 f.result()
     one_pass()  # warm (page in, build)
-    reps, t0 = 0, time.perf_counter()
+    reps, t0, best = 0, time.perf_counter(), float("inf")
     while True:
+        p0 = time.perf_counter()
         one_pass()
+        best = min(best, time.perf_counter() - p0)
         reps += 1
         el = time.perf_counter() - t0
-        if el >= min_seconds or reps >= max_reps:
+        if (el >= min_seconds and reps >= min_reps) or reps >= max_reps:
             break
-    per_pass = el / reps
-    return rows * T / per_pass, {"rows": rows, "seq_len": T, "passes": reps,
-                                 "seconds": round(el, 3)}
+    return rows * T / best, {"rows": rows, "seq_len": T, "passes": reps,
+                             "seconds": round(el, 3)}
 
 
 def _cpu_model():
@@ -698,12 +718,15 @@ def cpu_baseline(wl_name):
     wl = WORKLOADS[wl_name]
     threads = os.cpu_count() or 1
     rows = min(wl["N"], max(threads, int(4_194_304 * 2 // wl["T"])))
-    v, info = oracle_time(wl_name, rows, threads)
+    v, info = oracle_time(wl_name, rows, threads, min_seconds=8.0)
+    rows1 = max(1, rows // threads)
+    v1, info1 = oracle_time(wl_name, rows1, 1, min_seconds=3.0)
     return {"value": v, "unit": "env-steps/s", "cores": threads, "kind": "oracle",
-            "cpu": _cpu_model(),
+            "cpu": _cpu_model(), "value_1core": v1,
             "sample": f"{info['rows']} of {wl['N']} rows x {info['seq_len']} steps, "
-                      f"all estimators of the step, {info['passes']} passes in {info['seconds']} s, "
-                      f"rows split over {threads} threads"}
+                      f"all estimators of the step, best of {info['passes']} passes "
+                      f"({info['seconds']} s), rows split over {threads} threads; 1-core figure: "
+                      f"{info1['rows']} rows, best of {info1['passes']} passes"}
 
 
 def run_reference(args, wl_name):
