@@ -16,10 +16,13 @@ namespace rlscan {
 // (4 * (inputs + outputs)): tiles of 1024, 2048 or 4096 steps, whichever is
 // closest to TILE_BYTES_TARGET bytes of traffic, so the per-tile fixed cost
 // (barrier, warp scans, look-back) is amortised over enough data; 256
-// threads for 2048+ step tiles, 128 for 1024; as many ring stages
+// compute threads (4, 8 or 16 steps each); as many ring stages
 // (2..MAX_STAGES) as fit in SMEM_BUDGET_KB per CTA.  Sweeps on GB300 chose
-// the defaults: short kernels prefer a shallow ring (more CTAs per SM, and
-// every CTA's first tile arrives sooner).  The macros exist for such sweeps.
+// the defaults: short kernels are bound by each CTA's serial path through
+// its tiles, so they prefer short per-thread chains (more warps per tile)
+// and a shallow ring (more CTAs per SM, and every CTA's first tile arrives
+// sooner); the deferred kernels of long rows keep a ring of DEFER_STAGES.
+// The macros exist for such sweeps.
 #ifndef RLSCAN_TILE_BYTES_TARGET
 #define RLSCAN_TILE_BYTES_TARGET 30000
 #endif
@@ -27,10 +30,16 @@ namespace rlscan {
 #define RLSCAN_SMEM_BUDGET_KB 64
 #endif
 #ifndef RLSCAN_MAX_STAGES
-#define RLSCAN_MAX_STAGES 4
+#define RLSCAN_MAX_STAGES 2
 #endif
 #ifndef RLSCAN_THREADS_2048
 #define RLSCAN_THREADS_2048 256
+#endif
+#ifndef RLSCAN_LOWP_TILE_CAP
+#define RLSCAN_LOWP_TILE_CAP 2048
+#endif
+#ifndef RLSCAN_THREADS_1024
+#define RLSCAN_THREADS_1024 256
 #endif
 // Estimators with wide inputs (several words per step, e.g. [N,T,A]) move
 // far more bytes per step: 1024-step tiles, and a ring of WIDE_STAGES stages
@@ -80,9 +89,10 @@ struct Shape {
     // thread) so the register budget of three CTAs per SM holds
     static constexpr int TILE_BY_BYTES = TILE_RAW >= 3072 ? 4096 : (TILE_RAW >= 1536 ? 2048 : 1024);
     static constexpr int TILE = WIDE ? WideTileOf<E>::value
-                                     : ((IoOf<E>::LOWP && TILE_BY_BYTES > 2048) ? 2048 : TILE_BY_BYTES);
+                                     : ((IoOf<E>::LOWP && TILE_BY_BYTES > RLSCAN_LOWP_TILE_CAP)
+                                            ? RLSCAN_LOWP_TILE_CAP : TILE_BY_BYTES);
     static constexpr int THREADS = WIDE ? (TILE < 1024 ? 128 : RLSCAN_WIDE_THREADS)
-                                        : (TILE >= 4096 ? 256 : (TILE >= 2048 ? RLSCAN_THREADS_2048 : 128));
+                                        : (TILE >= 4096 ? 256 : (TILE >= 2048 ? RLSCAN_THREADS_2048 : RLSCAN_THREADS_1024));
     static constexpr int ITEMS = TILE / THREADS;
     static constexpr int STAGE_BYTES = narrow_bytes<E, TILE>();  // narrow arrays
     static constexpr int RAW = (RLSCAN_SMEM_BUDGET_KB * 1024) / STAGE_BYTES;

@@ -99,16 +99,17 @@ __device__ __forceinline__ void st_relaxed(unsigned long long *p, unsigned long 
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// Programmatic dependent launch: let the next kernel in the stream (if it
-// was launched with programmatic serialization) be scheduled now, and wait
-// until the previous kernel has completed and its writes are visible.
-// Both are no-ops for kernels launched without the attribute.
 __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t *ptr)
 {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
     return v;
 }
+
+// Programmatic dependent launch: let the next kernel in the stream (if it
+// was launched with programmatic serialization) be scheduled now, and wait
+// until the previous kernel has completed and its writes are visible.
+// Both are no-ops for kernels launched without the attribute.
 
 __device__ __forceinline__ void pdl_trigger_dependents()
 {

@@ -520,23 +520,23 @@ constexpr int block_threads() { return THREADS + 32; }
 #ifndef RLSCAN_MIN_BLOCKS
 #define RLSCAN_MIN_BLOCKS 3
 #endif
-// Two scans need more registers; two CTAs per SM is the most the wide
-// stages leave room for.
+// Two scans need more registers: three CTAs per SM at four steps per
+// thread, two at eight (four for a small 128-thread CTA); two CTAs per SM is
+// the most the wide stages leave room for.
 #ifndef RLSCAN_DEFER_MIN_BLOCKS
 #define RLSCAN_DEFER_MIN_BLOCKS 0  // 0: as the immediate-finish kernel
 #endif
-template <class E, bool DEFER, int THREADS>
+template <class E, bool DEFER, int THREADS, int ITEMS>
 constexpr int min_blocks()
 {
-    // small two-scan CTAs: keep four resident (the ring allows it)
     return (DEFER && RLSCAN_DEFER_MIN_BLOCKS > 0) ? RLSCAN_DEFER_MIN_BLOCKS
            : (WideOf<E>::NWIDE > 0) ? 2
-           : (E::K > 1) ? (THREADS <= 128 && !DEFER ? 4 : 2)
+           : (E::K > 1) ? (ITEMS <= 4 ? 3 : (THREADS <= 128 && !DEFER ? 4 : 2))
            : RLSCAN_MIN_BLOCKS;
 }
 
 template <class E, int THREADS, int ITEMS, int STAGES, bool DEFER>
-__global__ void __launch_bounds__(block_threads<THREADS>(), min_blocks<E, DEFER, THREADS>())
+__global__ void __launch_bounds__(block_threads<THREADS>(), min_blocks<E, DEFER, THREADS, ITEMS>())
 scan_kernel(const __grid_constant__ Params p)
 {
     constexpr int NIN = E::NIN, NOUT = E::NOUT, K = E::K;
