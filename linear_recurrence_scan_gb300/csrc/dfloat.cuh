@@ -38,4 +38,58 @@ __device__ __forceinline__ DF df_shfl_down(DF v, int off)
 
 __device__ __forceinline__ double df_value(DF v) { return static_cast<double>(v.hi) + static_cast<double>(v.lo); }
 
+// Whitening constants from the combined sum S and sum of squares Q of n
+// values (inv_n = 1 / n, inv_nm1 = 1 / (n - 1), NaN for n = 1): the mean,
+// the unbiased standard deviation sqrt((Q - S mean) / (n - 1)) (a negative
+// rounding residue reads as 0) and 1 / (sd + eps).
+struct Whitening {
+    float mean, sd, inv;
+};
+__device__ __forceinline__ Whitening whitening(DF sum, DF sumsq, double inv_n, double inv_nm1, float eps)
+{
+    const double S = df_value(sum), Q = df_value(sumsq);
+    const double mean = S * inv_n;
+    const double var = (Q - S * mean) * inv_nm1;
+    const float sd = sqrtf(static_cast<float>(var > 0.0 ? var : (var == var ? 0.0 : var)));
+    return Whitening{static_cast<float>(mean), sd, 1.f / (sd + eps)};
+}
+
+// Combine the per-CTA moment slots parts[c] = (sum hi, sum lo, sumsq hi,
+// sumsq lo), c < nparts, over threads 0..NT-1 in a fixed order (thread t
+// takes slots t, t + NT, ...; then a warp tree; then warp 0's lane 0 adds
+// the warps in order), so every caller gets the same bits.  red holds
+// NT / 32 pairs of DF; sync() is a barrier over the NT threads.  The
+// result is valid in thread 0.
+template <int NT, class Sync>
+__device__ __forceinline__ void combine_moment_slots(const float *parts, int nparts, int tid, DF (*red)[2], Sync sync,
+                                                     DF &sum, DF &sumsq)
+{
+    DF a{0.f, 0.f}, b{0.f, 0.f};
+    for (int c = tid; c < nparts; c += NT) {
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(parts + 4 * c));
+        a = df_add(a, DF{v.x, v.y});
+        b = df_add(b, DF{v.z, v.w});
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a = df_add(a, df_shfl_down(a, o));
+        b = df_add(b, df_shfl_down(b, o));
+    }
+    if ((tid & 31) == 0) {
+        red[tid >> 5][0] = a;
+        red[tid >> 5][1] = b;
+    }
+    sync();
+    if (tid == 0) {
+        a = DF{0.f, 0.f};
+        b = DF{0.f, 0.f};
+        for (int w = 0; w < NT / 32; ++w) {
+            a = df_add(a, red[w][0]);
+            b = df_add(b, red[w][1]);
+        }
+        sum = a;
+        sumsq = b;
+    }
+}
+
 }  // namespace rlscan

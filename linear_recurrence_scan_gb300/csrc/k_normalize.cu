@@ -36,59 +36,44 @@ __global__ void __launch_bounds__(kNormThreads) normalize_kernel(float *x, int64
 {
     ptx::pdl_trigger_dependents();
     ptx::pdl_wait_prerequisites();  // the scan kernel's outputs and moments are complete
+    // flat buffers: this block's first vectors are requested before the
+    // moments are combined, so their latency overlaps the combination
+    const bool flat = rs == T && vec;
+    float4 *x4 = reinterpret_cast<float4 *>(x);
+    const int64_t n4 = N * T / 4;
+    int64_t base = blockIdx.x * static_cast<int64_t>(kVecPerThread * kNormThreads);
+    float4 v[kVecPerThread];
+    auto load_chunk = [&] {
+#pragma unroll
+        for (int u = 0; u < kVecPerThread; ++u) {
+            const int64_t i = base + u * kNormThreads + threadIdx.x;
+            if (i < n4) v[u] = x4[i];
+        }
+    };
+    if (flat) load_chunk();
     __shared__ DF s_red[kNormThreads / 32][2];
     __shared__ float s_mi[2];
     {
-        // every thread loads its few slots at once, then warp and block trees
-        DF a{0.f, 0.f}, b{0.f, 0.f};
-        for (int c = threadIdx.x; c < nparts; c += kNormThreads) {
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(parts + 4 * c));
-            a = df_add(a, DF{v.x, v.y});
-            b = df_add(b, DF{v.z, v.w});
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            a = df_add(a, df_shfl_down(a, o));
-            b = df_add(b, df_shfl_down(b, o));
-        }
-        if ((threadIdx.x & 31) == 0) {
-            s_red[threadIdx.x >> 5][0] = a;
-            s_red[threadIdx.x >> 5][1] = b;
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        DF a{0.f, 0.f}, b{0.f, 0.f};
-        for (int w = 0; w < kNormThreads / 32; ++w) {
-            a = df_add(a, s_red[w][0]);
-            b = df_add(b, s_red[w][1]);
-        }
-        const double S = df_value(a), Q = df_value(b);
-        const double mean = S * inv_n;
-        const double var = (Q - S * mean) * inv_nm1;
-        const float sd = sqrtf(static_cast<float>(var > 0.0 ? var : (var == var ? 0.0 : var)));
-        s_mi[0] = static_cast<float>(mean);
-        s_mi[1] = 1.f / (sd + eps);
-        if (moments_out != nullptr && blockIdx.x == 0) {
-            moments_out[0] = static_cast<float>(mean);
-            moments_out[1] = sd;
+        DF sum, sumsq;
+        combine_moment_slots<kNormThreads>(parts, nparts, threadIdx.x, s_red, [] { __syncthreads(); }, sum, sumsq);
+        if (threadIdx.x == 0) {
+            const Whitening w = whitening(sum, sumsq, inv_n, inv_nm1, eps);
+            s_mi[0] = w.mean;
+            s_mi[1] = w.inv;
+            if (moments_out != nullptr && blockIdx.x == 0) {
+                moments_out[0] = w.mean;
+                moments_out[1] = w.sd;
+            }
         }
     }
     __syncthreads();
     const float m = s_mi[0], inv = s_mi[1];
-    if (rs == T && vec) {
-        // block b owns kVecPerThread * kNormThreads consecutive vectors; all of
-        // a thread's loads are issued before its stores
-        float4 *x4 = reinterpret_cast<float4 *>(x);
-        const int64_t n4 = N * T / 4;
-        for (int64_t base = blockIdx.x * static_cast<int64_t>(kVecPerThread * kNormThreads); base < n4;
-             base += static_cast<int64_t>(gridDim.x) * kVecPerThread * kNormThreads) {
-            float4 v[kVecPerThread];
-#pragma unroll
-            for (int u = 0; u < kVecPerThread; ++u) {
-                const int64_t i = base + u * kNormThreads + threadIdx.x;
-                if (i < n4) v[u] = x4[i];
-            }
+    if (flat) {
+        // block b owns kVecPerThread * kNormThreads consecutive vectors per
+        // step of the grid; all of a thread's loads are issued before its stores
+        const int64_t step = static_cast<int64_t>(gridDim.x) * kVecPerThread * kNormThreads;
+        for (bool first = true; base < n4; base += step, first = false) {
+            if (!first) load_chunk();
 #pragma unroll
             for (int u = 0; u < kVecPerThread; ++u) {
                 const int64_t i = base + u * kNormThreads + threadIdx.x;

@@ -194,38 +194,12 @@ rlscan_status launch_kernel(Kernel kernel, const Params &p, int64_t grid, int th
     return cudaGetLastError() == cudaSuccess ? RLSCAN_OK : RLSCAN_ERR_CUDA;
 }
 
+// Staging path and limits of a launch: bulk copies and vector stores when
+// every row is whole 16-byte units and the arrays are aligned (bulk copies
+// only from device memory).  Returns whether the tiles are bulk-copied.
 template <class E>
-rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stream, int64_t *grid_out = nullptr)
+bool bind_io(Params &p)
 {
-    using S = Shape<E>;
-    constexpr int TILE = S::TILE;
-    constexpr int BT = block_threads<S::THREADS>();
-    auto kernel = scan_kernel<E, S::THREADS, S::ITEMS, S::SHORT_STAGES, false>;
-    size_t smem = static_cast<size_t>(S::SHORT_STAGES) * S::STAGE_BYTES;
-
-    if (p.T <= TILE) {
-        p.packed = 1;
-        p.C = static_cast<int32_t>((p.T + S::ITEMS - 1) / S::ITEMS * S::ITEMS);
-        p.R = TILE / p.C;
-        p.tiles_per_row = 1;
-        p.num_tiles = (p.N + p.R - 1) / p.R;
-        p.dynamic = 0;
-        p.hdr = nullptr;
-        p.states = nullptr;
-    } else {
-        p.packed = 0;
-        p.C = TILE;
-        p.R = 1;
-        p.tiles_per_row = (p.T + TILE - 1) / TILE;
-        p.num_tiles = p.N * p.tiles_per_row;
-        const size_t need = kHeaderBytes + kStateBytes * E::K * static_cast<size_t>(p.num_tiles);
-        if (ws == nullptr || ws_bytes < need || !aligned16(ws)) return RLSCAN_ERR_WORKSPACE;
-        p.dynamic = 1;
-        p.hdr = static_cast<uint32_t *>(ws);
-        p.states = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
-    }
-
-    // bulk copies and vector stores: whole 16-byte units in every row
     bool tma = true;
     for (int j = 0; j < E::NIN; ++j) {
         const int units = 16 / IoOf<E>::in(j);
@@ -244,6 +218,49 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
     p.spin_limit_ns = spin_limit_ns();
     p.copy_limit_ns = 2000000000ull;  // bulk copies land in microseconds; never cut short
     p.withhold_tile = withhold_tile();
+    return tma;
+}
+
+// Packed tiling (whole rows per tile) of an estimator's shape.
+template <class E>
+void bind_packed(Params &p)
+{
+    using S = Shape<E>;
+    p.packed = 1;
+    p.C = static_cast<int32_t>((p.T + S::ITEMS - 1) / S::ITEMS * S::ITEMS);
+    p.R = S::TILE / p.C;
+    p.tiles_per_row = 1;
+    p.num_tiles = (p.N + p.R - 1) / p.R;
+    p.dynamic = 0;
+    p.hdr = nullptr;
+    p.states = nullptr;
+}
+
+template <class E>
+rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stream, int64_t *grid_out = nullptr)
+{
+    using S = Shape<E>;
+    constexpr int TILE = S::TILE;
+    constexpr int BT = block_threads<S::THREADS>();
+    auto kernel = scan_kernel<E, S::THREADS, S::ITEMS, S::SHORT_STAGES, false>;
+    size_t smem = static_cast<size_t>(S::SHORT_STAGES) * S::STAGE_BYTES;
+
+    if (p.T <= TILE) {
+        bind_packed<E>(p);
+    } else {
+        p.packed = 0;
+        p.C = TILE;
+        p.R = 1;
+        p.tiles_per_row = (p.T + TILE - 1) / TILE;
+        p.num_tiles = p.N * p.tiles_per_row;
+        const size_t need = kHeaderBytes + kStateBytes * E::K * static_cast<size_t>(p.num_tiles);
+        if (ws == nullptr || ws_bytes < need || !aligned16(ws)) return RLSCAN_ERR_WORKSPACE;
+        p.dynamic = 1;
+        p.hdr = static_cast<uint32_t *>(ws);
+        p.states = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
+    }
+
+    const bool tma = bind_io<E>(p);
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RLSCAN_ERR_CUDA;

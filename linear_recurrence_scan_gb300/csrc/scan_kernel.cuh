@@ -187,6 +187,12 @@ __device__ __forceinline__ Pair compose(Pair outer, Pair inner)
 
 constexpr uint32_t kTagAgg = 1u, kTagPrefix = 2u;
 
+// Longest pause between two polls of a predecessor's state (ns); the pause
+// starts at 32 ns and doubles.  0: poll without pausing.
+#ifndef RLSCAN_LB_NAP_MAX
+#define RLSCAN_LB_NAP_MAX 128
+#endif
+
 __device__ __forceinline__ unsigned long long pack_word(uint32_t tag, float v)
 {
     return (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(v);
@@ -451,8 +457,10 @@ __device__ inline float lookback_read(const Params &p, uint32_t epoch, int64_t g
             record_error(p, RLSCAN_ERR_TIMEOUT, static_cast<uint32_t>(g));
             return __int_as_float(0x7fc00000);
         }
-        __nanosleep(nap);
-        if (nap < 512) nap <<= 1;
+        if (RLSCAN_LB_NAP_MAX > 0) {
+            __nanosleep(nap);
+            if (nap < RLSCAN_LB_NAP_MAX) nap <<= 1;
+        }
     }
 }
 

@@ -1,7 +1,9 @@
-"""GAE with batch-normalised advantages (fused moments + in-place
-normalisation) against the float64 oracle: gae() then
-normalize_advantages().  The returns are compared with their own oracles
-(they use the raw advantages).
+"""GAE with batch-normalised advantages against the float64 oracle: gae()
+then normalize_advantages().  The returns are compared with their own
+oracles (they use the raw advantages).  The device path is the scan with
+per-CTA moment slots followed by the normalising pass; the shapes cover
+its flat (vector) walk, its strided and unaligned walks, packed and
+long-row scans.
 
 Tolerances: normalised advantages and returns |gpu - ref| <= 1e-4 + 1e-5 |ref|;
 the reported (mean, std) within 1e-5 relative (+1e-6 absolute for the mean).
@@ -50,12 +52,14 @@ def assert_disc(gpu, ref, what):
                              f"gpu {g[i]!r} ref {ref[i]!r}")
 
 
-# (N, T, row stride or None, mode): packed, one tile, look-back, deferred
-# look-back (few long rows), element-wise staging, strided rows
+# (N, T, row stride or None, mode): packed (one tile, many tiles,
+# truncations with a 2-D bootstrap, strided rows, a large batch), one tile
+# per row, look-back and deferred look-back, element-wise staging
 CASES = [
     (8, 128, None, "last"), (5, 37, None, "last"), (6, 1024, None, "last"),
     (3, 3000, None, "last"), (2, 40000, None, "2d"), (64, 1 << 16, None, "last"),
     (5, 100, 104, "2d"), (5, 100, 103, "last"), (4096, 1024, None, "last"),
+    (512, 256, None, "2d"), (20000, 512, None, "last"),
 ]
 IDS = [f"{n}x{t}" + (f"_rs{rs}" if rs else "") + f"_{m}" for n, t, rs, m in CASES]
 
@@ -102,6 +106,29 @@ def test_repeated_and_interleaved_calls():
         L().compute_gae(*args, None, 0.99, 0.95, None, dev(b["last_value"]))
         again = L().compute_gae_normalized(*args, None, 0.99, 0.95, None, dev(b["last_value"]))[0]
         torch.testing.assert_close(again, first, rtol=1e-6, atol=1e-6)
+
+
+def test_packed_repeated_and_interleaved_calls():
+    """Packed tiles are assigned to CTAs statically, so the moment slots are
+    summed in the same order every time: repeated calls, interleaved with
+    other entry points and other shapes on the same workspace, give the same
+    bits."""
+    N, T = 4096, 1024
+    b = synthetic.gae_batch(N, T, 5, 53, 0.01, 0.0, "last")
+    args = [dev(b[k]) for k in ("rewards", "values", "terminateds")]
+    first = L().compute_gae_normalized(*args, None, 0.99, 0.95, None, dev(b["last_value"]),
+                                       return_moments=True)
+    for _ in range(3):
+        L().compute_gae(*args, None, 0.99, 0.95, None, dev(b["last_value"]))
+        L().compute_gae_normalized(dev(b["rewards"][:64]), dev(b["values"][:64]), dev(b["terminateds"][:64]),
+                                   None, 0.99, 0.95, None, dev(b["last_value"][:64]))
+        again = L().compute_gae_normalized(*args, None, 0.99, 0.95, None, dev(b["last_value"]),
+                                           return_moments=True)
+        for x, y in zip(first, again):
+            assert torch.equal(x, y)
+    raw = oracle.gae(b["rewards"], b["values"], b["terminateds"], None, 0.99, 0.95, None, b["last_value"])
+    assert_disc(first[0], oracle.normalize_advantages(raw, 1e-8)[0], "normalized advantages")
+    L().workspace_status()  # raises if any wait timed out
 
 
 def test_single_value_gives_nan():
