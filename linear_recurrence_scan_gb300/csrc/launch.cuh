@@ -17,12 +17,13 @@ namespace rlscan {
 // closest to TILE_BYTES_TARGET bytes of traffic, so the per-tile fixed cost
 // (barrier, warp scans, look-back) is amortised over enough data; 256
 // compute threads (4, 8 or 16 steps each); as many ring stages
-// (2..MAX_STAGES) as fit in SMEM_BUDGET_KB per CTA.  Sweeps on GB300 chose
-// the defaults: short kernels are bound by each CTA's serial path through
-// its tiles, so they prefer short per-thread chains (more warps per tile)
-// and a shallow ring (more CTAs per SM, and every CTA's first tile arrives
-// sooner); the deferred kernels of long rows keep a ring of DEFER_STAGES.
-// The macros exist for such sweeps.
+// (2..MAX_STAGES) as fit in SMEM_BUDGET_KB per CTA, of which packed tiles
+// use PACKED_STAGES.  Sweeps on GB300 chose the defaults: short kernels are
+// bound by each CTA's serial path through its tiles, so they prefer short
+// per-thread chains (more warps per tile) and a shallow ring (every CTA's
+// first tile arrives sooner); split rows that finish at once keep a deeper
+// ring, and the deferred kernels of long rows a ring of DEFER_STAGES.  The
+// macros exist for such sweeps.
 #ifndef RLSCAN_TILE_BYTES_TARGET
 #define RLSCAN_TILE_BYTES_TARGET 30000
 #endif
@@ -30,7 +31,13 @@ namespace rlscan {
 #define RLSCAN_SMEM_BUDGET_KB 64
 #endif
 #ifndef RLSCAN_MAX_STAGES
-#define RLSCAN_MAX_STAGES 2
+#define RLSCAN_MAX_STAGES 3
+#endif
+// Packed tiles (whole rows, no look-back) use at most this many of the
+// ring's stages: a shallower ring gets every CTA's first tile sooner, while
+// split rows keep the deeper ring to hide their look-back waits.
+#ifndef RLSCAN_PACKED_STAGES
+#define RLSCAN_PACKED_STAGES 2
 #endif
 #ifndef RLSCAN_THREADS_2048
 #define RLSCAN_THREADS_2048 256
@@ -99,6 +106,7 @@ struct Shape {
     // ring of an immediate-finish launch, and of a deferred one
     static constexpr int SHORT_STAGES = WIDE ? RLSCAN_WIDE_STAGES
                                              : (RAW < 2 ? 2 : (RAW > RLSCAN_MAX_STAGES ? RLSCAN_MAX_STAGES : RAW));
+    static constexpr int PACKED_STAGES = SHORT_STAGES < RLSCAN_PACKED_STAGES ? SHORT_STAGES : RLSCAN_PACKED_STAGES;
     static constexpr int DEFER_STAGES = (WIDE || RLSCAN_DEFER_STAGES < 3) ? 0
                                         : (RLSCAN_DEFER_STAGES > SHORT_STAGES ? RLSCAN_DEFER_STAGES : SHORT_STAGES);
     static_assert(TILE == THREADS * ITEMS, "tile shape");
@@ -236,14 +244,16 @@ void bind_packed(Params &p)
     p.states = nullptr;
 }
 
-template <class E>
-rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stream, int64_t *grid_out = nullptr)
+// One launch with an immediate-finish ring of ST stages (or, for split rows
+// with several tiles of each row in flight, the deferred kernel).
+template <class E, int ST>
+rlscan_status launch_scan_ring(Params p, void *ws, size_t ws_bytes, cudaStream_t stream, int64_t *grid_out)
 {
     using S = Shape<E>;
     constexpr int TILE = S::TILE;
     constexpr int BT = block_threads<S::THREADS>();
-    auto kernel = scan_kernel<E, S::THREADS, S::ITEMS, S::SHORT_STAGES, false>;
-    size_t smem = static_cast<size_t>(S::SHORT_STAGES) * S::STAGE_BYTES;
+    auto kernel = scan_kernel<E, S::THREADS, S::ITEMS, ST, false>;
+    size_t smem = static_cast<size_t>(ST) * S::STAGE_BYTES;
 
     if (p.T <= TILE) {
         bind_packed<E>(p);
@@ -280,10 +290,10 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
         const int64_t copied = static_cast<int64_t>(narrow_copied<E>()) * (TILE + 8);
         const int64_t derived = static_cast<int64_t>(E::NIN - narrow_copied<E>()) * (TILE + 8);
         const int64_t staged_floats = copied + (wide_floats > derived ? wide_floats : derived);
-        wide_ok = wide_ok && static_cast<size_t>(S::SHORT_STAGES) * staged_floats * 4 <= dyn_limit;
+        wide_ok = wide_ok && static_cast<size_t>(ST) * staged_floats * 4 <= dyn_limit;
         p.wide_staged = wide_ok ? 1 : 0;
         p.stage_floats = static_cast<int32_t>(wide_ok ? staged_floats : copied + derived);
-        smem = static_cast<size_t>(S::SHORT_STAGES) * p.stage_floats * 4;
+        smem = static_cast<size_t>(ST) * p.stage_floats * 4;
     }
     int64_t slots = 0;
     RLSCAN_LAUNCH_TRY(kernel_facts(facts, kernel, dev, BT, smem, S::WIDE, smem, nullptr, &slots));
@@ -292,7 +302,7 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
     // once (their look-backs would otherwise wait on one another).
     if constexpr (S::DEFER_STAGES >= 3) {
         const bool want = !p.packed && (RLSCAN_DEFER_MODE == 1 ||
-                                        (RLSCAN_DEFER_MODE < 0 && slots * S::SHORT_STAGES >= 2 * p.N));
+                                        (RLSCAN_DEFER_MODE < 0 && slots * ST >= 2 * p.N));
         if (want) {
             auto dkernel = scan_kernel<E, S::THREADS, S::ITEMS, S::DEFER_STAGES, true>;
             static KernelFacts dfacts;
@@ -313,6 +323,14 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
     const int64_t grid = p.num_tiles < slots ? p.num_tiles : slots;
     if (grid_out != nullptr) *grid_out = grid;
     return launch_kernel(kernel, p, grid, BT, smem, stream);
+}
+
+template <class E>
+rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stream, int64_t *grid_out = nullptr)
+{
+    using S = Shape<E>;
+    if (p.T <= S::TILE) return launch_scan_ring<E, S::PACKED_STAGES>(p, ws, ws_bytes, stream, grid_out);
+    return launch_scan_ring<E, S::SHORT_STAGES>(p, ws, ws_bytes, stream, grid_out);
 }
 
 }  // namespace rlscan
