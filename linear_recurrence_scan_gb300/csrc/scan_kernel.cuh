@@ -531,6 +531,14 @@ constexpr int block_threads() { return THREADS + 32; }
 // Two scans need more registers: three CTAs per SM at four steps per
 // thread, two at eight (four for a small 128-thread CTA); two CTAs per SM is
 // the most the wide stages leave room for.
+#ifndef RLSCAN_K2_SHORT_BLOCKS
+#define RLSCAN_K2_SHORT_BLOCKS 3
+#endif
+// 1: in immediate-finish kernels each warp releases its share of a ring
+// slot as soon as its inputs are in registers (0: after the tile's warp scans)
+#ifndef RLSCAN_EARLY_RELEASE
+#define RLSCAN_EARLY_RELEASE 1
+#endif
 #ifndef RLSCAN_DEFER_MIN_BLOCKS
 #define RLSCAN_DEFER_MIN_BLOCKS 0  // 0: as the immediate-finish kernel
 #endif
@@ -539,7 +547,7 @@ constexpr int min_blocks()
 {
     return (DEFER && RLSCAN_DEFER_MIN_BLOCKS > 0) ? RLSCAN_DEFER_MIN_BLOCKS
            : (WideOf<E>::NWIDE > 0) ? 2
-           : (E::K > 1) ? (ITEMS <= 4 ? 3 : (THREADS <= 128 && !DEFER ? 4 : 2))
+           : (E::K > 1) ? (ITEMS <= 4 ? RLSCAN_K2_SHORT_BLOCKS : (THREADS <= 128 && !DEFER ? 4 : 2))
            : RLSCAN_MIN_BLOCKS;
 }
 
@@ -901,6 +909,11 @@ scan_kernel(const __grid_constant__ Params p)
         const ThreadSpan sp = thread_span<FWD, ITEMS>(p, tg, rit, col);
         float x[NIN][ITEMS], xn[NIN];
         load_inputs(stage, x, xn);
+        if constexpr (RLSCAN_EARLY_RELEASE && !DEFER) {
+            // this warp's inputs are in registers: its share of the slot is free
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&empty_bar[s]);
+        }
         float a[K][ITEMS], b[K][ITEMS];
         Keep keep;
         make_coeffs(x, xn, sp, rsc, a, b, keep);
@@ -926,7 +939,7 @@ scan_kernel(const __grid_constant__ Params p)
         }
         ptx::named_barrier(COMPUTE_BAR, THREADS);  // warp aggregates visible
         // every input is in registers: unless the tile is finished later, the slot is free
-        if (!defer && lane == 0) ptx::mbar_arrive(&empty_bar[s]);
+        if (!RLSCAN_EARLY_RELEASE && !defer && lane == 0) ptx::mbar_arrive(&empty_bar[s]);
 
         if (use_rsc) {
             const int s1 = (it + 1) % NST;
