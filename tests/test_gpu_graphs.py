@@ -60,3 +60,57 @@ def test_graph_replays_with_new_inputs():
         close(adv2, ref, f"graph fused gae (seed {seed})")
         close(disc, oracle.discounted_returns(b["rewards"], b["terminateds"], None, 0.99, None,
                                               b["last_value"]), f"graph discounted (seed {seed})")
+
+
+def test_graph_replays_other_kernels():
+    """Replays of the normalising path (scan with moment slots, then the
+    normalising pass), masked GAE and the [N,T,A] Retrace front end."""
+    N, T = 64, 3000
+    def batches(seed):
+        return (synthetic.gae_batch(N, T, seed, 96, 0.01, 0.0, "last"),
+                synthetic.llm_tokens_batch(N, T, seed),
+                synthetic.retrace_actions_batch(N, T, 4, seed, 97))
+    b0 = batches(0)
+    gkeys = ("rewards", "values", "terminateds", "last_value")
+    mkeys = ("rewards", "values", "terminateds", "mask")
+    rkeys = ("action_probs_target", "action_probs_behavior", "q_values", "next_q_values_all", "actions",
+             "rewards", "terminateds")
+    g = {k: torch.from_numpy(b0[0][k]).to(DEV) for k in gkeys}
+    m = {k: torch.from_numpy(b0[1][k]).to(DEV) for k in mkeys}
+    r = {k: torch.from_numpy(b0[2][k]).to(DEV) for k in rkeys}
+
+    def calls():
+        norm = L().compute_gae_normalized(g["rewards"], g["values"], g["terminateds"], None, 0.99, 0.95, None,
+                                          g["last_value"], return_moments=True)
+        masked = L().compute_gae(m["rewards"], m["values"], m["terminateds"], None, 1.0, 0.95, mask=m["mask"])
+        ret = L().compute_retrace(*(r[k] for k in rkeys), None, 0.99, 0.95)
+        return norm, masked, ret
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            calls()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        norm, masked, ret = calls()
+    for seed in (1, 2, 1):
+        b = batches(seed)
+        for dst, src, keys in ((g, b[0], gkeys), (m, b[1], mkeys), (r, b[2], rkeys)):
+            for k in keys:
+                dst[k].copy_(torch.from_numpy(src[k]))
+        graph.replay()
+        torch.cuda.synchronize()
+        bg, bm, br = b
+        raw = oracle.gae(bg["rewards"], bg["values"], bg["terminateds"], None, 0.99, 0.95, None, bg["last_value"])
+        want, (mean, sd) = oracle.normalize_advantages(raw, 1e-8)
+        close(norm[0], want, f"graph normalized advantages (seed {seed})")
+        mom = norm[-1].double().cpu().numpy()
+        assert abs(mom[0] - mean) <= 1e-6 + 1e-5 * abs(mean) and abs(mom[1] - sd) <= 1e-5 * sd
+        close(masked, oracle.gae_masked(bm["rewards"], bm["values"], bm["terminateds"], bm["mask"], None, 1.0,
+                                        0.95), f"graph masked gae (seed {seed})")
+        qret, adv = oracle.retrace_actions(*(br[k] for k in rkeys), None, 0.99, 0.95)
+        close(ret[0], qret, f"graph retrace targets (seed {seed})")
+        close(ret[1], adv, f"graph retrace advantages (seed {seed})")
