@@ -20,9 +20,11 @@
  *  - Pointers are owned by the caller: device memory, or page-locked host
  *    memory (cudaHostAlloc / cudaHostRegister), which the kernel reads and
  *    writes in place over the host link with plain loads and stores (zero
- *    copy; bulk asynchronous copies are used for device memory only).  The
- *    workspace must be device memory.  The library never allocates, frees
- *    or retains them.
+ *    copy; bulk asynchronous copies are used for device memory only).
+ *    Pageable host memory is read the same way on a device that reports
+ *    cudaDevAttrPageableMemoryAccess, and refused (RLSCAN_ERR_MEMORY, before
+ *    any work is enqueued) on one that does not.  The workspace must be
+ *    device memory.  The library never allocates, frees or retains them.
  *  - [N,T] arrays are float32, row-major, element stride 1, row stride
  *    `row_stride` elements (row_stride >= T), the same stride for every
  *    [N,T] argument of a call, inputs and outputs alike.  [N] arrays are
@@ -78,7 +80,10 @@ typedef enum rlscan_status {
     RLSCAN_ERR_CUDA = 6,          /* the CUDA runtime refused the launch */
     RLSCAN_ERR_INVALID_INPUT = 7, /* content check failed (only with RLSCAN_CHECKS=1) */
     RLSCAN_ERR_TIMEOUT = 8,       /* a cross-block wait gave up (reported by rlscan_workspace_status) */
-    RLSCAN_ERR_SCRATCH_LIMIT = 9  /* shape needs more scratch than rlscan_gae_noalloc's built-in buffer */
+    RLSCAN_ERR_SCRATCH_LIMIT = 9, /* shape needs more scratch than rlscan_gae_noalloc's built-in buffer */
+    RLSCAN_ERR_MEMORY = 10        /* a pointer the GPU cannot reach: neither device (or managed) memory nor
+                                     page-locked host memory, nor pageable memory on a device that
+                                     reads pageable memory */
 } rlscan_status;
 
 typedef enum rlscan_dtype {

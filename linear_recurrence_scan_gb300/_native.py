@@ -17,6 +17,7 @@ STATUS = {
     0: "RLSCAN_OK", 1: "RLSCAN_ERR_NULL", 2: "RLSCAN_ERR_SHAPE", 3: "RLSCAN_ERR_ARG_CONFLICT",
     4: "RLSCAN_ERR_ARG_VALUE", 5: "RLSCAN_ERR_WORKSPACE", 6: "RLSCAN_ERR_CUDA",
     7: "RLSCAN_ERR_INVALID_INPUT", 8: "RLSCAN_ERR_TIMEOUT", 9: "RLSCAN_ERR_SCRATCH_LIMIT",
+    10: "RLSCAN_ERR_MEMORY",
 }
 ENDS_AT, STARTS_AT = 0, 1
 BACKWARD, FORWARD = 0, 1

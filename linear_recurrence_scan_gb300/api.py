@@ -49,6 +49,15 @@ def _check(name, t, shape, device=None, dtypes=(torch.float32,)):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+def _contiguous(t):
+    """t with unit column stride and packed rows; a host copy stays
+    page-locked (the kernel reads host tensors in place)."""
+    c = t.contiguous()
+    if c is not t and not c.is_cuda:
+        c = c.pin_memory()
+    return c
+
+
 _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
@@ -90,7 +99,7 @@ class _Call:
         if t is None:
             return
         _check(name, t, (self.N,), self.device)
-        self.vecs[name] = t.contiguous()
+        self.vecs[name] = _contiguous(t)
 
     def finish(self, n_out, dtype=torch.float32):
         mats = self.mats.values()
@@ -101,7 +110,7 @@ class _Call:
             ok = all(self.T <= 1 or t.stride(1) == 1 for t in mats) and len(strides) == 1
             rs = strides.pop() if ok else self.T
             if not ok or rs < self.T:
-                self.mats = {k: t.contiguous() for k, t in self.mats.items()}
+                self.mats = {k: _contiguous(t) for k, t in self.mats.items()}
                 rs = self.T
             self.rs = max(rs, self.T)
         where = dict(device="cpu", pin_memory=True) if self.host else dict(device=self.device)
@@ -407,7 +416,7 @@ def compute_retrace(action_probs_target, action_probs_behavior, q_values, next_q
     else:
         ars = -1
     if ars < c.T * A:
-        wide = [t.contiguous() for t in wide]
+        wide = [_contiguous(t) for t in wide]
         ars = c.T * A
     ws, wsn, s = _ws_for(c)
     _native.check(_native.lib().rlscan_retrace_actions(

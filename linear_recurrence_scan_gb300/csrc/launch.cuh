@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include "params.cuh"
+#include "residency.cuh"
 #include "scan_kernel.cuh"
 
 namespace rlscan {
@@ -122,19 +123,6 @@ constexpr int kMaxDevices = 64;
 
 inline bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-// Page-locked host memory (cudaHostAlloc / cudaHostRegister): the kernel
-// reads and writes it in place over the host link (zero copy) with plain
-// loads and stores; bulk asynchronous copies are used for device memory only.
-inline bool host_memory(const void *ptr)
-{
-    if (ptr == nullptr) return false;
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    return a.type == cudaMemoryTypeHost;
-}
 
 // Per-device launch facts of one kernel: SM count, the dynamic shared
 // memory a CTA may opt into (the device limit less the kernel's static
@@ -206,7 +194,7 @@ rlscan_status launch_kernel(Kernel kernel, const Params &p, int64_t grid, int th
 // every row is whole 16-byte units and the arrays are aligned (bulk copies
 // only from device memory).  Returns whether the tiles are bulk-copied.
 template <class E>
-bool bind_io(Params &p)
+rlscan_status bind_io(Params &p, bool *tma_out)
 {
     bool tma = true;
     for (int j = 0; j < E::NIN; ++j) {
@@ -218,15 +206,25 @@ bool bind_io(Params &p)
         tma = tma && (p.T % units == 0) && (p.rs % units == 0) && (p.out[q] == nullptr || aligned16(p.out[q]));
     }
     p.vec = tma ? 1 : 0;
-    bool on_host = false;
-    for (int j = 0; j < E::NIN; ++j) on_host = on_host || host_memory(p.in[j]);
-    for (int w = 0; w < WideOf<E>::NWIDE; ++w) on_host = on_host || host_memory(p.wide[w]);
+    bool on_host = false, unreachable = false;
+    auto note = [&](const void *ptr, bool input) {
+        if (ptr == nullptr) return;
+        const Residency r = residency(ptr);
+        unreachable = unreachable || r == Residency::Unreachable;
+        on_host = on_host || (input && r == Residency::Host);
+    };
+    for (int j = 0; j < E::NIN; ++j) note(p.in[j], true);
+    for (int w = 0; w < WideOf<E>::NWIDE; ++w) note(p.wide[w], true);
+    for (int q = 0; q < E::NOUT; ++q) note(p.out[q], false);
+    note(p.rowscalar, false);
+    if (unreachable) return RLSCAN_ERR_MEMORY;
     tma = tma && !on_host;
     p.tma = tma ? 1 : 0;
     p.spin_limit_ns = spin_limit_ns();
     p.copy_limit_ns = 2000000000ull;  // bulk copies land in microseconds; never cut short
     p.withhold_tile = withhold_tile();
-    return tma;
+    *tma_out = tma;
+    return RLSCAN_OK;
 }
 
 // Packed tiling (whole rows per tile) of an estimator's shape.
@@ -264,13 +262,15 @@ rlscan_status launch_scan_ring(Params p, void *ws, size_t ws_bytes, cudaStream_t
         p.tiles_per_row = (p.T + TILE - 1) / TILE;
         p.num_tiles = p.N * p.tiles_per_row;
         const size_t need = kHeaderBytes + kStateBytes * E::K * static_cast<size_t>(p.num_tiles);
-        if (ws == nullptr || ws_bytes < need || !aligned16(ws)) return RLSCAN_ERR_WORKSPACE;
+        if (ws == nullptr || ws_bytes < need || !aligned16(ws) || residency(ws) != Residency::Device)
+            return RLSCAN_ERR_WORKSPACE;
         p.dynamic = 1;
         p.hdr = static_cast<uint32_t *>(ws);
         p.states = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kHeaderBytes);
     }
 
-    const bool tma = bind_io<E>(p);
+    bool tma = false;
+    RLSCAN_LAUNCH_TRY(bind_io<E>(p, &tma));
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RLSCAN_ERR_CUDA;

@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include "params.cuh"
+#include "residency.cuh"
 
 namespace rlscan {
 
@@ -94,6 +95,9 @@ rlscan_status run_checks(const float *term, const float *trunc, const float *bs,
                          int64_t T, int64_t rs, cudaStream_t stream)
 {
     if (!checks_enabled() || trunc == nullptr) return RLSCAN_OK;
+    for (const void *ptr : {static_cast<const void *>(term), static_cast<const void *>(trunc),
+                            static_cast<const void *>(bs)})
+        if (ptr != nullptr && residency(ptr) == Residency::Unreachable) return RLSCAN_ERR_MEMORY;
     const uint32_t zero = 0;
     if (cudaMemcpyToSymbolAsync(g_check_flags, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice,
                                 stream) != cudaSuccess)
@@ -128,6 +132,7 @@ rlscan_status run_action_checks(const int64_t *actions, int64_t N, int64_t T, in
                                 cudaStream_t stream)
 {
     if (!checks_enabled()) return RLSCAN_OK;
+    if (residency(actions) == Residency::Unreachable) return RLSCAN_ERR_MEMORY;
     const uint32_t zero = 0;
     if (cudaMemcpyToSymbolAsync(g_check_flags, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice,
                                 stream) != cudaSuccess)
@@ -200,6 +205,7 @@ RLSCAN_API const char *rlscan_status_string(rlscan_status status)
     case RLSCAN_ERR_INVALID_INPUT: return "input content check failed";
     case RLSCAN_ERR_TIMEOUT: return "a cross-block wait timed out";
     case RLSCAN_ERR_SCRATCH_LIMIT: return "shape needs more scratch than the built-in no-allocation buffer holds";
+    case RLSCAN_ERR_MEMORY: return "a pointer is in memory the GPU cannot reach (pageable host memory)";
     }
     return "unknown status";
 }
@@ -222,7 +228,8 @@ RLSCAN_API size_t rlscan_gae_normalized_workspace_bytes(int64_t N, int64_t T)
 RLSCAN_API rlscan_status rlscan_workspace_init(void *ws, size_t ws_bytes, rlscan_stream_t stream)
 {
     if (ws == nullptr) return RLSCAN_ERR_NULL;
-    if ((reinterpret_cast<uintptr_t>(ws) & 15u) != 0 || ws_bytes % 4 != 0) return RLSCAN_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 15u) != 0 || ws_bytes % 4 != 0 || residency(ws) != Residency::Device)
+        return RLSCAN_ERR_WORKSPACE;
     const size_t words = ws_bytes / 4;
     if (words == 0) return RLSCAN_OK;
     size_t blocks = (words + 255) / 256;
@@ -397,8 +404,10 @@ RLSCAN_API rlscan_status rlscan_gae_normalized(const float *rewards, const float
         (discounted_returns && discounted_returns == moments))
         return RLSCAN_ERR_ARG_CONFLICT;
     const size_t need = rlscan_gae_normalized_workspace_bytes(N, T);
-    if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u) != 0)
+    if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u) != 0 ||
+        residency(ws) != Residency::Device)
         return RLSCAN_ERR_WORKSPACE;
+    if (moments != nullptr && residency(moments) == Residency::Unreachable) return RLSCAN_ERR_MEMORY;
     RLSCAN_TRY(run_checks(terminateds, truncateds, bootstrap_values, N, T, row_stride, cs(stream)));
     Params p = base_params(N, T, row_stride);
     p.c0 = gamma;

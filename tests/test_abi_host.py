@@ -41,8 +41,8 @@ def test_library_exports_every_declared_function(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.rlscan_version() == (0 << 16) | (1 << 8) | 0
-    for code in range(9):
-        assert lib.rlscan_status_string(code)
+    for code in range(11):
+        assert lib.rlscan_status_string(code) and lib.rlscan_status_string(code) != b"unknown status"
     assert lib.rlscan_status_string(99) == b"unknown status"
 
 

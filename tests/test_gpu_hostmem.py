@@ -104,3 +104,55 @@ def test_plain_cpu_tensors_are_rejected():
     x = torch.zeros(2, 4)
     with pytest.raises(ValueError, match="pinned"):
         L().compute_gae(x, x, x)
+
+
+def test_strided_pinned_inputs_stay_page_locked():
+    """Pinned inputs whose strides differ are re-laid out; the copies must
+    stay page-locked (the kernel reads host tensors in place)."""
+    N, T = 8, 3000
+    b = synthetic.returns_batch(N, T, 9, 85)
+    r = pinned(b["rewards"])
+    wide = torch.zeros((N, T + 8), dtype=torch.float32).pin_memory()
+    wide[:, :T] = torch.from_numpy(b["values"])
+    v = wide[:, :T]                               # row stride T + 8, the others T
+    term = pinned(b["terminateds"])
+    last = torch.zeros(2 * N, dtype=torch.float32).pin_memory()
+    last[::2] = torch.from_numpy(b["last_value"])
+    h = L().compute_gae(r, v, term, None, 0.99, 0.95, None, last[::2])   # strided [N] vector too
+    d = L().compute_gae(device(b["rewards"]), device(b["values"]), device(b["terminateds"]), None, 0.99, 0.95,
+                        None, device(b["last_value"]))
+    same(h, d, "strided pinned gae")
+
+
+def test_pageable_memory_through_the_c_abi():
+    """Pageable host arrays passed to the C ABI: read and written in place on
+    a device that reads pageable memory (equal to the device path bit for
+    bit), refused with RLSCAN_ERR_MEMORY (output untouched) on one that
+    does not.  A page-locked host workspace is refused."""
+    import ctypes
+    from linear_recurrence_scan_gb300 import _native
+    lib = _native.lib()
+    N, T = 8, 3000
+    b = synthetic.returns_batch(N, T, 9, 86)
+    r, v, term = (np.ascontiguousarray(b[k], dtype=np.float32) for k in ("rewards", "values", "terminateds"))
+    last = np.ascontiguousarray(b["last_value"], dtype=np.float32)
+    out = np.zeros((N, T), dtype=np.float32)
+    wsn = lib.rlscan_workspace_bytes(N, T)
+    ws = torch.zeros(wsn, dtype=torch.uint8, device=DEV)
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = lib.rlscan_gae(r.ctypes.data, v.ctypes.data, term.ctypes.data, None, None, last.ctypes.data, N, T, T,
+                        0.99, 0.95, out.ctypes.data, ws.data_ptr(), wsn, s)
+    torch.cuda.synchronize()
+    if st == 0:
+        d = L().compute_gae(device(b["rewards"]), device(b["values"]), device(b["terminateds"]), None, 0.99, 0.95,
+                            None, device(b["last_value"]))
+        assert np.array_equal(out, d.cpu().numpy())
+    else:
+        assert _native.STATUS[st] == "RLSCAN_ERR_MEMORY", _native.STATUS.get(st, st)
+        assert not out.any()
+    host_ws = torch.zeros(wsn, dtype=torch.uint8).pin_memory()
+    rp, vp, tp = (pinned(b[k]) for k in ("rewards", "values", "terminateds"))
+    st = lib.rlscan_gae(rp.data_ptr(), vp.data_ptr(), tp.data_ptr(), None, None, pinned(last).data_ptr(), N, T, T,
+                        0.99, 0.95, pinned(out).data_ptr(), host_ws.data_ptr(), wsn, s)
+    torch.cuda.synchronize()
+    assert _native.STATUS[st] == "RLSCAN_ERR_WORKSPACE"
