@@ -43,6 +43,10 @@ FALLBACK_HBM_GBS = 6800.0
 # (fp32 inputs read once + outputs written once; [N] vectors and the
 # one-step halo are not counted)
 
+_VTRACE_VALUES = ("log_pi_target", "log_pi_behavior", "values", "rewards", "bootstrap_values")
+_RETRACE_VALUES = ("pi_taken", "mu_taken", "q_values", "expected_next_q", "rewards")
+
+
 def _cfg_workloads():
     c1, c2, c3, c4 = (synthetic.CONFIGS[i] for i in (1, 2, 3, 4))
     return {
@@ -99,6 +103,20 @@ def _cfg_workloads():
             desc="Retrace(lambda) on per-step inputs, no truncations", N=1024, T=16384,
             gen=lambda N, T: synthetic.config_batch(3, N=N, T=T),
             estimators=[("retrace", 32, c3)]),
+        "vtrace_compact_2048x4096": dict(
+            desc="V-trace with truncations and 2-D bootstrap on compact storage: bfloat16 "
+                 "log-probabilities, values, rewards and bootstrap values, uint8 flags, bfloat16 "
+                 "outputs (float32 arithmetic)", N=2048, T=4096,
+            gen=lambda N, T: synthetic.compact(synthetic.config_batch(2, N=N, T=T), values=_VTRACE_VALUES),
+            # 5 x 2 + 2 x 1 bytes read, 2 x 2 written
+            estimators=[("vtrace_compact", 16, c2)]),
+        "retrace_compact_1024x16384": dict(
+            desc="Retrace(lambda) on per-step inputs in compact storage: bfloat16 probabilities, "
+                 "Q-values and rewards, uint8 flags, bfloat16 outputs (float32 arithmetic)",
+            N=1024, T=16384,
+            gen=lambda N, T: synthetic.compact(synthetic.config_batch(3, N=N, T=T), values=_RETRACE_VALUES),
+            # 5 x 2 + 1 bytes read, 2 x 2 written
+            estimators=[("retrace_compact", 15, c3)]),
         "retrace_actions_1024x16384x4": dict(
             desc="Retrace(lambda) from [N,T,A] target probabilities and successor Q-values with "
                  "int64 actions (A = 4), reduced in-kernel, no truncations",
@@ -146,10 +164,14 @@ IO = {
     "gae_masked": (["rewards", "values", "terminateds", "mask"], [], 1),
     "gae_compact": (["rewards", "values", "terminateds"], ["last_value"], 1),
     "gae_returns_compact": (["rewards", "values", "terminateds"], ["last_value"], 3),
+    "vtrace_compact": (["log_pi_target", "log_pi_behavior", "values", "rewards", "terminateds",
+                        "truncateds", "bootstrap_values"], [], 2),
+    "retrace_compact": (["pi_taken", "mu_taken", "q_values", "expected_next_q", "rewards",
+                         "terminateds"], [], 2),
 }
 # output element bytes (default 4)
-OUT_BYTES = {"gae_returns_compact": 2}
-OUT_DTYPE = {"gae_returns_compact": "bf16"}
+OUT_BYTES = {"gae_returns_compact": 2, "vtrace_compact": 2, "retrace_compact": 2}
+OUT_DTYPE = {"gae_returns_compact": "bf16", "vtrace_compact": "bf16", "retrace_compact": "bf16"}
 # streams the end-to-end steps rotate over by default (copies of one step
 # overlap another's compute)
 E2E_STREAMS = 3
@@ -317,6 +339,18 @@ def _launcher(name, c, bufs, outs, N, T, ws, wsn, stream):
                                                       None, None, b["last_value"], N, T, T, g,
                                                       float(c["lambda_"]), 1, o[0], o[1], o[2], ws,
                                                       wsn, stream)
+    if name == "vtrace_compact":
+        return lambda: lib.rlscan_vtrace_compact(b["log_pi_target"], b["log_pi_behavior"], b["values"],
+                                                 b["rewards"], b["terminateds"], b["truncateds"],
+                                                 b["bootstrap_values"], None, N, T, T, g,
+                                                 float(c["rho_bar"]), float(c["c_bar"]), 1, o[0], o[1],
+                                                 ws, wsn, stream)
+    if name == "retrace_compact":
+        return lambda: lib.rlscan_retrace_compact(b["pi_taken"], b["mu_taken"], b["q_values"],
+                                                  b["expected_next_q"], b["rewards"], b["terminateds"],
+                                                  None, N, T, T, g, float(c["lambda_"]),
+                                                  float(c["c_bar"]), float(c["rho_bar"]), 1, o[0],
+                                                  o[1], ws, wsn, stream)
     if name == "gae_masked":
         return lambda: lib.rlscan_gae_masked(b["rewards"], b["values"], b["terminateds"], None, None,
                                              None, b["mask"], N, T, T, g, float(c["lambda_"]), o[0],
@@ -392,6 +426,18 @@ def _public_call(name, c, t):
         return list(Lb.compute_gae_and_returns(_bf16(t["rewards"]), _bf16(t["values"]),
                                                t["terminateds"], None, g, c["lambda_"], None,
                                                t["last_value"], out_dtype=torch.bfloat16))
+    if name == "vtrace_compact":
+        import torch
+        return list(Lb.compute_vtrace(_bf16(t["log_pi_target"]), _bf16(t["log_pi_behavior"]),
+                                      _bf16(t["values"]), _bf16(t["rewards"]), t["terminateds"],
+                                      t["truncateds"], g, c["rho_bar"], c["c_bar"],
+                                      _bf16(t["bootstrap_values"]), out_dtype=torch.bfloat16))
+    if name == "retrace_compact":
+        import torch
+        return list(Lb.compute_retrace_from_probs(
+            _bf16(t["pi_taken"]), _bf16(t["mu_taken"]), _bf16(t["q_values"]),
+            _bf16(t["expected_next_q"]), _bf16(t["rewards"]), t["terminateds"], None, g, c["lambda_"],
+            c["c_bar"], c["rho_bar"], out_dtype=torch.bfloat16))
     if name == "gae_normalized":
         return list(Lb.compute_gae_normalized(t["rewards"], t["values"], t["terminateds"], None, g,
                                               c["lambda_"], None, t["last_value"], 1e-8,
@@ -639,6 +685,16 @@ def _oracle_call(name, c, b):
             return adv
         return adv, oracle.discounted_returns(dec["rewards"], dec["terminateds"], None, g, None,
                                               b["last_value"])
+    if name == "vtrace_compact":
+        dec = {k: _decode(b[k]) for k in _VTRACE_VALUES + ("terminateds", "truncateds")}
+        return oracle.vtrace(dec["log_pi_target"], dec["log_pi_behavior"], dec["values"], dec["rewards"],
+                             dec["terminateds"], dec["truncateds"], g, c["rho_bar"], c["c_bar"],
+                             dec["bootstrap_values"])
+    if name == "retrace_compact":
+        dec = {k: _decode(b[k]) for k in _RETRACE_VALUES + ("terminateds",)}
+        return oracle.retrace(dec["pi_taken"], dec["mu_taken"], dec["q_values"], dec["expected_next_q"],
+                              dec["rewards"], dec["terminateds"], None, g, c["lambda_"], c["c_bar"],
+                              c["rho_bar"])
     if name == "gae_masked":
         return oracle.gae_masked(b["rewards"], b["values"], b["terminateds"], b["mask"], None, g,
                                  c["lambda_"])

@@ -297,6 +297,43 @@ rlscan_status rlscan_gae_returns_compact(const void *rewards, const void *values
                                          size_t ws_bytes, rlscan_stream_t stream);
 
 /*
+ * V-trace and Retrace(lambda) (per-step inputs) on compact storage, the
+ * same bfloat16 I/O plan (rl-triton paper Sec. 9.2-9.3) carried to the
+ * off-policy estimators: every value input in bfloat16 (V-trace
+ * log_pi_target, log_pi_behavior, values, rewards, bootstrap_values;
+ * Retrace pi_taken, mu_taken, q_values, expected_next_q, rewards), the
+ * flags in uint8 (0/1), both outputs in out_dtype.  The arithmetic is that
+ * of rlscan_vtrace / rlscan_retrace in float32 on the stored values (the
+ * ratio exp(lpt - lpb) or pi / mu is formed from the bfloat16 inputs read
+ * exactly).  Bytes per step: V-trace 36 -> 20 with float32 outputs, 16 with
+ * bf16 outputs (with truncation flags and a 2-D bootstrap); Retrace
+ * 32 -> 19 / 15.
+ * Inputs : as rlscan_vtrace / rlscan_retrace in the storage types above;
+ *          for V-trace the window bootstrap without truncateds is
+ *          last_value (float32 [N], nullable), and bootstrap_values
+ *          without truncateds is RLSCAN_ERR_ARG_CONFLICT.
+ * Outputs: V-trace targets and advantages, or Retrace targets and
+ *          advantages, each [N,T] of out_dtype (RLSCAN_F32 or RLSCAN_BF16,
+ *          else RLSCAN_ERR_ARG_VALUE).
+ * Alignment and content checks as for rlscan_gae_compact.
+ */
+rlscan_status rlscan_vtrace_compact(const void *log_pi_target, const void *log_pi_behavior,
+                                    const void *values, const void *rewards, const void *terminateds,
+                                    const void *truncateds, const void *bootstrap_values,
+                                    const float *last_value, int64_t N, int64_t T, int64_t row_stride,
+                                    float gamma, float rho_bar, float c_bar, rlscan_dtype out_dtype,
+                                    void *vtrace_targets, void *vtrace_advantages, void *ws,
+                                    size_t ws_bytes, rlscan_stream_t stream);
+
+rlscan_status rlscan_retrace_compact(const void *pi_taken, const void *mu_taken, const void *q_values,
+                                     const void *expected_next_q, const void *rewards,
+                                     const void *terminateds, const void *truncateds, int64_t N,
+                                     int64_t T, int64_t row_stride, float gamma, float lambda,
+                                     float c_bar, float rho_bar, rlscan_dtype out_dtype,
+                                     void *retrace_targets, void *advantages, void *ws, size_t ws_bytes,
+                                     rlscan_stream_t stream);
+
+/*
  * V-trace targets and advantages.
  * rl-triton API reference, compute_vtrace; rl-triton paper Table 1 row
  * "V-Trace" and Sec. 3.3.2.

@@ -52,6 +52,8 @@ SIGNATURES = {
     "rlscan_gae_normalized": ([_P] * 6 + [_I64] * 3 + [_F, _F, _F, _P, _P, _P, _P, _P, _SZ, _P], _I),
     "rlscan_gae_compact": ([_P] * 6 + [_I64] * 3 + [_F, _F, _I, _P, _P, _SZ, _P], _I),
     "rlscan_gae_returns_compact": ([_P] * 6 + [_I64] * 3 + [_F, _F, _I, _P, _P, _P, _P, _SZ, _P], _I),
+    "rlscan_vtrace_compact": ([_P] * 8 + [_I64] * 3 + [_F, _F, _F, _I, _P, _P, _P, _SZ, _P], _I),
+    "rlscan_retrace_compact": ([_P] * 7 + [_I64] * 3 + [_F, _F, _F, _F, _I, _P, _P, _P, _SZ, _P], _I),
     "rlscan_gae_masked": ([_P] * 7 + [_I64] * 3 + [_F, _F, _P, _P, _SZ, _P], _I),
     "rlscan_gae_returns": ([_P] * 6 + [_I64] * 3 + [_F, _F, _P, _P, _P, _P, _SZ, _P], _I),
     "rlscan_vtrace": ([_P] * 8 + [_I64] * 3 + [_F, _F, _F, _P, _P, _P, _SZ, _P], _I),

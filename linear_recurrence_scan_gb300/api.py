@@ -346,8 +346,39 @@ def compute_gae_normalized(rewards, values, terminateds, truncateds=None, gamma=
 
 
 def compute_vtrace(log_pi_target, log_pi_behavior, values, rewards, terminateds, truncateds=None,
-                   gamma=0.99, rho_bar=1.0, c_bar=1.0, bootstrap_values=None, last_value=None):
-    """V-trace (targets, advantages) (rl-triton API reference, compute_vtrace)."""
+                   gamma=0.99, rho_bar=1.0, c_bar=1.0, bootstrap_values=None, last_value=None,
+                   out_dtype=None):
+    """V-trace (targets, advantages) (rl-triton API reference, compute_vtrace).
+    bfloat16 rewards select compact storage: the log-probabilities, values
+    and bootstrap_values bfloat16 too, flags uint8 or bool, last_value
+    float32; ``out_dtype`` (float32 by default, or bfloat16) sets the output
+    type."""
+    if isinstance(rewards, torch.Tensor) and rewards.dtype == torch.bfloat16:
+        out_dtype = out_dtype or torch.float32
+        if out_dtype not in _OUT_DTYPES:
+            raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
+        c = _Call("rewards", rewards, _BF16)
+        for name, t in (("log_pi_target", log_pi_target), ("log_pi_behavior", log_pi_behavior),
+                        ("values", values)):
+            c.mat(name, t, dtypes=_BF16)
+        c.mat("terminateds", terminateds, dtypes=_FLAG8)
+        c.mat("truncateds", truncateds, False, _FLAG8)
+        c.mat("bootstrap_values", bootstrap_values, False, _BF16)
+        c.vec("last_value", last_value)
+        if last_value is not None and bootstrap_values is not None:
+            raise ValueError("pass either last_value or bootstrap_values, not both")
+        if bootstrap_values is not None and truncateds is None:
+            raise ValueError("compact storage: the window bootstrap is last_value (float32 [N])")
+        vs, adv = c.finish(2, out_dtype)
+        ws, wsn, s = _ws_for(c)
+        _native.check(_native.lib().rlscan_vtrace_compact(
+            c.m("log_pi_target"), c.m("log_pi_behavior"), c.m("values"), c.m("rewards"),
+            c.m("terminateds"), c.m("truncateds"), c.m("bootstrap_values"), c.v("last_value"),
+            c.N, c.T, c.rs, float(gamma), float(rho_bar), float(c_bar), _OUT_DTYPES[out_dtype],
+            _vp(vs), _vp(adv), ws, wsn, s), "rlscan_vtrace_compact")
+        return vs, adv
+    if out_dtype not in (None, torch.float32):
+        raise ValueError("bfloat16 outputs need compact (bfloat16) inputs")
     c = _Call("rewards", rewards)
     c.mat("log_pi_target", log_pi_target)
     c.mat("log_pi_behavior", log_pi_behavior)
@@ -429,10 +460,33 @@ def compute_retrace(action_probs_target, action_probs_behavior, q_values, next_q
 
 def compute_retrace_from_probs(pi_taken, mu_taken, q_values, expected_next_q, rewards,
                                terminateds, truncateds=None, gamma=0.99, lambda_=1.0, c_bar=1.0,
-                               rho_bar=1.0):
+                               rho_bar=1.0, out_dtype=None):
     """Retrace(lambda) (targets, advantages) from per-step inputs:
     pi(a_t|s_t), mu(a_t|s_t), Q(s_t,a_t), E_pi[Q(s_{t+1},.)] (rl-triton API
-    reference, compute_retrace, after its action-dimension reduction)."""
+    reference, compute_retrace, after its action-dimension reduction).
+    bfloat16 rewards select compact storage: the other value inputs
+    bfloat16 too, flags uint8 or bool; ``out_dtype`` (float32 by default, or
+    bfloat16) sets the output type."""
+    if isinstance(rewards, torch.Tensor) and rewards.dtype == torch.bfloat16:
+        out_dtype = out_dtype or torch.float32
+        if out_dtype not in _OUT_DTYPES:
+            raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
+        c = _Call("rewards", rewards, _BF16)
+        for name, t in (("pi_taken", pi_taken), ("mu_taken", mu_taken), ("q_values", q_values),
+                        ("expected_next_q", expected_next_q)):
+            c.mat(name, t, dtypes=_BF16)
+        c.mat("terminateds", terminateds, dtypes=_FLAG8)
+        c.mat("truncateds", truncateds, False, _FLAG8)
+        qret, adv = c.finish(2, out_dtype)
+        ws, wsn, s = _ws_for(c)
+        _native.check(_native.lib().rlscan_retrace_compact(
+            c.m("pi_taken"), c.m("mu_taken"), c.m("q_values"), c.m("expected_next_q"),
+            c.m("rewards"), c.m("terminateds"), c.m("truncateds"), c.N, c.T, c.rs,
+            float(gamma), float(lambda_), float(c_bar), float(rho_bar), _OUT_DTYPES[out_dtype],
+            _vp(qret), _vp(adv), ws, wsn, s), "rlscan_retrace_compact")
+        return qret, adv
+    if out_dtype not in (None, torch.float32):
+        raise ValueError("bfloat16 outputs need compact (bfloat16) inputs")
     c = _Call("rewards", rewards)
     for name, t in (("pi_taken", pi_taken), ("mu_taken", mu_taken), ("q_values", q_values),
                     ("expected_next_q", expected_next_q), ("rewards", rewards),

@@ -145,6 +145,7 @@ template <bool TRUNC, bool BS2D>
 struct VTrace {
     static_assert(TRUNC || !BS2D, "2-D bootstrap is read only with truncation flags");
     static constexpr int NIN = 5 + TRUNC + BS2D, NOUT = 2;
+    static constexpr unsigned FLAGS = (1u << 4) | (TRUNC ? (1u << 5) : 0u);  // 0/1 inputs
     static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = false, ROWSCALAR = !BS2D;
     static constexpr unsigned HALO = 1u << 2;
@@ -215,6 +216,7 @@ struct VTrace {
 template <bool TRUNC>
 struct Retrace {
     static constexpr int NIN = 6 + TRUNC, NOUT = 2;
+    static constexpr unsigned FLAGS = (1u << 5) | (TRUNC ? (1u << 6) : 0u);  // 0/1 inputs
     static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = false, ROWSCALAR = false;
     static constexpr unsigned HALO = (1u << 0) | (1u << 1) | (1u << 2);

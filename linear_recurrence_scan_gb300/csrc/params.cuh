@@ -88,6 +88,10 @@ rlscan_status launch_gae_compact(bool trunc, bool bs2d, bool bf16_out, Params p,
 rlscan_status launch_gae_returns_compact(bool trunc, bool bs2d, bool bf16_out, Params p, void *ws, size_t ws_bytes,
                                          cudaStream_t s);
 rlscan_status launch_vtrace(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
+rlscan_status launch_vtrace_compact(bool trunc, bool bs2d, bool bf16_out, Params p, void *ws, size_t ws_bytes,
+                                    cudaStream_t s);
+rlscan_status launch_retrace_compact(bool trunc, bool bf16_out, Params p, void *ws, size_t ws_bytes,
+                                     cudaStream_t s);
 rlscan_status launch_retrace(bool trunc, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_retrace_actions(bool trunc, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_lambda_returns(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);

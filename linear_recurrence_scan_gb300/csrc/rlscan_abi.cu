@@ -515,6 +515,82 @@ RLSCAN_API rlscan_status rlscan_gae_returns_compact(const void *rewards, const v
                                       p, ws, ws_bytes, cs(stream));
 }
 
+RLSCAN_API rlscan_status rlscan_vtrace_compact(const void *log_pi_target, const void *log_pi_behavior,
+                                               const void *values, const void *rewards, const void *terminateds,
+                                               const void *truncateds, const void *bootstrap_values,
+                                               const float *last_value, int64_t N, int64_t T, int64_t row_stride,
+                                               float gamma, float rho_bar, float c_bar, rlscan_dtype out_dtype,
+                                               void *vtrace_targets, void *vtrace_advantages, void *ws,
+                                               size_t ws_bytes, rlscan_stream_t stream)
+{
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (out_dtype != RLSCAN_F32 && out_dtype != RLSCAN_BF16) return RLSCAN_ERR_ARG_VALUE;
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!log_pi_target || !log_pi_behavior || !values || !rewards || !terminateds || !vtrace_targets ||
+        !vtrace_advantages)
+        return RLSCAN_ERR_NULL;
+    if (bootstrap_values && last_value) return RLSCAN_ERR_ARG_CONFLICT;
+    if (bootstrap_values && !truncateds) return RLSCAN_ERR_ARG_CONFLICT;  // window bootstrap: last_value
+    for (const void *o : {vtrace_targets, vtrace_advantages})
+        if (same_as_any(o, {log_pi_target, log_pi_behavior, values, rewards, terminateds, truncateds,
+                            bootstrap_values, last_value}))
+            return RLSCAN_ERR_ARG_CONFLICT;
+    if (vtrace_targets == vtrace_advantages) return RLSCAN_ERR_ARG_CONFLICT;
+    Params p = base_params(N, T, row_stride);
+    p.c0 = gamma;
+    p.c1 = rho_bar;
+    p.c2 = c_bar;
+    p.out[0] = static_cast<float *>(vtrace_targets);
+    p.out[1] = static_cast<float *>(vtrace_advantages);
+    p.in[0] = static_cast<const float *>(log_pi_target);
+    p.in[1] = static_cast<const float *>(log_pi_behavior);
+    p.in[2] = static_cast<const float *>(values);
+    p.in[3] = static_cast<const float *>(rewards);
+    p.in[4] = static_cast<const float *>(terminateds);
+    p.rowscalar = last_value;
+    if (truncateds) {
+        p.in[5] = static_cast<const float *>(truncateds);
+        p.in[6] = static_cast<const float *>(bootstrap_values);
+    }
+    return launch_vtrace_compact(truncateds != nullptr, bootstrap_values != nullptr, out_dtype == RLSCAN_BF16, p, ws,
+                                 ws_bytes, cs(stream));
+}
+
+RLSCAN_API rlscan_status rlscan_retrace_compact(const void *pi_taken, const void *mu_taken, const void *q_values,
+                                                const void *expected_next_q, const void *rewards,
+                                                const void *terminateds, const void *truncateds, int64_t N,
+                                                int64_t T, int64_t row_stride, float gamma, float lambda,
+                                                float c_bar, float rho_bar, rlscan_dtype out_dtype,
+                                                void *retrace_targets, void *advantages, void *ws, size_t ws_bytes,
+                                                rlscan_stream_t stream)
+{
+    RLSCAN_TRY(check_shape(N, T, row_stride));
+    if (out_dtype != RLSCAN_F32 && out_dtype != RLSCAN_BF16) return RLSCAN_ERR_ARG_VALUE;
+    if (N == 0 || T == 0) return RLSCAN_OK;
+    if (!pi_taken || !mu_taken || !q_values || !expected_next_q || !rewards || !terminateds || !retrace_targets ||
+        !advantages)
+        return RLSCAN_ERR_NULL;
+    for (const void *o : {retrace_targets, advantages})
+        if (same_as_any(o, {pi_taken, mu_taken, q_values, expected_next_q, rewards, terminateds, truncateds}))
+            return RLSCAN_ERR_ARG_CONFLICT;
+    if (retrace_targets == advantages) return RLSCAN_ERR_ARG_CONFLICT;
+    Params p = base_params(N, T, row_stride);
+    p.c0 = gamma;
+    p.c1 = lambda;
+    p.c2 = c_bar;
+    p.c3 = rho_bar;
+    p.out[0] = static_cast<float *>(retrace_targets);
+    p.out[1] = static_cast<float *>(advantages);
+    p.in[0] = static_cast<const float *>(pi_taken);
+    p.in[1] = static_cast<const float *>(mu_taken);
+    p.in[2] = static_cast<const float *>(q_values);
+    p.in[3] = static_cast<const float *>(expected_next_q);
+    p.in[4] = static_cast<const float *>(rewards);
+    p.in[5] = static_cast<const float *>(terminateds);
+    p.in[6] = static_cast<const float *>(truncateds);
+    return launch_retrace_compact(truncateds != nullptr, out_dtype == RLSCAN_BF16, p, ws, ws_bytes, cs(stream));
+}
+
 RLSCAN_API rlscan_status rlscan_vtrace(const float *log_pi_target, const float *log_pi_behavior,
                             const float *values, const float *rewards, const float *terminateds,
                             const float *truncateds, const float *bootstrap_values,

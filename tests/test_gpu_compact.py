@@ -124,3 +124,89 @@ def test_compact_rejects_mixed_storage():
         L().compute_gae(place(bf["rewards"], None), place(bf["values"], None),
                         place(fl["terminateds"], None), None, 0.99, 0.95,
                         place(bf["values"], None), None)
+
+
+def _bf(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16)
+
+
+def _u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(torch.uint8)
+
+
+OFF_SHAPES = [(8, 128, None), (5, 37, None), (4096, 1024, None), (3, 5000, None), (64, 1 << 16, None),
+              (5, 96, 112)]
+OFF_IDS = [f"{n}x{t}" + (f"_rs{rs}" if rs else "") for n, t, rs in OFF_SHAPES]
+
+
+@pytest.mark.parametrize("variant", ["last_value", "trunc_bs"])
+@pytest.mark.parametrize("shape", OFF_SHAPES, ids=OFF_IDS)
+def test_compact_vtrace(shape, variant):
+    """bf16 log-probabilities, values, rewards and bootstrap values, u8 flags;
+    the oracle runs on the decoded inputs."""
+    N, T, rs = shape
+    trunc = variant == "trunc_bs"
+    b = synthetic.vtrace_batch(N, T, 13 + T, 72, 0.01, 0.01 if trunc else 0.0, "2d" if trunc else "last")
+    vals = {k: _bf(b[k]) for k in ("log_pi_target", "log_pi_behavior", "values", "rewards")}
+    if trunc:
+        vals["bootstrap_values"] = _bf(b["bootstrap_values"])
+    fl = {"terminateds": _u8(b["terminateds"])}
+    if trunc:
+        fl["truncateds"] = _u8(b["truncateds"])
+    last = None if trunc else torch.from_numpy(b["last_value"])
+    dec = {k: v.float().numpy() for k, v in {**vals, **fl}.items()}
+    vs_ref, adv_ref = oracle.vtrace(dec["log_pi_target"], dec["log_pi_behavior"], dec["values"], dec["rewards"],
+                                    dec["terminateds"], dec.get("truncateds"), 0.99, 1.0, 1.0,
+                                    dec.get("bootstrap_values"), None if last is None else last.numpy())
+    args = [place(vals[k], rs) for k in ("log_pi_target", "log_pi_behavior", "values", "rewards")]
+    args += [place(fl["terminateds"], rs), place(fl.get("truncateds"), rs), 0.99, 1.0, 1.0,
+             place(vals.get("bootstrap_values"), rs), place(last, None)]
+    vs32, adv32 = L().compute_vtrace(*args)
+    assert vs32.dtype == torch.float32
+    assert_close(vs32, vs_ref, f"compact vtrace targets {variant}", False)
+    assert_close(adv32, adv_ref, f"compact vtrace advantages {variant}", False)
+    vs16, adv16 = L().compute_vtrace(*args, out_dtype=torch.bfloat16)
+    assert vs16.dtype == torch.bfloat16
+    assert_close(vs16, vs_ref, f"compact vtrace targets {variant} (bf16 out)", True)
+    assert_close(adv16, adv_ref, f"compact vtrace advantages {variant} (bf16 out)", True)
+    assert torch.equal(vs16.view(torch.int16), vs32.to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(adv16.view(torch.int16), adv32.to(torch.bfloat16).view(torch.int16))
+
+
+@pytest.mark.parametrize("variant", ["plain", "trunc"])
+@pytest.mark.parametrize("shape", OFF_SHAPES, ids=OFF_IDS)
+def test_compact_retrace(shape, variant):
+    """bf16 probabilities, Q-values and rewards, u8 flags."""
+    N, T, rs = shape
+    trunc = variant == "trunc"
+    b = synthetic.retrace_batch(N, T, 14 + T, 73, 0.01, 0.01 if trunc else 0.0)
+    vals = {k: _bf(b[k]) for k in ("pi_taken", "mu_taken", "q_values", "expected_next_q", "rewards")}
+    fl = {"terminateds": _u8(b["terminateds"])}
+    if trunc:
+        fl["truncateds"] = _u8(b["truncateds"])
+    dec = {k: v.float().numpy() for k, v in {**vals, **fl}.items()}
+    q_ref, adv_ref = oracle.retrace(dec["pi_taken"], dec["mu_taken"], dec["q_values"], dec["expected_next_q"],
+                                    dec["rewards"], dec["terminateds"], dec.get("truncateds"), 0.99, 0.95, 1.0, 1.0)
+    args = [place(vals[k], rs) for k in ("pi_taken", "mu_taken", "q_values", "expected_next_q", "rewards")]
+    args += [place(fl["terminateds"], rs), place(fl.get("truncateds"), rs), 0.99, 0.95, 1.0, 1.0]
+    q32, adv32 = L().compute_retrace_from_probs(*args)
+    assert_close(q32, q_ref, f"compact retrace targets {variant}", False)
+    assert_close(adv32, adv_ref, f"compact retrace advantages {variant}", False)
+    q16, adv16 = L().compute_retrace_from_probs(*args, out_dtype=torch.bfloat16)
+    assert_close(q16, q_ref, f"compact retrace targets {variant} (bf16 out)", True)
+    assert_close(adv16, adv_ref, f"compact retrace advantages {variant} (bf16 out)", True)
+    assert torch.equal(q16.view(torch.int16), q32.to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(adv16.view(torch.int16), adv32.to(torch.bfloat16).view(torch.int16))
+
+
+def test_compact_offpolicy_rejects_mixed_storage():
+    b = synthetic.vtrace_batch(4, 64, 3, 74, 0.01, 0.01, "2d")
+    lpt, lpb, v, r = (_bf(b[k]).to(DEV) for k in ("log_pi_target", "log_pi_behavior", "values", "rewards"))
+    term, trunc = _u8(b["terminateds"]).to(DEV), _u8(b["truncateds"]).to(DEV)
+    with pytest.raises(TypeError):
+        L().compute_vtrace(lpt, lpb, v.float(), r, term, trunc)
+    with pytest.raises(ValueError):  # 2-D bootstrap without truncation flags
+        L().compute_vtrace(lpt, lpb, v, r, term, None, bootstrap_values=_bf(b["bootstrap_values"]).to(DEV))
+    with pytest.raises(ValueError):  # bf16 outputs from float32 inputs
+        L().compute_retrace_from_probs(*(torch.ones(2, 8, device=DEV) for _ in range(6)),
+                                       out_dtype=torch.bfloat16)
