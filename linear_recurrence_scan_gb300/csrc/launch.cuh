@@ -92,15 +92,18 @@ struct Shape {
         return n;
     }
     static constexpr int BYTES_PER_STEP = in_sum() + IoOf<E>::OUT * E::NOUT;
-    static constexpr int TILE_RAW = RLSCAN_TILE_BYTES_TARGET / BYTES_PER_STEP;
+    // compact storage sizes its tile as if its outputs were bfloat16 either
+    // way, so float32 and bfloat16 outputs come from the same arithmetic (the
+    // bfloat16 ones are the float32 ones rounded)
+    static constexpr int SHAPE_BYTES = IoOf<E>::LOWP ? in_sum() + 2 * E::NOUT : BYTES_PER_STEP;
+    static constexpr int TILE_RAW = RLSCAN_TILE_BYTES_TARGET / SHAPE_BYTES;
     // compact storage moves few bytes per step: cap at 2048 (8 steps per
-    // thread) so the register budget of three CTAs per SM holds, and at 1024
-    // (4 steps) for estimators with four or more inputs, whose per-step
-    // registers would otherwise spill
+    // thread; estimators with four or more inputs then run two CTAs per SM,
+    // whose register budget holds their 8 steps)
     static constexpr int TILE_BY_BYTES = TILE_RAW >= 3072 ? 4096 : (TILE_RAW >= 1536 ? 2048 : 1024);
-    static constexpr int LOWP_CAP = E::NIN >= 4 ? 1024 : RLSCAN_LOWP_TILE_CAP;
     static constexpr int TILE = WIDE ? WideTileOf<E>::value
-                                     : ((IoOf<E>::LOWP && TILE_BY_BYTES > LOWP_CAP) ? LOWP_CAP : TILE_BY_BYTES);
+                                     : ((IoOf<E>::LOWP && TILE_BY_BYTES > RLSCAN_LOWP_TILE_CAP)
+                                            ? RLSCAN_LOWP_TILE_CAP : TILE_BY_BYTES);
     static constexpr int THREADS = WIDE ? (TILE < 1024 ? 128 : RLSCAN_WIDE_THREADS)
                                         : (TILE >= 4096 ? 256 : (TILE >= 2048 ? RLSCAN_THREADS_2048 : RLSCAN_THREADS_1024));
     static constexpr int ITEMS = TILE / THREADS;

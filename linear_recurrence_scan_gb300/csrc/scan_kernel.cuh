@@ -530,7 +530,9 @@ constexpr int block_threads() { return THREADS + 32; }
 #endif
 // Two scans need more registers: three CTAs per SM at four steps per
 // thread, two at eight (four for a small 128-thread CTA); two CTAs per SM is
-// the most the wide stages leave room for.
+// the most the wide stages leave room for, and what compact-storage
+// estimators with four or more inputs get at eight steps per thread
+// (their staged inputs unpack into many registers).
 #ifndef RLSCAN_K2_SHORT_BLOCKS
 #define RLSCAN_K2_SHORT_BLOCKS 3
 #endif
@@ -546,7 +548,7 @@ template <class E, bool DEFER, int THREADS, int ITEMS>
 constexpr int min_blocks()
 {
     return (DEFER && RLSCAN_DEFER_MIN_BLOCKS > 0) ? RLSCAN_DEFER_MIN_BLOCKS
-           : (WideOf<E>::NWIDE > 0) ? 2
+           : (WideOf<E>::NWIDE > 0 || (IoOf<E>::LOWP && E::NIN >= 4 && ITEMS >= 8)) ? 2
            : (E::K > 1) ? (ITEMS <= 4 ? RLSCAN_K2_SHORT_BLOCKS : (THREADS <= 128 && !DEFER ? 4 : 2))
            : RLSCAN_MIN_BLOCKS;
 }
