@@ -259,6 +259,24 @@ rlscan_status rlscan_gae_normalized(const float *rewards, const float *values,
                                     rlscan_stream_t stream);
 
 /*
+ * Bounds-check diagnostics (no counterpart on the pages).  A library built
+ * with RLSCAN_CHECK_BOUNDS=1 tests every global access of its scan kernels,
+ * and every bulk copy's source and shared-memory destination, against the
+ * extent of the argument it belongs to; a failed test skips the access and
+ * counts one violation.  rlscan_bounds_check synchronises the device, then
+ * stores the count and the site code of the first violation (1 copy source,
+ * 2 copy target, 3 element-wise load, 4 output store, 5 per-row scalar,
+ * 6 look-back state, 7 wide input, 8 moments slot, 9 ring stage); reset != 0
+ * zeroes them.  Returns 1 in a checked build, 0 in a normal build (nothing
+ * is checked; both values 0), -1 on a CUDA error.
+ * Positive control (checked build only): with the environment variable
+ * RLSCAN_TEST_CHECK_SHORT=1 every [N,T] argument is checked as if it held
+ * N-1 rows, so the accesses to the last row (all inside the real arrays)
+ * must be reported; their outputs are then not written.
+ */
+int rlscan_bounds_check(unsigned long long *violations, unsigned long long *first_site, int reset);
+
+/*
  * GAE and fused GAE + returns on compact storage: rewards, values and
  * bootstrap_values in bfloat16, terminateds and truncateds in uint8 (0/1),
  * outputs in float32 or bfloat16 (out_dtype).  rl-triton paper Sec. 9.3

@@ -11,7 +11,8 @@ import os
 import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "_build", "librlscan.so")
+# RLSCAN_LIB selects another build of the library (e.g. the checked build)
+LIB_PATH = os.environ.get("RLSCAN_LIB") or os.path.join(HERE, "_build", "librlscan.so")
 
 STATUS = {
     0: "RLSCAN_OK", 1: "RLSCAN_ERR_NULL", 2: "RLSCAN_ERR_SHAPE", 3: "RLSCAN_ERR_ARG_CONFLICT",
@@ -43,6 +44,7 @@ _I = ctypes.c_int
 SIGNATURES = {
     "rlscan_version": ([], _I),
     "rlscan_status_string": ([_I], ctypes.c_char_p),
+    "rlscan_bounds_check": ([_P, _P, _I], _I),
     "rlscan_workspace_bytes": ([_I64, _I64], _SZ),
     "rlscan_workspace_init": ([_P, _SZ, _P], _I),
     "rlscan_workspace_status": ([_P, _SZ, _P], _I),

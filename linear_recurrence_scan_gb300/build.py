@@ -47,18 +47,23 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link the library; returns its path.  Rebuilds only when a
-    source or header is newer than the library (or ``force``)."""
+CHECKED_DIR = os.path.join(OUT_DIR, "checked")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: str = OUT_DIR) -> str:
+    """Compile and link the library into ``out_dir``; returns its path.
+    Rebuilds only when a source or header is newer than the library (or
+    ``force``)."""
+    lib_path = os.path.join(out_dir, "librlscan.so")
     srcs = _sources()
     deps = srcs + _headers() + [os.path.abspath(__file__)]
-    if not force and not _stale(LIB, deps):
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+    if not force and not _stale(lib_path, deps):
+        return lib_path
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -69,13 +74,20 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib_path + ".tmp%d" % os.getpid()
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
+
+
+def build_checked(force: bool = False) -> str:
+    """The bounds-checked build (RLSCAN_CHECK_BOUNDS=1: every global access
+    and bulk copy of the scan kernels is tested against its argument's
+    extent, violations are counted and skipped), in its own directory."""
+    return build(force, extra_flags=("-DRLSCAN_CHECK_BOUNDS=1",), out_dir=CHECKED_DIR)
 
 
 if __name__ == "__main__":

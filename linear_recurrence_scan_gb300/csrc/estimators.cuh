@@ -32,6 +32,7 @@
 //       after the range (backward only; used for successor targets).
 #pragma once
 
+#include "checks.cuh"
 #include "params.cuh"
 #include "ptx.cuh"
 
@@ -342,7 +343,15 @@ struct RetraceActions : Retrace<TRUNC> {
                 const int64_t row = tg.row0 + i, t = tg.t0 + c;
                 pr = static_cast<const float *>(p.wide[0]) + row * p.wide_rs[0] + t * A;
                 nq = static_cast<const float *>(p.wide[1]) + row * p.wide_rs[1] + t * A;
-                a = __ldg(reinterpret_cast<const long long *>(p.wide[2]) + (row * p.wide_rs[2] >> 1) + t);
+                const long long *ap = reinterpret_cast<const long long *>(p.wide[2]) + (row * p.wide_rs[2] >> 1) + t;
+                if (!(span_ok(p, p.wide[0], wide_extent(p, 0), pr, 4u * A, kSiteWide) &&
+                      span_ok(p, p.wide[1], wide_extent(p, 1), nq, 4u * A, kSiteWide) &&
+                      span_ok(p, p.wide[2], wide_extent(p, 2), ap, 8, kSiteWide))) {
+                    ev[k] = 0.f;
+                    pv[k] = nan;
+                    continue;
+                }
+                a = __ldg(ap);
             }
             float eq = 0.f;
             for (int q = 0; q < A; ++q) eq = fmaf(pr[q], nq[q], eq);

@@ -228,6 +228,8 @@ rlscan_status bind_io(Params &p, bool *tma_out)
     p.spin_limit_ns = spin_limit_ns();
     p.copy_limit_ns = 2000000000ull;  // bulk copies land in microseconds; never cut short
     p.withhold_tile = withhold_tile();
+    p.bounds = bounds_counter();
+    p.check_rows = p.N - (check_short() ? 1 : 0);
     *tma_out = tma;
     return RLSCAN_OK;
 }

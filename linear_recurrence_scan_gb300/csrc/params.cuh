@@ -73,6 +73,12 @@ struct Params {
 
     // batch moments of output 0 (estimators that declare MOMENTS)
     float *mom_part;              // [gridDim.x][4] per-CTA sum and sum of squares, each a float pair
+
+    // checked builds only: violations counted and the first site (else NULL),
+    // and the rows the checks take each [N,T] array to span (N; fewer under
+    // the RLSCAN_TEST_CHECK_SHORT test hook, which must then be reported)
+    unsigned long long *bounds;
+    int64_t check_rows;
 };
 
 // Launchers (one translation unit per estimator family).
@@ -104,5 +110,8 @@ rlscan_status launch_linear(bool forward, Params p, void *ws, size_t ws_bytes, c
 uint64_t spin_limit_ns();
 int64_t withhold_tile();  // RLSCAN_TEST_WITHHOLD_TILE, -1 when unset
 bool pdl_enabled();  // programmatic dependent launch (RLSCAN_PDL=0 disables)
+// checked builds: the device counter of bounds violations (NULL otherwise)
+unsigned long long *bounds_counter();
+bool check_short();  // RLSCAN_TEST_CHECK_SHORT=1 in a checked build
 
 }  // namespace rlscan

@@ -15,6 +15,44 @@
 
 namespace rlscan {
 
+#ifndef RLSCAN_CHECK_BOUNDS
+#define RLSCAN_CHECK_BOUNDS 0
+#endif
+
+// Checked builds: one device counter per process (violations, first site),
+// allocated and zeroed at first use; normal builds have none.
+unsigned long long *bounds_counter()
+{
+#if RLSCAN_CHECK_BOUNDS
+    static unsigned long long *counter = [] {
+        unsigned long long *c = nullptr;
+        if (cudaMalloc(&c, 2 * sizeof(unsigned long long)) != cudaSuccess ||
+            cudaMemset(c, 0, 2 * sizeof(unsigned long long)) != cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess) {
+            cudaGetLastError();
+            return static_cast<unsigned long long *>(nullptr);
+        }
+        return c;
+    }();
+    return counter;
+#else
+    return nullptr;
+#endif
+}
+
+bool check_short()
+{
+#if RLSCAN_CHECK_BOUNDS
+    static const bool on = [] {
+        const char *s = std::getenv("RLSCAN_TEST_CHECK_SHORT");
+        return s != nullptr && s[0] == '1';
+    }();
+    return on;
+#else
+    return false;
+#endif
+}
+
 uint64_t spin_limit_ns()
 {
     static const uint64_t limit = [] {
@@ -208,6 +246,26 @@ RLSCAN_API const char *rlscan_status_string(rlscan_status status)
     case RLSCAN_ERR_MEMORY: return "a pointer is in memory the GPU cannot reach (pageable host memory)";
     }
     return "unknown status";
+}
+
+RLSCAN_API int rlscan_bounds_check(unsigned long long *violations, unsigned long long *first_site, int reset)
+{
+    if (violations != nullptr) *violations = 0;
+    if (first_site != nullptr) *first_site = 0;
+    unsigned long long *c = bounds_counter();
+    if (c == nullptr) return 0;
+    unsigned long long h[2] = {0, 0};
+    if (cudaDeviceSynchronize() != cudaSuccess || cudaMemcpy(h, c, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    if (violations != nullptr) *violations = h[0];
+    if (first_site != nullptr) *first_site = h[1];
+    if (reset && (cudaMemset(c, 0, sizeof(h)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)) {
+        cudaGetLastError();
+        return -1;
+    }
+    return 1;
 }
 
 RLSCAN_API size_t rlscan_workspace_bytes(int64_t N, int64_t T)

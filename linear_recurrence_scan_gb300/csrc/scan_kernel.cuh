@@ -60,6 +60,7 @@
 #include "dfloat.cuh"
 #include "estimators.cuh"
 #include "params.cuh"
+#include "checks.cuh"
 #include "ptx.cuh"
 
 namespace rlscan {
@@ -246,91 +247,94 @@ __device__ __forceinline__ TileGeo decode_tile(const Params &p, int64_t g)
 // (TILE + 4) * words floats: step e of the tile at e * words, the step after
 // the tile right behind the last one.
 template <class E, int TILE, int AST>
-__device__ void issue_tile_copies(const Params &p, const TileGeo &tg, float *stage, uint64_t *bar)
+__device__ void issue_tile_copies(const Params &p, const TileGeo &tg, float *stage, uint64_t *bar,
+                                  const float *smem_base)
 {
     constexpr int NW = WideOf<E>::NWIDE;
     constexpr unsigned DER = WideOf<E>::DERIVED;
     const bool wide = NW > 0 && p.wide_staged;
     float *wsm = stage + narrow_copied<E>() * AST;
-    if (p.packed) {
-        bool contig = p.rs == p.T && p.C == p.T;  // rows contiguous in global and in shared memory
+    // every copy of the tile as (shared destination, global source, bytes,
+    // the source array's base and extent), in issue order
+    uint32_t bytes = 0;
+    auto each = [&](auto &&f) {
+        if (p.packed) {
+            bool contig = p.rs == p.T && p.C == p.T;  // rows contiguous in global and in shared memory
 #pragma unroll
-        for (int w = 0; w < NW; ++w) contig = contig && (!wide || p.wide_rs[w] == p.T * p.wide_words[w]);
-        const int copies = contig ? 1 : tg.nrows;
-        const int64_t steps = contig ? static_cast<int64_t>(tg.nrows) * p.T : p.T;
-        const uint32_t nb = static_cast<uint32_t>(steps * 4);
-        uint32_t bytes = 0;
+            for (int w = 0; w < NW; ++w) contig = contig && (!wide || p.wide_rs[w] == p.T * p.wide_words[w]);
+            const int copies = contig ? 1 : tg.nrows;
+            const int64_t steps = contig ? static_cast<int64_t>(tg.nrows) * p.T : p.T;
+            const uint32_t nb = static_cast<uint32_t>(steps * 4);
+            for (int i = 0; i < copies; ++i) {
 #pragma unroll
-        for (int j = 0; j < E::NIN; ++j)
-            if (!((DER >> j) & 1u)) bytes += static_cast<uint32_t>(steps * IoOf<E>::in(j));
+                for (int j = 0; j < E::NIN; ++j) {
+                    if (!((DER >> j) & 1u)) {
+                        const int eb = IoOf<E>::in(j);
+                        f(elem0<E, TILE>(stage, j) + static_cast<int64_t>(i) * p.C * eb,
+                          reinterpret_cast<const char *>(p.in[j]) + (tg.row0 + i) * p.rs * eb,
+                          static_cast<uint32_t>(steps * eb), p.in[j], array_extent(p, eb));
+                    }
+                }
+                if (wide) {
+                    float *dst = wsm;
 #pragma unroll
-        for (int w = 0; w < NW; ++w)
-            if (wide) bytes += nb * static_cast<uint32_t>(p.wide_words[w]);
-        ptx::mbar_arrive_expect_tx(bar, bytes * static_cast<uint32_t>(copies));
-        for (int i = 0; i < copies; ++i) {
-#pragma unroll
-            for (int j = 0; j < E::NIN; ++j) {
-                if (!((DER >> j) & 1u)) {
-                    const int eb = IoOf<E>::in(j);
-                    ptx::bulk_g2s(elem0<E, TILE>(stage, j) + static_cast<int64_t>(i) * p.C * eb,
-                                  reinterpret_cast<const char *>(p.in[j]) + (tg.row0 + i) * p.rs * eb,
-                                  static_cast<uint32_t>(steps * eb), bar);
+                    for (int w = 0; w < NW; ++w) {
+                        const int W = p.wide_words[w];
+                        f(reinterpret_cast<char *>(dst + static_cast<int64_t>(i) * p.C * W),
+                          reinterpret_cast<const char *>(static_cast<const float *>(p.wide[w]) +
+                                                         (tg.row0 + i) * p.wide_rs[w]),
+                          nb * static_cast<uint32_t>(W), p.wide[w], wide_extent(p, w));
+                        dst += (TILE + 4) * W;
+                    }
                 }
             }
-            if (wide) {
-                float *dst = wsm;
+            return;
+        }
+        const int64_t base = tg.row0 * p.rs;
 #pragma unroll
-                for (int w = 0; w < NW; ++w) {
-                    const int W = p.wide_words[w];
-                    ptx::bulk_g2s(dst + static_cast<int64_t>(i) * p.C * W,
-                                  static_cast<const float *>(p.wide[w]) + (tg.row0 + i) * p.wide_rs[w],
-                                  nb * static_cast<uint32_t>(W), bar);
-                    dst += (TILE + 4) * W;
-                }
+        for (int j = 0; j < E::NIN; ++j) {
+            const int halo = 16 / IoOf<E>::in(j);  // steps in 16 bytes
+            int64_t lo = tg.t0, hi = tg.t0 + tg.len;
+            if ((E::HALO >> j) & 1u) {
+                if (!E::FWD && hi < p.T) hi += halo;   // next step (T a multiple of halo keeps it in the row)
+                if (E::FWD && lo > 0) lo -= halo;      // previous step
+            }
+            if (!((DER >> j) & 1u)) {
+                const int eb = IoOf<E>::in(j);
+                f(elem0<E, TILE>(stage, j) + (lo - tg.t0) * eb,
+                  reinterpret_cast<const char *>(p.in[j]) + (base + lo) * eb, static_cast<uint32_t>((hi - lo) * eb),
+                  p.in[j], array_extent(p, eb));
             }
         }
+        if (wide) {
+            // wide arrays: the tile and, backward, the four steps after it
+            const int64_t whi = (!E::FWD && tg.t0 + tg.len < p.T) ? tg.t0 + tg.len + 4 : tg.t0 + tg.len;
+            float *dst = wsm;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const int W = p.wide_words[w];
+                f(reinterpret_cast<char *>(dst),
+                  reinterpret_cast<const char *>(static_cast<const float *>(p.wide[w]) + tg.row0 * p.wide_rs[w] +
+                                                 tg.t0 * W),
+                  static_cast<uint32_t>((whi - tg.t0) * 4 * W), p.wide[w], wide_extent(p, w));
+                dst += (TILE + 4) * W;
+            }
+        }
+    };
+    bool ok = true;
+    each([&](char *dst, const char *src, uint32_t n, const void *base, uint64_t extent) {
+        bytes += n;
+        if constexpr (RLSCAN_CHECK_BOUNDS) {
+            const bool src_ok = span_ok(p, base, extent, src, n, kSiteCopySource);
+            ok = smem_ok(p, smem_base, dst, n, kSiteCopyTarget) && src_ok && ok;
+        }
+    });
+    if (!ok) {  // checked build: no copy of this tile is issued; the phase completes without data
+        ptx::mbar_arrive(bar);
         return;
     }
-    const int64_t base = tg.row0 * p.rs;
-    int64_t lo[E::NIN], hi[E::NIN];
-    uint32_t bytes = 0;
-#pragma unroll
-    for (int j = 0; j < E::NIN; ++j) {
-        const int halo = 16 / IoOf<E>::in(j);  // steps in 16 bytes
-        lo[j] = tg.t0;
-        hi[j] = tg.t0 + tg.len;
-        if ((E::HALO >> j) & 1u) {
-            if (!E::FWD && hi[j] < p.T) hi[j] += halo;   // next step (T a multiple of halo keeps it in the row)
-            if (E::FWD && lo[j] > 0) lo[j] -= halo;      // previous step
-        }
-        if (!((DER >> j) & 1u)) bytes += static_cast<uint32_t>((hi[j] - lo[j]) * IoOf<E>::in(j));
-    }
-    // wide arrays: the tile and, backward, the four steps after it
-    const int64_t whi = (!E::FWD && tg.t0 + tg.len < p.T) ? tg.t0 + tg.len + 4 : tg.t0 + tg.len;
-    if (wide) {
-#pragma unroll
-        for (int w = 0; w < NW; ++w) bytes += static_cast<uint32_t>((whi - tg.t0) * 4 * p.wide_words[w]);
-    }
     ptx::mbar_arrive_expect_tx(bar, bytes);
-#pragma unroll
-    for (int j = 0; j < E::NIN; ++j) {
-        if (!((DER >> j) & 1u)) {
-            const int eb = IoOf<E>::in(j);
-            ptx::bulk_g2s(elem0<E, TILE>(stage, j) + (lo[j] - tg.t0) * eb,
-                          reinterpret_cast<const char *>(p.in[j]) + (base + lo[j]) * eb,
-                          static_cast<uint32_t>((hi[j] - lo[j]) * eb), bar);
-        }
-    }
-    if (wide) {
-        float *dst = wsm;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const int W = p.wide_words[w];
-            ptx::bulk_g2s(dst, static_cast<const float *>(p.wide[w]) + tg.row0 * p.wide_rs[w] + tg.t0 * W,
-                          static_cast<uint32_t>((whi - tg.t0) * 4 * W), bar);
-            dst += (TILE + 4) * W;
-        }
-    }
+    each([&](char *dst, const char *src, uint32_t n, const void *, uint64_t) { ptx::bulk_g2s(dst, src, n, bar); });
 }
 
 // Element e of array j's tile region (e = -1: the step before the tile,
@@ -341,6 +345,7 @@ __device__ __forceinline__ void load_elem(const Params &p, float *stage, int j, 
     const int eb = IoOf<E>::in(j);
     char *dst = elem0<E, TILE>(stage, j) + static_cast<int64_t>(e) * eb;
     const char *from = reinterpret_cast<const char *>(p.in[j]) + src * eb;
+    if (!span_ok(p, p.in[j], array_extent(p, eb), from, eb, kSiteElementLoad)) return;
     if (eb == 4) copy_elem<4>(dst, from);
     else if (eb == 2) copy_elem<2>(dst, from);
     else copy_elem<1>(dst, from);
@@ -394,11 +399,13 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, uint6
 // Publishing side (one thread per tile and scan): the tile's aggregate map
 // `total`, or directly its inclusive value when that does not depend on
 // anything before the tile (first tile of the row, or b == 0).
+template <int K>
 __device__ __forceinline__ void publish_first(const Params &p, uint32_t epoch, int64_t slot, int64_t g,
                                               int64_t j, Pair total)
 {
     if (g == p.withhold_tile) return;  // test hook: successors must time out
     unsigned long long *st = p.states;
+    if (!state_ok(p, 2 * slot + 1, K)) return;
     if (j == 0 || total.b == 0.f) {
         ptx::st_relaxed(&st[2 * slot], pack_word((epoch << 2) | kTagPrefix, total.a));
     } else {
@@ -407,10 +414,12 @@ __device__ __forceinline__ void publish_first(const Params &p, uint32_t epoch, i
     }
 }
 
+template <int K>
 __device__ __forceinline__ void publish_inclusive(const Params &p, uint32_t epoch, int64_t slot, int64_t g,
                                                   float v)
 {
     if (g == p.withhold_tile) return;
+    if (!state_ok(p, 2 * slot, K)) return;
     ptx::st_relaxed(&p.states[2 * slot], pack_word((epoch << 2) | kTagPrefix, v));
 }
 
@@ -435,6 +444,7 @@ __device__ inline float lookback_read(const Params &p, uint32_t epoch, int64_t g
     bool fresh = true;  // (w0, w1) hold a probe of tile k
     for (;;) {
         if (!fresh) {
+            if (!state_ok(p, 2 * (k * K + sc) + 1, K)) return __int_as_float(0x7fc00000);
             w0 = ptx::ld_relaxed(&st[2 * (k * K + sc)]);
             w1 = ptx::ld_relaxed(&st[2 * (k * K + sc) + 1]);
         }
@@ -636,7 +646,7 @@ scan_kernel(const __grid_constant__ Params p)
                 const TileGeo tg = decode_tile<FWD, TILE>(p, g);
                 s_geo[s] = tg;
                 ptx::mbar_arrive(&meta_bar[s]);  // the tile is known before its data lands
-                if (tma) issue_tile_copies<E, TILE, AST>(p, tg, smem + s * SST, &full_bar[s]);
+                if (tma) issue_tile_copies<E, TILE, AST>(p, tg, smem + s * SST, &full_bar[s], smem);
                 else ptx::mbar_arrive(&full_bar[s]);
             }
         }
@@ -654,7 +664,10 @@ scan_kernel(const __grid_constant__ Params p)
         if (tile_ids[s] >= p.num_tiles) return 0.f;
         const TileGeo tg = s_geo[s];
         if (thread_span<FWD, ITEMS>(p, tg, rit, col).kb < 0) return 0.f;
-        return __ldg(p.rowscalar + (tg.row0 + rit) * p.rowscalar_stride);
+        const float *rs_ptr = p.rowscalar + (tg.row0 + rit) * p.rowscalar_stride;
+        const uint64_t rs_ext = static_cast<uint64_t>((p.check_rows - 1) * p.rowscalar_stride + 1) * 4u;
+        if (!span_ok(p, p.rowscalar, rs_ext, rs_ptr, 4, kSiteRowScalar)) return 0.f;
+        return __ldg(rs_ptr);
     };
     constexpr bool kRowScalar = E::ROWSCALAR;
     const bool use_rsc = kRowScalar && p.rowscalar != nullptr;
@@ -791,25 +804,28 @@ scan_kernel(const __grid_constant__ Params p)
                                 uint2 w;
                                 w.x = *reinterpret_cast<const uint32_t *>(&lo2);
                                 w.y = *reinterpret_cast<const uint32_t *>(&hi2);
-                                *reinterpret_cast<uint2 *>(dst + k) = w;
+                                if (span_ok(p, p.out[q], array_extent(p, 2), dst + k, 8, kSiteStore))
+                                    *reinterpret_cast<uint2 *>(dst + k) = w;
                             }
                         }
                     } else {
 #pragma unroll
                         for (int k = 0; k < ITEMS; ++k)
-                            if (k < sp.kv) dst[k] = __float2bfloat16_rn(o[q][k]);
+                            if (k < sp.kv && span_ok(p, p.out[q], array_extent(p, 2), dst + k, 2, kSiteStore))
+                                dst[k] = __float2bfloat16_rn(o[q][k]);
                     }
                 } else if (vec) {
 #pragma unroll
                     for (int k = 0; k < ITEMS; k += 4) {
-                        if (k < sp.kv)
+                        if (k < sp.kv && span_ok(p, p.out[q], array_extent(p, 4), p.out[q] + off + k, 16, kSiteStore))
                             *reinterpret_cast<float4 *>(p.out[q] + off + k) =
                                 make_float4(o[q][k], o[q][k + 1], o[q][k + 2], o[q][k + 3]);
                     }
                 } else {
 #pragma unroll
                     for (int k = 0; k < ITEMS; ++k)
-                        if (k < sp.kv) p.out[q][off + k] = o[q][k];
+                        if (k < sp.kv && span_ok(p, p.out[q], array_extent(p, 4), p.out[q] + off + k, 4, kSiteStore))
+                            p.out[q][off + k] = o[q][k];
                 }
             }
         }
@@ -828,7 +844,7 @@ scan_kernel(const __grid_constant__ Params p)
 #pragma unroll
             for (int sc = 0; sc < K; ++sc)
                 if (total[sc].b != 0.f)
-                    publish_inclusive(p, epoch, g * K + sc, g, fmaf(total[sc].b, carry[sc], total[sc].a));
+                    publish_inclusive<K>(p, epoch, g * K + sc, g, fmaf(total[sc].b, carry[sc], total[sc].a));
         }
     };
 
@@ -866,8 +882,10 @@ scan_kernel(const __grid_constant__ Params p)
         const int64_t j = pg / p.N;
         if (j > 0 && lane < K) {
             const int64_t slot = (pg - p.N) * K + lane;
-            pw0 = ptx::ld_relaxed(&p.states[2 * slot]);
-            pw1 = ptx::ld_relaxed(&p.states[2 * slot + 1]);
+            if (state_ok(p, 2 * slot + 1, K)) {
+                pw0 = ptx::ld_relaxed(&p.states[2 * slot]);
+                pw1 = ptx::ld_relaxed(&p.states[2 * slot + 1]);
+            }
         }
     };
 
@@ -885,6 +903,7 @@ scan_kernel(const __grid_constant__ Params p)
         const TileGeo tg = s_geo[s];
         const float rsc = !use_rsc ? 0.f : (rsc_ready ? rsc_next : load_row_scalar(s));
         float *stage = smem + s * SST;
+        if constexpr (RLSCAN_CHECK_BOUNDS) smem_ok(p, smem, stage, static_cast<uint64_t>(SST) * 4u, kSiteRing);
         const bool chained = !p.packed && tg.j > 0;  // needs its predecessor's value
 
         // predecessor states for an immediate look-back (lane sc < K reads
@@ -892,8 +911,10 @@ scan_kernel(const __grid_constant__ Params p)
         unsigned long long cw0 = 0, cw1 = 0;
         if (!defer && chained && lane < K) {
             const int64_t slot = (g - p.N) * K + lane;
-            cw0 = ptx::ld_relaxed(&p.states[2 * slot]);
-            cw1 = ptx::ld_relaxed(&p.states[2 * slot + 1]);
+            if (state_ok(p, 2 * slot + 1, K)) {
+                cw0 = ptx::ld_relaxed(&p.states[2 * slot]);
+                cw1 = ptx::ld_relaxed(&p.states[2 * slot + 1]);
+            }
         }
 
         if (!tma) {
@@ -967,7 +988,7 @@ scan_kernel(const __grid_constant__ Params p)
         if (!p.packed && warp == PUB_WARP && lane == 0) {
 #pragma unroll
             for (int sc = 0; sc < K; ++sc)
-                publish_first(p, epoch, g * K + sc, g, tg.j, compose(wa[PUB_WARP][sc], we[sc]));
+                publish_first<K>(p, epoch, g * K + sc, g, tg.j, compose(wa[PUB_WARP][sc], we[sc]));
         }
 
         if (!defer) {
@@ -1022,8 +1043,10 @@ scan_kernel(const __grid_constant__ Params p)
                 cs = df_add(cs, s_mom[w2][0]);
                 cq = df_add(cq, s_mom[w2][1]);
             }
-            *reinterpret_cast<float4 *>(p.mom_part + 4 * static_cast<int64_t>(blockIdx.x)) =
-                make_float4(cs.hi, cs.lo, cq.hi, cq.lo);
+            if (span_ok(p, p.mom_part, kMomentBytes, p.mom_part + 4 * static_cast<int64_t>(blockIdx.x), 16,
+                        kSiteMoments))
+                *reinterpret_cast<float4 *>(p.mom_part + 4 * static_cast<int64_t>(blockIdx.x)) =
+                    make_float4(cs.hi, cs.lo, cq.hi, cq.lo);
         }
     }
 
