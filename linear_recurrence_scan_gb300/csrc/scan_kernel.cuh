@@ -859,8 +859,11 @@ scan_kernel(const __grid_constant__ Params p)
     float prsc = 0.f;
     Pair pex[K], pwe[K], ptot[K];
     unsigned long long pw0 = 0, pw1 = 0;
+    // the pending tile's geometry stays in s_geo[ps] (and its id in
+    // tile_ids[ps]) until its stage is released, as the producer rewrites
+    // them only for the slot's next use
     auto finish_pending = [&]() {
-        const TileGeo tg = decode_tile<FWD, TILE>(p, pg);
+        const TileGeo tg = s_geo[ps];
         float carry[K];
 #pragma unroll
         for (int sc = 0; sc < K; ++sc) carry[sc] = 0.f;
@@ -879,8 +882,7 @@ scan_kernel(const __grid_constant__ Params p)
         pend = false;
     };
     auto prefetch_pending = [&]() {  // first predecessor state of the pending tile
-        const int64_t j = pg / p.N;
-        if (j > 0 && lane < K) {
+        if (s_geo[ps].j > 0 && lane < K) {
             const int64_t slot = (pg - p.N) * K + lane;
             if (state_ok(p, 2 * slot + 1, K)) {
                 pw0 = ptx::ld_relaxed(&p.states[2 * slot]);
