@@ -48,11 +48,13 @@ _RETRACE_VALUES = ("pi_taken", "mu_taken", "q_values", "expected_next_q", "rewar
 
 
 def _cfg_workloads():
-    c1, c2, c3, c4 = (synthetic.CONFIGS[i] for i in (1, 2, 3, 4))
+    W = synthetic.WORKLOADS
+    c1, c2, c3, c4 = (W[k] for k in ("gae_returns_4096x1024", "vtrace_2048x4096", "retrace_1024x16384",
+                                      "long_rows_64x1048576"))
     return {
         "gae_returns_4096x1024": dict(
             desc="GAE + discounted returns + TD(lambda) returns, last_value bootstrap, no truncations",
-            N=4096, T=1024, gen=lambda N, T: synthetic.config_batch(1, N=N, T=T),
+            N=4096, T=1024, gen=lambda N, T: synthetic.workload_batch("gae_returns_4096x1024", N=N, T=T),
             estimators=[("gae", 16, c1), ("discounted_returns", 12, c1), ("lambda_returns", 16, c1)],
             # the step's three outputs from one kernel: r, v, term read once,
             # advantages, lambda-returns, discounted returns written
@@ -60,7 +62,7 @@ def _cfg_workloads():
         "gae_normalized_4096x1024": dict(
             desc="GAE advantages normalised over the batch (fused moments + in-place pass) "
                  "and TD(lambda) returns, last_value bootstrap, no truncations",
-            N=4096, T=1024, gen=lambda N, T: synthetic.config_batch(1, N=N, T=T),
+            N=4096, T=1024, gen=lambda N, T: synthetic.workload_batch("gae_returns_4096x1024", N=N, T=T),
             # r, v, term read once; normalised advantages and lambda-returns written
             estimators=[("gae_normalized", 20, c1)]),
         "gae_masked_4096x8192": dict(
@@ -72,22 +74,22 @@ def _cfg_workloads():
         "gae_compact_4096x1024": dict(
             desc="GAE on compact storage: bfloat16 rewards and values, uint8 flags, float32 "
                  "advantages (float32 arithmetic), last_value bootstrap",
-            N=4096, T=1024, gen=lambda N, T: synthetic.compact(synthetic.config_batch(1, N=N, T=T)),
+            N=4096, T=1024, gen=lambda N, T: synthetic.compact(synthetic.workload_batch("gae_returns_4096x1024", N=N, T=T)),
             # 2 + 2 + 1 bytes read, 4 written
             estimators=[("gae_compact", 9, c1)]),
         "gae_returns_compact_4096x1024": dict(
             desc="GAE + discounted returns + TD(lambda) returns on compact storage: bfloat16 "
                  "values in and out, uint8 flags (float32 arithmetic), last_value bootstrap",
-            N=4096, T=1024, gen=lambda N, T: synthetic.compact(synthetic.config_batch(1, N=N, T=T)),
+            N=4096, T=1024, gen=lambda N, T: synthetic.compact(synthetic.workload_batch("gae_returns_4096x1024", N=N, T=T)),
             # 2 + 2 + 1 bytes read, 3 x 2 written
             estimators=[("gae_returns_compact", 11, c1)]),
         "gae_8x128": dict(
             desc="GAE with truncations and 2-D bootstrap", N=8, T=128,
-            gen=lambda N, T: synthetic.config_batch(0, N=N, T=T),
-            estimators=[("gae_trunc_bs", 24, synthetic.CONFIGS[0])]),
+            gen=lambda N, T: synthetic.workload_batch("gae_8x128", N=N, T=T),
+            estimators=[("gae_trunc_bs", 24, W["gae_8x128"])]),
         "vtrace_2048x4096": dict(
             desc="V-trace with truncations and 2-D bootstrap", N=2048, T=4096,
-            gen=lambda N, T: synthetic.config_batch(2, N=N, T=T),
+            gen=lambda N, T: synthetic.workload_batch("vtrace_2048x4096", N=N, T=T),
             estimators=[("vtrace", 36, c2)]),
         "vtrace_4096x1024": dict(
             desc="V-trace with truncations and 2-D bootstrap at the 4096 x 1024 shape "
@@ -101,20 +103,20 @@ def _cfg_workloads():
             estimators=[("retrace", 32, c3)]),
         "retrace_1024x16384": dict(
             desc="Retrace(lambda) on per-step inputs, no truncations", N=1024, T=16384,
-            gen=lambda N, T: synthetic.config_batch(3, N=N, T=T),
+            gen=lambda N, T: synthetic.workload_batch("retrace_1024x16384", N=N, T=T),
             estimators=[("retrace", 32, c3)]),
         "vtrace_compact_2048x4096": dict(
             desc="V-trace with truncations and 2-D bootstrap on compact storage: bfloat16 "
                  "log-probabilities, values, rewards and bootstrap values, uint8 flags, bfloat16 "
                  "outputs (float32 arithmetic)", N=2048, T=4096,
-            gen=lambda N, T: synthetic.compact(synthetic.config_batch(2, N=N, T=T), values=_VTRACE_VALUES),
+            gen=lambda N, T: synthetic.compact(synthetic.workload_batch("vtrace_2048x4096", N=N, T=T), values=_VTRACE_VALUES),
             # 5 x 2 + 2 x 1 bytes read, 2 x 2 written
             estimators=[("vtrace_compact", 16, c2)]),
         "retrace_compact_1024x16384": dict(
             desc="Retrace(lambda) on per-step inputs in compact storage: bfloat16 probabilities, "
                  "Q-values and rewards, uint8 flags, bfloat16 outputs (float32 arithmetic)",
             N=1024, T=16384,
-            gen=lambda N, T: synthetic.compact(synthetic.config_batch(3, N=N, T=T), values=_RETRACE_VALUES),
+            gen=lambda N, T: synthetic.compact(synthetic.workload_batch("retrace_1024x16384", N=N, T=T), values=_RETRACE_VALUES),
             # 5 x 2 + 1 bytes read, 2 x 2 written
             estimators=[("retrace_compact", 15, c3)]),
         "retrace_actions_1024x16384x4": dict(
@@ -126,7 +128,7 @@ def _cfg_workloads():
             estimators=[("retrace_actions", 64, c3)]),
         "long_rows_64x1048576": dict(
             desc="eligibility traces + episodic prefix sum (starts_at, integer inputs)",
-            N=64, T=1 << 20, gen=lambda N, T: synthetic.config_batch(4, N=N, T=T),
+            N=64, T=1 << 20, gen=lambda N, T: synthetic.workload_batch("long_rows_64x1048576", N=N, T=T),
             estimators=[("eligibility_traces", 12, c4), ("episodic_prefix_sum", 12, c4)]),
         "gae_64x1048576": dict(
             desc="GAE on 1M-step rows (last_value, no truncations)", N=64, T=1 << 20,

@@ -5,7 +5,7 @@ estimators' arithmetic.  The CUDA path (through the Python binding) and the
 CPU oracle receive the very same arrays from here, bit for bit.
 
 Every tensor has its own counter-based stream: numpy's Philox-4x64 generator
-keyed by ``(seed, config_id << 32 | tensor_id)``, so a tensor's values do not
+keyed by ``(seed, stream_id << 32 | tensor_id)``, so a tensor's values do not
 depend on which other tensors were drawn, or in which order.
 
 Recipes (num_envs x seq_len float32 buffers; the distributions follow the
@@ -61,51 +61,52 @@ _TENSOR_IDS = {
     "prompt_len": 25, "response_len": 26, "obs_starts": 27, "obs_len": 28, "outcome": 29,
 }
 
-# The five workloads used by the tests and the benchmark.  Shapes and
-# distribution parameters are those of the benchmark regimes the rl-triton
-# paper describes (massively parallel short rollouts through 1M-step rows).
-CONFIGS = {
-    0: dict(name="gae_8x128", N=8, T=128, kind="gae", p_term=0.01, p_trunc=0.005,
-            bootstrap="2d", gamma=0.99, lambda_=0.95),
-    1: dict(name="gae_returns_4096x1024", N=4096, T=1024, kind="returns", p_term=0.01,
-            p_trunc=0.0, bootstrap="last", gamma=0.99, lambda_=0.95),
-    2: dict(name="vtrace_2048x4096", N=2048, T=4096, kind="vtrace", p_term=0.002,
-            p_trunc=0.001, bootstrap="2d", gamma=0.99, rho_bar=1.0, c_bar=1.0),
-    3: dict(name="retrace_1024x16384", N=1024, T=16384, kind="retrace", p_term=0.001,
-            p_trunc=0.0, gamma=0.99, lambda_=0.95, c_bar=1.0, rho_bar=1.0),
-    4: dict(name="long_rows_64x1048576", N=64, T=1 << 20, kind="long_rows", p_start=1e-4,
-            gamma=0.99, lambda_=0.9),
+# The five workloads used by the tests and the benchmark, by name.  Shapes
+# and distribution parameters are those of the benchmark regimes the
+# rl-triton paper describes (massively parallel short rollouts through
+# 1M-step rows); `stream` is the workload's component of the generator key.
+WORKLOADS = {
+    "gae_8x128": dict(stream=0, N=8, T=128, kind="gae", p_term=0.01, p_trunc=0.005,
+                      bootstrap="2d", gamma=0.99, lambda_=0.95),
+    "gae_returns_4096x1024": dict(stream=1, N=4096, T=1024, kind="returns", p_term=0.01,
+                                  p_trunc=0.0, bootstrap="last", gamma=0.99, lambda_=0.95),
+    "vtrace_2048x4096": dict(stream=2, N=2048, T=4096, kind="vtrace", p_term=0.002,
+                             p_trunc=0.001, bootstrap="2d", gamma=0.99, rho_bar=1.0, c_bar=1.0),
+    "retrace_1024x16384": dict(stream=3, N=1024, T=16384, kind="retrace", p_term=0.001,
+                               p_trunc=0.0, gamma=0.99, lambda_=0.95, c_bar=1.0, rho_bar=1.0),
+    "long_rows_64x1048576": dict(stream=4, N=64, T=1 << 20, kind="long_rows", p_start=1e-4,
+                                 gamma=0.99, lambda_=0.9),
 }
 
 
-def stream(seed: int, config_id: int, name: str) -> np.random.Generator:
-    """Independent Philox stream for one named tensor of one config."""
+def stream(seed: int, stream_id: int, name: str) -> np.random.Generator:
+    """Independent Philox stream for one named tensor of one workload."""
     tid = _TENSOR_IDS[name]
     key = np.array([seed & 0xFFFFFFFFFFFFFFFF,
-                    ((config_id & 0xFFFFFFFF) << 32) | (tid & 0xFFFFFFFF)], dtype=np.uint64)
+                    ((stream_id & 0xFFFFFFFF) << 32) | (tid & 0xFFFFFFFF)], dtype=np.uint64)
     return np.random.Generator(np.random.Philox(key=key))
 
 
-def normal(seed, config_id, name, shape, std=1.0):
-    x = stream(seed, config_id, name).standard_normal(shape, dtype=np.float32)
+def normal(seed, stream_id, name, shape, std=1.0):
+    x = stream(seed, stream_id, name).standard_normal(shape, dtype=np.float32)
     if std != 1.0:
         x *= np.float32(std)
     return x
 
 
-def bernoulli(seed, config_id, name, shape, p):
-    u = stream(seed, config_id, name).random(shape, dtype=np.float32)
+def bernoulli(seed, stream_id, name, shape, p):
+    u = stream(seed, stream_id, name).random(shape, dtype=np.float32)
     return (u < np.float32(p)).astype(np.float32)
 
 
-def uniform(seed, config_id, name, shape, lo, hi):
-    u = stream(seed, config_id, name).random(shape, dtype=np.float32)
+def uniform(seed, stream_id, name, shape, lo, hi):
+    u = stream(seed, stream_id, name).random(shape, dtype=np.float32)
     return (np.float32(lo) + u * np.float32(hi - lo)).astype(np.float32)
 
 
-def uniform_int(seed, config_id, name, shape, lo, hi):
+def uniform_int(seed, stream_id, name, shape, lo, hi):
     """Integers uniform in [lo, hi] inclusive, stored as float32."""
-    return stream(seed, config_id, name).integers(lo, hi + 1, shape).astype(np.float32)
+    return stream(seed, stream_id, name).integers(lo, hi + 1, shape).astype(np.float32)
 
 
 def _flags(N, T, seed, cid, p_term, p_trunc):
@@ -132,17 +133,17 @@ def _bootstrap(N, T, seed, cid, term, trunc, mode):
     return None, None
 
 
-def gae_batch(N, T, seed=0, config_id=0, p_term=0.01, p_trunc=0.005, bootstrap="2d"):
-    term, trunc = _flags(N, T, seed, config_id, p_term, p_trunc)
-    bs, last = _bootstrap(N, T, seed, config_id, term, trunc, bootstrap)
-    return dict(rewards=normal(seed, config_id, "rewards", (N, T)),
-                values=normal(seed, config_id, "values", (N, T)),
+def gae_batch(N, T, seed=0, stream_id=0, p_term=0.01, p_trunc=0.005, bootstrap="2d"):
+    term, trunc = _flags(N, T, seed, stream_id, p_term, p_trunc)
+    bs, last = _bootstrap(N, T, seed, stream_id, term, trunc, bootstrap)
+    return dict(rewards=normal(seed, stream_id, "rewards", (N, T)),
+                values=normal(seed, stream_id, "values", (N, T)),
                 terminateds=term, truncateds=trunc, bootstrap_values=bs, last_value=last)
 
 
-def returns_batch(N, T, seed=0, config_id=1, p_term=0.01, p_trunc=0.0, bootstrap="last"):
+def returns_batch(N, T, seed=0, stream_id=1, p_term=0.01, p_trunc=0.0, bootstrap="last"):
     """GAE inputs plus the TD(lambda) caller-side ``next_values``."""
-    b = gae_batch(N, T, seed, config_id, p_term, p_trunc, bootstrap)
+    b = gae_batch(N, T, seed, stream_id, p_term, p_trunc, bootstrap)
     nv = np.empty((N, T), dtype=np.float32)
     nv[:, :-1] = b["values"][:, 1:]
     if b["last_value"] is not None:
@@ -157,23 +158,23 @@ def returns_batch(N, T, seed=0, config_id=1, p_term=0.01, p_trunc=0.0, bootstrap
     return b
 
 
-def vtrace_batch(N, T, seed=0, config_id=2, p_term=0.002, p_trunc=0.001, bootstrap="2d"):
-    b = gae_batch(N, T, seed, config_id, p_term, p_trunc, bootstrap)
-    lpb = normal(seed, config_id, "log_pi_behavior", (N, T))
-    lpt = (lpb + normal(seed, config_id, "log_ratio", (N, T), std=0.5)).astype(np.float32)
+def vtrace_batch(N, T, seed=0, stream_id=2, p_term=0.002, p_trunc=0.001, bootstrap="2d"):
+    b = gae_batch(N, T, seed, stream_id, p_term, p_trunc, bootstrap)
+    lpb = normal(seed, stream_id, "log_pi_behavior", (N, T))
+    lpt = (lpb + normal(seed, stream_id, "log_ratio", (N, T), std=0.5)).astype(np.float32)
     b.update(log_pi_target=lpt, log_pi_behavior=lpb)
     return b
 
 
-def retrace_batch(N, T, seed=0, config_id=3, p_term=0.001, p_trunc=0.0):
-    term, trunc = _flags(N, T, seed, config_id, p_term, p_trunc)
-    mu = uniform(seed, config_id, "mu_taken", (N, T), 0.05, 1.0)
-    eps = normal(seed, config_id, "pi_log_ratio", (N, T), std=0.5)
+def retrace_batch(N, T, seed=0, stream_id=3, p_term=0.001, p_trunc=0.0):
+    term, trunc = _flags(N, T, seed, stream_id, p_term, p_trunc)
+    mu = uniform(seed, stream_id, "mu_taken", (N, T), 0.05, 1.0)
+    eps = normal(seed, stream_id, "pi_log_ratio", (N, T), std=0.5)
     pi = (mu * np.exp(eps)).astype(np.float32)
     return dict(pi_taken=pi, mu_taken=mu,
-                q_values=normal(seed, config_id, "q_values", (N, T)),
-                expected_next_q=normal(seed, config_id, "expected_next_q", (N, T)),
-                rewards=normal(seed, config_id, "rewards", (N, T)),
+                q_values=normal(seed, stream_id, "q_values", (N, T)),
+                expected_next_q=normal(seed, stream_id, "expected_next_q", (N, T)),
+                rewards=normal(seed, stream_id, "rewards", (N, T)),
                 terminateds=term, truncateds=trunc)
 
 
@@ -183,48 +184,48 @@ def _softmax(z):
     return (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
 
 
-def retrace_actions_batch(N, T, A=4, seed=0, config_id=3, p_term=0.001, p_trunc=0.0):
-    term, trunc = _flags(N, T, seed, config_id, p_term, p_trunc)
-    z = normal(seed, config_id, "action_logits", (N, T, A))
+def retrace_actions_batch(N, T, A=4, seed=0, stream_id=3, p_term=0.001, p_trunc=0.0):
+    term, trunc = _flags(N, T, seed, stream_id, p_term, p_trunc)
+    z = normal(seed, stream_id, "action_logits", (N, T, A))
     target = _softmax(z)
-    z += normal(seed, config_id, "behavior_logit_noise", (N, T, A), std=0.5)
+    z += normal(seed, stream_id, "behavior_logit_noise", (N, T, A), std=0.5)
     behavior = _softmax(z)
     del z
-    u = stream(seed, config_id, "actions").random((N, T), dtype=np.float32)
+    u = stream(seed, stream_id, "actions").random((N, T), dtype=np.float32)
     cdf = np.cumsum(behavior, axis=-1)
     actions = np.minimum((u[..., None] >= cdf).sum(axis=-1), A - 1).astype(np.int64)
     del cdf
     mu = np.take_along_axis(behavior, actions[..., None], axis=-1)[..., 0]
     del behavior
     return dict(action_probs_target=target, action_probs_behavior=np.ascontiguousarray(mu),
-                q_values=normal(seed, config_id, "q_values", (N, T)),
-                next_q_values_all=normal(seed, config_id, "next_q_all", (N, T, A)),
+                q_values=normal(seed, stream_id, "q_values", (N, T)),
+                next_q_values_all=normal(seed, stream_id, "next_q_all", (N, T, A)),
                 actions=actions,
-                rewards=normal(seed, config_id, "rewards", (N, T)),
+                rewards=normal(seed, stream_id, "rewards", (N, T)),
                 terminateds=term, truncateds=trunc)
 
 
-def llm_tokens_batch(N, T, seed=0, config_id=6):
-    prompt = stream(seed, config_id, "prompt_len").integers(64, 512, N)
+def llm_tokens_batch(N, T, seed=0, stream_id=6):
+    prompt = stream(seed, stream_id, "prompt_len").integers(64, 512, N)
     prompt = np.minimum(prompt, T // 2)
     lo = np.maximum(1, T // 4)
-    resp = stream(seed, config_id, "response_len").integers(0, 1 << 30, N)
+    resp = stream(seed, stream_id, "response_len").integers(0, 1 << 30, N)
     resp = lo + resp % np.maximum(1, T - prompt - lo + 1)
     end = np.minimum(prompt + resp, T)                     # first padding token
     t = np.arange(T)[None, :]
     response = (t >= prompt[:, None]) & (t < end[:, None])
     obs = np.zeros((N, T), dtype=bool)
-    starts = stream(seed, config_id, "obs_starts").random((N, T), dtype=np.float32) < 1.0 / 256
-    lens = stream(seed, config_id, "obs_len").integers(16, 128, (N, T))
+    starts = stream(seed, stream_id, "obs_starts").random((N, T), dtype=np.float32) < 1.0 / 256
+    lens = stream(seed, stream_id, "obs_len").integers(16, 128, (N, T))
     rows, cols = np.nonzero(starts & response)
     for r, c in zip(rows, cols):
         obs[r, c:c + lens[r, c]] = True
     mask = (response & ~obs).astype(np.float32)
-    values = np.where(response, normal(seed, config_id, "values", (N, T)), np.float32(0))
+    values = np.where(response, normal(seed, stream_id, "values", (N, T)), np.float32(0))
     rewards = np.zeros((N, T), np.float32)
     term = np.zeros((N, T), np.float32)
     last = np.maximum(end - 1, 0)
-    outcome = normal(seed, config_id, "outcome", (N,))
+    outcome = normal(seed, stream_id, "outcome", (N,))
     rewards[np.arange(N), last] = outcome
     term[np.arange(N), last] = 1.0
     return dict(rewards=rewards, values=values.astype(np.float32), terminateds=term, mask=mask)
@@ -249,39 +250,40 @@ def compact(batch, values=("rewards", "values", "bootstrap_values"),
     return out
 
 
-def long_rows_batch(N, T, seed=0, config_id=4, p_start=1e-4):
-    starts = bernoulli(seed, config_id, "episode_starts", (N, T), p_start)
+def long_rows_batch(N, T, seed=0, stream_id=4, p_start=1e-4):
+    starts = bernoulli(seed, stream_id, "episode_starts", (N, T), p_start)
     ends = np.zeros_like(starts)
     ends[:, :-1] = starts[:, 1:]
-    return dict(inputs=uniform_int(seed, config_id, "inputs", (N, T), 0, 9),
+    return dict(inputs=uniform_int(seed, stream_id, "inputs", (N, T), 0, 9),
                 prefix_dones=starts,
-                gradients=normal(seed, config_id, "gradients", (N, T)),
+                gradients=normal(seed, stream_id, "gradients", (N, T)),
                 trace_dones=ends)
 
 
-def linear_scan_batch(N, T, seed=0, config_id=5, p_zero=0.01, with_carry=True):
+def linear_scan_batch(N, T, seed=0, stream_id=5, p_zero=0.01, with_carry=True):
     """alpha ~ N(0,1); beta ~ U(0,1) with a fraction p_zero set to 0; carry ~ N(0,1)."""
-    beta = uniform(seed, config_id, "beta", (N, T), 0.0, 1.0)
+    beta = uniform(seed, stream_id, "beta", (N, T), 0.0, 1.0)
     if p_zero > 0:
-        beta[bernoulli(seed, config_id, "beta_zero", (N, T), p_zero) > 0] = 0.0
-    return dict(alpha=normal(seed, config_id, "alpha", (N, T)), beta=beta,
-                carry=normal(seed, config_id, "carry", (N,)) if with_carry else None)
+        beta[bernoulli(seed, stream_id, "beta_zero", (N, T), p_zero) > 0] = 0.0
+    return dict(alpha=normal(seed, stream_id, "alpha", (N, T)), beta=beta,
+                carry=normal(seed, stream_id, "carry", (N,)) if with_carry else None)
 
 
-def config_batch(config_id, seed=0, N=None, T=None):
-    """Inputs of one of the five workloads (optionally at a smaller shape)."""
-    c = CONFIGS[config_id]
+def workload_batch(name, seed=0, N=None, T=None):
+    """Inputs of one of the five named workloads (optionally at a smaller shape)."""
+    c = WORKLOADS[name]
+    sid = c["stream"]
     N = c["N"] if N is None else N
     T = c["T"] if T is None else T
     kind = c["kind"]
     if kind == "gae":
-        return gae_batch(N, T, seed, config_id, c["p_term"], c["p_trunc"], c["bootstrap"])
+        return gae_batch(N, T, seed, sid, c["p_term"], c["p_trunc"], c["bootstrap"])
     if kind == "returns":
-        return returns_batch(N, T, seed, config_id, c["p_term"], c["p_trunc"], c["bootstrap"])
+        return returns_batch(N, T, seed, sid, c["p_term"], c["p_trunc"], c["bootstrap"])
     if kind == "vtrace":
-        return vtrace_batch(N, T, seed, config_id, c["p_term"], c["p_trunc"], c["bootstrap"])
+        return vtrace_batch(N, T, seed, sid, c["p_term"], c["p_trunc"], c["bootstrap"])
     if kind == "retrace":
-        return retrace_batch(N, T, seed, config_id, c["p_term"], c["p_trunc"])
+        return retrace_batch(N, T, seed, sid, c["p_term"], c["p_trunc"])
     if kind == "long_rows":
-        return long_rows_batch(N, T, seed, config_id, c["p_start"])
+        return long_rows_batch(N, T, seed, sid, c["p_start"])
     raise KeyError(kind)

@@ -178,7 +178,7 @@ def test_invalid_action_poisons_only_its_row():
 def test_full_size_1024x16384_a4():
     """The benchmark workload (1024 x 16384, A = 4), every element."""
     b = synthetic.retrace_actions_batch(1024, 16384, 4)
-    c = synthetic.CONFIGS[3]
+    c = synthetic.WORKLOADS["retrace_1024x16384"]
     params = (c["gamma"], c["lambda_"], c["c_bar"], c["rho_bar"])
     ref, got = run_both(b, params)
     assert_disc(got[0], ref[0], "targets 1024x16384")

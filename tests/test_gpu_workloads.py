@@ -37,37 +37,37 @@ def assert_disc(gpu, ref, what):
     assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} off, max err {err.max()}"
 
 
-def test_config0_gae_8x128():
-    c = synthetic.CONFIGS[0]
-    b = synthetic.config_batch(0)
+def test_gae_8x128():
+    c = synthetic.WORKLOADS["gae_8x128"]
+    b = synthetic.workload_batch("gae_8x128")
     ref = oracle.gae(b["rewards"], b["values"], b["terminateds"], b["truncateds"], c["gamma"],
                      c["lambda_"], b["bootstrap_values"])
     got = L().compute_gae(dev(b["rewards"]), dev(b["values"]), dev(b["terminateds"]),
                           dev(b["truncateds"]), c["gamma"], c["lambda_"], dev(b["bootstrap_values"]))
-    assert_disc(got, ref, "config 0 gae")
+    assert_disc(got, ref, "gae 8x128")
 
 
-def test_config1_gae_returns_4096x1024():
-    c = synthetic.CONFIGS[1]
-    b = synthetic.config_batch(1)
+def test_gae_returns_4096x1024():
+    c = synthetic.WORKLOADS["gae_returns_4096x1024"]
+    b = synthetic.workload_batch("gae_returns_4096x1024")
     g, l = c["gamma"], c["lambda_"]
     r, v, term, last, nv = (dev(b[k]) for k in ("rewards", "values", "terminateds", "last_value",
                                                 "next_values"))
     assert_disc(L().compute_gae(r, v, term, None, g, l, None, last),
                 oracle.gae(b["rewards"], b["values"], b["terminateds"], None, g, l, None,
-                           b["last_value"]), "config 1 gae")
+                           b["last_value"]), "gae 4096x1024")
     assert_disc(L().compute_discounted_returns(r, term, None, g, None, last),
                 oracle.discounted_returns(b["rewards"], b["terminateds"], None, g, None,
-                                          b["last_value"]), "config 1 discounted")
+                                          b["last_value"]), "discounted returns 4096x1024")
     assert_disc(L().compute_lambda_returns(r, nv, term, None, g, l, None, last),
                 oracle.lambda_returns(b["rewards"], b["next_values"], b["terminateds"], None, g,
-                                      l, None, b["last_value"]), "config 1 lambda returns")
+                                      l, None, b["last_value"]), "lambda returns 4096x1024")
 
 
-def test_config1_fused_gae_returns_4096x1024():
+def test_fused_gae_returns_4096x1024():
     """The fused kernel on the same workload matches all three oracles."""
-    c = synthetic.CONFIGS[1]
-    b = synthetic.config_batch(1)
+    c = synthetic.WORKLOADS["gae_returns_4096x1024"]
+    b = synthetic.workload_batch("gae_returns_4096x1024")
     g, l = c["gamma"], c["lambda_"]
     adv, lam, disc = L().compute_gae_and_returns(dev(b["rewards"]), dev(b["values"]),
                                                  dev(b["terminateds"]), None, g, l, None,
@@ -102,17 +102,17 @@ def _retrace(b, c):
     assert_disc(got[1], ref[1], "retrace advantages")
 
 
-def test_config2_vtrace_2048x4096():
-    _vtrace(synthetic.config_batch(2), synthetic.CONFIGS[2])
+def test_vtrace_2048x4096():
+    _vtrace(synthetic.workload_batch("vtrace_2048x4096"), synthetic.WORKLOADS["vtrace_2048x4096"])
 
 
-def test_config3_retrace_1024x16384():
-    _retrace(synthetic.config_batch(3), synthetic.CONFIGS[3])
+def test_retrace_1024x16384():
+    _retrace(synthetic.workload_batch("retrace_1024x16384"), synthetic.WORKLOADS["retrace_1024x16384"])
 
 
-def test_config4_long_rows_64x1m():
-    c = synthetic.CONFIGS[4]
-    b = synthetic.config_batch(4)
+def test_long_rows_64x1m():
+    c = synthetic.WORKLOADS["long_rows_64x1048576"]
+    b = synthetic.workload_batch("long_rows_64x1048576")
     ref = oracle.episodic_prefix_sum(b["inputs"], b["prefix_dones"], None, "starts_at")
     got = L().compute_episodic_prefix_sum(dev(b["inputs"]), dev(b["prefix_dones"]), None,
                                           "starts_at")
@@ -120,7 +120,7 @@ def test_config4_long_rows_64x1m():
     ref = oracle.eligibility_traces(b["gradients"], b["trace_dones"], c["gamma"], c["lambda_"])
     got = L().compute_eligibility_traces(dev(b["gradients"]), dev(b["trace_dones"]), c["gamma"],
                                          c["lambda_"])
-    assert_disc(got, ref, "config 4 eligibility traces")
+    assert_disc(got, ref, "eligibility traces 64x1M")
 
 
 @pytest.mark.parametrize("kind", ["gae", "vtrace", "retrace"])
@@ -129,7 +129,7 @@ def test_million_step_rows(kind):
     of their own workloads (the long-row regime of the throughput target)."""
     N, T = 64, 1 << 20
     if kind == "gae":
-        c = synthetic.CONFIGS[1]
+        c = synthetic.WORKLOADS["gae_returns_4096x1024"]
         b = synthetic.gae_batch(N, T, 0, 41, c["p_term"], 0.0, "last")
         ref = oracle.gae(b["rewards"], b["values"], b["terminateds"], None, c["gamma"],
                          c["lambda_"], None, b["last_value"])
@@ -137,8 +137,8 @@ def test_million_step_rows(kind):
                               c["gamma"], c["lambda_"], None, dev(b["last_value"]))
         assert_disc(got, ref, "gae 64x1M")
     elif kind == "vtrace":
-        c = synthetic.CONFIGS[2]
+        c = synthetic.WORKLOADS["vtrace_2048x4096"]
         _vtrace(synthetic.vtrace_batch(N, T, 0, 42, c["p_term"], c["p_trunc"], "2d"), c)
     else:
-        c = synthetic.CONFIGS[3]
+        c = synthetic.WORKLOADS["retrace_1024x16384"]
         _retrace(synthetic.retrace_batch(N, T, 0, 43, c["p_term"], 0.0), c)

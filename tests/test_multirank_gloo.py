@@ -40,7 +40,7 @@ def _worker(rank, world, port, q):
     try:
         import oracle
         from linear_recurrence_scan_gb300 import synthetic
-        b = synthetic.config_batch(1, N=37, T=64)
+        b = synthetic.workload_batch("gae_returns_4096x1024", N=37, T=64)
         s, e = shard_rows(37, rank, world)
         part = oracle.gae(b["rewards"][s:e], b["values"][s:e], b["terminateds"][s:e], None,
                           0.99, 0.95, None, b["last_value"][s:e])
@@ -66,7 +66,7 @@ def test_two_gloo_ranks_shard_rows_without_exchange():
         assert p.exitcode == 0
     import oracle
     from linear_recurrence_scan_gb300 import synthetic
-    b = synthetic.config_batch(1, N=37, T=64)
+    b = synthetic.workload_batch("gae_returns_4096x1024", N=37, T=64)
     full = oracle.gae(b["rewards"], b["values"], b["terminateds"], None, 0.99, 0.95, None,
                       b["last_value"])
     stitched = np.concatenate([p for _, p in sorted(gathered, key=lambda x: x[0])])
