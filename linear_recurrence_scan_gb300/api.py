@@ -9,6 +9,7 @@ library or an ordinary CPU tensor raises.
 """
 from __future__ import annotations
 
+import collections
 import ctypes
 import threading
 
@@ -58,6 +59,22 @@ def _contiguous(t):
     return c
 
 
+# Page-locked tensors a call reads or writes in place (its host arguments,
+# outputs and copies) are referenced here until the stream has passed the
+# call: torch's pinned-memory cache only tracks blocks used by its own
+# copies, and could otherwise hand a block the caller has dropped to another
+# tensor while the kernel still uses it.  (Device tensors need no such care:
+# the caching allocator reuses them in stream order.)
+_held_lock = threading.Lock()
+_held = collections.deque()  # (event recorded after the call, tensors), in call order
+
+
+def _release_finished():
+    with _held_lock:
+        while _held and _held[0][0].query():
+            _held.popleft()
+
+
 _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
@@ -86,6 +103,18 @@ class _Call:
         self.shape = ref.shape
         self.mats = {ref_name: ref}
         self.vecs = {}
+        self.outs = []
+        self.extra = []  # other tensors the call uses in place (wide inputs, actions)
+        self.any_host = self.host
+
+    def contiguous(self, t):
+        return _contiguous(t)
+
+    def keep(self, *ts):
+        for t in ts:
+            if t is not None:
+                self.extra.append(t)
+                self.any_host = self.any_host or not t.is_cuda
 
     def mat(self, name, t, required=True, dtypes=(torch.float32,)):
         if t is None:
@@ -94,12 +123,14 @@ class _Call:
             return
         _check(name, t, self.shape, self.device, dtypes)
         self.mats[name] = t
+        self.any_host = self.any_host or not t.is_cuda
 
     def vec(self, name, t):
         if t is None:
             return
         _check(name, t, (self.N,), self.device)
-        self.vecs[name] = _contiguous(t)
+        self.vecs[name] = self.contiguous(t)
+        self.any_host = self.any_host or not t.is_cuda
 
     def finish(self, n_out, dtype=torch.float32):
         mats = self.mats.values()
@@ -110,7 +141,7 @@ class _Call:
             ok = all(self.T <= 1 or t.stride(1) == 1 for t in mats) and len(strides) == 1
             rs = strides.pop() if ok else self.T
             if not ok or rs < self.T:
-                self.mats = {k: _contiguous(t) for k, t in self.mats.items()}
+                self.mats = {k: self.contiguous(t) for k, t in self.mats.items()}
                 rs = self.T
             self.rs = max(rs, self.T)
         where = dict(device="cpu", pin_memory=True) if self.host else dict(device=self.device)
@@ -130,6 +161,23 @@ class _Call:
 
     def stream(self):
         return _stream_handle(self.device)
+
+    def launched(self, status, what):
+        """Raise on an error status; otherwise keep the page-locked tensors
+        of this call until the stream has passed it."""
+        _native.check(status, what)
+        if not (self.any_host or _held) or torch.cuda.is_current_stream_capturing():
+            return  # a captured graph replays on memory its owner keeps alive
+        if self.any_host:
+            host = [t for t in (*self.mats.values(), *self.vecs.values(), *self.outs, *self.extra)
+                    if not t.is_cuda]
+            if host:
+                ev = torch.cuda.Event()
+                ev.record(torch.cuda.current_stream(self.device))
+                with _held_lock:
+                    _held.append((ev, host))
+        if _held:
+            _release_finished()
 
 
 _ws_lock = threading.Lock()
@@ -232,7 +280,7 @@ def compute_gae(rewards, values, terminateds, truncateds=None, gamma=0.99, lambd
         c, (out,) = _compact_call(rewards, values, terminateds, truncateds, bootstrap_values,
                                   last_value, 1, out_dtype or torch.float32)
         ws, wsn, s = _ws_for(c)
-        _native.check(_native.lib().rlscan_gae_compact(
+        c.launched(_native.lib().rlscan_gae_compact(
             c.m("rewards"), c.m("values"), c.m("terminateds"), c.m("truncateds"),
             c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma),
             float(lambda_), _OUT_DTYPES[out_dtype or torch.float32], _vp(out), ws, wsn, s),
@@ -252,12 +300,12 @@ def compute_gae(rewards, values, terminateds, truncateds=None, gamma=0.99, lambd
     (out,) = c.finish(1)
     ws, wsn, s = _ws_for(c)
     if mask is not None:
-        _native.check(_native.lib().rlscan_gae_masked(
+        c.launched(_native.lib().rlscan_gae_masked(
             c.m("rewards"), c.m("values"), c.m("terminateds"), c.m("truncateds"),
             c.m("bootstrap_values"), c.v("last_value"), c.m("mask"), c.N, c.T, c.rs,
             float(gamma), float(lambda_), _vp(out), ws, wsn, s), "rlscan_gae_masked")
         return out
-    _native.check(_native.lib().rlscan_gae(
+    c.launched(_native.lib().rlscan_gae(
         c.m("rewards"), c.m("values"), c.m("terminateds"), c.m("truncateds"),
         c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma), float(lambda_),
         _vp(out), ws, wsn, s), "rlscan_gae")
@@ -280,7 +328,7 @@ def compute_gae_and_returns(rewards, values, terminateds, truncateds=None, gamma
                                 last_value, len(outputs), out_dtype or torch.float32)
         by_name = dict(zip(outputs, outs))
         ws, wsn, s = _ws_for(c)
-        _native.check(_native.lib().rlscan_gae_returns_compact(
+        c.launched(_native.lib().rlscan_gae_returns_compact(
             c.m("rewards"), c.m("values"), c.m("terminateds"), c.m("truncateds"),
             c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma),
             float(lambda_), _OUT_DTYPES[out_dtype or torch.float32],
@@ -300,7 +348,7 @@ def compute_gae_and_returns(rewards, values, terminateds, truncateds=None, gamma
     outs = c.finish(len(outputs))
     by_name = dict(zip(outputs, outs))
     ws, wsn, s = _ws_for(c)
-    _native.check(_native.lib().rlscan_gae_returns(
+    c.launched(_native.lib().rlscan_gae_returns(
         c.m("rewards"), c.m("values"), c.m("terminateds"), c.m("truncateds"),
         c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma), float(lambda_),
         _vp(by_name.get("advantages")), _vp(by_name.get("lambda_returns")),
@@ -336,7 +384,7 @@ def compute_gae_normalized(rewards, values, terminateds, truncateds=None, gamma=
     s = c.stream()
     need = _native.lib().rlscan_gae_normalized_workspace_bytes(c.N, c.T)
     ws, wsn = _workspace(c.device, s, need)
-    _native.check(_native.lib().rlscan_gae_normalized(
+    c.launched(_native.lib().rlscan_gae_normalized(
         c.m("rewards"), c.m("values"), c.m("terminateds"), c.m("truncateds"),
         c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma), float(lambda_),
         float(eps), _vp(by_name["advantages"]), _vp(by_name.get("lambda_returns")),
@@ -371,7 +419,7 @@ def compute_vtrace(log_pi_target, log_pi_behavior, values, rewards, terminateds,
             raise ValueError("compact storage: the window bootstrap is last_value (float32 [N])")
         vs, adv = c.finish(2, out_dtype)
         ws, wsn, s = _ws_for(c)
-        _native.check(_native.lib().rlscan_vtrace_compact(
+        c.launched(_native.lib().rlscan_vtrace_compact(
             c.m("log_pi_target"), c.m("log_pi_behavior"), c.m("values"), c.m("rewards"),
             c.m("terminateds"), c.m("truncateds"), c.m("bootstrap_values"), c.v("last_value"),
             c.N, c.T, c.rs, float(gamma), float(rho_bar), float(c_bar), _OUT_DTYPES[out_dtype],
@@ -392,7 +440,7 @@ def compute_vtrace(log_pi_target, log_pi_behavior, values, rewards, terminateds,
         raise ValueError("pass either last_value or bootstrap_values, not both")
     vs, adv = c.finish(2)
     ws, wsn, s = _ws_for(c)
-    _native.check(_native.lib().rlscan_vtrace(
+    c.launched(_native.lib().rlscan_vtrace(
         c.m("log_pi_target"), c.m("log_pi_behavior"), c.m("values"), c.m("rewards"),
         c.m("terminateds"), c.m("truncateds"), c.m("bootstrap_values"), c.v("last_value"),
         c.N, c.T, c.rs, float(gamma), float(rho_bar), float(c_bar), _vp(vs), _vp(adv),
@@ -447,10 +495,11 @@ def compute_retrace(action_probs_target, action_probs_behavior, q_values, next_q
     else:
         ars = -1
     if ars < c.T * A:
-        wide = [_contiguous(t) for t in wide]
+        wide = [c.contiguous(t) for t in wide]
         ars = c.T * A
+    c.keep(*wide, acts)
     ws, wsn, s = _ws_for(c)
-    _native.check(_native.lib().rlscan_retrace_actions(
+    c.launched(_native.lib().rlscan_retrace_actions(
         _vp(wide[0]), c.m("action_probs_behavior"), c.m("q_values"), _vp(wide[1]), _vp(acts),
         c.m("rewards"), c.m("terminateds"), c.m("truncateds"), c.N, c.T, A, c.rs, ars,
         float(gamma), float(lambda_), float(c_bar), float(rho_bar), _vp(qret), _vp(adv),
@@ -479,7 +528,7 @@ def compute_retrace_from_probs(pi_taken, mu_taken, q_values, expected_next_q, re
         c.mat("truncateds", truncateds, False, _FLAG8)
         qret, adv = c.finish(2, out_dtype)
         ws, wsn, s = _ws_for(c)
-        _native.check(_native.lib().rlscan_retrace_compact(
+        c.launched(_native.lib().rlscan_retrace_compact(
             c.m("pi_taken"), c.m("mu_taken"), c.m("q_values"), c.m("expected_next_q"),
             c.m("rewards"), c.m("terminateds"), c.m("truncateds"), c.N, c.T, c.rs,
             float(gamma), float(lambda_), float(c_bar), float(rho_bar), _OUT_DTYPES[out_dtype],
@@ -495,7 +544,7 @@ def compute_retrace_from_probs(pi_taken, mu_taken, q_values, expected_next_q, re
     c.mat("truncateds", truncateds, False)
     qret, adv = c.finish(2)
     ws, wsn, s = _ws_for(c)
-    _native.check(_native.lib().rlscan_retrace(
+    c.launched(_native.lib().rlscan_retrace(
         c.m("pi_taken"), c.m("mu_taken"), c.m("q_values"), c.m("expected_next_q"),
         c.m("rewards"), c.m("terminateds"), c.m("truncateds"), c.N, c.T, c.rs,
         float(gamma), float(lambda_), float(c_bar), float(rho_bar), _vp(qret), _vp(adv),
@@ -517,7 +566,7 @@ def compute_lambda_returns(rewards, next_values, terminateds, truncateds=None, g
         raise ValueError("pass either last_value or bootstrap_values, not both")
     (out,) = c.finish(1)
     ws, wsn, s = _ws_for(c)
-    _native.check(_native.lib().rlscan_lambda_returns(
+    c.launched(_native.lib().rlscan_lambda_returns(
         c.m("rewards"), c.m("next_values"), c.m("terminateds"), c.m("truncateds"),
         c.m("bootstrap_values"), c.v("last_value"), c.N, c.T, c.rs, float(gamma), float(lambda_),
         _vp(out), ws, wsn, s), "rlscan_lambda_returns")
@@ -536,7 +585,7 @@ def compute_discounted_returns(rewards, terminateds, truncateds=None, gamma=0.99
         raise ValueError("pass either last_value or bootstrap_values, not both")
     (out,) = c.finish(1)
     ws, wsn, s = _ws_for(c)
-    _native.check(_native.lib().rlscan_discounted_returns(
+    c.launched(_native.lib().rlscan_discounted_returns(
         c.m("rewards"), c.m("terminateds"), c.m("truncateds"), c.m("bootstrap_values"),
         c.v("last_value"), c.N, c.T, c.rs, float(gamma), _vp(out), ws, wsn, s),
         "rlscan_discounted_returns")
@@ -551,7 +600,7 @@ def compute_eligibility_traces(gradients, dones, gamma, lambda_, seed_values=Non
     c.vec("seed_values", seed_values)
     (out,) = c.finish(1)
     ws, wsn, s = _ws_for(c)
-    _native.check(_native.lib().rlscan_eligibility_traces(
+    c.launched(_native.lib().rlscan_eligibility_traces(
         c.m("gradients"), c.m("dones"), c.v("seed_values"), c.N, c.T, c.rs, float(gamma),
         float(lambda_), _vp(out), ws, wsn, s), "rlscan_eligibility_traces")
     return out
@@ -567,7 +616,7 @@ def compute_episodic_prefix_sum(inputs, dones, seed_values=None, boundary="ends_
     c.vec("seed_values", seed_values)
     (out,) = c.finish(1)
     ws, wsn, s = _ws_for(c)
-    _native.check(_native.lib().rlscan_episodic_prefix_sum(
+    c.launched(_native.lib().rlscan_episodic_prefix_sum(
         c.m("inputs"), c.m("dones"), c.v("seed_values"),
         _native.ENDS_AT if boundary == "ends_at" else _native.STARTS_AT,
         c.N, c.T, c.rs, _vp(out), ws, wsn, s), "rlscan_episodic_prefix_sum")
@@ -584,7 +633,7 @@ def linear_scan(alpha, beta, carry=None, direction="backward"):
     c.vec("carry", carry)
     (out,) = c.finish(1)
     ws, wsn, s = _ws_for(c)
-    _native.check(_native.lib().rlscan_linear_scan(
+    c.launched(_native.lib().rlscan_linear_scan(
         c.m("alpha"), c.m("beta"), c.v("carry"),
         _native.BACKWARD if direction == "backward" else _native.FORWARD,
         c.N, c.T, c.rs, _vp(out), ws, wsn, s), "rlscan_linear_scan")

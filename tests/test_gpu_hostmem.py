@@ -156,3 +156,36 @@ def test_pageable_memory_through_the_c_abi():
                         0.99, 0.95, pinned(out).data_ptr(), host_ws.data_ptr(), wsn, s)
     torch.cuda.synchronize()
     assert _native.STATUS[st] == "RLSCAN_ERR_WORKSPACE"
+
+
+def test_pinned_copies_outlive_the_kernel_that_reads_them():
+    """A strided pinned input is re-laid out into a page-locked copy that the
+    kernel reads over the host link after the call has returned.  The copy
+    must stay referenced until the stream has passed the call: right after
+    each call, fresh pinned blocks of the same size are allocated and
+    overwritten (what a freed copy's block would be handed to), and every
+    result must still equal the device-memory one.  Once the stream has
+    synchronised, the next call releases the copies."""
+    import linear_recurrence_scan_gb300.api as api
+    N, T = 256, 4096
+    b = synthetic.returns_batch(N, T, 11, 86)
+    d = L().compute_gae(device(b["rewards"]), device(b["values"]), device(b["terminateds"]), None, 0.99, 0.95,
+                        None, device(b["last_value"]))
+    outs, junk = [], []
+    for _ in range(4):
+        wide = torch.zeros((N, T + 4), dtype=torch.float32).pin_memory()
+        wide[:, :T] = torch.from_numpy(b["values"])
+        v = wide[:, :T]                          # row stride T + 4: every input is copied
+        outs.append(L().compute_gae(pinned(b["rewards"]), v, pinned(b["terminateds"]), None, 0.99, 0.95, None,
+                                    pinned(b["last_value"])))
+        del wide, v
+        for _ in range(3):                       # blocks a released copy could be handed to
+            j = torch.empty((N, T), dtype=torch.float32).pin_memory()
+            j.fill_(float("nan"))
+            junk.append(j)
+    for i, h in enumerate(outs):
+        same(h, d, f"pinned copies, call {i}")
+    torch.cuda.synchronize()
+    L().compute_gae(device(b["rewards"]), device(b["values"]), device(b["terminateds"]), None, 0.99, 0.95,
+                    None, device(b["last_value"]))
+    assert len(api._held) == 0
