@@ -46,6 +46,15 @@ def test_version_and_status_strings(lib):
     assert lib.rlscan_status_string(99) == b"unknown status"
 
 
+def test_normal_build_has_no_bounds_checking(lib):
+    """Only the checked build counts bounds violations; the normal build
+    reports 0 (not checked) and zeroes both values, without a device."""
+    v, site = ctypes.c_ulonglong(7), ctypes.c_ulonglong(7)
+    assert lib.rlscan_bounds_check(ctypes.addressof(v), ctypes.addressof(site), 1) == 0
+    assert v.value == 0 and site.value == 0
+    assert lib.rlscan_bounds_check(None, None, 0) == 0
+
+
 def test_workspace_bytes(lib):
     assert lib.rlscan_workspace_bytes(0, 100) == 0
     assert lib.rlscan_workspace_bytes(10, 0) == 0
