@@ -1,15 +1,22 @@
 """Throughput benchmark: env-steps/s and achieved HBM GB/s per estimator.
 
-Default workload (N=1): GAE + discounted returns + TD(lambda) returns on a
-4096 x 1024 float32 rollout buffer with a last_value bootstrap (one "step"
-= the three estimators over one batch).  Other workloads: --workload.
+Default run (N=1): the headline workload is the largest single-GPU
+configuration, eligibility traces + episodic prefix sums on 64 rows of 2^20
+float32 steps (one "step" = both estimators over one batch); every other
+named workload is measured in the same run with the same protocol and
+reported under "workloads" (GAE + discounted returns + TD(lambda) on 4096 x
+1024, V-trace 2048 x 4096, Retrace 1024 x 16384, GAE / V-trace / Retrace on
+2^20-step rows, and the fused, masked, normalised, compact and [N,T,A]
+variants).  --workload picks another headline (then alone).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload gae_returns_4096x1024|...]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--trials R]
+                  [--impl ours|reference] [--workload NAME] [--suite auto|on|off]
 
-Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
-(rows are independent: weak scaling, no collective on the data path); the
-time is the max over ranks.
+Timing: W warm-up steps, then R trials of K back-to-back steps, one CUDA
+event pair per trial; the reported time is the best trial's mean.  Prints
+one JSON line (rank 0).  Under torchrun each rank runs its own batch (rows
+are independent: weak scaling, no collective on the data path); times are
+the max over ranks.
 """
 from __future__ import annotations
 
@@ -182,6 +189,68 @@ E2E_STREAMS = 3
 LAUNCHES = {"gae_normalized": 2}
 
 
+
+METRIC = "env-steps/sec and achieved HBM GB/s (% of GB300 peak) per estimator, 1 GPU"
+
+# The headline workload (the largest single-GPU configuration: 64 rows of
+# 2^20 steps, eligibility traces + episodic prefix sums) and the workloads
+# measured beside it in the same run (every estimator at its named shape,
+# GAE / V-trace / Retrace on 2^20-step rows, and the fused, masked,
+# normalised, compact and [N,T,A] variants).
+HEADLINE = "long_rows_64x1048576"
+SUITE = ["gae_8x128", "gae_returns_4096x1024", "vtrace_2048x4096", "retrace_1024x16384",
+         "gae_64x1048576", "vtrace_64x1048576", "retrace_64x1048576",
+         "vtrace_4096x1024", "retrace_4096x1024",
+         "gae_normalized_4096x1024", "gae_masked_4096x8192", "gae_compact_4096x1024",
+         "gae_returns_compact_4096x1024", "vtrace_compact_2048x4096",
+         "retrace_compact_1024x16384", "retrace_actions_1024x16384x4"]
+
+
+def step_kernels_of(wl_name):
+    """Kernels of one step: the fused kernel when the workload has one, else
+    one kernel per estimator."""
+    wl = WORKLOADS[wl_name]
+    return [wl["fused"]] if wl.get("fused") else list(wl["estimators"])
+
+
+prep_kernels = step_kernels_of
+
+
+def l2_plan(wl_name):
+    """Rotating input sets so that consecutive steps never find their inputs
+    in the 129 MB L2: one set when a step's inputs + outputs exceed 4x L2,
+    else enough sets to cover 4x L2.  Returns (sets, bytes per set)."""
+    wl = WORKLOADS[wl_name]
+    N, T = wl["N"], wl["T"]
+    batch = wl["gen"](min(N, 2), min(T, 256))
+    kernels = step_kernels_of(wl_name)
+    need_in = sorted({k for (n, _, _) in kernels for k in IO[n][0] + IO[n][1]})
+    in_bytes = 0
+    for k in need_in:
+        v = batch[k]
+        per_elem = v.itemsize * (int(np.prod(v.shape[2:])) if v.ndim > 2 else 1)
+        in_bytes += per_elem * (N * T if v.ndim >= 2 else N)
+    out_bytes = sum(IO[n][2] * N * T * OUT_BYTES.get(n, 4) for (n, _, _) in kernels)
+    set_bytes = in_bytes + out_bytes
+    n_sets = 1 if set_bytes > 4 * L2_BYTES else min(16, max(2, math.ceil(4 * L2_BYTES / set_bytes)))
+    return n_sets, set_bytes
+
+
+def workload_config(wl_name):
+    """The `config` object of a workload: the same in both arms."""
+    wl = WORKLOADS[wl_name]
+    n_sets, set_bytes = l2_plan(wl_name)
+    if n_sets == 1:
+        l2 = f"inputs larger than L2: {set_bytes / 1e6:.0f} MB per step > 4 x 129 MB"
+    else:
+        l2 = (f"{n_sets} rotating input sets of {set_bytes / 1e6:.1f} MB "
+              f"({n_sets * set_bytes / 1e6:.0f} MB > 129 MB L2)")
+    return {"workload": wl_name, "description": wl["desc"], "num_envs": wl["N"],
+            "seq_len": wl["T"], "estimators": [e[0] for e in wl["estimators"]],
+            "parallelism": "rows: one independent batch per GPU (weak scaling, no collective)",
+            "l2": l2}
+
+
 def _csrc_hash():
     h = hashlib.sha256()
     d = os.path.join(ROOT, "linear_recurrence_scan_gb300", "csrc")
@@ -202,17 +271,16 @@ def _measured_peak():
 
 
 def _ncu_traffic(kernel, workload):
-    """DRAM bytes per launch that an ncu capture recorded for this kernel and
-    workload (profiles/traffic.md, a fenced JSON block), if the capture was
-    taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "traffic.md")
+    """DRAM bytes per launch (read + write) that ncu recorded for this kernel
+    and workload (profiles/traffic.json), if the capture was taken on the
+    current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            text = f.read()
-        rec = json.loads(text.split("```json", 1)[1].split("```", 1)[0])
+            rec = json.load(f)
     except Exception:
         return None
-    e = rec.get(f"{kernel}@{workload}")
+    e = rec.get("records", {}).get(f"{kernel}@{workload}")
     if not e or e.get("csrc_sha") != _csrc_hash():
         return None
     return e.get("dram_bytes_per_launch")
@@ -450,112 +518,165 @@ def _public_call(name, c, t):
     raise KeyError(name)
 
 
-def run_ours(args, wl_name, rank, world, local_rank):
-    import torch
-    from linear_recurrence_scan_gb300 import _native, build
-    build.build()
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    wl = WORKLOADS[wl_name]
-    N, T = wl["N"], wl["T"]
-    batch = wl["gen"](N, T)
-    names = [e[0] for e in wl["estimators"]]
-    fused = wl.get("fused")
-    # the step: one fused kernel when the workload has one, else each estimator
-    step_kernels = [fused] if fused else list(wl["estimators"])
-    all_kernels = step_kernels + ([e for e in wl["estimators"]] if fused else [])
-    need_in = sorted({k for (n, _, _) in all_kernels for k in IO[n][0] + IO[n][1]})
-    host = {k: batch[k] for k in need_in}
-    set_bytes = sum(v.nbytes for v in host.values()) + sum(
-        IO[n][2] * N * T * OUT_BYTES.get(n, 4) for (n, _, _) in step_kernels)
-    n_sets = 1 if set_bytes > 4 * L2_BYTES else min(16, max(2, math.ceil(4 * L2_BYTES / set_bytes)))
-    stream = torch.cuda.current_stream(dev)
-    sh = ctypes.c_void_p(stream.cuda_stream)
-    lib = _native.lib()
-    wsn = max(lib.rlscan_workspace_bytes(N, T), lib.rlscan_gae_normalized_workspace_bytes(N, T))
-    ws = None
-    if wsn:
-        ws_t = torch.empty(wsn, dtype=torch.uint8, device=dev)
-        _native.check(lib.rlscan_workspace_init(ctypes.c_void_p(ws_t.data_ptr()), wsn, sh), "init")
-        ws = ctypes.c_void_p(ws_t.data_ptr())
-    sets = []
-    keep = []  # every set's tensors stay allocated: the launchers hold raw pointers
-    for _ in range(n_sets):
-        bufs = {k: torch.from_numpy(v).to(dev) for k, v in host.items()}
-        keep.append(bufs)
-        calls = {}
-        for (name, bps, c) in all_kernels:
-            odt = torch.bfloat16 if OUT_DTYPE.get(name) == "bf16" else torch.float32
-            outs = [torch.empty((N, T), dtype=odt, device=dev) for _ in range(IO[name][2])]
-            keep.append(outs)
-            calls[name] = _launcher(name, c, bufs, outs, N, T, ws, wsn, sh)
-        sets.append(calls)
-    ptrs = [t.data_ptr() for group in keep for t in (group.values() if isinstance(group, dict) else group)]
-    assert len(ptrs) == len(set(ptrs)), "input sets must not share memory"
-    torch.cuda.synchronize()
+class _Prepared:
+    """One workload resident on the device: rotating input sets, outputs,
+    workspace and one ABI launcher per kernel and set."""
 
-    def run(kernels, i):
-        calls = sets[i % n_sets]
+    def __init__(self, wl_name, dev, stream):
+        import torch
+        from linear_recurrence_scan_gb300 import _native
+        self.name = wl_name
+        self.wl = wl = WORKLOADS[wl_name]
+        self.N, self.T = N, T = wl["N"], wl["T"]
+        self.step_kernels = step_kernels_of(wl_name)
+        self.all_kernels = self.step_kernels + (list(wl["estimators"]) if wl.get("fused") else [])
+        self.n_sets, self.set_bytes = l2_plan(wl_name)
+        need_in = sorted({k for (n, _, _) in self.all_kernels for k in IO[n][0] + IO[n][1]})
+        batch = wl["gen"](N, T)
+        self.host = {k: batch[k] for k in need_in}
+        del batch
+        self.stream = stream
+        sh = ctypes.c_void_p(stream.cuda_stream)
+        lib = _native.lib()
+        self.wsn = wsn = max(lib.rlscan_workspace_bytes(N, T), lib.rlscan_gae_normalized_workspace_bytes(N, T))
+        ws = None
+        self.keep = []  # every set's tensors stay allocated: the launchers hold raw pointers
+        if wsn:
+            ws_t = torch.empty(wsn, dtype=torch.uint8, device=dev)
+            self.keep.append([ws_t])
+            _native.check(lib.rlscan_workspace_init(ctypes.c_void_p(ws_t.data_ptr()), wsn, sh), "init")
+            ws = ctypes.c_void_p(ws_t.data_ptr())
+        self.sets = []
+        for _ in range(self.n_sets):
+            bufs = {k: torch.from_numpy(v).to(dev) for k, v in self.host.items()}
+            self.keep.append(bufs)
+            calls = {}
+            for (name, _, c) in self.all_kernels:
+                odt = torch.bfloat16 if OUT_DTYPE.get(name) == "bf16" else torch.float32
+                outs = [torch.empty((N, T), dtype=odt, device=dev) for _ in range(IO[name][2])]
+                self.keep.append(outs)
+                calls[name] = _launcher(name, c, bufs, outs, N, T, ws, wsn, sh)
+            self.sets.append(calls)
+        ptrs = [t.data_ptr() for group in self.keep
+                for t in (group.values() if isinstance(group, dict) else group)]
+        assert len(ptrs) == len(set(ptrs)), "input sets must not share memory"
+        torch.cuda.synchronize()
+
+    def run(self, kernels, i):
+        from linear_recurrence_scan_gb300 import _native
+        calls = self.sets[i % self.n_sets]
         for (name, _, _) in kernels:
             st = calls[name]()
             if st != 0:
                 raise _native.RlscanError(st, name)
 
-    def region(kernels, K, offset):
+    def region(self, kernels, K, offset, world):
         """K steps of `kernels` back to back on the stream, one CUDA event
         pair around the whole region (none between launches, which would
         serialise them); barrier + synchronize on both sides.  Returns ms
-        per step and the host wall time of the region."""
+        per step (max over ranks) and the host wall time of the region."""
+        import torch
         t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
-        t0e.record(stream)
+        t0e.record(self.stream)
         for i in range(K):
-            run(kernels, offset + i)
-        t1e.record(stream)
+            self.run(kernels, offset + i)
+        t1e.record(self.stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
-        return t0e.elapsed_time(t1e) / K, wall
+        return max_over_ranks(t0e.elapsed_time(t1e) / K), wall
 
-    def launch_durations(kernels, K):
-        """Average device duration of each kernel: K launches of that kernel
-        alone, back to back, timed as one region, three times."""
-        out = {}
-        for e in kernels:
-            out[e[0]] = [region([e], K, args.warmup + r * K)[0] for r in range(3)]
-        return out
+    def trials(self, kernels, K, n_trials, offset, world):
+        """`n_trials` regions of K steps; ms per step of each trial and the
+        total host wall time."""
+        out, wall = [], 0.0
+        for r in range(n_trials):
+            ms, w = self.region(kernels, K, offset + r * K, world)
+            out.append(ms)
+            wall += w
+        return out, wall
 
-    sampler = ClockSampler(local_rank)
-    sampler.start()
-    time.sleep(0.3)
-    for i in range(args.warmup):
-        run(step_kernels, i)
-    torch.cuda.synchronize()
-    K = args.steps
-    ms_step, wall = region(step_kernels, K, args.warmup)
-    ms_step = max_over_ranks(ms_step)
+    def free(self):
+        import torch
+        self.keep.clear()
+        self.sets.clear()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
+def _kernel_stats(name, bps, trial_ms, steps_per_call, peak, workload):
+    """Per-launch figures of one kernel from its trials: the reported
+    duration is the best trial's mean (the pages' minimum over trials)."""
+    ts = np.array(trial_ms, dtype=np.float64)
+    us = float(ts.min() * 1e3)
+    gbs = bps * steps_per_call / (us * 1e-6) / 1e9
+    alg = bps * steps_per_call
+    traffic = _ncu_traffic(name, workload)
+    return {"us_mean": round(us, 2), "us_trials": [round(float(t) * 1e3, 2) for t in ts],
+            "env_steps_per_s": steps_per_call / (us * 1e-6), "bytes_per_env_step": bps,
+            "algorithmic_bytes_per_launch": alg,
+            "gb_per_s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
+            "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
+            "traffic": traffic, "traffic_over_algorithmic": (round(traffic / alg, 4)
+                                                             if traffic else None)}
+
+
+def _auto_steps(prep, kernels, world, target_ms=25.0, lo=20, hi=4000):
+    """Steps per trial so that a trial of `kernels` lasts about `target_ms`."""
+    ms, _ = prep.region(kernels, 3, 0, world)
+    return int(min(hi, max(lo, math.ceil(target_ms / max(ms, 1e-4)))))
+
+
+def measure_workload(prep, K, n_trials, warmup, world, peak):
+    """Step timing and per-kernel / per-estimator figures of one prepared
+    workload.  K steps per trial (None: sized to ~25 ms a trial)."""
+    wl = prep.wl
+    step_kernels = prep.step_kernels
+    for i in range(warmup):
+        prep.run(step_kernels, i)
+    if K is None:
+        K = _auto_steps(prep, step_kernels, world)
+    trial_ms, wall = prep.trials(step_kernels, K, n_trials, warmup, world)
+    ms_step = min(trial_ms)
+    steps_per_call = prep.N * prep.T
     # per-launch durations of the step's kernels (the step itself when it is one kernel)
-    per_kernel = ({step_kernels[0][0]: [ms_step]} if len(step_kernels) == 1
-                  else launch_durations(step_kernels, K))
+    if len(step_kernels) == 1:
+        per_kernel = {step_kernels[0][0]: trial_ms}
+    else:
+        per_kernel = {e[0]: prep.trials([e], K, n_trials, warmup, world)[0] for e in step_kernels}
     per_est_times = per_kernel
-    if fused:  # the estimators one kernel each, for the per-estimator figures
-        for i in range(args.warmup):
-            run(wl["estimators"], i)
-        per_est_times = launch_durations(wl["estimators"], K)
+    if wl.get("fused"):  # the estimators one kernel each, for the per-estimator figures
+        for i in range(warmup):
+            prep.run(wl["estimators"], i)
+        per_est_times = {e[0]: prep.trials([e], K, n_trials, warmup, world)[0] for e in wl["estimators"]}
+    step = {n: _kernel_stats(n, bps, per_kernel[n], steps_per_call, peak, prep.name)
+            for (n, bps, _) in step_kernels}
+    per_est = {n: _kernel_stats(n, bps, per_est_times[n], steps_per_call, peak, prep.name)
+               for (n, bps, _) in wl["estimators"]}
+    dominant = max(step_kernels, key=lambda e: min(per_kernel[e[0]]))[0]
+    return {"K": K, "trials_ms": [round(t, 5) for t in trial_ms], "ms_per_step": ms_step,
+            "wall": wall, "step": step, "per_estimator": per_est, "dominant": dominant,
+            "env_steps_per_s": world * steps_per_call / (ms_step * 1e-3)}
 
-    # e2e through the public API: pinned host inputs -> device, the step's
-    # call(s), results back to pinned host memory, every step.  Consecutive
-    # steps go to E2E_STREAMS streams in turn (each with its own device and
-    # host buffers), so one step's upload, another's compute and a third's
-    # download overlap, as a pipeline of rollout batches would run.
+
+def run_e2e(args, prep, dev, world):
+    """End to end through the public API: pinned host inputs -> device, the
+    step's call(s), results back to pinned host memory, every step.
+    Consecutive steps go to E2E_STREAMS streams in turn (each with its own
+    device and host buffers), so one step's upload, another's compute and a
+    third's download overlap, as a pipeline of rollout batches would run."""
+    import torch
+    N, T = prep.N, prep.T
+    step_kernels = prep.step_kernels
     e2e_in = sorted({k for (n, _, _) in step_kernels for k in IO[n][0] + IO[n][1]})
-    pinned = {k: torch.from_numpy(host[k]).pin_memory() for k in e2e_in}
+    pinned = {k: torch.from_numpy(prep.host[k]).pin_memory() for k in e2e_in}
     NS = max(1, args.e2e_streams)
     e2e_streams = [torch.cuda.Stream(dev) for _ in range(NS)]
     dsets = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pinned.items()}
@@ -565,7 +686,6 @@ def run_ours(args, wl_name, rank, world, local_rank):
               for (n, _, _) in step_kernels for _ in range(IO[n][2])] for _ in range(NS)]
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = sum(o.numel() * o.element_size() for o in hsets[0])
-
     zero_copy = args.e2e_mode == "zerocopy"
 
     def e2e_step(i):
@@ -588,64 +708,119 @@ def run_ours(args, wl_name, rank, world, local_rank):
     for i in range(max(NS, min(args.warmup, 3))):
         e2e_step(i)
     torch.cuda.synchronize()
+    K = args.e2e_steps if args.e2e_steps > 0 else args.steps
     e0 = time.perf_counter()
     for i in range(K):
         e2e_step(i)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - e0) / K)
+    res = {"value": world * N * T / e2e_s, "unit": "env-steps/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+           "path": ("public compute_* API on pinned host tensors: the kernel reads the inputs "
+                    "and writes the pinned outputs over the host link (zero copy)"
+                    if zero_copy else
+                    "pinned host -> device copies, public compute_* API, results -> pinned host")
+                   + f"; steps round-robin over {NS} streams"}
+    del pinned, dsets, hsets
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def capture_schedule(args, wl_name, warm=3, count=6):
+    """A fixed launch schedule for DRAM-traffic captures: for each kernel of
+    the workload (the step's and, for a fused step, each estimator's), `warm`
+    launches then `count` more, back to back over the rotating input sets,
+    with a synchronize between kernels.  Timing is not taken here; under
+    `ncu --cache-control none` each launch's DRAM counters then include the
+    write-back of its predecessor's outputs, so the mean over the `count`
+    launches is one launch's read + write traffic.  Returns the schedule."""
+    import torch
+    from linear_recurrence_scan_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    prep = _Prepared(wl_name, dev, torch.cuda.current_stream(dev))
+    sched = []
+    for e in prep.all_kernels:
+        for i in range(warm + count):
+            prep.run([e], i)
+        torch.cuda.synchronize()
+        sched.append({"kernel": e[0], "warm": warm, "count": count,
+                      "algorithmic_bytes_per_launch": e[1] * prep.N * prep.T})
+    prep.free()
+    return {"workload": wl_name, "capture": sched}
+
+
+def run_ours(args, wl_name, rank, world, local_rank, sub_workloads=()):
+    import torch
+    from linear_recurrence_scan_gb300 import build
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = _measured_peak()
+    wl = WORKLOADS[wl_name]
+    names = [e[0] for e in wl["estimators"]]
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    prep = _Prepared(wl_name, dev, stream)
+    m = measure_workload(prep, args.steps, args.trials, args.warmup, world, peak)
+    K = m["K"]
+    e2e = run_e2e(args, prep, dev, world)
+    prep.free()
+    del prep
+
+    # the other workloads: same protocol, steps per trial sized to ~25 ms
+    subs = {}
+    for sub in sub_workloads:
+        if sub == wl_name:
+            continue
+        p = _Prepared(sub, dev, stream)
+        sm = measure_workload(p, None, args.trials, args.warmup, world, peak)
+        p.free()
+        del p
+        subs[sub] = {"config": workload_config(sub),
+                     "steps": sm["K"], "trials": args.trials,
+                     "ms_per_step": sm["ms_per_step"], "trials_ms": sm["trials_ms"],
+                     "env_steps_per_s": sm["env_steps_per_s"],
+                     "step": sm["step"], "per_estimator": sm["per_estimator"]}
     clocks = sampler.stop()
 
-    steps_per_call = N * T
-    peak, peak_kind = _measured_peak()
-
-    def kernel_stats(name, bps, ts):
-        ts = np.array(ts)
-        avg_us = float(ts.mean() * 1e3)
-        gbs = bps * steps_per_call / (avg_us * 1e-6) / 1e9
-        return {"us_mean": round(avg_us, 2), "us_median": round(float(np.median(ts)) * 1e3, 2),
-                "env_steps_per_s": steps_per_call / (avg_us * 1e-6), "bytes_per_env_step": bps,
-                "gb_per_s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
-                "frac_of_nominal_8tbs": round(gbs / 8000.0, 4)}
-    per_est = {n: kernel_stats(n, bps, per_est_times[n]) for (n, bps, _) in wl["estimators"]}
-    step_stats = {n: kernel_stats(n, bps, per_kernel[n]) for (n, bps, _) in step_kernels}
-    dominant = max(step_kernels, key=lambda e: sum(per_kernel[e[0]]))[0]
-    d = step_stats[dominant]
+    d = m["step"][m["dominant"]]
     result = {
-        "metric": "env-steps/sec and achieved HBM GB/s (% of GB300 peak) per estimator, 1 GPU",
-        "value": world * steps_per_call / (ms_step * 1e-3),
+        "metric": METRIC,
+        "value": m["env_steps_per_s"],
         "unit": "env-steps/s",
-        "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": ms_step,
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "trials": args.trials,
+        "ms_per_step": m["ms_per_step"], "trials_ms": m["trials_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if not any(n.endswith("_compact") for n in names) else
                  "f32 arithmetic on bf16 values / u8 flags", "data": "synthetic",
-        "config": {"workload": wl_name, "description": wl["desc"], "num_envs": N, "seq_len": T,
-                   "estimators": names,
-                   "step_kernels": [n for (n, _, _) in step_kernels],
-                   "parallelism": f"rows, {world} independent batch(es)",
-                   "l2": f"{n_sets} rotating input sets of {set_bytes / 1e6:.0f} MB "
-                         f"({n_sets * set_bytes / 1e6:.0f} MB > 129 MB L2)"},
-        "step": step_stats,
-        "per_estimator": per_est,
-        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": d["gb_per_s"], "peak": peak,
+        "config": workload_config(wl_name),
+        "step_kernels": [n for (n, _, _) in prep_kernels(wl_name)],
+        "step": m["step"],
+        "per_estimator": m["per_estimator"],
+        "roofline": {"bound": "hbm", "kernel": m["dominant"], "achieved": d["gb_per_s"], "peak": peak,
                      "peak_source": peak_kind, "unit": "GB/s", "frac": d["frac_of_measured_hbm"],
-                     "traffic": _ncu_traffic(dominant, wl_name),
-                     "algorithmic_bytes_per_launch": d["bytes_per_env_step"] * steps_per_call},
-        "e2e": {"value": world * steps_per_call / e2e_s, "unit": "env-steps/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "path": ("public compute_* API on pinned host tensors: the kernel reads the inputs "
-                         "and writes the pinned outputs over the host link (zero copy)"
-                         if zero_copy else
-                         "pinned host -> device copies, public compute_* API, results -> pinned host")
-                        + f"; steps round-robin over {NS} streams"},
-        "gpu_launches": K * sum(LAUNCHES.get(n, 1) for (n, _, _) in step_kernels),
-        "full_call_us": round(wall / K * 1e6, 2),
-        "timing": "CUDA events around K back-to-back steps (no events between launches); "
-                  "per-kernel durations from K back-to-back launches of that kernel alone; "
-                  "full_call_us: host wall time of the timed region per step",
-        "wall_s_timed": round(wall, 4),
+                     "traffic": d["traffic"],
+                     "algorithmic_bytes_per_launch": d["algorithmic_bytes_per_launch"]},
+        "e2e": e2e,
+        "gpu_launches": args.trials * K * sum(LAUNCHES.get(n, 1) for (n, _, _) in prep_kernels(wl_name)),
+        "full_call_us": round(m["wall"] / (args.trials * K) * 1e6, 2),
+        "timing": (f"{args.trials} trials of K back-to-back steps, one CUDA event pair per trial on "
+                   "the launching stream (none between launches, which would serialise them), "
+                   "barrier + synchronize around each trial; ms_per_step is the best trial's mean "
+                   "(the pages' minimum over trials); per-kernel durations from trials of that "
+                   "kernel alone; gpu_launches counts the step trials; full_call_us: host wall "
+                   "time per step over the step trials"),
+        "wall_s_timed": round(m["wall"], 4),
         "clocks": clocks,
     }
+    if subs:
+        result["workloads"] = subs
     return result
 
 
@@ -772,19 +947,23 @@ def _cpu_model():
         return "unknown"
 
 
-def cpu_baseline(wl_name):
+def cpu_baseline(wl_name, seconds=8.0, one_core=True):
+    """The oracle as it stands on the host cores, on a bounded sample of the
+    workload (whole rows, every estimator of the workload)."""
     wl = WORKLOADS[wl_name]
     threads = os.cpu_count() or 1
     rows = min(wl["N"], max(threads, int(4_194_304 * 2 // wl["T"])))
-    v, info = oracle_time(wl_name, rows, threads, min_seconds=8.0)
-    rows1 = max(1, rows // threads)
-    v1, info1 = oracle_time(wl_name, rows1, 1, min_seconds=3.0)
-    return {"value": v, "unit": "env-steps/s", "cores": threads, "kind": "oracle",
-            "cpu": _cpu_model(), "value_1core": v1,
-            "sample": f"{info['rows']} of {wl['N']} rows x {info['seq_len']} steps, "
-                      f"all estimators of the step, best of {info['passes']} passes "
-                      f"({info['seconds']} s), rows split over {threads} threads; 1-core figure: "
-                      f"{info1['rows']} rows, best of {info1['passes']} passes"}
+    v, info = oracle_time(wl_name, rows, threads, min_seconds=seconds)
+    out = {"value": v, "unit": "env-steps/s", "cores": threads, "kind": "oracle", "cpu": _cpu_model(),
+           "sample": f"{info['rows']} of {wl['N']} rows x {info['seq_len']} steps, "
+                     f"all estimators of the workload, best of {info['passes']} passes "
+                     f"({info['seconds']} s), rows split over {threads} threads"}
+    if one_core:
+        rows1 = max(1, rows // threads)
+        v1, info1 = oracle_time(wl_name, rows1, 1, min_seconds=seconds / 3)
+        out["value_1core"] = v1
+        out["sample"] += f"; 1-core figure: {info1['rows']} rows, best of {info1['passes']} passes"
+    return out
 
 
 def run_reference(args, wl_name):
@@ -810,13 +989,11 @@ def run_reference(args, wl_name):
     v = rows * wl["T"] / el
     sample = (f"{rows} of {wl['N']} rows x {wl['T']} steps per step, all estimators, "
               f"rows split over {threads} threads")
-    return {"impl": "reference",
-            "metric": "env-steps/sec and achieved HBM GB/s (% of GB300 peak) per estimator, 1 GPU",
+    return {"impl": "reference", "metric": METRIC,
             "value": v, "unit": "env-steps/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": el * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl_name, "description": wl["desc"], "num_envs": wl["N"],
-                       "seq_len": wl["T"], "estimators": [e[0] for e in wl["estimators"]]},
+            "config": workload_config(wl_name),
             "cpu_baseline": {"value": v, "unit": "env-steps/s", "cores": threads, "kind": "oracle",
                              "cpu": _cpu_model(), "sample": sample},
             "e2e": {"value": v, "unit": "env-steps/s", "h2d_bytes_per_step": 0,
@@ -826,17 +1003,24 @@ def run_reference(args, wl_name):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=200, help="steps per timed trial (headline)")
     ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--trials", type=int, default=5, help="timed trials of K steps each")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gae_returns_4096x1024", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--suite", choices=["auto", "on", "off"], default="auto",
+                    help="also measure the other workloads (auto: with the headline workload at N=1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--capture-traffic", action="store_true",
+                    help="run the fixed launch schedule of a DRAM-traffic capture (no timing)")
     ap.add_argument("--e2e-streams", type=int, default=E2E_STREAMS,
                     help="streams the end-to-end steps rotate over")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="end-to-end steps (0: --steps)")
     ap.add_argument("--e2e-mode", choices=["zerocopy", "copies"], default="copies",
                     help="end-to-end leg: kernels on the pinned host buffers, or explicit copies")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    args.trials = max(1, args.trials)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -848,15 +1032,23 @@ def main():
         print(json.dumps(run_reference(args, args.workload)))
         return
 
+    if args.capture_traffic:
+        if rank == 0:
+            print(json.dumps(capture_schedule(args, args.workload)))
+        return
+
+    suite = (args.suite == "on" or (args.suite == "auto" and args.workload == HEADLINE)) and world == 1
     if world > 1:
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    res = run_ours(args, args.workload, rank, world, local_rank)
+    res = run_ours(args, args.workload, rank, world, local_rank, SUITE if suite else ())
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(args.workload)
+            for sub, rec in res.get("workloads", {}).items():
+                rec["cpu_baseline"] = cpu_baseline(sub, seconds=1.5, one_core=False)
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist

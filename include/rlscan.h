@@ -214,10 +214,16 @@ rlscan_status rlscan_gae_returns(const float *rewards, const float *values,
  * before any device work.  Same arguments and results as rlscan_gae, minus
  * the workspace.  The first call on a device looks up the buffer's address
  * and zeroes it on `stream`; make that first call before any stream
- * capture.  Every call clears the buffer's header on `stream` before its
- * kernel; calls that share the buffer and overlap on the GPU (unordered
- * streams) race and must not be issued.  A timed-out cross-block wait shows
- * up as NaN outputs (this variant has no status query).
+ * capture.  The address is kept for the life of the process: tearing the
+ * device's primary context down between calls (cudaDeviceReset) is not
+ * supported.  Argument conflicts (as rlscan_gae) are refused before the
+ * buffer is touched; a call refused later (a content check with
+ * RLSCAN_CHECKS=1, a failed launch) may already have enqueued the header
+ * clear, which is harmless.  Every call clears the buffer's header on
+ * `stream` before its kernel; calls that share the buffer and overlap on
+ * the GPU (unordered streams) race and must not be issued.  A timed-out
+ * cross-block wait shows up as NaN outputs (this variant has no status
+ * query); later calls are unaffected.
  */
 rlscan_status rlscan_gae_noalloc(const float *rewards, const float *values,
                                  const float *terminateds, const float *truncateds,
@@ -232,9 +238,12 @@ rlscan_status rlscan_gae_noalloc(const float *rewards, const float *values,
  *   adv_t <- (A_t - mean) / (std + eps)
  * with mean and the unbiased (n - 1) standard deviation of all N*T raw GAE
  * advantages A_t of the call (rlscan_gae's values).  The scan kernel also
- * accumulates the batch moments (sum and sum of squares, per CTA in double
- * precision); a second kernel, ordered after it on `stream`, combines the
- * per-CTA sums in CTA order and normalises the advantages in place.
+ * accumulates the batch moments (sum and sum of squares): each thread sums
+ * its advantages of a tile in float and carries the totals across tiles as
+ * float pairs (unevaluated sums hi + lo, combined with Knuth's TwoSum), the
+ * CTA combines its threads' pairs the same way and writes one pair per
+ * moment; a second kernel, ordered after it on `stream`, combines the
+ * per-CTA pairs in CTA order and normalises the advantages in place.
  * lambda_returns (A_t + V_t) and discounted_returns are computed from the
  * RAW advantages, as in rlscan_gae_returns.
  * Inputs : as rlscan_gae_returns; eps >= 0 (else RLSCAN_ERR_ARG_VALUE).

@@ -149,6 +149,7 @@ struct VTrace {
     static constexpr unsigned FLAGS = (1u << 4) | (TRUNC ? (1u << 5) : 0u);  // 0/1 inputs
     static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = false, ROWSCALAR = !BS2D;
+    static constexpr bool LB_ROW_MAJOR = true;  // measured faster on 2^20-step rows
     static constexpr unsigned HALO = 1u << 2;
     static constexpr int TR = 5, BS = 5 + TRUNC;
     template <int I> struct Keep { float rho[I]; };
@@ -516,6 +517,7 @@ struct Prefix {
     static constexpr int NIN = 2, NOUT = 1;
     static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = true, ROWSCALAR = true;
+    static constexpr bool LB_CHAIN = true;  // beta = 1 within episodes
     static constexpr unsigned HALO = STARTS_AT ? 0u : (1u << 1);
     template <int I> struct Keep {};
 
@@ -554,6 +556,7 @@ struct Linear {
     static constexpr int NIN = 2, NOUT = 1;
     static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = FORWARD, ROWSCALAR = true;
+    static constexpr bool LB_CHAIN = true;  // beta is the caller's: often 1
     static constexpr unsigned HALO = 0;
     template <int I> struct Keep {};
 

@@ -49,6 +49,11 @@ namespace rlscan {
 #ifndef RLSCAN_THREADS_1024
 #define RLSCAN_THREADS_1024 256
 #endif
+// Packed tiles (whole rows) drawn from the workspace header's ticket when a
+// workspace is given (1), or assigned statically (0).
+#ifndef RLSCAN_PACKED_DYNAMIC
+#define RLSCAN_PACKED_DYNAMIC 0
+#endif
 // Estimators with wide inputs (several words per step, e.g. [N,T,A]) move
 // far more bytes per step: 1024-step tiles, and a ring of WIDE_STAGES stages
 // whose size depends on the runtime width (one CTA per SM at A = 4).
@@ -262,6 +267,16 @@ rlscan_status launch_scan_ring(Params p, void *ws, size_t ws_bytes, cudaStream_t
 
     if (p.T <= TILE) {
         bind_packed<E>(p);
+        // Packed tiles need no look-back, but when the caller's workspace is
+        // at hand its header's ticket hands them out dynamically, so CTAs on
+        // faster SMs take more tiles and all finish together.  Kernels that
+        // accumulate moments keep the static order (their per-CTA sums, and
+        // so the normalised outputs, are then the same bits on every call).
+        if (RLSCAN_PACKED_DYNAMIC && !MomentsOf<E>::value && ws != nullptr && ws_bytes >= kHeaderBytes &&
+            aligned16(ws) && residency(ws) == Residency::Device) {
+            p.dynamic = 1;
+            p.hdr = static_cast<uint32_t *>(ws);
+        }
     } else {
         p.packed = 0;
         p.C = TILE;

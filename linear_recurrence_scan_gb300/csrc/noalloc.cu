@@ -15,13 +15,18 @@
 // library holds kScratchBytes of it until the process exits.  In host code
 // the array's name is only a host-side stand-in; its device address is
 // looked up with cudaGetSymbolAddress once per device, with that device
-// current, the first time this entry point runs there.  That first call
-// also zeroes the buffer, so it should happen before any stream capture.
+// current, the first time this entry point runs there, and kept for the
+// life of the process (a cudaDeviceReset, or any other teardown of the
+// device's primary context, between calls is not supported: the module is
+// reloaded and the kept address may no longer be the buffer's).  That
+// first call also zeroes the buffer, so it should happen before any stream
+// capture.
 // All calls share the buffer: each call clears the buffer header (tile
 // ticket and counters) on its stream before launching, and the tile states
 // themselves are tagged per call, so stale contents are never consumed.
 // Calls whose executions overlap on the GPU (different streams, no
 // ordering) race on the buffer and must not be issued.
+#include <initializer_list>
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -71,6 +76,14 @@ extern "C" RLSCAN_API rlscan_status rlscan_gae_noalloc(
     if (N < 0 || T < 0 || row_stride < T) return RLSCAN_ERR_SHAPE;
     if (N == 0 || T == 0) return RLSCAN_OK;
     if (!rewards || !values || !terminateds || !advantages) return RLSCAN_ERR_NULL;
+    // rlscan_gae's own argument conflicts, checked before the shared buffer
+    // is touched, so a rejected call enqueues nothing
+    if (bootstrap_values && last_value) return RLSCAN_ERR_ARG_CONFLICT;
+    if (last_value && truncateds) return RLSCAN_ERR_ARG_CONFLICT;
+    for (const void *in : {static_cast<const void *>(rewards), static_cast<const void *>(values),
+                           static_cast<const void *>(terminateds), static_cast<const void *>(truncateds),
+                           static_cast<const void *>(bootstrap_values), static_cast<const void *>(last_value)})
+        if (in != nullptr && in == static_cast<const void *>(advantages)) return RLSCAN_ERR_ARG_CONFLICT;
     const size_t need = rlscan_workspace_bytes(N, T);
     if (need > kScratchBytes) return RLSCAN_ERR_SCRATCH_LIMIT;
     void *ws = nullptr;

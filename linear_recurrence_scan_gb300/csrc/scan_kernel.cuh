@@ -109,6 +109,35 @@ struct MomentsOf<E, std::void_t<decltype(E::MOMENTS)>> {
     static constexpr bool value = E::MOMENTS;
 };
 
+// Estimators whose tile aggregates usually keep a nonzero decay (beta = 1
+// within episodes: prefix sums, the generic scan): a chained tile cannot
+// resolve its carry from its nearest predecessor's aggregate alone, so the
+// deferred kernel prefetches a window of predecessor states (see
+// RLSCAN_LB_WINDOW) instead of one.
+template <class E, class = void>
+struct ChainOf {
+    static constexpr bool value = false;
+};
+template <class E>
+struct ChainOf<E, std::void_t<decltype(E::LB_CHAIN)>> {
+    static constexpr bool value = E::LB_CHAIN;
+};
+
+// Estimators whose look-back states are laid out row-major (see state_pos):
+// the chain estimators and those that declare LB_ROW_MAJOR.
+template <class E, class = void>
+struct RowMajorDecl {
+    static constexpr bool value = false;
+};
+template <class E>
+struct RowMajorDecl<E, std::void_t<decltype(E::LB_ROW_MAJOR)>> {
+    static constexpr bool value = E::LB_ROW_MAJOR;
+};
+template <class E>
+struct RowMajorOf {
+    static constexpr bool value = ChainOf<E>::value || RowMajorDecl<E>::value;
+};
+
 // Shared-memory slot of narrow input j within a stage: the copied arrays
 // first, in input order, then the derived ones.  The wide region starts
 // after the copied arrays and overlays the derived slots: prepass() reads
@@ -188,6 +217,8 @@ __device__ __forceinline__ Pair compose(Pair outer, Pair inner)
 
 constexpr uint32_t kTagAgg = 1u, kTagPrefix = 2u;
 
+
+
 // Longest pause between two polls of a predecessor's state (ns); the pause
 // starts at 32 ns and doubles.  0: poll without pausing.
 #ifndef RLSCAN_LB_NAP_MAX
@@ -205,10 +236,30 @@ __device__ __forceinline__ void record_error(const Params &p, uint32_t code, uin
     if (atomicCAS(&p.hdr[kHdrError], 0u, code) == 0u) atomicExch(&p.hdr[kHdrDetail], detail);
 }
 
+// Where tile (row, j)'s states sit in the workspace (in units of K states):
+// ticket order (j N + row: the tiles in flight together side by side) or
+// row-major (row tiles_per_row + j: a row's tiles side by side, so the tiles
+// that run together write different cache lines and a tile's predecessors
+// share its line).  The predecessor of position q is q - state_step<RM>(p).
+// The layout is private to one launch; each estimator takes the one that
+// measured faster for it (RowMajorOf), RLSCAN_STATE_ROW_MAJOR = 0 or 1
+// forces one for all.
+#ifndef RLSCAN_STATE_ROW_MAJOR
+#define RLSCAN_STATE_ROW_MAJOR -1
+#endif
+template <bool RM>
+__device__ __forceinline__ int64_t state_pos(const Params &p, int64_t g, int64_t row, int64_t j)
+{
+    return RM ? row * p.tiles_per_row + j : g;  // ticket g = j N + row
+}
+template <bool RM>
+__device__ __forceinline__ int64_t state_step(const Params &p) { return RM ? 1 : p.N; }
+
 struct TileGeo {
     int64_t row0;  // first row of the tile
     int64_t t0;    // first time step held by the tile
     int64_t j;     // position of the tile within its row, in scan order
+    int64_t pos;   // position of the tile's look-back states (state_pos)
     int32_t nrows; // rows present (packed) or 1
     int32_t len;   // time steps present per row
 };
@@ -216,7 +267,7 @@ struct TileGeo {
 // Tile g -> rows and time range.  Packed: rows [g R, g R + R).  Long rows:
 // ticket g = j * N + row (all rows' j-th tiles before any (j+1)-th tile);
 // j counts tiles in scan order (from t = T-1 backward, from t = 0 forward).
-template <bool FWD, int TILE>
+template <bool FWD, int TILE, bool RM>
 __device__ __forceinline__ TileGeo decode_tile(const Params &p, int64_t g)
 {
     TileGeo tg;
@@ -227,6 +278,7 @@ __device__ __forceinline__ TileGeo decode_tile(const Params &p, int64_t g)
         tg.t0 = 0;
         tg.len = static_cast<int32_t>(p.T);
         tg.j = 0;
+        tg.pos = 0;
     } else {
         tg.j = g / p.N;
         tg.row0 = g - tg.j * p.N;
@@ -235,6 +287,7 @@ __device__ __forceinline__ TileGeo decode_tile(const Params &p, int64_t g)
         const int64_t rem = p.T - tg.t0;
         tg.len = rem < TILE ? static_cast<int32_t>(rem) : TILE;
         tg.nrows = 1;
+        tg.pos = state_pos<RM>(p, g, tg.row0, tg.j);
     }
     return tg;
 }
@@ -424,20 +477,21 @@ __device__ __forceinline__ void publish_inclusive(const Params &p, uint32_t epoc
 }
 
 // Reading side (one thread per warp and scan): the value entering tile g
-// (position j > 0 of its row) from its scan-order predecessor, i.e. A at the
-// step just outside the tile, for scan `sc` of K.  (w0, w1) are the
-// predecessor's state words as fetched when the tile started.  Walks back
+// (state position pos, position j > 0 of its row) from its scan-order
+// predecessor, i.e. A at the step just outside the tile, for scan `sc` of K.
+// (w0, w1) are the predecessor's state words as fetched earlier.  Walks back
 // through aggregates until an inclusive value, a zero decay, or the row's
 // first tile; every wait is bounded.
-template <int K>
-__device__ inline float lookback_read(const Params &p, uint32_t epoch, int64_t g, int64_t j, int sc,
+template <int K, bool RM>
+__device__ inline float lookback_read(const Params &p, uint32_t epoch, int64_t g, int64_t pos, int64_t j, int sc,
                                       unsigned long long w0, unsigned long long w1)
 {
     const unsigned long long *st = p.states;
     const uint32_t tagA = (epoch << 2) | kTagAgg;
     const uint32_t tagP = (epoch << 2) | kTagPrefix;
     Pair acc{0.f, 1.f};
-    int64_t k = g - p.N;
+    const int64_t step = state_step<RM>(p);
+    int64_t k = pos - step;  // state position of the tile being read
     int64_t left = j;  // predecessors not yet folded in
     uint64_t waited_since = 0;
     uint32_t nap = 32;
@@ -455,7 +509,7 @@ __device__ inline float lookback_read(const Params &p, uint32_t epoch, int64_t g
             acc = compose(acc, Pair{__uint_as_float(static_cast<uint32_t>(w0)),
                                     __uint_as_float(static_cast<uint32_t>(w1))});
             if (acc.b == 0.f || --left == 0) return acc.a;
-            k -= p.N;
+            k -= step;
             waited_since = 0;
             nap = 32;
             continue;
@@ -551,6 +605,26 @@ constexpr int block_threads() { return THREADS + 32; }
 #ifndef RLSCAN_EARLY_RELEASE
 #define RLSCAN_EARLY_RELEASE 1
 #endif
+// Look-back window of the deferred kernels of chain estimators: lanes
+// 0..W-1 of every warp fetch the states of the W nearest predecessors when
+// the pending tile's finishing iteration starts, and the walk composes them
+// with a shuffle reduction (one round trip, already in flight, instead of a
+// chain of dependent loads); it falls back to the serial walk when the
+// window holds no resolved value.  0: off.  RLSCAN_LB_WINDOW_ALL=1 applies
+// it to every single-scan estimator.
+#ifndef RLSCAN_LB_WINDOW
+#define RLSCAN_LB_WINDOW 8
+#endif
+#ifndef RLSCAN_LB_WINDOW_ALL
+#define RLSCAN_LB_WINDOW_ALL 0
+#endif
+// Start-up: the barriers are initialised (and made visible) before the
+// wait for the previous kernel, so the producer issues its first copies as
+// soon as that wait ends (1; 0: one block-wide barrier after the wait).
+// Measured: 0.3-1.3 % on every kernel, the short ones most.
+#ifndef RLSCAN_EARLY_START
+#define RLSCAN_EARLY_START 1
+#endif
 #ifndef RLSCAN_DEFER_MIN_BLOCKS
 #define RLSCAN_DEFER_MIN_BLOCKS 0  // 0: as the immediate-finish kernel
 #endif
@@ -578,6 +652,9 @@ scan_kernel(const __grid_constant__ Params p)
     static_assert(TILE >= kSmallestTile && K * (TILE >= kMinTile ? 1 : kMinTile / TILE) <= kMaxScans,
                   "the workspace holds kMaxScans states per 1024 steps");
     constexpr int NWIDE = WideOf<E>::NWIDE;
+    constexpr int LBW = (DEFER && K == 1 && (ChainOf<E>::value || RLSCAN_LB_WINDOW_ALL)) ? RLSCAN_LB_WINDOW : 0;
+    constexpr bool RM = RLSCAN_STATE_ROW_MAJOR < 0 ? RowMajorOf<E>::value : RLSCAN_STATE_ROW_MAJOR != 0;
+    static_assert(LBW >= 0 && LBW <= 32, "look-back window: at most one warp of states");
     static_assert(NWIDE == 0 || !FWD, "wide inputs are staged for backward recurrences only");
 
     extern __shared__ __align__(128) float smem[];
@@ -607,12 +684,24 @@ scan_kernel(const __grid_constant__ Params p)
         }
         ptx::fence_mbar_init();
     }
-    // nothing global is touched before the previous kernel has completed
-    ptx::pdl_wait_prerequisites();
     __shared__ uint32_t s_epoch;
-    if (tid == 0) s_epoch = p.dynamic ? (ptx::ld_relaxed_u32(&p.hdr[kHdrEpoch]) & 0x3FFFFFFFu) : 0u;
-    __syncthreads();
-    const uint32_t epoch = s_epoch;  // tag of this call's tile states
+    if (RLSCAN_EARLY_START) {
+        // the barriers are initialised while the previous kernel drains; after
+        // the wait the producer issues its first copies at once, and only the
+        // compute warps meet to share the epoch
+        __syncthreads();
+        ptx::pdl_wait_prerequisites();
+        if (warp < WARPS) {
+            if (tid == 0) s_epoch = p.dynamic ? (ptx::ld_relaxed_u32(&p.hdr[kHdrEpoch]) & 0x3FFFFFFFu) : 0u;
+            ptx::named_barrier(1, THREADS);
+        }
+    } else {
+        // nothing global is touched before the previous kernel has completed
+        ptx::pdl_wait_prerequisites();
+        if (tid == 0) s_epoch = p.dynamic ? (ptx::ld_relaxed_u32(&p.hdr[kHdrEpoch]) & 0x3FFFFFFFu) : 0u;
+        __syncthreads();
+    }
+    const uint32_t epoch = warp < WARPS ? s_epoch : 0u;  // tag of this call's tile states (compute warps)
 
     if (warp == WARPS) {
         // Producer (lane 0 of the extra warp): for ring slot s of iteration
@@ -643,7 +732,7 @@ scan_kernel(const __grid_constant__ Params p)
                     ptx::mbar_arrive(&full_bar[s]);
                     break;
                 }
-                const TileGeo tg = decode_tile<FWD, TILE>(p, g);
+                const TileGeo tg = decode_tile<FWD, TILE, RM>(p, g);
                 s_geo[s] = tg;
                 ptx::mbar_arrive(&meta_bar[s]);  // the tile is known before its data lands
                 if (tma) issue_tile_copies<E, TILE, AST>(p, tg, smem + s * SST, &full_bar[s], smem);
@@ -657,9 +746,11 @@ scan_kernel(const __grid_constant__ Params p)
     const int col = p.packed ? li - rit * p.C : li;
 
     // Row scalar of this thread's row when the row's boundary step falls in
-    // its range.  Fetched one tile ahead once that tile is known (its slot's
-    // meta phase has completed; its data may still be in flight), so the
-    // latency is hidden.
+    // its range.  Fetched as soon as its tile is known (the slot's meta phase
+    // has completed; its data may still be in flight): for the next tile when
+    // a tile starts, else for this tile before waiting for its data, so the
+    // load's latency never holds the tile (one thread's wait would hold the
+    // whole CTA at the tile's barrier).
     auto load_row_scalar = [&](int s) -> float {
         if (tile_ids[s] >= p.num_tiles) return 0.f;
         const TileGeo tg = s_geo[s];
@@ -687,26 +778,73 @@ scan_kernel(const __grid_constant__ Params p)
         for (int j = 0; j < NIN; ++j) {
             const int eb = IoOf<E>::in(j);
             const char *aj = elem0<E, TILE>(stage, j) + li * eb;
-#pragma unroll
-            for (int k = 0; k < ITEMS; k += 4) {
+            // four consecutive steps of array j from `q` (one 16-, 8- or
+            // 4-byte shared-memory load): float32, bf16 (a float's upper 16
+            // bits each) or uint8
+            auto load4 = [&](const char *q, float (&v)[4]) {
                 if (eb == 4) {
-                    const float4 v = *reinterpret_cast<const float4 *>(aj + 4 * k);
-                    x[j][k] = v.x;
-                    x[j][k + 1] = v.y;
-                    x[j][k + 2] = v.z;
-                    x[j][k + 3] = v.w;
-                } else if (eb == 2) {  // four bf16: a float's upper 16 bits each
-                    const uint2 v = *reinterpret_cast<const uint2 *>(aj + 2 * k);
-                    x[j][k] = __uint_as_float(v.x << 16);
-                    x[j][k + 1] = __uint_as_float(v.x & 0xffff0000u);
-                    x[j][k + 2] = __uint_as_float(v.y << 16);
-                    x[j][k + 3] = __uint_as_float(v.y & 0xffff0000u);
-                } else {               // four uint8
-                    const uint32_t v = *reinterpret_cast<const uint32_t *>(aj + k);
-                    x[j][k] = static_cast<float>(v & 0xffu);
-                    x[j][k + 1] = static_cast<float>((v >> 8) & 0xffu);
-                    x[j][k + 2] = static_cast<float>((v >> 16) & 0xffu);
-                    x[j][k + 3] = static_cast<float>(v >> 24);
+                    const float4 w = *reinterpret_cast<const float4 *>(q);
+                    v[0] = w.x;
+                    v[1] = w.y;
+                    v[2] = w.z;
+                    v[3] = w.w;
+                } else if (eb == 2) {
+                    const uint2 w = *reinterpret_cast<const uint2 *>(q);
+                    v[0] = __uint_as_float(w.x << 16);
+                    v[1] = __uint_as_float(w.x & 0xffff0000u);
+                    v[2] = __uint_as_float(w.y << 16);
+                    v[3] = __uint_as_float(w.y & 0xffff0000u);
+                } else {
+                    const uint32_t w = *reinterpret_cast<const uint32_t *>(q);
+                    v[0] = static_cast<float>(w & 0xffu);
+                    v[1] = static_cast<float>((w >> 8) & 0xffu);
+                    v[2] = static_cast<float>((w >> 16) & 0xffu);
+                    v[3] = static_cast<float>(w >> 24);
+                }
+            };
+            if constexpr (ITEMS == 8) {
+                if (eb == 2) {  // eight bf16 in one 16-byte load (lanes 16 bytes apart: conflict-free)
+                    const uint4 w = *reinterpret_cast<const uint4 *>(aj);
+                    const uint32_t h[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        x[j][2 * q] = __uint_as_float(h[q] << 16);
+                        x[j][2 * q + 1] = __uint_as_float(h[q] & 0xffff0000u);
+                    }
+                } else if (eb == 1) {  // eight uint8 in one 8-byte load (conflict-free)
+                    const uint2 w = *reinterpret_cast<const uint2 *>(aj);
+                    const uint32_t h[2] = {w.x, w.y};
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        x[j][4 * q] = static_cast<float>(h[q] & 0xffu);
+                        x[j][4 * q + 1] = static_cast<float>((h[q] >> 8) & 0xffu);
+                        x[j][4 * q + 2] = static_cast<float>((h[q] >> 16) & 0xffu);
+                        x[j][4 * q + 3] = static_cast<float>(h[q] >> 24);
+                    }
+                } else {
+                    // Two 16-byte chunks per thread: consecutive lanes' first
+                    // chunks lie 2 chunks apart, so in one shared-memory
+                    // wavefront (8 lanes of 16-byte loads) lanes l and l + 4
+                    // would hit the same banks.  Lanes 4..7 of each group of 8
+                    // read their second chunk first (two-way conflicts gone),
+                    // then the chunks are put back in order.
+                    const bool sw = ((lane >> 2) & 1) != 0;
+                    float c0[4], c1[4];
+                    load4(aj + (sw ? 16 : 0), c0);
+                    load4(aj + (sw ? 0 : 16), c1);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        x[j][q] = sw ? c1[q] : c0[q];
+                        x[j][q + 4] = sw ? c0[q] : c1[q];
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < ITEMS; k += 4) {
+                    float v[4];
+                    load4(aj + k * eb, v);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) x[j][k + q] = v[q];
                 }
             }
             float nb = 0.f;
@@ -834,18 +972,61 @@ scan_kernel(const __grid_constant__ Params p)
     // Value entering a chained tile per scan (lane sc < K walks scan sc from
     // the prefetched predecessor words), broadcast to the warp; the
     // publishing warp then publishes the tile's inclusive values.
-    auto carry_in = [&](int64_t g, int64_t j, const Pair (&total)[K], unsigned long long w0,
+    auto carry_in = [&](int64_t g, int64_t pos, int64_t j, const Pair (&total)[K], unsigned long long w0,
                         unsigned long long w1, float (&carry)[K]) {
         float mine = 0.f;
-        if (lane < K) mine = lookback_read<K>(p, epoch, g, j, lane, w0, w1);
+        if (lane < K) mine = lookback_read<K, RM>(p, epoch, g, pos, j, lane, w0, w1);
 #pragma unroll
         for (int sc = 0; sc < K; ++sc) carry[sc] = __shfl_sync(0xffffffffu, mine, sc);
         if (warp == PUB_WARP && lane == 0) {
 #pragma unroll
             for (int sc = 0; sc < K; ++sc)
                 if (total[sc].b != 0.f)
-                    publish_inclusive<K>(p, epoch, g * K + sc, g, fmaf(total[sc].b, carry[sc], total[sc].a));
+                    publish_inclusive<K>(p, epoch, pos * K + sc, g, fmaf(total[sc].b, carry[sc], total[sc].a));
         }
+    };
+
+    // Windowed variant (chain estimators, deferred tiles, one scan): lane l
+    // holds the state words of the tile l + 1 positions back in the row.  The
+    // nearest lane with a resolved value (an inclusive value, or an
+    // aggregate with b = 0), all lanes before it holding aggregates, gives
+    // the carry as the composition of lanes 0..f in order (lane 0 outermost),
+    // reduced across the warp; otherwise lane 0 walks serially from its own
+    // words (waits, timeouts and NaN as in lookback_read).
+    auto carry_in_window = [&](int64_t g, int64_t pos, int64_t j, const Pair (&total)[K], unsigned long long w0,
+                               unsigned long long w1, float (&carry)[K]) {
+        const uint32_t tagA = (epoch << 2) | kTagAgg;
+        const uint32_t tagP = (epoch << 2) | kTagPrefix;
+        const int n = j < LBW ? static_cast<int>(j) : LBW;
+        const bool in = lane < n;
+        const bool isP = in && static_cast<uint32_t>(w0 >> 32) == tagP;
+        const bool isA = in && !isP && static_cast<uint32_t>(w0 >> 32) == tagA &&
+                         static_cast<uint32_t>(w1 >> 32) == tagA;
+        Pair v{0.f, 1.f};
+        if (isP) v = Pair{__uint_as_float(static_cast<uint32_t>(w0)), 0.f};
+        else if (isA) v = Pair{__uint_as_float(static_cast<uint32_t>(w0)), __uint_as_float(static_cast<uint32_t>(w1))};
+        const unsigned resolved = __ballot_sync(0xffffffffu, isP || (isA && v.b == 0.f));
+        const unsigned missing = __ballot_sync(0xffffffffu, in && !isP && !isA);
+        const int f = __ffs(resolved) - 1;  // nearest resolved lane, -1 if none
+        float c;
+        if (resolved != 0u && (missing & ((2u << f) - 1u)) == 0u) {
+            if (lane > f) v = Pair{0.f, 1.f};
+#pragma unroll
+            for (int off = 1; off < LBW; off <<= 1) {
+                Pair o;
+                o.a = __shfl_down_sync(0xffffffffu, v.a, off);
+                o.b = __shfl_down_sync(0xffffffffu, v.b, off);
+                if (lane + off < 32) v = compose(v, o);
+            }
+            c = __shfl_sync(0xffffffffu, v.a, 0);
+        } else {
+            float mine = 0.f;
+            if (lane == 0) mine = lookback_read<K, RM>(p, epoch, g, pos, j, 0, w0, w1);
+            c = __shfl_sync(0xffffffffu, mine, 0);
+        }
+        carry[0] = c;
+        if (warp == PUB_WARP && lane == 0 && total[0].b != 0.f)
+            publish_inclusive<K>(p, epoch, pos * K, g, fmaf(total[0].b, c, total[0].a));
     };
 
     // Deferred finishing (long rows with several tiles of a row in flight):
@@ -856,6 +1037,8 @@ scan_kernel(const __grid_constant__ Params p)
     bool pend = false;
     int ps = 0;
     int64_t pg = 0;
+    // state position of the pending tile (its geometry stays in s_geo[ps])
+    auto pending_pos = [&]() { return RM ? s_geo[ps].pos : pg; };
     float prsc = 0.f;
     Pair pex[K], pwe[K], ptot[K];
     unsigned long long pw0 = 0, pw1 = 0;
@@ -867,7 +1050,10 @@ scan_kernel(const __grid_constant__ Params p)
         float carry[K];
 #pragma unroll
         for (int sc = 0; sc < K; ++sc) carry[sc] = 0.f;
-        if (tg.j > 0) carry_in(pg, tg.j, ptot, pw0, pw1, carry);
+        if (tg.j > 0) {
+            if constexpr (LBW > 0) carry_in_window(pg, pending_pos(), tg.j, ptot, pw0, pw1, carry);
+            else carry_in(pg, pending_pos(), tg.j, ptot, pw0, pw1, carry);
+        }
         const ThreadSpan sp = thread_span<FWD, ITEMS>(p, tg, rit, col);
         float x[NIN][ITEMS], xn[NIN];
         load_inputs(smem + ps * SST, x, xn);
@@ -881,9 +1067,20 @@ scan_kernel(const __grid_constant__ Params p)
         if (lane == 0) ptx::mbar_arrive(&empty_bar[ps]);  // the pending tile's stage is free
         pend = false;
     };
-    auto prefetch_pending = [&]() {  // first predecessor state of the pending tile
+    auto prefetch_pending = [&]() {  // nearest predecessor states of the pending tile
+        if constexpr (LBW > 0) {  // lane l: the tile l + 1 positions back (one scan)
+            pw0 = pw1 = 0ull;
+            if (lane < LBW && lane < s_geo[ps].j) {
+                const int64_t slot = pending_pos() - static_cast<int64_t>(lane + 1) * state_step<RM>(p);
+                if (state_ok(p, 2 * slot + 1, K)) {
+                    pw0 = ptx::ld_relaxed(&p.states[2 * slot]);
+                    pw1 = ptx::ld_relaxed(&p.states[2 * slot + 1]);
+                }
+            }
+            return;
+        }
         if (s_geo[ps].j > 0 && lane < K) {
-            const int64_t slot = (pg - p.N) * K + lane;
+            const int64_t slot = (pending_pos() - state_step<RM>(p)) * K + lane;
             if (state_ok(p, 2 * slot + 1, K)) {
                 pw0 = ptx::ld_relaxed(&p.states[2 * slot]);
                 pw1 = ptx::ld_relaxed(&p.states[2 * slot + 1]);
@@ -908,11 +1105,12 @@ scan_kernel(const __grid_constant__ Params p)
         if constexpr (RLSCAN_CHECK_BOUNDS) smem_ok(p, smem, stage, static_cast<uint64_t>(SST) * 4u, kSiteRing);
         const bool chained = !p.packed && tg.j > 0;  // needs its predecessor's value
 
+
         // predecessor states for an immediate look-back (lane sc < K reads
         // scan sc), fetched early so their latency overlaps the tile's work
         unsigned long long cw0 = 0, cw1 = 0;
         if (!defer && chained && lane < K) {
-            const int64_t slot = (g - p.N) * K + lane;
+            const int64_t slot = ((RM ? tg.pos : g) - state_step<RM>(p)) * K + lane;
             if (state_ok(p, 2 * slot + 1, K)) {
                 cw0 = ptx::ld_relaxed(&p.states[2 * slot]);
                 cw1 = ptx::ld_relaxed(&p.states[2 * slot + 1]);
@@ -990,7 +1188,8 @@ scan_kernel(const __grid_constant__ Params p)
         if (!p.packed && warp == PUB_WARP && lane == 0) {
 #pragma unroll
             for (int sc = 0; sc < K; ++sc)
-                publish_first<K>(p, epoch, g * K + sc, g, tg.j, compose(wa[PUB_WARP][sc], we[sc]));
+                publish_first<K>(p, epoch, (RM ? tg.pos : g) * K + sc, g, tg.j,
+                                 compose(wa[PUB_WARP][sc], we[sc]));
         }
 
         if (!defer) {
@@ -1001,7 +1200,7 @@ scan_kernel(const __grid_constant__ Params p)
                 Pair total[K];
 #pragma unroll
                 for (int sc = 0; sc < K; ++sc) total[sc] = compose(wa[PUB_WARP][sc], we[sc]);
-                carry_in(g, tg.j, total, cw0, cw1, carry);
+                carry_in(g, (RM ? tg.pos : g), tg.j, total, cw0, cw1, carry);
             }
             float x_in[K];
 #pragma unroll

@@ -35,6 +35,10 @@ def test_reference_arm_prints_one_contract_line():
     assert d["value"] > 0 and d["unit"] == "env-steps/s" and d["higher_is_better"] is True
     assert d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["config"]["workload"] == "gae_8x128"
+    sys.path.insert(0, ROOT)
+    import bench
+    # both arms print the same config object for a workload
+    assert d["config"] == bench.workload_config("gae_8x128")
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
@@ -64,8 +68,8 @@ def bench_module():
 
 def test_traffic_record_only_for_the_recorded_sources(bench_module, monkeypatch):
     b = bench_module
-    with open(os.path.join(ROOT, "profiles", "traffic.md")) as f:
-        rec = json.loads(f.read().split("```json", 1)[1].split("```", 1)[0])
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)["records"]
     key = "gae_returns@gae_returns_4096x1024"
     entry = rec[key]
     monkeypatch.setattr(b, "_csrc_hash", lambda: entry["csrc_sha"])
@@ -100,3 +104,26 @@ def test_every_workload_generates_its_inputs(bench_module):
         assert shapes, name
         for k, s in shapes.items():
             assert s[:2] == (4, T), (name, k, s)
+
+
+def test_default_headline_is_the_largest_configuration(bench_module):
+    b = bench_module
+    assert b.HEADLINE == "long_rows_64x1048576"
+    sizes = {n: w["N"] * w["T"] for n, w in b.WORKLOADS.items()}
+    assert sizes[b.HEADLINE] == max(sizes.values())
+    # every named workload is measured beside the headline, each once
+    assert len(set(b.SUITE)) == len(b.SUITE) and b.HEADLINE not in b.SUITE
+    assert set(b.SUITE) | {b.HEADLINE} == set(b.WORKLOADS)
+
+
+def test_l2_plan_rotates_small_workloads_only(bench_module):
+    b = bench_module
+    for name in b.WORKLOADS:
+        n_sets, set_bytes = b.l2_plan(name)
+        assert set_bytes > 0
+        if set_bytes > 4 * b.L2_BYTES:
+            assert n_sets == 1, name
+        else:
+            assert n_sets * set_bytes > 129 * 1024 * 1024 or n_sets == 16, name
+    assert b.l2_plan("long_rows_64x1048576")[0] == 1
+    assert b.l2_plan("gae_returns_4096x1024")[0] >= 4
