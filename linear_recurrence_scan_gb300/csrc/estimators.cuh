@@ -46,6 +46,20 @@ __device__ __forceinline__ float done_of(float term, float trunc) { return fminf
 // undefined ratio such as 0/0 shows in the outputs instead of being clipped
 __device__ __forceinline__ float clip_above(float clip, float x) { return clip < x ? clip : x; }
 
+// Importance ratios.  RLSCAN_FAST_RATIO=1 (default) takes CUDA's fast
+// intrinsics __expf and __fdividef (relative error of a few 1e-7 for the
+// log-ratios and probabilities of these estimators) instead of the
+// correctly rounded expf and IEEE division; the ratio is clipped and
+// multiplies terms whose own float32 rounding is of that size, so the
+// outputs stay far inside the parity bound.  Measured: compact Retrace
+// 1024 x 16384 55.2 -> 48.4 us, compact V-trace 33.4 -> 32.4 us; the
+// float32 kernels, bandwidth-bound, unchanged.
+#ifndef RLSCAN_FAST_RATIO
+#define RLSCAN_FAST_RATIO 1
+#endif
+__device__ __forceinline__ float ratio_exp(float log_ratio) { return RLSCAN_FAST_RATIO ? __expf(log_ratio) : expf(log_ratio); }
+__device__ __forceinline__ float ratio_div(float num, float den) { return RLSCAN_FAST_RATIO ? __fdividef(num, den) : num / den; }
+
 // ---------------------------------------------------------------------------
 // GAE: alpha = r + gamma (1-term) Vn - V, beta = gamma lambda (1-done), A_T = 0.
 // Inputs: 0 rewards, 1 values, 2 terminateds, [3 truncateds], [3+TRUNC bootstrap].
@@ -176,7 +190,7 @@ struct VTrace {
 #pragma unroll
         for (int k = 0; k < I; ++k) {
             const bool last = (EDGE && k == kb);
-            const float ratio = expf(x[0][k] - x[1][k]);
+            const float ratio = ratio_exp(x[0][k] - x[1][k]);
             const float rho = clip_above(p.c1, ratio), c = clip_above(p.c2, ratio);
             const float term = x[4][k];
             const float vn = successor<I>(x, k, last, (k + 1 < I) ? x[2][k + 1] : xn[2], rsc);
@@ -232,11 +246,11 @@ struct Retrace {
         float c[I + 1];
 #pragma unroll
         for (int k = 0; k < I; ++k) {
-            const float ratio = x[0][k] / x[1][k];
+            const float ratio = ratio_div(x[0][k], x[1][k]);
             c[k] = lam * clip_above(p.c2, ratio);
             keep.rho[k] = clip_above(p.c3, ratio);
         }
-        c[I] = lam * clip_above(p.c2, xn[0] / xn[1]);
+        c[I] = lam * clip_above(p.c2, ratio_div(xn[0], xn[1]));
 #pragma unroll
         for (int k = 0; k < I; ++k) {
             const bool last = (EDGE && k == kb);

@@ -49,6 +49,9 @@ namespace rlscan {
 #ifndef RLSCAN_THREADS_1024
 #define RLSCAN_THREADS_1024 256
 #endif
+#ifndef RLSCAN_LOWP_THREADS_1024
+#define RLSCAN_LOWP_THREADS_1024 256
+#endif
 // Estimators with wide inputs (several words per step, e.g. [N,T,A]) move
 // far more bytes per step: 1024-step tiles, and a ring of WIDE_STAGES stages
 // whose size depends on the runtime width (one CTA per SM at A = 4).
@@ -105,7 +108,9 @@ struct Shape {
                                      : ((IoOf<E>::LOWP && TILE_BY_BYTES > RLSCAN_LOWP_TILE_CAP)
                                             ? RLSCAN_LOWP_TILE_CAP : TILE_BY_BYTES);
     static constexpr int THREADS = WIDE ? (TILE < 1024 ? 128 : RLSCAN_WIDE_THREADS)
-                                        : (TILE >= 4096 ? 256 : (TILE >= 2048 ? RLSCAN_THREADS_2048 : RLSCAN_THREADS_1024));
+                                        : (TILE >= 4096 ? 256 : (TILE >= 2048 ? RLSCAN_THREADS_2048
+                                                                              : (IoOf<E>::LOWP ? RLSCAN_LOWP_THREADS_1024
+                                                                                               : RLSCAN_THREADS_1024)));
     static constexpr int ITEMS = TILE / THREADS;
     static constexpr int STAGE_BYTES = narrow_bytes<E, TILE>();  // narrow arrays
     static constexpr int RAW = (RLSCAN_SMEM_BUDGET_KB * 1024) / STAGE_BYTES;
@@ -118,21 +123,29 @@ struct Shape {
     static_assert(TILE == THREADS * ITEMS, "tile shape");
 };
 
-// Packed launches (whole rows, T <= 1024) of single-scan estimators whose
-// own shape is 2048 steps or more: 1024-step tiles on 128 threads x 8
-// steps.  Rows this short gain from the smaller CTAs (five per SM instead
-// of three, a shorter serial path through each tile, a 4-warp composition);
-// measured on 4096 x 1024: GAE 14.65 -> 14.28 us, discounted returns 11.83
-// -> 11.17, TD(lambda) 14.31 -> 13.64 (the two-scan and the 1024-step
-// estimators lost with this shape and keep their own).
+#ifndef RLSCAN_SHORT_THREADS
+#define RLSCAN_SHORT_THREADS 128
+#endif
+#ifndef RLSCAN_SHORT_STAGES
+#define RLSCAN_SHORT_STAGES 2
+#endif
+// Packed launches (whole rows, T <= 1024) of single-scan or compact-storage
+// estimators whose own shape is 2048 steps or more: 1024-step tiles on 128
+// threads x 8 steps.  Rows this short gain from the smaller CTAs (five per
+// SM instead of three, a shorter serial path through each tile, a 4-warp
+// composition); measured on 4096 x 1024: GAE 14.65 -> 14.28 us, discounted
+// returns 11.83 -> 11.17, TD(lambda) 14.31 -> 13.64, compact GAE 11.56 ->
+// 11.06, compact fused GAE + returns 14.88 -> 13.84 (the float32 two-scan
+// step and the 1024-step estimators lost with this shape and keep their
+// own).
 template <class E>
 struct ShortShape {
-    static constexpr bool ENABLED = !Shape<E>::WIDE && !IoOf<E>::LOWP && !MomentsOf<E>::value && E::K == 1 &&
+    static constexpr bool ENABLED = !Shape<E>::WIDE && !MomentsOf<E>::value && (E::K == 1 || IoOf<E>::LOWP) &&
                                     Shape<E>::TILE >= 2048;
     static constexpr bool WIDE = false;
     static constexpr int TILE = 1024;
-    static constexpr int THREADS = 128;
-    static constexpr int ITEMS = 8;
+    static constexpr int THREADS = RLSCAN_SHORT_THREADS;
+    static constexpr int ITEMS = TILE / THREADS;
     static constexpr int STAGE_BYTES = narrow_bytes<E, TILE>();
     static constexpr int DEFER_STAGES = 0;
 };
@@ -355,7 +368,7 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
     using S = Shape<E>;
     if constexpr (ShortShape<E>::ENABLED) {
         using Q = ShortShape<E>;
-        if (p.T <= Q::TILE) return launch_scan_ring<E, Q, S::PACKED_STAGES>(p, ws, ws_bytes, stream, grid_out);
+        if (p.T <= Q::TILE) return launch_scan_ring<E, Q, RLSCAN_SHORT_STAGES>(p, ws, ws_bytes, stream, grid_out);
     }
     if (p.T <= S::TILE) return launch_scan_ring<E, S, S::PACKED_STAGES>(p, ws, ws_bytes, stream, grid_out);
     return launch_scan_ring<E, S, S::SHORT_STAGES>(p, ws, ws_bytes, stream, grid_out);

@@ -628,10 +628,14 @@ constexpr int block_threads() { return THREADS + 32; }
 #ifndef RLSCAN_DEFER_MIN_BLOCKS
 #define RLSCAN_DEFER_MIN_BLOCKS 0  // 0: as the immediate-finish kernel
 #endif
+#ifndef RLSCAN_SHORT_MIN_BLOCKS
+#define RLSCAN_SHORT_MIN_BLOCKS 3
+#endif
 template <class E, bool DEFER, int THREADS, int ITEMS>
 constexpr int min_blocks()
 {
     return (DEFER && RLSCAN_DEFER_MIN_BLOCKS > 0) ? RLSCAN_DEFER_MIN_BLOCKS
+           : (THREADS <= 128 && E::K == 1 && WideOf<E>::NWIDE == 0) ? RLSCAN_SHORT_MIN_BLOCKS
            : (WideOf<E>::NWIDE > 0 || (IoOf<E>::LOWP && E::NIN >= 4 && ITEMS >= 8)) ? 2
            : (E::K > 1) ? (ITEMS <= 4 ? RLSCAN_K2_SHORT_BLOCKS : (THREADS <= 128 && !DEFER ? 4 : 2))
            : RLSCAN_MIN_BLOCKS;
@@ -850,7 +854,19 @@ scan_kernel(const __grid_constant__ Params p)
             float nb = 0.f;
             if ((E::HALO >> j) & 1u) {
                 const char *q = FWD ? aj - eb : aj + ITEMS * eb;
-                nb = eb == 4 ? to_float<4>(q) : (eb == 2 ? to_float<2>(q) : to_float<1>(q));
+                if (ITEMS == 8 && eb == 4) {
+                    // the neighbour step is the adjacent lane's last (forward)
+                    // or first (backward) step: a shuffle, and a shared-memory
+                    // read only at the warp's edge (lanes 32 bytes apart
+                    // reading one float each would be an 8-way bank conflict);
+                    // at 4 steps per thread or narrower types the read's
+                    // smaller conflict measured cheaper than the shuffle
+                    nb = FWD ? __shfl_up_sync(0xffffffffu, x[j][ITEMS - 1], 1)
+                             : __shfl_down_sync(0xffffffffu, x[j][0], 1);
+                    if (lane == (FWD ? 0 : 31)) nb = to_float<4>(q);
+                } else {
+                    nb = eb == 4 ? to_float<4>(q) : (eb == 2 ? to_float<2>(q) : to_float<1>(q));
+                }
             }
             xn[j] = nb;
         }
