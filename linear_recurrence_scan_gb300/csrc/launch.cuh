@@ -52,6 +52,14 @@ namespace rlscan {
 #ifndef RLSCAN_LOWP_THREADS_1024
 #define RLSCAN_LOWP_THREADS_1024 256
 #endif
+// Packed launches with a workspace at hand: the last RLSCAN_PACKED_DYN_TAIL
+// tiles per CTA are drawn from the workspace ticket instead of assigned
+// statically (0: all static).  Measured on 4096 x 1024: GAE 13.88 -> 13.35
+// us, TD(lambda) 13.53 -> 12.83, discounted returns 11.00 -> 10.69, V-trace
+// 25.4 -> 23.9 (two or three dynamic tiles per CTA did no better).
+#ifndef RLSCAN_PACKED_DYN_TAIL
+#define RLSCAN_PACKED_DYN_TAIL 1
+#endif
 // Estimators with wide inputs (several words per step, e.g. [N,T,A]) move
 // far more bytes per step: 1024-step tiles, and a ring of WIDE_STAGES stages
 // whose size depends on the runtime width (one CTA per SM at A = 4).
@@ -358,6 +366,21 @@ rlscan_status launch_scan_ring(Params p, void *ws, size_t ws_bytes, cudaStream_t
     }
     if (MomentsOf<E>::value && slots > kMaxMomentCtas) slots = kMaxMomentCtas;  // one moments slot per CTA
     const int64_t grid = p.num_tiles < slots ? p.num_tiles : slots;
+    // Packed tiles: all but the last RLSCAN_PACKED_DYN_TAIL per CTA go out
+    // statically (no atomic on the producer's path); the rest come from the
+    // workspace ticket, so CTAs on faster SMs take more of them and all end
+    // together.  Kernels that accumulate moments keep the static order (their
+    // per-CTA sums, and so the normalised outputs, are the same bits on
+    // every call); without a usable workspace all tiles are static.
+    if (p.packed && RLSCAN_PACKED_DYN_TAIL > 0 && !MomentsOf<E>::value && ws != nullptr &&
+        ws_bytes >= kHeaderBytes && aligned16(ws) && residency(ws) == Residency::Device) {
+        const int64_t per_cta = p.num_tiles / grid;
+        if (per_cta > RLSCAN_PACKED_DYN_TAIL) {
+            p.dynamic = 1;
+            p.hdr = static_cast<uint32_t *>(ws);
+            p.static_tiles = (per_cta - RLSCAN_PACKED_DYN_TAIL) * grid;
+        }
+    }
     if (grid_out != nullptr) *grid_out = grid;
     return launch_kernel(kernel, p, grid, BT, smem, stream);
 }

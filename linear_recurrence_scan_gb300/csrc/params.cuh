@@ -55,7 +55,8 @@ struct Params {
     int32_t packed;            // 1: tiles hold whole rows; 0: rows split into tiles
     int32_t tma;               // 1: bulk asynchronous copies; 0: element-wise loads
     int32_t vec;               // 1: rows in whole 16-byte units: vector stores
-    int32_t dynamic;           // 1: tile ids from the workspace ticket (look-back)
+    int32_t dynamic;           // 1: tile ids from the workspace ticket (look-back, or a packed tail)
+    int64_t static_tiles;      // tiles [0, static_tiles) go to CTAs statically (b, b + grid, ...)
     unsigned long long *states;
     uint32_t *hdr;
     uint64_t spin_limit_ns;    // bound on every look-back wait

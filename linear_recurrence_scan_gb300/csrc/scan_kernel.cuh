@@ -625,6 +625,12 @@ constexpr int block_threads() { return THREADS + 32; }
 #ifndef RLSCAN_EARLY_START
 #define RLSCAN_EARLY_START 1
 #endif
+// Where a CTA counts itself out of a dynamic launch: right after its
+// producer's last ticket draw (1), or at the end of the kernel after a block
+// barrier and a fence (0).
+#ifndef RLSCAN_EARLY_EXIT_COUNT
+#define RLSCAN_EARLY_EXIT_COUNT 1
+#endif
 #ifndef RLSCAN_DEFER_MIN_BLOCKS
 #define RLSCAN_DEFER_MIN_BLOCKS 0  // 0: as the immediate-finish kernel
 #endif
@@ -724,16 +730,33 @@ scan_kernel(const __grid_constant__ Params p)
                                 p.spin_limit_ns + p.copy_limit_ns))
                     record_error(p, RLSCAN_ERR_TIMEOUT, 0x40000000u | static_cast<uint32_t>(s));
                 int64_t g;
-                if (p.dynamic) {
-                    g = static_cast<int64_t>(atomicAdd(reinterpret_cast<unsigned long long *>(p.hdr), 1ull));
-                } else {
+                if (static_next < p.static_tiles || !p.dynamic) {
                     g = static_next;
                     static_next += gridDim.x;
+                } else {
+                    g = p.static_tiles +
+                        static_cast<int64_t>(atomicAdd(reinterpret_cast<unsigned long long *>(p.hdr), 1ull));
                 }
                 tile_ids[s] = g;
                 if (g >= p.num_tiles) {
                     ptx::mbar_arrive(&meta_bar[s]);
                     ptx::mbar_arrive(&full_bar[s]);
+                    // Every ticket this CTA draws has been drawn (the draw that
+                    // just returned g is performed): count this CTA out.  The
+                    // last one re-arms the ticket and advances the epoch for
+                    // the next call on the workspace (whose CTAs read them only
+                    // after this kernel has completed); this call's CTAs keep
+                    // the epoch they read at start.  Done here, a tile or two
+                    // before the CTA's compute ends, the round trips stay off
+                    // the kernel's end.
+                    if (RLSCAN_EARLY_EXIT_COUNT && p.dynamic) {
+                        const uint32_t done = atomicAdd(&p.hdr[kHdrExit], 1u);
+                        if (done == gridDim.x - 1) {
+                            atomicExch(reinterpret_cast<unsigned long long *>(p.hdr), 0ull);
+                            atomicExch(&p.hdr[kHdrExit], 0u);
+                            atomicAdd(&p.hdr[kHdrEpoch], 1u);
+                        }
+                    }
                     break;
                 }
                 const TileGeo tg = decode_tile<FWD, TILE, RM>(p, g);
@@ -1274,7 +1297,7 @@ scan_kernel(const __grid_constant__ Params p)
             if ((lost_stages >> s2) & 1u) wait_phase(&full_bar[s2], (lost_parity >> s2) & 1u, p.copy_limit_ns);
     }
     }  // compute warps
-    if (p.dynamic) {
+    if (!RLSCAN_EARLY_EXIT_COUNT && p.dynamic) {
         __syncthreads();  // every ticket this CTA will draw has been drawn
         if (tid == THREADS) {
             __threadfence();
