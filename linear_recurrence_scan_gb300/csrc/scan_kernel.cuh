@@ -631,11 +631,19 @@ constexpr int block_threads() { return THREADS + 32; }
 #ifndef RLSCAN_EARLY_EXIT_COUNT
 #define RLSCAN_EARLY_EXIT_COUNT 1
 #endif
+// 1: the swapped float32 reads at 8 steps per thread (0: plain reads with
+// their two-way conflicts; measured 4-5 % slower on 2^20-step rows)
+#ifndef RLSCAN_F32_SWAP
+#define RLSCAN_F32_SWAP 1
+#endif
 #ifndef RLSCAN_DEFER_MIN_BLOCKS
 #define RLSCAN_DEFER_MIN_BLOCKS 0  // 0: as the immediate-finish kernel
 #endif
+// Resident CTAs the 128-thread short-row kernels are compiled for (their
+// register budget): 4 measured best (GAE 4096 x 1024 13.35 -> 13.06 us; 5
+// and 6 lost on discounted returns and TD(lambda)).
 #ifndef RLSCAN_SHORT_MIN_BLOCKS
-#define RLSCAN_SHORT_MIN_BLOCKS 3
+#define RLSCAN_SHORT_MIN_BLOCKS 4
 #endif
 template <class E, bool DEFER, int THREADS, int ITEMS>
 constexpr int min_blocks()
@@ -855,7 +863,7 @@ scan_kernel(const __grid_constant__ Params p)
                     // would hit the same banks.  Lanes 4..7 of each group of 8
                     // read their second chunk first (two-way conflicts gone),
                     // then the chunks are put back in order.
-                    const bool sw = ((lane >> 2) & 1) != 0;
+                    const bool sw = RLSCAN_F32_SWAP && ((lane >> 2) & 1) != 0;
                     float c0[4], c1[4];
                     load4(aj + (sw ? 16 : 0), c0);
                     load4(aj + (sw ? 0 : 16), c1);
