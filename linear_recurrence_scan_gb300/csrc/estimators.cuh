@@ -164,6 +164,7 @@ struct VTrace {
     static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = false, ROWSCALAR = !BS2D;
     static constexpr bool LB_ROW_MAJOR = true;  // measured faster on 2^20-step rows
+    static constexpr int LB_NAP_MAX = 0;        // polls without pausing (likewise)
     static constexpr unsigned HALO = 1u << 2;
     static constexpr int TR = 5, BS = 5 + TRUNC;
     template <int I> struct Keep { float rho[I]; };
@@ -496,6 +497,7 @@ struct Eligibility {
     static constexpr int NIN = 2, NOUT = 1;
     static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = true, ROWSCALAR = true;
+    static constexpr int DEFER_RING = 4;  // long rows: a fourth stage measured faster
     static constexpr unsigned HALO = 1u << 1;
     template <int I> struct Keep {};
 

@@ -82,6 +82,18 @@ namespace rlscan {
 #define RLSCAN_DEFER_MODE -1
 #endif
 
+// Ring of the deferred kernel: RLSCAN_DEFER_STAGES unless the estimator
+// declares DEFER_RING (eligibility traces: 4, 141 -> 138 us on 64 rows of
+// 2^20 steps; the other long-row kernels lost with a fourth stage).
+template <class E, class = void>
+struct DeferRingOf {
+    static constexpr int value = RLSCAN_DEFER_STAGES;
+};
+template <class E>
+struct DeferRingOf<E, std::void_t<decltype(E::DEFER_RING)>> {
+    static constexpr int value = E::DEFER_RING;
+};
+
 // Tile of a wide-input estimator: 1024 steps unless it declares WIDE_TILE
 // (a smaller tile keeps two or three CTAs per SM when its stage is large).
 template <class E, class = void>
@@ -126,8 +138,9 @@ struct Shape {
     static constexpr int SHORT_STAGES = WIDE ? RLSCAN_WIDE_STAGES
                                              : (RAW < 2 ? 2 : (RAW > RLSCAN_MAX_STAGES ? RLSCAN_MAX_STAGES : RAW));
     static constexpr int PACKED_STAGES = SHORT_STAGES < RLSCAN_PACKED_STAGES ? SHORT_STAGES : RLSCAN_PACKED_STAGES;
-    static constexpr int DEFER_STAGES = (WIDE || RLSCAN_DEFER_STAGES < 3) ? 0
-                                        : (RLSCAN_DEFER_STAGES > SHORT_STAGES ? RLSCAN_DEFER_STAGES : SHORT_STAGES);
+    static constexpr int DEFER_RING = DeferRingOf<E>::value;
+    static constexpr int DEFER_STAGES = (WIDE || DEFER_RING < 3) ? 0
+                                        : (DEFER_RING > SHORT_STAGES ? DEFER_RING : SHORT_STAGES);
     static_assert(TILE == THREADS * ITEMS, "tile shape");
 };
 

@@ -220,10 +220,20 @@ constexpr uint32_t kTagAgg = 1u, kTagPrefix = 2u;
 
 
 // Longest pause between two polls of a predecessor's state (ns); the pause
-// starts at 32 ns and doubles.  0: poll without pausing.
+// starts at 32 ns and doubles.  0: poll without pausing.  An estimator may
+// declare its own (LB_NAP_MAX): V-trace polls without pausing (64 rows of
+// 2^20 steps 367 -> 363 us; 512 ns cost it 21 %).
 #ifndef RLSCAN_LB_NAP_MAX
 #define RLSCAN_LB_NAP_MAX 128
 #endif
+template <class E, class = void>
+struct NapOf {
+    static constexpr int value = RLSCAN_LB_NAP_MAX;
+};
+template <class E>
+struct NapOf<E, std::void_t<decltype(E::LB_NAP_MAX)>> {
+    static constexpr int value = E::LB_NAP_MAX;
+};
 
 __device__ __forceinline__ unsigned long long pack_word(uint32_t tag, float v)
 {
@@ -482,7 +492,7 @@ __device__ __forceinline__ void publish_inclusive(const Params &p, uint32_t epoc
 // (w0, w1) are the predecessor's state words as fetched earlier.  Walks back
 // through aggregates until an inclusive value, a zero decay, or the row's
 // first tile; every wait is bounded.
-template <int K, bool RM>
+template <int K, bool RM, int NAP>
 __device__ inline float lookback_read(const Params &p, uint32_t epoch, int64_t g, int64_t pos, int64_t j, int sc,
                                       unsigned long long w0, unsigned long long w1)
 {
@@ -521,9 +531,9 @@ __device__ inline float lookback_read(const Params &p, uint32_t epoch, int64_t g
             record_error(p, RLSCAN_ERR_TIMEOUT, static_cast<uint32_t>(g));
             return __int_as_float(0x7fc00000);
         }
-        if (RLSCAN_LB_NAP_MAX > 0) {
+        if (NAP > 0) {
             __nanosleep(nap);
-            if (nap < RLSCAN_LB_NAP_MAX) nap <<= 1;
+            if (nap < NAP) nap <<= 1;
         }
     }
 }
@@ -672,6 +682,7 @@ scan_kernel(const __grid_constant__ Params p)
     constexpr int NWIDE = WideOf<E>::NWIDE;
     constexpr int LBW = (DEFER && K == 1 && (ChainOf<E>::value || RLSCAN_LB_WINDOW_ALL)) ? RLSCAN_LB_WINDOW : 0;
     constexpr bool RM = RLSCAN_STATE_ROW_MAJOR < 0 ? RowMajorOf<E>::value : RLSCAN_STATE_ROW_MAJOR != 0;
+    constexpr int LBNAP = NapOf<E>::value;
     static_assert(LBW >= 0 && LBW <= 32, "look-back window: at most one warp of states");
     static_assert(NWIDE == 0 || !FWD, "wide inputs are staged for backward recurrences only");
 
@@ -1022,7 +1033,7 @@ scan_kernel(const __grid_constant__ Params p)
     auto carry_in = [&](int64_t g, int64_t pos, int64_t j, const Pair (&total)[K], unsigned long long w0,
                         unsigned long long w1, float (&carry)[K]) {
         float mine = 0.f;
-        if (lane < K) mine = lookback_read<K, RM>(p, epoch, g, pos, j, lane, w0, w1);
+        if (lane < K) mine = lookback_read<K, RM, LBNAP>(p, epoch, g, pos, j, lane, w0, w1);
 #pragma unroll
         for (int sc = 0; sc < K; ++sc) carry[sc] = __shfl_sync(0xffffffffu, mine, sc);
         if (warp == PUB_WARP && lane == 0) {
@@ -1068,7 +1079,7 @@ scan_kernel(const __grid_constant__ Params p)
             c = __shfl_sync(0xffffffffu, v.a, 0);
         } else {
             float mine = 0.f;
-            if (lane == 0) mine = lookback_read<K, RM>(p, epoch, g, pos, j, 0, w0, w1);
+            if (lane == 0) mine = lookback_read<K, RM, LBNAP>(p, epoch, g, pos, j, 0, w0, w1);
             c = __shfl_sync(0xffffffffu, mine, 0);
         }
         carry[0] = c;
