@@ -144,9 +144,6 @@ struct Shape {
     static_assert(TILE == THREADS * ITEMS, "tile shape");
 };
 
-#ifndef RLSCAN_SHORT_SHAPE
-#define RLSCAN_SHORT_SHAPE 1
-#endif
 #ifndef RLSCAN_SHORT_THREADS
 #define RLSCAN_SHORT_THREADS 128
 #endif
@@ -164,8 +161,8 @@ struct Shape {
 // own).
 template <class E>
 struct ShortShape {
-    static constexpr bool ENABLED = RLSCAN_SHORT_SHAPE && !Shape<E>::WIDE && !MomentsOf<E>::value &&
-                                    (E::K == 1 || IoOf<E>::LOWP) && Shape<E>::TILE >= 2048;
+    static constexpr bool ENABLED = !Shape<E>::WIDE && !MomentsOf<E>::value && (E::K == 1 || IoOf<E>::LOWP) &&
+                                    Shape<E>::TILE >= 2048;
     static constexpr bool WIDE = false;
     static constexpr int TILE = 1024;
     static constexpr int THREADS = RLSCAN_SHORT_THREADS;
