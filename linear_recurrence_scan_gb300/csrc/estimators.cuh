@@ -498,6 +498,7 @@ struct Eligibility {
     static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = true, ROWSCALAR = true;
     static constexpr int DEFER_RING = 4;  // long rows: a fourth stage measured faster
+    static constexpr bool LB_LATE = true;  // ... and a later predecessor fetch
     static constexpr unsigned HALO = 1u << 1;
     template <int I> struct Keep {};
 
