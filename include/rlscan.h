@@ -247,9 +247,12 @@ rlscan_status rlscan_gae_noalloc(const float *rewards, const float *values,
  * float pairs (unevaluated sums hi + lo, combined with Knuth's TwoSum), the
  * CTA combines its threads' pairs the same way and writes one pair per
  * moment; a second kernel, ordered after it on `stream`, combines the
- * per-CTA pairs in CTA order and normalises the advantages in place.
+ * per-CTA pairs in CTA order (every block the same way, so the result is
+ * the same bits on every call), derives the mean and standard deviation in
+ * float-pair arithmetic and normalises the advantages in place.
  * lambda_returns (A_t + V_t) and discounted_returns are computed from the
- * RAW advantages, as in rlscan_gae_returns.
+ * RAW advantages, as in rlscan_gae_returns; the scan solves one recurrence
+ * per step when discounted_returns is NULL and two otherwise.
  * Inputs : as rlscan_gae_returns; eps >= 0 (else RLSCAN_ERR_ARG_VALUE).
  * Outputs: advantages [N,T] (normalised; required); lambda_returns,
  *          discounted_returns [N,T] nullable; moments: nullable device

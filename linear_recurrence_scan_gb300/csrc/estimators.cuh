@@ -43,8 +43,14 @@ namespace est {
 __device__ __forceinline__ float done_of(float term, float trunc) { return fminf(1.f, term + trunc); }
 
 // min(clip, x) that keeps a NaN x (fminf would return the clip), so an
-// undefined ratio such as 0/0 shows in the outputs instead of being clipped
-__device__ __forceinline__ float clip_above(float clip, float x) { return clip < x ? clip : x; }
+// undefined ratio such as 0/0 shows in the outputs instead of being clipped:
+// the NaN-propagating form of the minimum (PTX min.NaN.f32, one instruction)
+__device__ __forceinline__ float clip_above(float clip, float x)
+{
+    float r;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(clip), "f"(x));
+    return r;
+}
 
 // Importance ratios.  RLSCAN_FAST_RATIO=1 (default) takes CUDA's fast
 // intrinsics __expf and __fdividef (relative error of a few 1e-7 for the
@@ -167,9 +173,14 @@ struct VTrace {
     static constexpr int LB_NAP_MAX = 0;        // polls without pausing (likewise)
     static constexpr unsigned HALO = 1u << 2;
     static constexpr int TR = 5, BS = 5 + TRUNC;
-    template <int I> struct Keep { float rho[I]; };
+    // alpha and the weight w = rho gamma (1-term) (1-trunc) of the successor:
+    // adv_t = rho (r + gamma (1-term) vs_{t+1} - V) is alpha_t + w_t D_{t+1}
+    // (vs_{t+1} = D_{t+1} + V_{t+1}, and alpha_t holds the V_{t+1} and
+    // bootstrap terms), alpha_t itself at the row's last step
+    template <int I> struct Keep { float a[I], w[I]; };
 
-    // successor of x at element k: bootstrap rule shared by Vn and vsn
+    // successor of x at element k: the next value, or the bootstrap at a
+    // truncation and at the row's last step
     template <int I>
     __device__ static float successor(const float (&x)[NIN][I], int k, bool last, float nxt, float rsc)
     {
@@ -198,9 +209,13 @@ struct VTrace {
             float done;
             if constexpr (TRUNC) done = done_of(term, x[TR][k]);
             else done = term;
-            a[0][k] = rho * (fmaf(g * (1.f - term), vn, x[3][k]) - x[2][k]);
-            b[0][k] = g * c * (1.f - done);
-            keep.rho[k] = rho;
+            const float gt = g * (1.f - term);
+            const float gc = g * c;
+            a[0][k] = rho * (fmaf(gt, vn, x[3][k]) - x[2][k]);
+            b[0][k] = fmaf(-gc, done, gc);  // gamma c (1 - done)
+            keep.a[k] = a[0][k];
+            if constexpr (TRUNC) keep.w[k] = rho * gt * (1.f - x[TR][k]);
+            else keep.w[k] = rho * gt;
         }
     }
     template <int I>
@@ -210,15 +225,12 @@ struct VTrace {
                                 const Params &p, float rsc, const float (&A)[K][I], const float (&A_after)[K],
                                 const Keep<I> &keep, float (&o)[NOUT][I])
     {
-        const float g = p.c0;
 #pragma unroll
         for (int k = 0; k < I; ++k) {
             const bool last = (EDGE && k == kb);
-            const float vs_next = (k + 1 < I) ? A[0][k + 1] + x[2][k + 1] : A_after[0] + xn[2];
-            const float nvs = successor<I>(x, k, last, vs_next, rsc);
-            const float term = x[4][k];
+            const float d_next = (k + 1 < I) ? A[0][k + 1] : A_after[0];
             o[0][k] = A[0][k] + x[2][k];
-            o[1][k] = keep.rho[k] * (fmaf(g * (1.f - term), nvs, x[3][k]) - x[2][k]);
+            o[1][k] = last ? keep.a[k] : fmaf(keep.w[k], d_next, keep.a[k]);
         }
     }
 };
@@ -237,21 +249,24 @@ struct Retrace {
     static constexpr int K = 1;  // affine recurrences per step
     static constexpr bool FWD = false, ROWSCALAR = false;
     static constexpr unsigned HALO = (1u << 0) | (1u << 1) | (1u << 2);
-    template <int I> struct Keep { float rho[I]; };
+    // adv_t = rho (r + gamma (1-term) Qret_{t+1} - Q) with Qret_{t+1} =
+    // D_{t+1} + Q_{t+1} (0 after the row's last step) is u_t + w_t D_{t+1}:
+    // u = rho (r + gamma (1-term) Q_{t+1} - Q), w = rho gamma (1-term)
+    template <int I> struct Keep { float u[I], w[I]; };
 
     template <int I, bool EDGE>
     __device__ static void coeffs(const float (&x)[NIN][I], const float (&xn)[NIN], int kb,
                                   const Params &p, float, float (&a)[K][I], float (&b)[K][I], Keep<I> &keep)
     {
-        const float g = p.c0, lam = p.c1;
-        float c[I + 1];
+        const float g = p.c0, gl = p.c0 * p.c1;
+        float c[I + 1];  // min(c_bar, ratio); the trace coefficient is lambda times it
 #pragma unroll
         for (int k = 0; k < I; ++k) {
             const float ratio = ratio_div(x[0][k], x[1][k]);
-            c[k] = lam * clip_above(p.c2, ratio);
-            keep.rho[k] = clip_above(p.c3, ratio);
+            c[k] = clip_above(p.c2, ratio);
+            keep.w[k] = clip_above(p.c3, ratio);  // rho, until the second loop
         }
-        c[I] = lam * clip_above(p.c2, ratio_div(xn[0], xn[1]));
+        c[I] = clip_above(p.c2, ratio_div(xn[0], xn[1]));
 #pragma unroll
         for (int k = 0; k < I; ++k) {
             const bool last = (EDGE && k == kb);
@@ -259,9 +274,13 @@ struct Retrace {
             float done;
             if constexpr (TRUNC) done = done_of(term, x[6][k]);
             else done = term;
-            const float cn = last ? 0.f : c[k + 1];
-            a[0][k] = fmaf(g * (1.f - term), x[3][k], x[4][k]) - x[2][k];
-            b[0][k] = g * cn * (1.f - done);
+            const float gcn = last ? 0.f : gl * c[k + 1];
+            const float gt = g * (1.f - term);
+            a[0][k] = fmaf(gt, x[3][k], x[4][k]) - x[2][k];
+            b[0][k] = fmaf(-gcn, done, gcn);  // gamma lambda min(c_bar, ratio_{t+1}) (1 - done)
+            const float qn = last ? 0.f : ((k + 1 < I) ? x[2][k + 1] : xn[2]);
+            keep.u[k] = keep.w[k] * (fmaf(gt, qn, x[4][k]) - x[2][k]);
+            keep.w[k] *= gt;
         }
     }
     template <int I>
@@ -271,14 +290,12 @@ struct Retrace {
                                 const Params &p, float, const float (&A)[K][I], const float (&A_after)[K],
                                 const Keep<I> &keep, float (&o)[NOUT][I])
     {
-        const float g = p.c0;
 #pragma unroll
         for (int k = 0; k < I; ++k) {
             const bool last = (EDGE && k == kb);
-            const float qn = last ? 0.f : ((k + 1 < I) ? A[0][k + 1] + x[2][k + 1] : A_after[0] + xn[2]);
-            const float term = x[5][k];
+            const float d_next = (k + 1 < I) ? A[0][k + 1] : A_after[0];
             o[0][k] = A[0][k] + x[2][k];
-            o[1][k] = keep.rho[k] * (fmaf(g * (1.f - term), qn, x[4][k]) - x[2][k]);
+            o[1][k] = last ? keep.u[k] : fmaf(keep.w[k], d_next, keep.u[k]);
         }
     }
 };
@@ -675,6 +692,28 @@ struct GAEReturns {
 template <bool TRUNC, bool BS2D>
 struct GAEReturnsMoments : GAEReturns<TRUNC, BS2D> {
     static constexpr bool MOMENTS = true;
+};
+
+// The same without the discounted returns: one scan (GAE), outputs 0
+// advantages and 1 lambda-returns (A + V), and the batch moments of the
+// advantages.
+template <bool TRUNC, bool BS2D>
+struct GAELambdaMoments : GAE<TRUNC, BS2D> {
+    using Base = GAE<TRUNC, BS2D>;
+    static constexpr int NOUT = 2;
+    static constexpr bool MOMENTS = true;
+
+    template <int I, bool EDGE>
+    __device__ static void post(const float (&x)[Base::NIN][I], const float (&)[Base::NIN], int, const Params &,
+                                float, const float (&A)[1][I], const float (&)[1],
+                                const typename Base::template Keep<I> &, float (&o)[NOUT][I])
+    {
+#pragma unroll
+        for (int k = 0; k < I; ++k) {
+            o[0][k] = A[0][k];
+            o[1][k] = A[0][k] + x[1][k];
+        }
+    }
 };
 
 // Compact storage of an estimator's inputs and outputs: value inputs in

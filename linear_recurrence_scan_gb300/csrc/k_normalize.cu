@@ -1,46 +1,58 @@
-// k_normalize.cu -- fused GAE + returns with the batch moments of the
+// k_normalize.cu -- GAE with its returns and the batch moments of the
 // advantages, and the pass that normalises the advantages with them
 // (advantage normalisation, the planned extension of the rl-triton paper,
 // Sec. 9.3, read as the usual per-batch whitening
 // (A - mean) / (std + eps) with the unbiased standard deviation).
-#include "dfloat.cuh"
 #include "launch.cuh"
 
 namespace rlscan {
 
-rlscan_status launch_gae_moments(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s,
-                                 int64_t *grid)
+namespace {
+
+// The scan with the batch moments: one scan (advantages and
+// lambda-returns) unless the discounted returns are asked for too.
+rlscan_status launch_gae_moments(bool trunc, bool bs2d, bool discounted, Params p, void *ws, size_t ws_bytes,
+                                 cudaStream_t s, int64_t *grid)
 {
+    if (!discounted) {
+        if (!trunc) return launch_scan<est::GAELambdaMoments<false, false>>(p, ws, ws_bytes, s, grid);
+        if (!bs2d) return launch_scan<est::GAELambdaMoments<true, false>>(p, ws, ws_bytes, s, grid);
+        return launch_scan<est::GAELambdaMoments<true, true>>(p, ws, ws_bytes, s, grid);
+    }
     if (!trunc) return launch_scan<est::GAEReturnsMoments<false, false>>(p, ws, ws_bytes, s, grid);
     if (!bs2d) return launch_scan<est::GAEReturnsMoments<true, false>>(p, ws, ws_bytes, s, grid);
     return launch_scan<est::GAEReturnsMoments<true, true>>(p, ws, ws_bytes, s, grid);
 }
 
-namespace {
-
 constexpr int kNormThreads = 256;
 constexpr int kVecPerThread = 8;
 
-// x <- (x - mean) / (std + eps) over an [N, T] buffer with row stride rs.
-// Every block first combines the scan kernel's per-CTA slots
-// (sum and sum of squares as float pairs) in the same fixed order -- so all
-// blocks agree bit for bit -- into mean = S / n and the unbiased variance
-// (Q - S mean) / (n - 1) (inv_n = 1 / n and inv_nm1 = 1 / (n - 1) from the
-// host; NaN for n = 1).  Contiguous buffers are walked as one flat array
-// (float4 when aligned, four vectors in flight per thread), strided ones row
-// by row.
-__global__ void __launch_bounds__(kNormThreads) normalize_kernel(float *x, int64_t N, int64_t T, int64_t rs,
-                                                                 const float *parts, int nparts, double inv_n,
-                                                                 double inv_nm1, float eps, float *moments_out,
-                                                                 int vec)
+// What the normalising pass needs from the scan: the per-CTA moment slots
+// to combine and the batch size.
+struct NormArgs {
+    float *x;                 // advantages [N, T], row stride rs
+    int64_t N, T, rs;
+    const float *parts;       // per-CTA moment slots
+    int nparts;               // scan CTAs
+    float inv_n[2], inv_nm1[2], eps;
+    float *moments_out;       // nullable: (mean, std)
+    int vec;                  // rows in whole float4 units, aligned
+};
+
+// x <- (x - mean) / (std + eps).  Every block combines the scan's slots
+// itself, in the same fixed order (so all blocks agree bit for bit), while
+// its first vectors are in flight: measured faster than one combination by
+// the scan's last CTA (a fence, a count and a serial combination at the
+// scan's end; GAE + lambda-returns 4096 x 1024, 23.8 -> 23.1 us).
+// Contiguous buffers are walked as one flat array (float4 when aligned,
+// eight vectors in flight per thread), strided ones row by row.
+__global__ void __launch_bounds__(kNormThreads) normalize_kernel(const __grid_constant__ NormArgs a)
 {
     ptx::pdl_trigger_dependents();
     ptx::pdl_wait_prerequisites();  // the scan kernel's outputs and moments are complete
-    // flat buffers: this block's first vectors are requested before the
-    // moments are combined, so their latency overlaps the combination
-    const bool flat = rs == T && vec;
-    float4 *x4 = reinterpret_cast<float4 *>(x);
-    const int64_t n4 = N * T / 4;
+    const bool flat = a.rs == a.T && a.vec;
+    float4 *x4 = reinterpret_cast<float4 *>(a.x);
+    const int64_t n4 = a.N * a.T / 4;
     int64_t base = blockIdx.x * static_cast<int64_t>(kVecPerThread * kNormThreads);
     float4 v[kVecPerThread];
     auto load_chunk = [&] {
@@ -51,19 +63,17 @@ __global__ void __launch_bounds__(kNormThreads) normalize_kernel(float *x, int64
         }
     };
     if (flat) load_chunk();
-    __shared__ DF s_red[kNormThreads / 32][2];
     __shared__ float s_mi[2];
-    {
-        DF sum, sumsq;
-        combine_moment_slots<kNormThreads>(parts, nparts, threadIdx.x, s_red, [] { __syncthreads(); }, sum, sumsq);
-        if (threadIdx.x == 0) {
-            const Whitening w = whitening(sum, sumsq, inv_n, inv_nm1, eps);
-            s_mi[0] = w.mean;
-            s_mi[1] = w.inv;
-            if (moments_out != nullptr && blockIdx.x == 0) {
-                moments_out[0] = w.mean;
-                moments_out[1] = w.sd;
-            }
+    __shared__ DF s_red[kNormThreads / 32][2];
+    DF sum, sumsq;
+    combine_moment_slots<kNormThreads>(a.parts, a.nparts, threadIdx.x, s_red, [] { __syncthreads(); }, sum, sumsq);
+    if (threadIdx.x == 0) {
+        const Whitening w = whitening(sum, sumsq, DF{a.inv_n[0], a.inv_n[1]}, DF{a.inv_nm1[0], a.inv_nm1[1]}, a.eps);
+        s_mi[0] = w.mean;
+        s_mi[1] = w.inv;
+        if (a.moments_out != nullptr && blockIdx.x == 0) {
+            a.moments_out[0] = w.mean;
+            a.moments_out[1] = w.sd;
         }
     }
     __syncthreads();
@@ -90,52 +100,45 @@ __global__ void __launch_bounds__(kNormThreads) normalize_kernel(float *x, int64
     }
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kNormThreads;
     const int64_t first = blockIdx.x * static_cast<int64_t>(kNormThreads) + threadIdx.x;
-    if (rs == T) {
-        const int64_t n = N * T;
-        for (int64_t i = first; i < n; i += stride) x[i] = (x[i] - m) * inv;
+    if (a.rs == a.T) {
+        const int64_t n = a.N * a.T;
+        for (int64_t i = first; i < n; i += stride) a.x[i] = (a.x[i] - m) * inv;
         return;
     }
-    for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
-        float *r = x + row * rs;
-        if (vec) {
+    for (int64_t row = blockIdx.x; row < a.N; row += gridDim.x) {
+        float *r = a.x + row * a.rs;
+        if (a.vec) {
             float4 *r4 = reinterpret_cast<float4 *>(r);
-            for (int64_t c = threadIdx.x; c < T / 4; c += kNormThreads) {
-                float4 v = r4[c];
-                v.x = (v.x - m) * inv;
-                v.y = (v.y - m) * inv;
-                v.z = (v.z - m) * inv;
-                v.w = (v.w - m) * inv;
-                r4[c] = v;
+            for (int64_t c = threadIdx.x; c < a.T / 4; c += kNormThreads) {
+                float4 w = r4[c];
+                w.x = (w.x - m) * inv;
+                w.y = (w.y - m) * inv;
+                w.z = (w.z - m) * inv;
+                w.w = (w.w - m) * inv;
+                r4[c] = w;
             }
         } else {
-            for (int64_t c = threadIdx.x; c < T; c += kNormThreads) r[c] = (r[c] - m) * inv;
+            for (int64_t c = threadIdx.x; c < a.T; c += kNormThreads) r[c] = (r[c] - m) * inv;
         }
     }
 }
 
-}  // namespace
-
-rlscan_status launch_normalize(float *x, int64_t N, int64_t T, int64_t rs, const float *parts, int64_t nparts,
-                               float eps, float *moments_out, cudaStream_t stream)
+rlscan_status launch_normalize(const NormArgs &a, cudaStream_t stream)
 {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return RLSCAN_ERR_CUDA;
-    const bool vec = (T % 4 == 0) && (rs % 4 == 0) && aligned16(x);
     int64_t blocks;
-    if (rs == T && vec) {
-        blocks = (N * T / 4 + kVecPerThread * kNormThreads - 1) / (kVecPerThread * kNormThreads);
+    if (a.rs == a.T && a.vec) {
+        blocks = (a.N * a.T / 4 + kVecPerThread * kNormThreads - 1) / (kVecPerThread * kNormThreads);
     } else {
-        const int64_t work = rs == T ? N * T : N * kNormThreads;
+        const int64_t work = a.rs == a.T ? a.N * a.T : a.N * kNormThreads;
         blocks = (work + kNormThreads - 1) / kNormThreads;
     }
-    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * 8;  // one wave; each block re-reads the slots
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * 8;  // one wave
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    const double n = static_cast<double>(N) * static_cast<double>(T);
-    const double inv_n = 1.0 / n;
-    const double inv_nm1 = n > 1.0 ? 1.0 / (n - 1.0) : __builtin_nan("");
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
     cfg.blockDim = dim3(kNormThreads);
@@ -145,12 +148,35 @@ rlscan_status launch_normalize(float *x, int64_t N, int64_t T, int64_t rs, const
     attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, normalize_kernel, x, N, T, rs, parts, static_cast<int>(nparts), inv_n, inv_nm1, eps,
-                           moments_out, vec ? 1 : 0) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, normalize_kernel, a) != cudaSuccess) {
         cudaGetLastError();
         return RLSCAN_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? RLSCAN_OK : RLSCAN_ERR_CUDA;
+}
+
+}  // namespace
+
+rlscan_status launch_gae_normalized(bool trunc, bool bs2d, bool discounted, Params p, float *moments_out,
+                                    void *ws, size_t ws_bytes, cudaStream_t s)
+{
+    int64_t grid = 0;
+    RLSCAN_LAUNCH_TRY(launch_gae_moments(trunc, bs2d, discounted, p, ws, ws_bytes, s, &grid));
+    NormArgs a;
+    a.x = p.out[0];
+    a.N = p.N;
+    a.T = p.T;
+    a.rs = p.rs;
+    a.parts = p.mom_part;
+    a.nparts = static_cast<int>(grid);
+    a.inv_n[0] = p.mom_inv[0];
+    a.inv_n[1] = p.mom_inv[1];
+    a.inv_nm1[0] = p.mom_inv[2];
+    a.inv_nm1[1] = p.mom_inv[3];
+    a.eps = p.c2;
+    a.moments_out = moments_out;
+    a.vec = (p.T % 4 == 0) && (p.rs % 4 == 0) && aligned16(p.out[0]) ? 1 : 0;
+    return launch_normalize(a, s);
 }
 
 }  // namespace rlscan

@@ -150,6 +150,9 @@ struct Shape {
 #ifndef RLSCAN_SHORT_STAGES
 #define RLSCAN_SHORT_STAGES 2
 #endif
+#ifndef RLSCAN_MOM_SHORT
+#define RLSCAN_MOM_SHORT 1
+#endif
 // Packed launches (whole rows, T <= 1024) of single-scan or compact-storage
 // estimators whose own shape is 2048 steps or more: 1024-step tiles on 128
 // threads x 8 steps.  Rows this short gain from the smaller CTAs (five per
@@ -161,8 +164,8 @@ struct Shape {
 // own).
 template <class E>
 struct ShortShape {
-    static constexpr bool ENABLED = !Shape<E>::WIDE && !MomentsOf<E>::value && (E::K == 1 || IoOf<E>::LOWP) &&
-                                    Shape<E>::TILE >= 2048;
+    static constexpr bool ENABLED = !Shape<E>::WIDE && (E::K == 1 || IoOf<E>::LOWP) &&
+                                    (Shape<E>::TILE >= 2048 || (RLSCAN_MOM_SHORT && MomentsOf<E>::value));
     static constexpr bool WIDE = false;
     static constexpr int TILE = 1024;
     static constexpr int THREADS = RLSCAN_SHORT_THREADS;

@@ -72,8 +72,11 @@ struct Params {
     int32_t stage_floats;         // floats per ring stage (narrow and wide regions)
     int32_t A;                    // number of actions
 
-    // batch moments of output 0 (estimators that declare MOMENTS)
+    // batch moments of output 0 (estimators that declare MOMENTS); c2 holds
+    // eps, mom_inv the normalising pass's 1 / n and 1 / (n - 1) (n = N T)
+    // as float pairs (hi, lo)
     float *mom_part;              // [gridDim.x][4] per-CTA sum and sum of squares, each a float pair
+    float mom_inv[4];
 
     // checked builds only: violations counted and the first site (else NULL),
     // and the rows the checks take each [N,T] array to span (N; fewer under
@@ -85,10 +88,8 @@ struct Params {
 // Launchers (one translation unit per estimator family).
 rlscan_status launch_gae(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_gae_returns(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
-rlscan_status launch_gae_moments(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s,
-                                 int64_t *grid);
-rlscan_status launch_normalize(float *x, int64_t N, int64_t T, int64_t rs, const float *parts, int64_t nparts,
-                               float eps, float *moments_out, cudaStream_t s);
+rlscan_status launch_gae_normalized(bool trunc, bool bs2d, bool discounted, Params p, float *moments_out,
+                                    void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_gae_masked(bool trunc, bool bs2d, Params p, void *ws, size_t ws_bytes, cudaStream_t s);
 rlscan_status launch_gae_compact(bool trunc, bool bs2d, bool bf16_out, Params p, void *ws, size_t ws_bytes,
                                  cudaStream_t s);

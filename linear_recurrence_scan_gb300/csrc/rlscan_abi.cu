@@ -476,13 +476,22 @@ RLSCAN_API rlscan_status rlscan_gae_normalized(const float *rewards, const float
     p.in[0] = rewards;
     p.in[1] = values;
     p.in[2] = terminateds;
+    p.c2 = eps;
     p.mom_part = reinterpret_cast<float *>(static_cast<char *>(ws) + (need - kMomentBytes));
-    int64_t grid = 0;
-    rlscan_status st;
+    {
+        // 1 / n and 1 / (n - 1) as float pairs (NaN for n = 1)
+        const double n = static_cast<double>(N) * static_cast<double>(T);
+        const double inv[2] = {1.0 / n, n > 1.0 ? 1.0 / (n - 1.0) : __builtin_nan("")};
+        for (int i = 0; i < 2; ++i) {
+            p.mom_inv[2 * i] = static_cast<float>(inv[i]);
+            p.mom_inv[2 * i + 1] = static_cast<float>(inv[i] - static_cast<double>(p.mom_inv[2 * i]));
+        }
+    }
+    const bool disc = discounted_returns != nullptr;
     if (truncateds) {
         p.in[3] = truncateds;
         p.in[4] = bootstrap_values;
-        st = launch_gae_moments(true, bootstrap_values != nullptr, p, ws, ws_bytes, cs(stream), &grid);
+        return launch_gae_normalized(true, bootstrap_values != nullptr, disc, p, moments, ws, ws_bytes, cs(stream));
     } else {
         if (last_value) {
             p.rowscalar = last_value;
@@ -490,10 +499,8 @@ RLSCAN_API rlscan_status rlscan_gae_normalized(const float *rewards, const float
             p.rowscalar = bootstrap_values + (T - 1);
             p.rowscalar_stride = row_stride;
         }
-        st = launch_gae_moments(false, false, p, ws, ws_bytes, cs(stream), &grid);
+        return launch_gae_normalized(false, false, disc, p, moments, ws, ws_bytes, cs(stream));
     }
-    if (st != RLSCAN_OK) return st;
-    return launch_normalize(advantages, N, T, row_stride, p.mom_part, grid, eps, moments, cs(stream));
 }
 
 namespace {

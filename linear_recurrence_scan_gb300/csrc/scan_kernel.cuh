@@ -607,6 +607,9 @@ constexpr int block_threads() { return THREADS + 32; }
 // the most the wide stages leave room for, and what compact-storage
 // estimators with four or more inputs get at eight steps per thread
 // (their staged inputs unpack into many registers).
+#ifndef RLSCAN_LOWP_BLOCKS
+#define RLSCAN_LOWP_BLOCKS 2
+#endif
 #ifndef RLSCAN_K2_SHORT_BLOCKS
 #define RLSCAN_K2_SHORT_BLOCKS 3
 #endif
@@ -673,7 +676,8 @@ constexpr int min_blocks()
 {
     return (DEFER && RLSCAN_DEFER_MIN_BLOCKS > 0) ? RLSCAN_DEFER_MIN_BLOCKS
            : (THREADS <= 128 && E::K == 1 && WideOf<E>::NWIDE == 0) ? RLSCAN_SHORT_MIN_BLOCKS
-           : (WideOf<E>::NWIDE > 0 || (IoOf<E>::LOWP && E::NIN >= 4 && ITEMS >= 8)) ? 2
+           : WideOf<E>::NWIDE > 0 ? 2
+           : (IoOf<E>::LOWP && E::NIN >= 4 && ITEMS >= 8) ? RLSCAN_LOWP_BLOCKS
            : (E::K > 1) ? (ITEMS <= 4 ? RLSCAN_K2_SHORT_BLOCKS : (THREADS <= 128 && !DEFER ? 4 : 2))
            : RLSCAN_MIN_BLOCKS;
 }
@@ -1302,7 +1306,8 @@ scan_kernel(const __grid_constant__ Params p)
 
     if constexpr (MOM) {
         // CTA total of the moments (float pairs), delivered to this CTA's
-        // slot; the normalising pass combines the slots after this kernel
+        // slot; every block of the normalising pass combines the slots in
+        // CTA order after this kernel (the same bits on every call)
         __shared__ DF s_mom[WARPS][2];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {

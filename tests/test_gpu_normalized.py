@@ -1,9 +1,11 @@
 """GAE with batch-normalised advantages against the float64 oracle: gae()
 then normalize_advantages().  The returns are compared with their own
 oracles (they use the raw advantages).  The device path is the scan with
-per-CTA moment slots followed by the normalising pass; the shapes cover
-its flat (vector) walk, its strided and unaligned walks, packed and
-long-row scans.
+per-CTA moment slots followed by the normalising pass (every block of which
+combines the slots); the shapes cover its flat
+(vector) walk, its strided and unaligned walks, packed and long-row scans,
+each with the discounted returns requested (two scans per step) and
+without them (one scan).
 
 Tolerances: normalised advantages and returns |gpu - ref| <= 1e-4 + 1e-5 |ref|;
 the reported (mean, std) within 1e-5 relative (+1e-6 absolute for the mean).
@@ -64,8 +66,9 @@ CASES = [
 IDS = [f"{n}x{t}" + (f"_rs{rs}" if rs else "") + f"_{m}" for n, t, rs, m in CASES]
 
 
+@pytest.mark.parametrize("with_disc", [True, False], ids=["two_scans", "one_scan"])
 @pytest.mark.parametrize("case", CASES, ids=IDS)
-def test_normalized_parity(case):
+def test_normalized_parity(case, with_disc):
     N, T, rs, mode = case
     b = synthetic.gae_batch(N, T, 3, 51, 0.01, 0.005 if mode == "2d" else 0.0, mode)
     g, lam, eps = 0.99, 0.95, 1e-8
@@ -73,10 +76,12 @@ def test_normalized_parity(case):
     bs, last = b["bootstrap_values"], b["last_value"]
     raw = oracle.gae(b["rewards"], b["values"], b["terminateds"], trunc, g, lam, bs, last)
     want, (mean, sd) = oracle.normalize_advantages(raw, eps)
-    adv, lret, disc, mom = L().compute_gae_normalized(
+    outputs = ("advantages", "lambda_returns") + (("discounted_returns",) if with_disc else ())
+    got = L().compute_gae_normalized(
         dev(b["rewards"], rs), dev(b["values"], rs), dev(b["terminateds"], rs), dev(trunc, rs), g,
-        lam, dev(bs, rs), dev(last), eps,
-        outputs=("advantages", "lambda_returns", "discounted_returns"), return_moments=True)
+        lam, dev(bs, rs), dev(last), eps, outputs=outputs, return_moments=True)
+    adv, lret, mom = got[0], got[1], got[-1]
+    disc = got[2] if with_disc else None
     assert_disc(adv, want, "normalized advantages")
     m = mom.double().cpu().numpy()
     assert abs(m[0] - mean) <= 1e-6 + 1e-5 * abs(mean), (m, mean)
@@ -88,16 +93,17 @@ def test_normalized_parity(case):
         lam_ref = oracle.lambda_returns(b["rewards"], nv, b["terminateds"], None, g, lam, None, last)
         disc_ref = oracle.discounted_returns(b["rewards"], b["terminateds"], None, g, None, last)
         assert_disc(lret, lam_ref, "lambda returns")
-        assert_disc(disc, disc_ref, "discounted returns")
     else:
         assert_disc(lret, raw + b["values"].astype(np.float64), "lambda returns = raw A + V")
         disc_ref = oracle.discounted_returns(b["rewards"], b["terminateds"], trunc, g, bs, None)
+    if with_disc:
         assert_disc(disc, disc_ref, "discounted returns")
 
 
 def test_repeated_and_interleaved_calls():
-    """The per-call moments counter re-arms itself: repeated calls, and calls
-    interleaved with other entry points on the same workspace, agree."""
+    """Repeated calls, and calls interleaved with other entry points on the
+    same workspace, agree (long rows: look-back tile states and moment slots
+    share the workspace)."""
     N, T = 64, 1 << 14
     b = synthetic.gae_batch(N, T, 4, 52, 0.01, 0.0, "last")
     args = [dev(b[k]) for k in ("rewards", "values", "terminateds")]
@@ -129,6 +135,44 @@ def test_packed_repeated_and_interleaved_calls():
     raw = oracle.gae(b["rewards"], b["values"], b["terminateds"], None, 0.99, 0.95, None, b["last_value"])
     assert_disc(first[0], oracle.normalize_advantages(raw, 1e-8)[0], "normalized advantages")
     L().workspace_status()  # raises if any wait timed out
+
+
+def test_moments_region_over_stale_tile_states():
+    """The moments region of a small normalising call lies where a larger
+    call on the same workspace left its look-back tile states; the scan
+    writes every slot the pass combines, so stale words there change
+    nothing (one- and two-scan kernels)."""
+    import ctypes
+    from linear_recurrence_scan_gb300 import _native
+    lib = _native.lib()
+    vp = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    big = lib.rlscan_workspace_bytes(64, 1 << 16)
+    N, T = 256, 1024
+    need = lib.rlscan_gae_normalized_workspace_bytes(N, T)
+    assert need < big
+    ws = torch.empty(big, dtype=torch.uint8, device=DEV)
+    assert lib.rlscan_workspace_init(vp(ws), big, s) == 0
+    b = synthetic.gae_batch(64, 1 << 16, 6, 54, 0.01, 0.0, "last")
+    d = {k: dev(b[k]) for k in ("rewards", "values", "terminateds", "last_value")}
+    out = torch.empty((64, 1 << 16), device=DEV)
+    for _ in range(2):  # tile states of two calls (two epochs) over the region
+        assert lib.rlscan_gae(vp(d["rewards"]), vp(d["values"]), vp(d["terminateds"]), None, None,
+                              vp(d["last_value"]), 64, 1 << 16, 1 << 16, 0.99, 0.95, vp(out), vp(ws), big, s) == 0
+    c = synthetic.gae_batch(N, T, 7, 55, 0.01, 0.0, "last")
+    e = {k: dev(c[k]) for k in ("rewards", "values", "terminateds", "last_value")}
+    raw = oracle.gae(c["rewards"], c["values"], c["terminateds"], None, 0.99, 0.95, None, c["last_value"])
+    want, (mean, sd) = oracle.normalize_advantages(raw, 1e-8)
+    for disc in (None, torch.empty((N, T), device=DEV)):
+        adv = torch.empty((N, T), device=DEV)
+        mom = torch.empty(2, device=DEV)
+        assert lib.rlscan_gae_normalized(vp(e["rewards"]), vp(e["values"]), vp(e["terminateds"]), None, None,
+                                         vp(e["last_value"]), N, T, T, 0.99, 0.95, 1e-8, vp(adv), None, vp(disc),
+                                         vp(mom), vp(ws), need, s) == 0
+        assert_disc(adv, want, "normalized advantages over stale states")
+        m = mom.double().cpu().numpy()
+        assert abs(m[0] - mean) <= 1e-6 + 1e-5 * abs(mean) and abs(m[1] - sd) <= 1e-5 * sd, (m, mean, sd)
+    assert lib.rlscan_workspace_status(vp(ws), big, s) == 0
 
 
 def test_single_value_gives_nan():
