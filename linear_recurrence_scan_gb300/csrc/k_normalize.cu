@@ -24,8 +24,14 @@ rlscan_status launch_gae_moments(bool trunc, bool bs2d, bool discounted, Params 
     return launch_scan<est::GAEReturnsMoments<true, true>>(p, ws, ws_bytes, s, grid);
 }
 
-constexpr int kNormThreads = 256;
-constexpr int kVecPerThread = 8;
+#ifndef RLSCAN_NORM_THREADS
+#define RLSCAN_NORM_THREADS 256
+#endif
+#ifndef RLSCAN_NORM_VEC
+#define RLSCAN_NORM_VEC 8
+#endif
+constexpr int kNormThreads = RLSCAN_NORM_THREADS;
+constexpr int kVecPerThread = RLSCAN_NORM_VEC;
 
 // What the normalising pass needs from the scan: the per-CTA moment slots
 // to combine and the batch size.

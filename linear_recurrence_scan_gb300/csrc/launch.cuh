@@ -34,6 +34,16 @@ namespace rlscan {
 #ifndef RLSCAN_MAX_STAGES
 #define RLSCAN_MAX_STAGES 3
 #endif
+// Compact storage (bf16 / uint8) moves about half the bytes per step and
+// is bound by its issue rate: a deeper ring of split-row tiles keeps more
+// copies in flight while its two CTAs per SM compute (3 stages: V-trace
+// 2048 x 4096 26.9 -> 26.6 us, Retrace 1024 x 16384 46.3 -> 45.7 us).
+#ifndef RLSCAN_LOWP_SMEM_BUDGET_KB
+#define RLSCAN_LOWP_SMEM_BUDGET_KB 80
+#endif
+#ifndef RLSCAN_LOWP_MAX_STAGES
+#define RLSCAN_LOWP_MAX_STAGES 3
+#endif
 // Packed tiles (whole rows, no look-back) use at most this many of the
 // ring's stages: a shallower ring gets every CTA's first tile sooner, while
 // split rows keep the deeper ring to hide their look-back waits.
@@ -133,10 +143,11 @@ struct Shape {
                                                                                                : RLSCAN_THREADS_1024)));
     static constexpr int ITEMS = TILE / THREADS;
     static constexpr int STAGE_BYTES = narrow_bytes<E, TILE>();  // narrow arrays
-    static constexpr int RAW = (RLSCAN_SMEM_BUDGET_KB * 1024) / STAGE_BYTES;
+    static constexpr int RAW = ((IoOf<E>::LOWP ? RLSCAN_LOWP_SMEM_BUDGET_KB : RLSCAN_SMEM_BUDGET_KB) * 1024) /
+                               STAGE_BYTES;
+    static constexpr int MAXST = IoOf<E>::LOWP ? RLSCAN_LOWP_MAX_STAGES : RLSCAN_MAX_STAGES;
     // ring of an immediate-finish launch, and of a deferred one
-    static constexpr int SHORT_STAGES = WIDE ? RLSCAN_WIDE_STAGES
-                                             : (RAW < 2 ? 2 : (RAW > RLSCAN_MAX_STAGES ? RLSCAN_MAX_STAGES : RAW));
+    static constexpr int SHORT_STAGES = WIDE ? RLSCAN_WIDE_STAGES : (RAW < 2 ? 2 : (RAW > MAXST ? MAXST : RAW));
     static constexpr int PACKED_STAGES = SHORT_STAGES < RLSCAN_PACKED_STAGES ? SHORT_STAGES : RLSCAN_PACKED_STAGES;
     static constexpr int DEFER_RING = DeferRingOf<E>::value;
     static constexpr int DEFER_STAGES = (WIDE || DEFER_RING < 3) ? 0

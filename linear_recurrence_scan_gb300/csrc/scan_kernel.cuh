@@ -192,6 +192,19 @@ __device__ __forceinline__ const char *elem0(const float *stage, int j)
     return reinterpret_cast<const char *>(stage) + region_off<E, TILE>(j) + 16;
 }
 
+// Byte r of w (an integer 0..255) as a float.  RLSCAN_U8_PRMT=1: one byte
+// permute builds the float 2^23 + byte (bits 0x4B0000bb) and one subtraction
+// removes 2^23, exact for every byte; 0: integer extract and conversion.
+#ifndef RLSCAN_U8_PRMT
+#define RLSCAN_U8_PRMT 1
+#endif
+__device__ __forceinline__ float u8_to_float(uint32_t w, int r)
+{
+    if (RLSCAN_U8_PRMT)
+        return __uint_as_float(__byte_perm(w, 0x4B000000u, static_cast<uint32_t>(r) | 0x7540u)) - 8388608.f;
+    return static_cast<float>((w >> (8 * r)) & 0xffu);
+}
+
 // one stored element of `bytes` bytes as a float: bf16 (the upper half of a
 // float), uint8 (an integer 0..255) or float
 template <int BYTES>
@@ -860,10 +873,8 @@ scan_kernel(const __grid_constant__ Params p)
                     v[3] = __uint_as_float(w.y & 0xffff0000u);
                 } else {
                     const uint32_t w = *reinterpret_cast<const uint32_t *>(q);
-                    v[0] = static_cast<float>(w & 0xffu);
-                    v[1] = static_cast<float>((w >> 8) & 0xffu);
-                    v[2] = static_cast<float>((w >> 16) & 0xffu);
-                    v[3] = static_cast<float>(w >> 24);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) v[r] = u8_to_float(w, r);
                 }
             };
             if constexpr (ITEMS == 8) {
@@ -880,10 +891,8 @@ scan_kernel(const __grid_constant__ Params p)
                     const uint32_t h[2] = {w.x, w.y};
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
-                        x[j][4 * q] = static_cast<float>(h[q] & 0xffu);
-                        x[j][4 * q + 1] = static_cast<float>((h[q] >> 8) & 0xffu);
-                        x[j][4 * q + 2] = static_cast<float>((h[q] >> 16) & 0xffu);
-                        x[j][4 * q + 3] = static_cast<float>(h[q] >> 24);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) x[j][4 * q + r] = u8_to_float(h[q], r);
                     }
                 } else {
                     // Two 16-byte chunks per thread: consecutive lanes' first
