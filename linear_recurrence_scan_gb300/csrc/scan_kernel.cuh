@@ -657,6 +657,11 @@ constexpr int block_threads() { return THREADS + 32; }
 #ifndef RLSCAN_EARLY_EXIT_COUNT
 #define RLSCAN_EARLY_EXIT_COUNT 1
 #endif
+// 1: bf16 inputs at 8 steps per thread take their neighbour step by a
+// shuffle too (0: a 2-byte shared-memory read with its bank conflicts)
+#ifndef RLSCAN_HALO_SHFL_NARROW
+#define RLSCAN_HALO_SHFL_NARROW 0
+#endif
 // 1: the swapped float32 reads at 8 steps per thread (0: plain reads with
 // their two-way conflicts; measured 4-5 % slower on 2^20-step rows)
 #ifndef RLSCAN_F32_SWAP
@@ -923,7 +928,7 @@ scan_kernel(const __grid_constant__ Params p)
             float nb = 0.f;
             if ((E::HALO >> j) & 1u) {
                 const char *q = FWD ? aj - eb : aj + ITEMS * eb;
-                if (ITEMS == 8 && eb == 4) {
+                if (ITEMS == 8 && (eb == 4 || (RLSCAN_HALO_SHFL_NARROW && eb == 2))) {
                     // the neighbour step is the adjacent lane's last (forward)
                     // or first (backward) step: a shuffle, and a shared-memory
                     // read only at the warp's edge (lanes 32 bytes apart
@@ -932,7 +937,7 @@ scan_kernel(const __grid_constant__ Params p)
                     // smaller conflict measured cheaper than the shuffle
                     nb = FWD ? __shfl_up_sync(0xffffffffu, x[j][ITEMS - 1], 1)
                              : __shfl_down_sync(0xffffffffu, x[j][0], 1);
-                    if (lane == (FWD ? 0 : 31)) nb = to_float<4>(q);
+                    if (lane == (FWD ? 0 : 31)) nb = eb == 4 ? to_float<4>(q) : to_float<2>(q);
                 } else {
                     nb = eb == 4 ? to_float<4>(q) : (eb == 2 ? to_float<2>(q) : to_float<1>(q));
                 }
