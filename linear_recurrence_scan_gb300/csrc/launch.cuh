@@ -164,6 +164,16 @@ struct Shape {
 #ifndef RLSCAN_MOM_SHORT
 #define RLSCAN_MOM_SHORT 1
 #endif
+// Compact storage on split rows: 1024-step tiles on 128 threads x 8 with a
+// three-stage ring from this many rows on (fewer rows keep the regular
+// shape, whose deferred kernel they need).  Measured: compact V-trace
+// 2048 x 4096 26.5 -> 25.7 us, compact Retrace 1024 x 16384 45.8 -> 45.2.
+#ifndef RLSCAN_LOWP_SPLIT_MIN_ROWS
+#define RLSCAN_LOWP_SPLIT_MIN_ROWS 512
+#endif
+#ifndef RLSCAN_LOWP_SPLIT_STAGES
+#define RLSCAN_LOWP_SPLIT_STAGES 3
+#endif
 // Packed launches (whole rows, T <= 1024) of single-scan or compact-storage
 // estimators whose own shape is 2048 steps or more: 1024-step tiles on 128
 // threads x 8 steps.  Rows this short gain from the smaller CTAs (five per
@@ -419,6 +429,14 @@ rlscan_status launch_scan(Params p, void *ws, size_t ws_bytes, cudaStream_t stre
     if constexpr (ShortShape<E>::ENABLED) {
         using Q = ShortShape<E>;
         if (p.T <= Q::TILE) return launch_scan_ring<E, Q, RLSCAN_SHORT_STAGES>(p, ws, ws_bytes, stream, grid_out);
+    }
+    if constexpr (ShortShape<E>::ENABLED && IoOf<E>::LOWP) {
+        // compact storage: the short-row shape for split rows too (a
+        // three-stage ring), unless the rows are few enough for the
+        // deferred kernel of the regular shape
+        using Q = ShortShape<E>;
+        if (p.T > S::TILE && p.N >= RLSCAN_LOWP_SPLIT_MIN_ROWS)
+            return launch_scan_ring<E, Q, RLSCAN_LOWP_SPLIT_STAGES>(p, ws, ws_bytes, stream, grid_out);
     }
     if (p.T <= S::TILE) return launch_scan_ring<E, S, S::PACKED_STAGES>(p, ws, ws_bytes, stream, grid_out);
     return launch_scan_ring<E, S, S::SHORT_STAGES>(p, ws, ws_bytes, stream, grid_out);

@@ -67,8 +67,11 @@ def assert_close(got, ref, what, bf16):
                              f"gpu {g[i]!r} ref {ref[i]!r}")
 
 
+# (N, T, row stride): packed rows, split rows on few rows (the regular shape,
+# deferred finishing on the longest), split rows on 512 or more rows (the
+# short-row shape with look-back), strided and unaligned rows
 SHAPES = [(8, 128, None), (5, 37, None), (4096, 1024, None), (3, 3000, None), (2, 40000, None),
-          (64, 1 << 16, None), (5, 96, 112), (5, 96, 104)]
+          (64, 1 << 16, None), (600, 5000, None), (520, 2100, 2104), (5, 96, 112), (5, 96, 104)]
 SIDS = [f"{n}x{t}" + (f"_rs{rs}" if rs else "") for n, t, rs in SHAPES]
 VARIANTS = ["plain", "last_value", "trunc", "trunc_bs"]
 
@@ -94,8 +97,8 @@ def test_compact_gae(shape, variant):
 
 @pytest.mark.parametrize("variant", ["last_value", "trunc_bs"])
 @pytest.mark.parametrize("shape", [(8, 128, None), (4096, 1024, None), (3, 5000, None),
-                                   (64, 1 << 16, None)], ids=["8x128", "4096x1024", "3x5000",
-                                                              "64x65536"])
+                                   (64, 1 << 16, None), (600, 5000, None)],
+                         ids=["8x128", "4096x1024", "3x5000", "64x65536", "600x5000"])
 def test_compact_gae_returns(shape, variant):
     N, T, rs = shape
     bf, fl, last, dec = compact_batch(N, T, variant, 12 + T, torch.bool)
@@ -135,7 +138,7 @@ def _u8(a):
 
 
 OFF_SHAPES = [(8, 128, None), (5, 37, None), (4096, 1024, None), (3, 5000, None), (64, 1 << 16, None),
-              (5, 96, 112)]
+              (600, 5000, None), (520, 2100, 2104), (5, 96, 112)]
 OFF_IDS = [f"{n}x{t}" + (f"_rs{rs}" if rs else "") for n, t, rs in OFF_SHAPES]
 
 
